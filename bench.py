@@ -1,0 +1,390 @@
+"""Benchmark of the CSA Lightning-Indexer training step on GB300.
+
+One step = the whole hot path on one batch of synthetic input already resident in HBM:
+csa_indexer_fwd (scores + top-k) then csa_indexer_bwd (full-CSA teacher, KL, dQ_idx / dW / dK_idx).
+Workload: the BSHD bf16 configuration (b=2, sq=4096, ratio 4, H=64, D=192, H_I=64, D_I=128, topk 512,
+window 128).  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+--impl reference times the float64 CPU oracle (the baseline arm) on a bounded row sample per step.
+For N > 1 (torchrun) every rank runs its own independent batch (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "query-tokens/s for CSA indexer fwd+bwd (full-CSA teacher); % of roofline"
+UNIT = "query-tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="bshd_bf16")
+    ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="target seconds of the oracle baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc(cfg) -> dict:
+    return {"workload": (f"{cfg.name}: layout={cfg.layout} b={cfg.batch} sq={cfg.seqlen} ratio={cfg.ratio} "
+                         f"H={cfg.heads} D={cfg.head_dim} H_I={cfg.idx_heads} D_I={cfg.idx_dim} topk={cfg.topk} "
+                         f"window={cfg.window} sparse_loss={int(cfg.sparse)} dtype={cfg.dtype}"),
+            "global_batch": cfg.batch, "seq_len": cfg.seqlen}
+
+
+# ------------------------------------------------------------------ algorithmic work per step
+
+def algorithmic(cfg, inp):
+    """Per-stage algorithmic FLOPs and minimal HBM bytes of one step (exact sums over rows)."""
+    from oracle import oracle as O  # geometry only (key counts per row)
+    P = O.Problem.from_inputs(inp)
+    rows = np.arange(P.rows)
+    if cfg.layout == "thd":
+        cu, cur = inp.cu_seqlens_q, inp.cu_seqlens_q_unpadded
+        b = np.searchsorted(cu, rows, side="right") - 1
+        s = rows - cu[b]
+        v = np.where(s < (cur[b + 1] - cur[b]), (s + 1) // cfg.ratio, 0)
+        wn = np.where(s < (cur[b + 1] - cur[b]), np.minimum(cfg.window, s + 1), 0)
+    else:
+        s = rows % cfg.seqlen if cfg.layout == "bshd" else rows // cfg.batch
+        v = (s + 1) // cfg.ratio
+        wn = np.minimum(cfg.window, s + 1)
+    K = P.K
+    k = np.minimum(v, K) if cfg.sparse else v
+    k = np.where(v > 0, k, 0)
+    wn = np.where(v > 0, wn, 0)
+    HI, DI, H, D = cfg.idx_heads, cfg.idx_dim, cfg.heads, cfg.head_dim
+    eb = 2 if cfg.dtype == "bf16" else 4
+    n = P.rows
+    nk = inp.k_idx.shape[0] * (inp.k_idx.shape[1] if cfg.layout != "thd" else 1)
+    fl = {
+        "score_topk": float(np.sum(2.0 * HI * DI * v)),
+        "teacher": float(np.sum(2.0 * H * D * (k + wn))),
+        "kl_grad": float(np.sum(6.0 * HI * DI * k)),
+    }
+    by = {
+        # q_idx + w read, ids + selscore written, k_idx read once
+        "score_topk": n * (HI * DI * eb + HI * 4 + 2 * K * 4) + nk * DI * eb,
+        # q read, kv window rows and kv_c read once, ids read, teacher kept on chip (bwd) / written (teacher call)
+        "teacher": n * (H * D * eb + D * eb + K * 4) + nk * D * eb,
+        # q_idx, w, ids, selscore read; dq, dw written; k_idx read, dk written
+        "kl_grad": n * (2 * HI * DI * eb + 2 * HI * 4 + 2 * K * 4) + 2 * nk * DI * eb,
+    }
+    return fl, by
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        mhz, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def cpu_oracle_rate(inp, seconds: float):
+    """Time the float64 oracle (as it stands) on a stratified row sample; returns (rows/s, rows, secs, cores)."""
+    from oracle import oracle as O
+    P = O.Problem.from_inputs(inp)
+    n = P.rows
+    take = 64
+    while True:
+        rows = np.linspace(0, n - 1, min(take, n)).astype(np.int32)
+        t0 = time.perf_counter()
+        P.step(inp, rows=rows, want_dk=True)
+        dt = time.perf_counter() - t0
+        if dt >= seconds / 4 or take >= n:
+            break
+        take = int(min(n, take * max(2.0, seconds / 4 / max(dt, 1e-3))))
+    # the timed sample: scale to about `seconds`
+    take = int(min(n, max(len(rows), len(rows) * seconds / max(dt, 1e-6))))
+    rows = np.linspace(0, n - 1, take).astype(np.int32)
+    t0 = time.perf_counter()
+    P.step(inp, rows=rows, want_dk=True)
+    dt = time.perf_counter() - t0
+    return len(rows) / dt, len(rows), dt, O.num_threads()
+
+
+# ------------------------------------------------------------------ arms
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        torch.distributed.init_process_group(backend)
+    return world, rank, local
+
+
+def run_reference(args, cfg):
+    # under torchrun only rank 0 runs the CPU baseline; the other ranks exit without work
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    from sparse_attention_indexer_tcgen05_gb300 import synth
+    from oracle import oracle as O
+    inp = synth.generate(cfg)
+    P = O.Problem.from_inputs(inp)
+    n = P.rows
+    # each step: a bounded stratified sample of the workload's rows (offset per step)
+    per_step = max(16, min(n, 256))
+    times = []
+    for it in range(args.warmup + args.steps):
+        off = it % 7
+        rows = np.unique(np.clip(np.linspace(off, n - 1, per_step).astype(np.int32), 0, n - 1))
+        t0 = time.perf_counter()
+        P.step(inp, rows=rows, want_dk=True)
+        dt = time.perf_counter() - t0
+        if it >= args.warmup:
+            times.append((len(rows), dt))
+    rows_done = sum(r for r, _ in times)
+    secs = sum(t for _, t in times)
+    value = rows_done / secs
+    ms_per_step = 1e3 * n / value  # time the oracle would take for one full step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_desc(cfg),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle",
+                         "sample": f"{per_step} stratified rows of {n} per step, full step work per row "
+                                   f"(scores, top-k, teacher, KL, gradients incl. dK contributions)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, cfg):
+    import torch
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from sparse_attention_indexer_tcgen05_gb300 import binding as B
+    from sparse_attention_indexer_tcgen05_gb300 import synth, workload
+
+    # weak scaling: each rank an independent batch of the same shape
+    cfg_r = cfg.replace(seed=cfg.seed + 1000 * rank) if rank else cfg
+    inp = synth.generate(cfg_r)
+    d = workload.to_device(inp, dev)
+    p = d.params
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(max(p.workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    ids = torch.empty((p.rows, p.K), dtype=torch.int32, device=dev)
+    sel = torch.empty((p.rows, p.K), dtype=torch.float32, device=dev)
+    outs = (torch.empty((), dtype=torch.float32, device=dev), torch.empty_like(d.q_idx), torch.empty_like(d.w),
+            torch.empty_like(d.k_idx))
+
+    def step():
+        B.csa_indexer_fwd(p, *d.indexer, workspace=ws, ids=ids, selscore=sel)
+        B.csa_indexer_bwd(p, *d.indexer, *d.teacher_side, ids, sel, workspace=ws, out=outs)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    B.csa_check_device_status(dev)
+
+    # ---- timed region: K steps, inputs resident in HBM (inputs exceed L2, so no flush between steps)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = B.csa_kernel_launches()
+    with ClockSampler(local) as clk:
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        barrier()
+    launches = B.csa_kernel_launches() - launches0
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * p.rows / (ms_per_step / 1e3)
+    B.csa_check_device_status(dev)
+    path = B.csa_last_path()
+
+    # ---- per-stage times (dominant kernel for the roofline), same stream, CUDA events
+    fl, by = algorithmic(cfg, inp)
+    teacher_buf = torch.empty((p.rows, p.teacher_width), dtype=torch.float32, device=dev)
+    stage_ms = {}
+
+    def timed(fn, reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    reps = max(3, min(args.steps, 10))
+    stage_ms["score_topk"] = timed(lambda: B.csa_indexer_fwd(p, *d.indexer, workspace=ws, ids=ids, selscore=sel), reps)
+    stage_ms["teacher"] = timed(lambda: B.csa_teacher(p, *d.teacher_side, ids, workspace=ws, out=teacher_buf), reps)
+    stage_ms["kl_grad"] = timed(lambda: B.csa_indexer_bwd(p, *d.indexer, *d.teacher_side, ids, sel,
+                                                         teacher=teacher_buf, workspace=ws, out=outs), reps)
+    dom = max(stage_ms, key=stage_ms.get)
+    import json as _j
+    peaks = _j.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
+    tensor_peak = peaks["bf16_tflops"] if peaks else 1900.0
+    hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
+    peak_src = "measured" if peaks else "fallback"
+    achieved_tf = fl[dom] / (stage_ms[dom] / 1e3) / 1e12
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        tr = _j.load(open(tr_path))
+        if tr.get("path") == path and dom in tr.get("per_launch_bytes", {}):
+            traffic = tr["per_launch_bytes"][dom]
+    roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": achieved_tf / tensor_peak, "traffic": traffic, "kernel": dom, "peak_source": peak_src,
+                "stage_ms": stage_ms,
+                "stage_frac_tensor": {k: fl[k] / (stage_ms[k] / 1e3) / 1e12 / tensor_peak for k in stage_ms},
+                "stage_frac_hbm": {k: by[k] / (stage_ms[k] / 1e3) / 1e9 / hbm_peak for k in stage_ms},
+                "algorithmic_flops": fl, "algorithmic_bytes": by}
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    host = {n: workload.tensor_to_torch(getattr(inp, n), cfg.dtype if n not in ("w", "sink") else "f32", "cpu",
+                                        pin=True)
+            for n in ("q_idx", "w", "k_idx", "q", "kv", "kv_c", "sink")}
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+
+    def e2e_step():
+        for n, t in host.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        B.csa_indexer_fwd(p, dev_in["q_idx"], dev_in["w"], dev_in["k_idx"], workspace=ws, ids=ids, selscore=sel)
+        B.csa_indexer_bwd(p, dev_in["q_idx"], dev_in["w"], dev_in["k_idx"], dev_in["q"], dev_in["kv"], dev_in["kv_c"],
+                          dev_in["sink"], ids, sel, workspace=ws, out=outs)
+        loss_host.copy_(outs[0], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            rate, nrows, secs, cores = cpu_oracle_rate(inp, args.cpu_sample_s)
+            cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                   "sample": f"{nrows} stratified rows of {p.rows} ({secs:.1f} s), full step work per row"}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+            "config": {**workload_desc(cfg), "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "inputs exceed L2 (q 201 MB + q_idx 134 MB > 129 MB); no flush",
+                       "path": path},
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": world * p.rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": 4},
+            "gpu_launches": launches, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def main():
+    args = parse()
+    from sparse_attention_indexer_tcgen05_gb300 import synth
+    cfg = synth.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

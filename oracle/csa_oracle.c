@@ -150,7 +150,7 @@ static double orc_dot(const double *a, const double *b, int n)
 
 /* ---------------------------------------------------------------- step 1: scores */
 
-/* I[t,s] for one row and compressed key with global id g. */
+/* I[t,s] for one row and compressed key with global id g; r indexes the row's q_idx and w. */
 static double orc_score(const orc_params *P, const double *q_idx, const double *w, const double *k_idx,
                         long r, long g)
 {
@@ -164,17 +164,21 @@ static double orc_score(const orc_params *P, const double *q_idx, const double *
     return I;
 }
 
+/* Row-dependent inputs (q_idx, w, q) hold either every row (compact = 0, indexed by memory row) or
+ * only the listed rows in list order (compact = 1).  This is storage only; the arithmetic is the same. */
+#define ORC_SRC(i, r) (compact ? (long)(i) : (long)(r))
+
 /* Dense indexer scores of the listed rows: out[i][j] = I[row_i, j] for visible local keys j,
  * -inf elsewhere.  out is [nrows][orc_key_width]. */
 void orc_scores(const orc_params *P, const double *q_idx, const double *w, const double *k_idx,
-                const int32_t *rows, int nrows, double *out)
+                const int32_t *rows, int nrows, int compact, double *out)
 {
     const int NC = orc_key_width(P);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int i = 0; i < nrows; i++) {
         orc_row R = orc_decode(P, rows[i]);
         for (int j = 0; j < NC; j++)
-            out[(long)i * NC + j] = j < R.v ? orc_score(P, q_idx, w, k_idx, rows[i], orc_gid(P, &R, j))
+            out[(long)i * NC + j] = j < R.v ? orc_score(P, q_idx, w, k_idx, ORC_SRC(i, rows[i]), orc_gid(P, &R, j))
                                             : -INFINITY;
     }
 }
@@ -253,7 +257,7 @@ int orc_teacher_width(const orc_params *P)
  * normalisation of [BUG] sec. 2 excerpt.  Each exp is taken relative to the head's largest term,
  * which changes no ratio.  ids is [nrows][K] for the listed rows; out is [nrows][teacher width]. */
 void orc_teacher(const orc_params *P, const double *q, const double *kv, const double *kv_c,
-                 const double *sink, const int32_t *ids, const int32_t *rows, int nrows, double *out)
+                 const double *sink, const int32_t *ids, const int32_t *rows, int nrows, int compact, double *out)
 {
     const int H = P->heads, D = P->head_dim, K = orc_topk_width(P), NC = orc_key_width(P);
     const int TW = orc_teacher_width(P);
@@ -276,7 +280,7 @@ void orc_teacher(const orc_params *P, const double *q, const double *kv, const d
         double *wl = malloc(sizeof(double) * (size_t)(nW > 0 ? nW : 1));
         double *T = calloc((size_t)nC, sizeof(double));
         for (int h = 0; h < H; h++) {
-            const double *qh = q + (r * H + h) * D;
+            const double *qh = q + (ORC_SRC(i, r) * H + h) * D;
             double m = sink[h];
             for (int k = 0; k < nC; k++) {
                 c[k] = P->scale * orc_dot(qh, kv_c + orc_crow(P, gid[k]) * D, D);
@@ -348,7 +352,7 @@ double orc_loss_factor(const orc_params *P)
  * dq: [nrows][HI][DI], dw: [nrows][HI] (rows in list order); dk: [compressed rows][DI], accumulated
  * (the caller zeroes it); loss_rows (optional): [nrows] unscaled L_t. */
 double orc_loss_grads(const orc_params *P, const double *q_idx, const double *w, const double *k_idx,
-                      const int32_t *ids, const double *teacher, const int32_t *rows, int nrows,
+                      const int32_t *ids, const double *teacher, const int32_t *rows, int nrows, int compact,
                       long n_key_rows, double *loss_rows, double *dq, double *dw, double *dk)
 {
     const int HI = P->idx_heads, DI = P->idx_dim, K = orc_topk_width(P), NC = orc_key_width(P);
@@ -381,7 +385,7 @@ double orc_loss_grads(const orc_params *P, const double *q_idx, const double *w,
         double *t = malloc(sizeof(double) * (size_t)n);
         double *g = malloc(sizeof(double) * (size_t)n);
         for (int k = 0; k < n; k++) {
-            I[k] = orc_score(P, q_idx, w, k_idx, r, gid[k]);
+            I[k] = orc_score(P, q_idx, w, k_idx, ORC_SRC(i, r), gid[k]);
             t[k] = teacher[(long)i * TW + slot[k]];
         }
         double L = orc_kl_row(t, I, n, g, NULL);
@@ -391,12 +395,13 @@ double orc_loss_grads(const orc_params *P, const double *q_idx, const double *w,
             const double gs = f * g[k];
             const long kr = orc_crow(P, gid[k]);
             const double *kk = k_idx + kr * DI;
+            const long src = ORC_SRC(i, r);
             for (int j = 0; j < HI; j++) {
-                const double *qj = q_idx + (r * HI + j) * DI;
+                const double *qj = q_idx + (src * HI + j) * DI;
                 double x = orc_dot(qj, kk, DI);
                 if (x <= 0.0) continue;
                 if (dw) dw[(long)i * HI + j] += gs * x;
-                const double a = gs * w[r * HI + j];
+                const double a = gs * w[src * HI + j];
                 if (dq) for (int d = 0; d < DI; d++) dq[((long)i * HI + j) * DI + d] += a * kk[d];
                 if (dk_local) {
                     double *dkr = dk_local + ((long)tid * n_key_rows + kr) * DI;

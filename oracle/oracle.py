@@ -57,14 +57,14 @@ def _load():
             lib.orc_topk_width.argtypes = [P]
             lib.orc_rows.argtypes = [P]
             lib.orc_teacher_width.argtypes = [P]
-            lib.orc_scores.argtypes = [P, vp, vp, vp, vp, i32, vp]
+            lib.orc_scores.argtypes = [P, vp, vp, vp, vp, i32, i32, vp]
             lib.orc_topk.argtypes = [P, vp, vp, i32, vp]
-            lib.orc_teacher.argtypes = [P, vp, vp, vp, vp, vp, vp, i32, vp]
+            lib.orc_teacher.argtypes = [P, vp, vp, vp, vp, vp, vp, i32, i32, vp]
             lib.orc_kl_row.argtypes = [vp, vp, i32, vp, vp]
             lib.orc_kl_row.restype = dbl
             lib.orc_loss_factor.argtypes = [P]
             lib.orc_loss_factor.restype = dbl
-            lib.orc_loss_grads.argtypes = [P, vp, vp, vp, vp, vp, vp, i32, ctypes.c_long, vp, vp, vp, vp]
+            lib.orc_loss_grads.argtypes = [P, vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_long, vp, vp, vp, vp]
             lib.orc_loss_grads.restype = dbl
             lib.orc_num_threads.restype = i32
             _lib = lib
@@ -140,12 +140,14 @@ class Problem:
         return np.ascontiguousarray(rows, dtype=np.int32)
 
     # steps --------------------------------------------------------------
-    def scores(self, q_idx, w, k_idx, rows=None) -> np.ndarray:
-        """Dense float64 indexer scores [len(rows), key_width]; -inf where not visible."""
+    def scores(self, q_idx, w, k_idx, rows=None, compact=False) -> np.ndarray:
+        """Dense float64 indexer scores [len(rows), key_width]; -inf where not visible.
+        compact=True: q_idx and w hold only the listed rows, in list order."""
         rows = self._rows(rows)
         qi, ww, ki = _f64(q_idx), _f64(w), _f64(k_idx)
         out = np.empty((len(rows), self.key_width), np.float64)
-        self.lib.orc_scores(ctypes.byref(self.p), _ptr(qi), _ptr(ww), _ptr(ki), _ptr(rows), len(rows), _ptr(out))
+        self.lib.orc_scores(ctypes.byref(self.p), _ptr(qi), _ptr(ww), _ptr(ki), _ptr(rows), len(rows), int(compact),
+                            _ptr(out))
         return out
 
     def topk(self, scores, rows=None) -> np.ndarray:
@@ -157,19 +159,21 @@ class Problem:
         self.lib.orc_topk(ctypes.byref(self.p), _ptr(sc), _ptr(rows), len(rows), _ptr(ids))
         return ids
 
-    def teacher(self, q, kv, kv_c, sink, ids, rows=None) -> np.ndarray:
-        """Full-CSA teacher [len(rows), teacher_width] for the given ids of those rows."""
+    def teacher(self, q, kv, kv_c, sink, ids, rows=None, compact=False) -> np.ndarray:
+        """Full-CSA teacher [len(rows), teacher_width] for the given ids of those rows.
+        compact=True: q holds only the listed rows, in list order."""
         rows = self._rows(rows)
         qq, kvv, kc, sk = _f64(q), _f64(kv), _f64(kv_c), _f64(sink)
         ids = np.ascontiguousarray(ids, dtype=np.int32)
         assert ids.shape == (len(rows), self.K)
         out = np.empty((len(rows), self.teacher_width), np.float64)
         self.lib.orc_teacher(ctypes.byref(self.p), _ptr(qq), _ptr(kvv), _ptr(kc), _ptr(sk), _ptr(ids), _ptr(rows),
-                             len(rows), _ptr(out))
+                             len(rows), int(compact), _ptr(out))
         return out
 
-    def loss_grads(self, q_idx, w, k_idx, ids, teacher, rows=None, want_dk=True):
-        """(loss, loss_rows, dq[rows,HI,DI], dw[rows,HI], dk[key rows, DI] or None) for the listed rows."""
+    def loss_grads(self, q_idx, w, k_idx, ids, teacher, rows=None, want_dk=True, compact=False):
+        """(loss, loss_rows, dq[rows,HI,DI], dw[rows,HI], dk[key rows, DI] or None) for the listed rows.
+        compact=True: q_idx and w hold only the listed rows, in list order."""
         rows = self._rows(rows)
         qi, ww, ki = _f64(q_idx), _f64(w), _f64(k_idx)
         ids = np.ascontiguousarray(ids, dtype=np.int32)
@@ -181,19 +185,28 @@ class Problem:
         dw = np.empty((len(rows), HI), np.float64)
         dk = np.zeros((n_key_rows, DI), np.float64) if want_dk else None
         loss = self.lib.orc_loss_grads(ctypes.byref(self.p), _ptr(qi), _ptr(ww), _ptr(ki), _ptr(ids), _ptr(te),
-                                       _ptr(rows), len(rows), n_key_rows, _ptr(lr), _ptr(dq), _ptr(dw), _ptr(dk))
+                                       _ptr(rows), len(rows), int(compact), n_key_rows, _ptr(lr), _ptr(dq), _ptr(dw),
+                                       _ptr(dk))
         return loss, lr, dq, dw, dk
 
-    def step(self, inp_or_arrays, rows=None):
-        """Whole step on the listed rows (all rows by default): ids, selected scores, teacher, loss
-        and gradients, all from the oracle's own float64 selection."""
-        a = inp_or_arrays
-        rows = self._rows(rows)
-        sc = self.scores(a.q_idx.values, a.w.values, a.k_idx.values, rows)
+    def step(self, inp, rows=None, want_dk=True):
+        """Whole step on the listed rows (all rows by default): scores, ids, teacher, loss and gradients,
+        all from the oracle's own float64 selection.  With a row list, only those rows of the row-dependent
+        inputs are widened to float64 (compact mode)."""
+        if rows is None:
+            rows = self._rows(None)
+            qi, ww, qq = inp.q_idx.values, inp.w.values, inp.q.values
+            compact = False
+        else:
+            rows = self._rows(rows)
+            qi, ww, qq = inp.q_idx.rows_f32(rows), inp.w.rows_f32(rows), inp.q.rows_f32(rows)
+            compact = True
+        sc = self.scores(qi, ww, inp.k_idx.values, rows, compact=compact)
         ids = self.topk(sc, rows)
-        te = self.teacher(a.q.values, a.kv.values, a.kv_c.values, a.sink.values, ids, rows)
-        loss, lr, dq, dw, dk = self.loss_grads(a.q_idx.values, a.w.values, a.k_idx.values, ids, te, rows)
-        return dict(scores=sc, ids=ids, teacher=te, loss=loss, loss_rows=lr, dq=dq, dw=dw, dk=dk)
+        te = self.teacher(qq, inp.kv.values, inp.kv_c.values, inp.sink.values, ids, rows, compact=compact)
+        loss, lr, dq, dw, dk = self.loss_grads(qi, ww, inp.k_idx.values, ids, te, rows, want_dk=want_dk,
+                                               compact=compact)
+        return dict(scores=sc, ids=ids, teacher=te, loss=loss, loss_rows=lr, dq=dq, dw=dw, dk=dk, rows=rows)
 
 
 def kl_row(t, I, want_grad=True):

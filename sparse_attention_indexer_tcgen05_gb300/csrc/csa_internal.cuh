@@ -1,0 +1,167 @@
+// csa_internal.cuh -- device-side geometry and helpers shared by the CSA indexer kernels.
+//
+// Row geometry follows the layouts of the C ABI (include/csa_indexer.h): a query row t sits in
+// segment b at 0-based position s (1-based i = s + 1) and sees the compressed keys j < i / r
+// ("[Bug] DSV4 unfused CSA indexer loss ..." (Megatron-LM issue #5776), sec. 1 excerpt: the
+// compressed causal mask where(arange(n_c) >= positions // ratio, -inf, 0), anchored per segment).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/csa_indexer.h"
+
+namespace csa {
+
+// Everything a kernel needs to place a row, a key or a window position.
+struct Geo {
+    int layout;        // CSA_SBHD / CSA_BSHD / CSA_THD
+    int B;             // sequences (SBHD/BSHD) or segments (THD)
+    int S;             // sequence length (SBHD/BSHD) or physical rows (THD)
+    int rows;          // query rows
+    int nc;            // compressed keys per sequence (SBHD/BSHD); unused in THD
+    int ratio, window;
+    int K;             // top-k width
+    int NC;            // dense key width
+    int TW;            // teacher width
+    int H, D, HI, DI;
+    long long key_rows;
+    float scale;       // sigma
+    int sparse;
+    float factor;      // loss_coeff / rows (mean) or loss_coeff (sum)
+    const int *cu_q;   // THD physical offsets
+    const int *cu_real;// THD unpadded offsets (== cu_q when none given)
+    const int *cu_c;   // THD compressed offsets (built on device from cu_real)
+};
+
+struct Row {
+    int b, s, len, v;
+    bool pad;
+    long long c_base;  // THD: first compressed row of the segment
+};
+
+__device__ __forceinline__ Row decode_row(const Geo &g, long long r)
+{
+    Row R;
+    R.c_base = 0;
+    if (g.layout == CSA_SBHD) {
+        R.s = (int)(r / g.B);
+        R.b = (int)(r % g.B);
+        R.len = g.S;
+    } else if (g.layout == CSA_BSHD) {
+        R.b = (int)(r / g.S);
+        R.s = (int)(r % g.S);
+        R.len = g.S;
+    } else {
+        // largest b with cu_q[b] <= r (empty segments resolve to the last of equal offsets)
+        int lo = 0, hi = g.B - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (__ldg(g.cu_q + mid) <= r) lo = mid; else hi = mid - 1;
+        }
+        R.b = lo;
+        R.s = (int)(r - __ldg(g.cu_q + lo));
+        R.len = __ldg(g.cu_real + lo + 1) - __ldg(g.cu_real + lo);
+        R.c_base = __ldg(g.cu_c + lo);
+    }
+    R.pad = R.s >= R.len;
+    int v = R.pad ? 0 : (R.s + 1) / g.ratio;
+    // guards against inconsistent caller metadata (max_seqlen_q, key_rows): a row never addresses more
+    // keys than the dense key axis holds, nor compressed rows past the end of k_idx / kv_c
+    if (v > g.NC) v = g.NC;
+    if (g.layout == CSA_THD && R.c_base + v > g.key_rows) v = R.c_base < g.key_rows ? (int)(g.key_rows - R.c_base) : 0;
+    R.v = v;
+    return R;
+}
+
+// memory row of original position p of the row's segment (query-like tensors)
+__device__ __forceinline__ long long q_row(const Geo &g, const Row &R, int p)
+{
+    if (g.layout == CSA_SBHD) return (long long)p * g.B + R.b;
+    if (g.layout == CSA_BSHD) return (long long)R.b * g.S + p;
+    return (long long)__ldg(g.cu_q + R.b) + p;
+}
+
+// global id of the row's local compressed key j
+__device__ __forceinline__ long long key_gid(const Geo &g, const Row &R, int j)
+{
+    if (g.layout == CSA_THD) return R.c_base + j;
+    return (long long)R.b * g.nc + j;
+}
+
+// memory row of the compressed key with global id gid
+__device__ __forceinline__ long long key_row(const Geo &g, long long gid)
+{
+    if (g.layout == CSA_SBHD) return (gid % g.nc) * g.B + gid / g.nc;
+    return gid;
+}
+
+template <typename T> __device__ __forceinline__ float ldf(const T *p, long long i);
+template <> __device__ __forceinline__ float ldf<float>(const float *p, long long i) { return __ldg(p + i); }
+template <> __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p, long long i)
+{
+    return __bfloat162float(p[i]);
+}
+
+// plain (non-.nc) load, valid for shared memory as well as global
+template <typename T> __device__ __forceinline__ float lds(const T *p, int i);
+template <> __device__ __forceinline__ float lds<float>(const float *p, int i) { return p[i]; }
+template <> __device__ __forceinline__ float lds<__nv_bfloat16>(const __nv_bfloat16 *p, int i)
+{
+    return __bfloat162float(p[i]);
+}
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Order-preserving map of an fp32 score to uint32 (larger score -> larger key); -0.0 maps like +0.0.
+__device__ __forceinline__ uint32_t score_key(float x)
+{
+    uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+// Count of kernel launches made by the library in this process (diagnostics; see csa_kernel_launches).
+void note_launches(int n);
+
+// ---------------------------------------------------------------- launchers (k_generic.cu)
+
+cudaError_t launch_build_cu_c(const Geo &g, int *cu_c, cudaStream_t st);
+template <typename T>
+cudaError_t launch_score_topk_generic(const Geo &g, const T *q_idx, const float *w, const T *k_idx,
+                                      int32_t *ids, float *selscore, float *dump, long long dump_row0,
+                                      long long dump_rows, cudaStream_t st);
+template <typename T>
+cudaError_t launch_teacher_generic(const Geo &g, const T *q, const T *kv, const T *kv_c, const float *sink,
+                                   const int32_t *ids, float *teacher, cudaStream_t st);
+cudaError_t launch_kl(const Geo &g, const int32_t *ids, const float *selscore, const float *dense_scores,
+                      const float *teacher, float *gbuf, float *row_loss, cudaStream_t st);
+template <typename T>
+cudaError_t launch_grad_generic(const Geo &g, const T *q_idx, const float *w, const T *k_idx,
+                                const int32_t *ids, const float *gbuf, T *dq_idx, float *dw, float *dk_acc,
+                                cudaStream_t st);
+template <typename T>
+cudaError_t launch_finalize(const Geo &g, const float *dk_acc, T *dk_idx, const float *row_loss, float *loss,
+                            cudaStream_t st);
+
+size_t score_topk_generic_smem(const Geo &g);
+size_t teacher_generic_smem(const Geo &g);
+size_t grad_generic_smem(const Geo &g);
+
+}  // namespace csa

@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
 from typing import Optional
 
 import numpy as np
@@ -32,7 +33,7 @@ TENSOR_IDS = {
     "doclens": 8, "variant": 9,
 }
 
-_CHUNK = 1 << 24  # elements drawn per call, bounds host memory for huge tensors
+_BLOCK = 1 << 22  # elements per independently seeded block (parallel, thread-count independent)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -80,9 +81,12 @@ CONFIGS = {
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (round-to-nearest-even); returns the uint16 bit patterns."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    r = (u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))) >> np.uint32(16)
-    return r.astype(np.uint16)
+    u = np.array(x, dtype=np.float32, copy=True).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    u += np.uint32(0x7FFF)
+    u += lsb
+    u >>= np.uint32(16)
+    return u.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -93,30 +97,64 @@ def _rng(seed: int, tensor: str, extra: int = 0) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, TENSOR_IDS[tensor], extra])))
 
 
-def _normal(rng: np.random.Generator, n: int, std: float) -> np.ndarray:
-    out = np.empty(n, dtype=np.float32)
-    for i in range(0, n, _CHUNK):
-        m = min(_CHUNK, n - i)
-        out[i:i + m] = rng.standard_normal(m, dtype=np.float32) * np.float32(std)
+def _blocks(n: int, fill):
+    """Run fill(block_index, start, stop) over fixed blocks of _BLOCK elements, on a thread pool."""
+    nb = (n + _BLOCK - 1) // _BLOCK
+    if nb <= 1:
+        for i in range(nb):
+            fill(i, 0, n)
+        return
+    import concurrent.futures as cf
+    with cf.ThreadPoolExecutor(max_workers=min(nb, os.cpu_count() or 4)) as ex:
+        list(ex.map(lambda i: fill(i, i * _BLOCK, min(n, (i + 1) * _BLOCK)), range(nb)))
+
+
+def _normal_into(seed: int, tensor: str, n: int, std: float, dtype: str):
+    """N(0, std^2) draws, one seeded stream per block: float32 values, or bf16 bit patterns."""
+    out = np.empty(n, dtype=np.uint16 if dtype == "bf16" else np.float32)
+
+    def fill(i, a, b):
+        x = _rng(seed, tensor, 1 + i).standard_normal(b - a, dtype=np.float32) * np.float32(std)
+        out[a:b] = f32_to_bf16_bits(x) if dtype == "bf16" else x
+
+    _blocks(n, fill)
     return out
 
 
-@dataclasses.dataclass
 class Tensor:
-    """One input tensor: exact float32 values, plus bf16 bit patterns when the dtype is bf16."""
-    values: np.ndarray                 # float32, exactly representable in the tensor's dtype
-    bits: Optional[np.ndarray] = None  # uint16 bf16 patterns (same shape) or None for f32
+    """One input tensor: bf16 bit patterns (bf16 tensors) or float32 values (fp32 tensors).
+
+    ``values`` gives the exact float32 values (computed on demand for bf16); ``rows_f32(idx)`` gives the values
+    of selected rows of the flattened leading dims without widening the whole tensor.
+    """
+
+    def __init__(self, values: Optional[np.ndarray] = None, bits: Optional[np.ndarray] = None, lead: int = 1):
+        assert (values is None) != (bits is None) or values is not None
+        self._values = values
+        self.bits = bits
+        self.lead = lead  # number of leading dims that index rows
+
+    @property
+    def values(self) -> np.ndarray:
+        if self._values is None:
+            self._values = bf16_bits_to_f32(self.bits).reshape(self.bits.shape)
+        return self._values
 
     @property
     def shape(self):
-        return self.values.shape
+        return (self.bits if self.bits is not None else self._values).shape
+
+    def rows_f32(self, idx) -> np.ndarray:
+        src = self.bits if self.bits is not None else self._values
+        flat = src.reshape((-1,) + src.shape[self.lead:])
+        sel = flat[np.asarray(idx)]
+        return bf16_bits_to_f32(sel).reshape(sel.shape) if self.bits is not None else np.array(sel, np.float32)
 
 
-def _make(values: np.ndarray, dtype: str) -> Tensor:
+def _make(values: np.ndarray, dtype: str, lead: int = 1) -> Tensor:
     if dtype == "bf16":
-        bits = f32_to_bf16_bits(values)
-        return Tensor(bf16_bits_to_f32(bits).reshape(values.shape), bits.reshape(values.shape))
-    return Tensor(np.ascontiguousarray(values, dtype=np.float32))
+        return Tensor(bits=f32_to_bf16_bits(values).reshape(values.shape), lead=lead)
+    return Tensor(np.ascontiguousarray(values, dtype=np.float32), lead=lead)
 
 
 def thd_doc_lengths(cfg: Config):
@@ -180,27 +218,25 @@ def generate(cfg: Config, skip=()) -> Inputs:
     (used by callers that need only the indexer-side tensors)."""
     cu = cur = None
     max_len = 0
+    n_c_rows = 0
     if cfg.layout == "thd":
         cu, cur, max_len = thd_doc_lengths(cfg)
         # compressed rows are laid out per segment by physical length // ratio; since only the
         # last segment carries padding, the unpadded packing cumsum(real // ratio) is a prefix
         n_c_rows = int(sum((cu[i + 1] - cu[i]) // cfg.ratio for i in range(len(cu) - 1)))
-        lead_q, lead_c = _lead_shapes(cfg, n_c_rows)
-        if cfg.layout == "thd":
-            max_len = int(max_len)
-    else:
-        lead_q, lead_c = _lead_shapes(cfg, 0)
+    # All draws are made in the canonical (BSHD/THD) order; SBHD is a transpose of the same draw,
+    # so a BSHD and an SBHD input of one config hold the same logical values.
+    canon = cfg if cfg.layout != "sbhd" else cfg.replace(layout="bshd")
+    cq, cc = _lead_shapes(canon, n_c_rows)
+    nlead = 2 if canon.layout != "thd" else 1
 
     def normal_tensor(name, shape, std):
         if name in skip:
             return Tensor(np.zeros((0,), np.float32))
         n = int(np.prod(shape))
-        return _make(_normal(_rng(cfg.seed, name), n, std).reshape(shape), cfg.dtype)
+        arr = _normal_into(cfg.seed, name, n, std, cfg.dtype).reshape(shape)
+        return Tensor(bits=arr, lead=nlead) if cfg.dtype == "bf16" else Tensor(arr, lead=nlead)
 
-    # All normals are drawn in the canonical (BSHD/THD) order; SBHD is a transpose of the same draw,
-    # so a BSHD and an SBHD input of one config hold the same logical values.
-    canon = cfg if cfg.layout != "sbhd" else cfg.replace(layout="bshd")
-    cq, cc = _lead_shapes(canon, 0 if cfg.layout != "thd" else lead_c[0])
     q_idx = normal_tensor("q_idx", cq + (cfg.idx_heads, cfg.idx_dim), 1.0 / math.sqrt(cfg.idx_dim))
     k_idx = normal_tensor("k_idx", cc + (cfg.idx_dim,), 1.0 / math.sqrt(cfg.idx_dim))
     q = normal_tensor("q", cq + (cfg.heads, cfg.head_dim), 1.0 / math.sqrt(cfg.head_dim))
@@ -210,8 +246,14 @@ def generate(cfg: Config, skip=()) -> Inputs:
         w = Tensor(np.zeros((0,), np.float32))
     else:
         n = int(np.prod(cq)) * cfg.idx_heads
-        w = Tensor(_rng(cfg.seed, "w").random(n, dtype=np.float32).reshape(cq + (cfg.idx_heads,)))
-    sink = Tensor(_normal(_rng(cfg.seed, "sink"), cfg.heads, cfg.sink_std))
+        wv = np.empty(n, np.float32)
+
+        def fill(i, a, b):
+            wv[a:b] = _rng(cfg.seed, "w", 1 + i).random(b - a, dtype=np.float32)
+
+        _blocks(n, fill)
+        w = Tensor(wv.reshape(cq + (cfg.idx_heads,)), lead=nlead)
+    sink = Tensor(_rng(cfg.seed, "sink").standard_normal(cfg.heads, dtype=np.float32) * np.float32(cfg.sink_std))
 
     inp = Inputs(cfg, q_idx, w, k_idx, q, kv, kv_c, sink, cu, cur, max_len)
     if cfg.layout == "sbhd":
@@ -220,11 +262,11 @@ def generate(cfg: Config, skip=()) -> Inputs:
 
 
 def _swap01(t: Tensor) -> Tensor:
-    if t.values.ndim < 2:
+    if len(t.shape) < 2:
         return t
-    v = np.ascontiguousarray(np.swapaxes(t.values, 0, 1))
-    b = None if t.bits is None else np.ascontiguousarray(np.swapaxes(t.bits, 0, 1))
-    return Tensor(v, b)
+    if t.bits is not None:
+        return Tensor(bits=np.ascontiguousarray(np.swapaxes(t.bits, 0, 1)), lead=t.lead)
+    return Tensor(np.ascontiguousarray(np.swapaxes(t.values, 0, 1)), lead=t.lead)
 
 
 def to_sbhd(inp: Inputs) -> Inputs:
@@ -241,9 +283,9 @@ def to_thd(inp: Inputs) -> Inputs:
     B, S = c.batch, c.seqlen
 
     def flat(t: Tensor) -> Tensor:
-        v = t.values.reshape((-1,) + t.values.shape[2:])
-        b = None if t.bits is None else t.bits.reshape((-1,) + t.bits.shape[2:])
-        return Tensor(np.ascontiguousarray(v), None if b is None else np.ascontiguousarray(b))
+        if t.bits is not None:
+            return Tensor(bits=np.ascontiguousarray(t.bits.reshape((-1,) + t.bits.shape[2:])), lead=1)
+        return Tensor(np.ascontiguousarray(t.values.reshape((-1,) + t.values.shape[2:])), lead=1)
 
     cu = (np.arange(B + 1) * S).astype(np.int32)
     c2 = c.replace(layout="thd", seqlen=B * S, batch=0)
@@ -266,7 +308,7 @@ def dense_variant(inp: Inputs, v: int) -> Inputs:
         D = c.head_dim
         u = rng.standard_normal(D, dtype=np.float32) / np.float32(math.sqrt(D))
         vals = inp.kv.values + np.float32(3.0 * sign) * u
-        kv = _make(vals.astype(np.float32), c.dtype)
+        kv = _make(vals.astype(np.float32), c.dtype, lead=inp.kv.lead)
     else:
         h = int(rng.integers(0, c.heads))
         s = inp.sink.values.copy()
