@@ -159,8 +159,8 @@ def test_batch_split_dk():
         sub = synth.Inputs(cfg.replace(batch=1), *(synth.Tensor(t.values[b:b + 1], lead=2) for t in
                                                    (inp.q_idx, inp.w, inp.k_idx, inp.q, inp.kv, inp.kv_c)), inp.sink)
         one = U.gpu_step(workload.to_device(sub))
-        got = full["dk"][b * n_c:(b + 1) * n_c].double()
-        exp = one["dk"].double() / 2
+        got = full["dk"].reshape(-1, 128)[b * n_c:(b + 1) * n_c].double()
+        exp = one["dk"].reshape(-1, 128).double() / 2
         rel = float((got - exp).norm() / exp.norm())
         assert rel <= 1e-5, rel
         ids_b = full["ids"][b * 512:(b + 1) * 512]
