@@ -43,7 +43,7 @@
  * Row semantics (row t of segment b at 1-based position i; r = compress_ratio):
  *   visible keys    j < i / r (integer division) -- the compressed causal mask of [BUG] sec. 1 excerpt
  *                   (where(arange(n_c) >= positions // ratio, -inf, 0)), anchored per segment;
- *   K               = min(topk, n_c) (SBHD/BSHD) or min(topk, max_seqlen_q / r) (THD)
+ *   K               = min(topk, n_c) (SBHD/BSHD) or min(topk, max_seqlen_q / r) (THD, longest unpadded segment)
  *                     ([BUG] sec. 1 excerpts: min(index_topk, n_compressed / max_seqlen_compressed));
  *   selection       the k_t = min(K, v_t) largest scores, ties to the lower key index (-0.0 == +0.0);
  *   global ids      b * n_c + j (SBHD/BSHD) or cu_c[b] + j (THD) ([PR] item 1: global ids b*S_k + local);
@@ -87,7 +87,8 @@ typedef struct {
     int32_t seqlen;                       /* SBHD/BSHD: sequence length S.  THD: physical rows T */
     const int32_t *cu_seqlens_q;          /* THD: device [batch+1], physical offsets (non-decreasing) */
     const int32_t *cu_seqlens_q_unpadded; /* THD: device [batch+1] or NULL; real lengths <= physical */
-    int32_t max_seqlen_q;                 /* THD: host-known longest physical segment (no device sync) */
+    int32_t max_seqlen_q;                 /* THD: host-known longest UNPADDED segment (no device sync); the
+                                             key width is max_seqlen_q / r (padding rows see no keys) */
     int32_t key_rows;                     /* THD: rows of k_idx / kv_c (T_c).  SBHD/BSHD: 0 or B * (S / r) */
     int32_t compress_ratio;               /* r >= 1 */
     int32_t window;                       /* W >= 0 original-KV positions (query included) */

@@ -39,7 +39,7 @@ typedef struct {
     int seqlen;                 /* SBHD/BSHD: sequence length S.  THD: physical rows T */
     const int32_t *cu_q;        /* THD: [nseg+1] physical segment offsets */
     const int32_t *cu_q_real;   /* THD: [nseg+1] unpadded offsets, or NULL (= cu_q) */
-    int max_seqlen;             /* THD: longest physical segment */
+    int max_seqlen;             /* THD: longest unpadded segment (sets the dense key width) */
     int ratio, window, topk;
     int heads, head_dim, idx_heads, idx_dim;
     double scale;               /* main-attention softmax scale sigma */

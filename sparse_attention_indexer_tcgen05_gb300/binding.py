@@ -99,7 +99,7 @@ class Params:
     """Geometry and flags of one step (the C struct csa_params plus references to its cu_seqlens tensors).
 
     For THD, ``cu_seqlens_q`` / ``cu_seqlens_q_unpadded`` are int32 CUDA tensors, ``batch`` is the number of
-    segments, ``seqlen`` the physical rows, ``max_seqlen_q`` the longest physical segment (host int) and
+    segments, ``seqlen`` the physical rows, ``max_seqlen_q`` the longest unpadded segment (host int) and
     ``key_rows`` the rows of k_idx / kv_c.
     """
 

@@ -1,5 +1,37 @@
-// k_score_tc.cu -- tcgen05 indexer-score + top-k kernel (placeholder until the tensor-core path lands).
+// k_score_tc.cu -- indexer score GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), fused
+// with the ReLU.w head reduction, the compressed causal mask and an exact per-row top-k in shared memory.
+//
+// What it computes ("[Bug] DSV4 unfused CSA indexer loss uses a compressed-only teacher ..." (Megatron-LM
+// issue #5776), sec. 1 excerpt: mask where(arange(n_c) >= positions // ratio, -inf, 0) and
+// min(index_topk, n_compressed); sec. 3 excerpt: invalid slots -1; "Megatron-LM PR #8539" item 1: global ids):
+//   I[t,s] = sum_j w[t,j] * max(0, q_idx[t,j] . k_idx[s]) for the keys s < i_t / r, then the K largest per row
+//   (ties to the lower key), written as ascending global ids with their fp32 scores.
+//
+// Shape taken: bf16 values, H_I = 64 indexer heads, D_I = 128, key axis <= 1024 (the score rows of one work
+// item live in shared memory).  Other shapes use the CUDA-core kernels.
+//
+// Mapping.  A work item is 4 consecutive query positions of one sequence (or THD segment).  The MMA computes
+// D[key, (row, head)] = k_idx[key] . q_idx[row, head] with M = 128 keys (A = a k_idx tile, K-major, streamed
+// by TMA), N = 4 rows x 64 heads = 256 (B = the item's q_idx rows, K-major, resident), K = 128 (8 MMAs of
+// K = 16).  With keys on TMEM lanes and (row, head) on columns, each epilogue thread owns one key and reduces
+// the 64 heads of a row in registers: no cross-thread reduction.  TMEM holds two 256-column accumulators
+// (double buffer), so the epilogue of one key tile overlaps the MMAs of the next.
+//
+// Roles (one CTA per SM, persistent, static round-robin over items ordered heaviest first):
+//   warp 0      TMA producer: B (q_idx rows, 64 KB, 2 buffers) and A (k_idx K-halves, 16 KB, 4 stages)
+//   warp 1      TMEM allocation and the single-thread tcgen05.mma issue
+//   warps 2..9  epilogue (TMEM -> registers -> ReLU.w reduction -> shared score rows), then the top-k:
+//               a warp pair per row finds the exact k-th largest score by a bitwise search on
+//               order-preserving keys and writes the selection by a stable compaction.
+//
+// Every mbarrier wait is bounded: on expiry the kernel records an error code (read back by
+// csa_check_device_status), stops waiting (so every role still runs its loops to the end with uniform
+// control flow), drains its own TMA copies and MMAs with timer-bounded waits, frees TMEM and returns.
 #include "csa_tc.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdlib.h>
 
 namespace csa {
 
@@ -13,19 +45,616 @@ cudaError_t tc_read_clear_error(int *flag)
     return cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(int));
 }
 
-bool tc_score_supported(const Geo &, bool) { return false; }
-size_t tc_workspace_bytes(const Geo &) { return 0; }
+namespace tcs {
 
-cudaError_t launch_score_topk_tc(const Geo &, const __nv_bfloat16 *, const float *, const __nv_bfloat16 *,
-                                 int32_t *, float *, void *, cudaStream_t)
+constexpr int ROWS = 4;                       // query rows per work item
+constexpr int HI = 64, DI = 128;              // indexer heads / dim taken by this kernel
+constexpr int NKEY = 128;                     // keys per tile (MMA M)
+constexpr int NCOL = ROWS * HI;               // MMA N = 256
+constexpr int NCMAX = 1024;                   // longest key axis held in shared memory
+constexpr int A_HALF = NKEY * 64 * 2;         // 16 KB: one 64-wide K-half of a key tile
+constexpr int A_STAGES = 4;
+constexpr int B_HALF = NCOL * 64 * 2;         // 32 KB
+constexpr int B_BUF = 2 * B_HALF;             // 64 KB
+constexpr int THREADS = 320;
+constexpr int EPI = 256;
+constexpr int TMEM_COLS = 512;
+
+constexpr int OFF_A = 0;
+constexpr int OFF_B = OFF_A + A_STAGES * A_HALF;           // 64 KB
+constexpr int OFF_SC = OFF_B + 2 * B_BUF;                  // 192 KB
+constexpr int OFF_W = OFF_SC + ROWS * NCMAX * 4;           // 208 KB
+constexpr int OFF_MISC = OFF_W + ROWS * HI * 4;            // 209 KB
+constexpr int SMEM_BYTES = OFF_MISC + 1024;
+constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;              // slack to align the base to 1024 B
+
+constexpr long long kTimeoutCycles = 4000000000LL;         // ~2 s at 2 GHz
+
+// instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16 (10-12 = 1), both
+// K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NCOL >> 3) << 17) |
+                           ((uint32_t)(NKEY >> 4) << 24);
+
+struct Args {
+    Geo g;
+    const float *w;
+    int32_t *ids;
+    float *selscore;
+    float *dump;
+    long long dump_row0, dump_rows;
+    const int *cu_g;     // THD: work-item offsets per segment [nseg+1]
+    int total;           // SBHD/BSHD: number of work items (THD: read from cu_g[nseg])
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n)
 {
-    return cudaErrorNotSupported;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(su32(b)), "r"(parity)
+                 : "memory");
+    return ok != 0;
 }
 
-cudaError_t launch_score_dump_tc(const Geo &, const __nv_bfloat16 *, const float *, const __nv_bfloat16 *, float *,
-                                 long long, long long, void *, cudaStream_t)
+// Bounded wait.  Once any role has given up (abort set), waits return at once so that control flow stays
+// uniform and the kernel runs to its end.
+__device__ __forceinline__ void wait_bar(uint64_t *b, uint32_t parity, volatile int *abort_flag, int site)
 {
-    return cudaErrorNotSupported;
+    if (*abort_flag) return;
+    if (mbar_try(b, parity)) return;
+    const long long t0 = clock64();
+    while (!mbar_try(b, parity)) {
+        if (*abort_flag) return;
+        if (clock64() - t0 > kTimeoutCycles) {
+            *abort_flag = 1;
+            atomicExch(&g_tc_error, site);
+            return;
+        }
+    }
+}
+
+// Timer-only bounded wait (used to drain our own copies / MMAs even after an abort).
+__device__ __forceinline__ void drain_bar(uint64_t *b, uint32_t parity)
+{
+    const long long t0 = clock64();
+    while (!mbar_try(b, parity))
+        if (clock64() - t0 > kTimeoutCycles) {
+            atomicExch(&g_tc_error, 99);
+            return;
+        }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+                 ::"r"(su32(dst)), "l"(map), "r"(su32(bar)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+                 ::"r"(su32(dst)), "l"(map), "r"(su32(bar)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle (8-row atoms of 1024 B, SBO = 1024 B).
+__device__ __forceinline__ uint64_t sdesc(const void *p)
+{
+    const uint64_t a = su32(p);
+    return ((a & 0x3FFFFull) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(IDESC), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// ------------------------------------------------------------------ work items
+
+struct Item {
+    int b, n;                 // segment / sequence, rows present (1..4)
+    long long row[ROWS];      // memory rows
+    int v[ROWS];              // visible keys per row
+    int vmax;
+    long long gid0;           // global id of local key 0
+    long long key_y;          // TMA row coordinate of local key 0 (2D maps)
+};
+
+__device__ __forceinline__ int item_total(const Args &a)
+{
+    return a.g.layout == CSA_THD ? __ldg(a.cu_g + a.g.B) : a.total;
+}
+
+__device__ Item decode_item(const Args &a, int i, int total)
+{
+    const Geo &g = a.g;
+    Item it;
+    int s0, len_phys, len_real;
+    long long c_base = 0;
+    if (g.layout == CSA_THD) {
+        const int ir = total - 1 - i;  // later segments first
+        int lo = 0, hi = g.B - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (__ldg(a.cu_g + mid) <= ir) lo = mid; else hi = mid - 1;
+        }
+        it.b = lo;
+        s0 = (ir - __ldg(a.cu_g + lo)) * ROWS;
+        len_phys = __ldg(g.cu_q + lo + 1) - __ldg(g.cu_q + lo);
+        len_real = __ldg(g.cu_real + lo + 1) - __ldg(g.cu_real + lo);
+        c_base = __ldg(g.cu_c + lo);
+        it.gid0 = c_base;
+        it.key_y = c_base;
+    } else {
+        const int groups = (g.S + ROWS - 1) / ROWS;
+        it.b = i % g.B;
+        s0 = (groups - 1 - i / g.B) * ROWS;  // latest positions (most keys) first
+        len_phys = len_real = g.S;
+        it.gid0 = (long long)it.b * g.nc;
+        it.key_y = it.gid0;
+    }
+    it.n = 0;
+    it.vmax = 0;
+    for (int k = 0; k < ROWS; k++) {
+        const int s = s0 + k;
+        it.v[k] = 0;
+        it.row[k] = -1;
+        if (s >= len_phys) continue;
+        it.n = k + 1;
+        if (g.layout == CSA_SBHD) it.row[k] = (long long)s * g.B + it.b;
+        else if (g.layout == CSA_BSHD) it.row[k] = (long long)it.b * g.S + s;
+        else it.row[k] = (long long)__ldg(g.cu_q + it.b) + s;
+        int v = s < len_real ? (s + 1) / g.ratio : 0;
+        if (v > g.NC) v = g.NC;
+        if (g.layout == CSA_THD && c_base + v > g.key_rows) v = c_base < g.key_rows ? (int)(g.key_rows - c_base) : 0;
+        it.v[k] = v;
+        it.vmax = v > it.vmax ? v : it.vmax;
+    }
+    return it;
+}
+
+// ------------------------------------------------------------------ top-k of one row (a warp pair)
+
+__device__ __forceinline__ int pair_sum(int x, int *slots, int par, int wsel, int bar_id)
+{
+    const int s = __reduce_add_sync(0xffffffffu, x);
+    if ((threadIdx.x & 31) == 0) slots[par * 2 + wsel] = s;
+    named_bar(bar_id, 64);
+    return slots[par * 2] + slots[par * 2 + 1];
+}
+
+// exclusive prefix of x over the 64 threads of the pair (thread order = element order); returns the total
+__device__ __forceinline__ int pair_excl(int x, int *slots, int wsel, int bar_id, int &total)
+{
+    const int lane = threadIdx.x & 31;
+    int inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) slots[4 + wsel] = inc;
+    named_bar(bar_id, 64);
+    const int w0 = slots[4], w1 = slots[5];
+    total = w0 + w1;
+    named_bar(bar_id, 64);
+    return inc - x + (wsel ? w0 : 0);
+}
+
+__device__ void select_row(const Args &a, const Item &it, int k, const float *sc, int pt, int wsel, int bar_id,
+                           int *slots)
+{
+    const Geo &g = a.g;
+    const int v = it.v[k];
+    const int K = g.K;
+    const int kk = v < K ? v : K;
+    const long long r = it.row[k];
+    int32_t *orow = a.ids + r * K;
+    float *srow = a.selscore + r * K;
+    if (kk == v) {
+        // every visible key is selected: ascending order as is
+        for (int j = pt; j < v; j += 64) {
+            orow[j] = (int32_t)(it.gid0 + j);
+            srow[j] = sc[j];
+        }
+    } else {
+        constexpr int PER = NCMAX / 64;  // 16 consecutive elements per thread
+        uint32_t key[PER];
+#pragma unroll
+        for (int e = 0; e < PER; e++) {
+            const int j = pt * PER + e;
+            key[e] = j < v ? score_key(sc[j]) : 0u;
+        }
+        // the k-th largest key: the largest T with #(key >= T) >= kk, built bit by bit
+        uint32_t T = 0u;
+        for (int bit = 31; bit >= 0; bit--) {
+            const uint32_t cand = T | (1u << bit);
+            int c = 0;
+#pragma unroll
+            for (int e = 0; e < PER; e++) c += key[e] >= cand;
+            if (pair_sum(c, slots, bit & 1, wsel, bar_id) >= kk) T = cand;
+        }
+        int gt = 0, eq = 0;
+#pragma unroll
+        for (int e = 0; e < PER; e++) {
+            gt += key[e] > T;
+            eq += key[e] == T;
+        }
+        int gt_tot, eq_tot;
+        const int gt_before = pair_excl(gt, slots, wsel, bar_id, gt_tot);
+        const int eq_before = pair_excl(eq, slots, wsel, bar_id, eq_tot);
+        const int need_eq = kk - gt_tot;
+        int er = eq_before;
+        int pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+#pragma unroll
+        for (int e = 0; e < PER; e++) {
+            const int j = pt * PER + e;
+            const bool is_eq = key[e] == T;
+            const bool sel = key[e] > T || (is_eq && er < need_eq);
+            er += is_eq;
+            if (sel && j < v) {
+                orow[pos] = (int32_t)(it.gid0 + j);
+                srow[pos] = sc[j];
+                pos++;
+            }
+        }
+    }
+    for (int s = kk + pt; s < K; s += 64) {
+        orow[s] = -1;
+        srow[s] = -INFINITY;
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(THREADS, 1)
+score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *sA = smem + OFF_A;
+    unsigned char *sB = smem + OFF_B;
+    float *sSC = reinterpret_cast<float *>(smem + OFF_SC);
+    float *sW = reinterpret_cast<float *>(smem + OFF_W);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
+    uint64_t *a_full = bars, *a_empty = bars + 4, *b_full = bars + 8, *b_empty = bars + 10;
+    uint64_t *t_full = bars + 12, *t_empty = bars + 14, *mma_done = bars + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 160);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 168);
+    int *pair_slots = reinterpret_cast<int *>(smem + OFF_MISC + 256);  // 4 pairs x 8 ints
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo &g = a.g;
+    const bool sbhd = g.layout == CSA_SBHD;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < A_STAGES; i++) { mbar_init(a_full + i, 1); mbar_init(a_empty + i, 1); }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(b_full + i, 1);
+            mbar_init(b_empty + i, 1);
+            mbar_init(t_full + i, 1);
+            mbar_init(t_empty + i, 8);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total = item_total(a);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int hs = 0, ai = 0;
+            int last_hs[A_STAGES] = {-1, -1, -1, -1};
+            int last_ai[2] = {-1, -1};
+            for (int i = blockIdx.x; i < total; i += gridDim.x) {
+                const Item it = decode_item(a, i, total);
+                if (it.vmax == 0) continue;
+                const int bb = ai & 1;
+                wait_bar(b_empty + bb, ((ai >> 1) & 1) ^ 1, abort_flag, 1);
+                mbar_expect_tx(b_full + bb, B_BUF);
+                for (int k = 0; k < ROWS; k++) {
+                    const long long row = k < it.n ? it.row[k] : it.row[0];
+                    for (int kh = 0; kh < 2; kh++)
+                        tma_load_3d(sB + bb * B_BUF + kh * B_HALF + k * (HI * 128), &map_q, b_full + bb, kh * 64, 0,
+                                    (int)row);
+                }
+                last_ai[bb] = ai;
+                ai++;
+                const int nt = (it.vmax + NKEY - 1) / NKEY;
+                for (int t = 0; t < nt; t++)
+                    for (int kh = 0; kh < 2; kh++) {
+                        const int st = hs % A_STAGES;
+                        wait_bar(a_empty + st, ((hs / A_STAGES) & 1) ^ 1, abort_flag, 2);
+                        mbar_expect_tx(a_full + st, A_HALF);
+                        if (sbhd)
+                            tma_load_3d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, it.b, t * NKEY);
+                        else
+                            tma_load_2d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, (int)(it.key_y + t * NKEY));
+                        last_hs[st] = hs;
+                        hs++;
+                    }
+            }
+            // our own copies must land before the CTA exits
+            for (int st = 0; st < A_STAGES; st++)
+                if (last_hs[st] >= 0) drain_bar(a_full + st, (last_hs[st] / A_STAGES) & 1);
+            for (int bb = 0; bb < 2; bb++)
+                if (last_ai[bb] >= 0) drain_bar(b_full + bb, (last_ai[bb] >> 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int hs = 0, ai = 0, tc = 0;
+            for (int i = blockIdx.x; i < total; i += gridDim.x) {
+                const Item it = decode_item(a, i, total);
+                if (it.vmax == 0) continue;
+                const int bb = ai & 1;
+                wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, 3);
+                fence_after();
+                const int nt = (it.vmax + NKEY - 1) / NKEY;
+                for (int t = 0; t < nt; t++) {
+                    const int tb = tc & 1;
+                    wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, 4);
+                    fence_after();
+                    const uint32_t d = tmem + (uint32_t)(tb * NCOL);
+                    for (int kh = 0; kh < 2; kh++) {
+                        const int st = hs % A_STAGES;
+                        wait_bar(a_full + st, (hs / A_STAGES) & 1, abort_flag, 5);
+                        fence_after();
+                        const unsigned char *pa = sA + st * A_HALF;
+                        const unsigned char *pb = sB + bb * B_BUF + kh * B_HALF;
+#pragma unroll
+                        for (int k = 0; k < 4; k++)
+                            mma_bf16(d, sdesc(pa + k * 32), sdesc(pb + k * 32), (kh | k) != 0);
+                        mma_commit(a_empty + st);
+                        hs++;
+                    }
+                    mma_commit(t_full + tb);
+                    tc++;
+                }
+                mma_commit(b_empty + bb);
+                ai++;
+            }
+            mma_commit(mma_done);
+            drain_bar(mma_done, 0);
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue + selection (warps 2..9)
+        const int e = warp - 2;           // 0..7
+        const int quad = warp & 3;        // TMEM lane quadrant this warp may access
+        const int half = e >> 2;          // rows {2 half, 2 half + 1}
+        const int et = threadIdx.x - 64;  // 0..255
+        int tc = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+            const Item it = decode_item(a, i, total);
+            named_bar(1, EPI);  // the previous item's selection has finished with sW / sSC
+            {
+                const int k = et >> 6, h = et & 63;
+                sW[et] = k < it.n ? __ldg(a.w + it.row[k] * HI + h) : 0.f;
+            }
+            named_bar(1, EPI);
+            const int nt = (it.vmax + NKEY - 1) / NKEY;
+            for (int t = 0; t < nt; t++) {
+                const int tb = tc & 1;
+                wait_bar(t_full + tb, (tc >> 1) & 1, abort_flag, 6);
+                fence_after();
+                const int j = t * NKEY + quad * 32 + lane;
+#pragma unroll
+                for (int rr = 0; rr < 2; rr++) {
+                    const int k = half * 2 + rr;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 2; c++) {
+                        float x[32];
+                        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NCOL + k * HI + c * 32), x);
+                        const float *wk = sW + k * HI + c * 32;
+#pragma unroll
+                        for (int h = 0; h < 32; h++) acc = fmaf(wk[h], fmaxf(x[h], 0.f), acc);
+                    }
+                    if (k < it.n && j < it.v[k]) sSC[k * NCMAX + j] = acc;
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(t_empty + tb);
+                tc++;
+            }
+            named_bar(1, EPI);  // every score of the item is in shared memory
+            // one warp pair per row: warps e and e + 4
+            const int k = e & 3;
+            const int wsel = e >> 2;
+            const int pt = wsel * 32 + lane;
+            if (k < it.n) {
+                const float *sc = sSC + k * NCMAX;
+                const long long r = it.row[k];
+                if (a.dump != nullptr && r >= a.dump_row0 && r < a.dump_row0 + a.dump_rows) {
+                    float *out = a.dump + (r - a.dump_row0) * (long long)g.NC;
+                    for (int jj = pt; jj < g.NC; jj += 64) out[jj] = jj < it.v[k] ? sc[jj] : -INFINITY;
+                }
+                if (a.ids != nullptr) select_row(a, it, k, sc, pt, wsel, 2 + k, pair_slots + k * 8);
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+}
+
+// THD: work-item offsets per segment, cu_g[b+1] = cu_g[b] + ceil(physical length / 4)
+__global__ void build_cu_g_kernel(const int *cu_q, int nseg, int *cu_g)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int acc = 0;
+    cu_g[0] = 0;
+    for (int b = 0; b < nseg; b++) {
+        int len = cu_q[b + 1] - cu_q[b];
+        acc += len > 0 ? (len + ROWS - 1) / ROWS : 0;
+        cu_g[b + 1] = acc;
+    }
+}
+
+}  // namespace tcs
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+static bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                   const cuuint32_t *box)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_score_supported(const Geo &g, bool bf16)
+{
+    const char *f = getenv("CSA_FORCE_GENERIC");
+    if (f != nullptr && f[0] == '1') return false;
+    return bf16 && g.HI == tcs::HI && g.DI == tcs::DI && g.NC >= 1 && g.NC <= tcs::NCMAX && g.K >= 1 &&
+           g.rows > 0 && g.key_rows > 0;
+}
+
+size_t tc_workspace_bytes(const Geo &g) { return sizeof(int) * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1); }
+
+static cudaError_t launch_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
+                             int32_t *ids, float *selscore, float *dump, long long row0, long long nrows, void *ws,
+                             cudaStream_t st)
+{
+    using namespace tcs;
+    CUtensorMap mq, mk;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)DI, (cuuint64_t)HI, (cuuint64_t)g.rows};
+        const cuuint64_t strides[2] = {(cuuint64_t)DI * 2, (cuuint64_t)HI * DI * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)HI, 1};
+        if (!encode(&mq, q_idx, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    if (g.layout == CSA_SBHD) {
+        const cuuint64_t dims[3] = {(cuuint64_t)DI, (cuuint64_t)g.B, (cuuint64_t)g.nc};
+        const cuuint64_t strides[2] = {(cuuint64_t)DI * 2, (cuuint64_t)g.B * DI * 2};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)NKEY};
+        if (!encode(&mk, k_idx, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    } else {
+        const cuuint64_t dims[2] = {(cuuint64_t)DI, (cuuint64_t)g.key_rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)DI * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)NKEY};
+        if (!encode(&mk, k_idx, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    Args a;
+    a.g = g;
+    a.w = w;
+    a.ids = ids;
+    a.selscore = selscore;
+    a.dump = dump;
+    a.dump_row0 = row0;
+    a.dump_rows = nrows;
+    a.cu_g = nullptr;
+    a.total = 0;
+    int upper;
+    if (g.layout == CSA_THD) {
+        int *cu_g = static_cast<int *>(ws);
+        build_cu_g_kernel<<<1, 32, 0, st>>>(g.cu_q, g.B, cu_g);
+        note_launches(1);
+        a.cu_g = cu_g;
+        upper = (g.rows + ROWS - 1) / ROWS + g.B;
+    } else {
+        a.total = g.B * ((g.S + ROWS - 1) / ROWS);
+        upper = a.total;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(score_topk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const int grid = upper < sms ? (upper > 0 ? upper : 1) : sms;
+    score_topk_tc_kernel<<<grid, THREADS, SMEM_ALLOC, st>>>(mq, mk, a);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_score_topk_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w,
+                                 const __nv_bfloat16 *k_idx, int32_t *ids, float *selscore, void *ws,
+                                 cudaStream_t st)
+{
+    return launch_tc(g, q_idx, w, k_idx, ids, selscore, nullptr, 0, 0, ws, st);
+}
+
+cudaError_t launch_score_dump_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w,
+                                 const __nv_bfloat16 *k_idx, float *dump, long long row0, long long nrows, void *ws,
+                                 cudaStream_t st)
+{
+    return launch_tc(g, q_idx, w, k_idx, nullptr, nullptr, dump, row0, nrows, ws, st);
 }
 
 }  // namespace csa

@@ -160,7 +160,7 @@ def _make(values: np.ndarray, dtype: str, lead: int = 1) -> Tensor:
 def thd_doc_lengths(cfg: Config):
     """Seeded document lengths for a packed THD batch.
 
-    Returns (cu_seqlens_q, cu_seqlens_q_unpadded, max_seqlen_q): lengths ~ U{lo..hi} are drawn
+    Returns (cu_seqlens_q, cu_seqlens_q_unpadded, max_seqlen_q = longest unpadded segment): lengths ~ U{lo..hi} are drawn
     while the running total fits in cfg.seqlen; the remaining tokens are padding absorbed into
     the last segment (physical offsets), and the unpadded offsets stop at the real total.
     """
@@ -180,7 +180,7 @@ def thd_doc_lengths(cfg: Config):
     real = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     phys = real.copy()
     phys[-1] = cfg.seqlen
-    max_len = int(np.max(np.diff(phys)))
+    max_len = int(np.max(np.diff(real)))  # longest unpadded segment: padding rows see no keys
     return phys, real, max_len
 
 
