@@ -196,7 +196,7 @@ template <typename T>
 csa_status run_teacher(Plan &P, const void *q, const void *kv, const void *kv_c, const float *sink,
                        const int32_t *ids, float *teacher, cudaStream_t st)
 {
-    CSA_TRY(check_smem(teacher_generic_smem(P.g)));
+    CSA_TRY(check_smem(teacher_generic_smem(P.g, sizeof(T) == 2)));
     CSA_CUDA(launch_teacher_generic<T>(P.g, (const T *)q, (const T *)kv, (const T *)kv_c, sink, ids, teacher, st));
     return CSA_OK;
 }

@@ -161,7 +161,7 @@ cudaError_t launch_finalize(const Geo &g, const float *dk_acc, T *dk_idx, const 
                             cudaStream_t st);
 
 size_t score_topk_generic_smem(const Geo &g);
-size_t teacher_generic_smem(const Geo &g);
+size_t teacher_generic_smem(const Geo &g, bool bf16);
 size_t grad_generic_smem(const Geo &g);
 
 }  // namespace csa

@@ -223,8 +223,6 @@ size_t teacher_generic_smem(const Geo &g, bool bf16)
     size_t cap = (size_t)(g.TW > 0 ? g.TW : 1);
     return q_bytes + sizeof(float) * ((size_t)kWarps * g.D + 2 * (size_t)kWarps * g.H + g.H + cap);
 }
-size_t teacher_generic_smem(const Geo &g) { return teacher_generic_smem(g, true) > teacher_generic_smem(g, false)
-                                                   ? teacher_generic_smem(g, true) : teacher_generic_smem(g, false); }
 
 // Support slot -> global key id of the row, or -1 when the slot is not in C.  Sparse: the slot's id,
 // accepted only when it is a visible key of this row (ids outside that range are treated as invalid,

@@ -296,23 +296,21 @@ def to_thd(inp: Inputs) -> Inputs:
 def dense_variant(inp: Inputs, v: int) -> Inputs:
     """Teacher-sensitivity variant v of the dense-loss sweep.
 
-    Variants 0..3 add s_v * 3 * u_v to every original-KV (window) row, u_v ~ N(0,1)/sqrt(D)
-    seeded, s_v = +1/-1 alternating.  Variants 4..7 add +3/-3 to the sink of one seeded head.
-    Only window values or one head's sink change; the indexer inputs and compressed KV do not.
+    Variants 0..3 move every original-KV (window) value by +3 or -3: kv += 3 * e_v with e_v a seeded
+    +-1 vector over the head dimension (the same for every row).  Variants 4..7 add +3 / -3 to the sink
+    of one seeded head.  Only window values or one head's sink change; indexer inputs and compressed KV
+    do not.
     """
     c = inp.cfg
     rng = _rng(c.seed, "variant", v)
-    sign = 1.0 if v % 2 == 0 else -1.0
     kv, sink = inp.kv, inp.sink
     if v < 4:
-        D = c.head_dim
-        u = rng.standard_normal(D, dtype=np.float32) / np.float32(math.sqrt(D))
-        vals = inp.kv.values + np.float32(3.0 * sign) * u
-        kv = _make(vals.astype(np.float32), c.dtype, lead=inp.kv.lead)
+        e = np.where(rng.random(c.head_dim) < 0.5, -3.0, 3.0).astype(np.float32)
+        kv = _make((inp.kv.values + e).astype(np.float32), c.dtype, lead=inp.kv.lead)
     else:
         h = int(rng.integers(0, c.heads))
         s = inp.sink.values.copy()
-        s[h] += np.float32(3.0 * sign)
+        s[h] += np.float32(3.0 if v % 2 == 0 else -3.0)
         sink = Tensor(s)
     return dataclasses.replace(inp, kv=kv, sink=sink)
 

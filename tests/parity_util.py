@@ -202,7 +202,8 @@ def check_step(inp, d=None, rows=None, full_dk=True, report=None):
     e_dw = rel_l2(dw[same], ref["dw"][same])
     assert e_dq <= GRAD_TOL and e_dw <= GRAD_TOL, f"dq {e_dq} dw {e_dw}"
     out = dict(recall=recall, teacher_err=max(t_err, t_err2), dq_err=e_dq, dw_err=e_dw, rows=len(rws),
-               same_rows=int(same.sum()), path=B.csa_last_path())
+               same_rows=int(same.sum()), path=B.csa_last_path(),
+               _oracle_teacher=ref["teacher"], _gpu_teacher_oracle_ids=te_o)
     dk = to_np(gpu["dk"]).reshape(-1, c.idx_dim)
     if rows is None:
         e_dk = rel_l2(dk, ref["dk"])
