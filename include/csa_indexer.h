@@ -166,6 +166,30 @@ csa_status csa_indexer_bwd(const csa_params *p, const void *q_idx, const float *
                            float *loss_out, float *row_loss_out, void *dq_idx, float *dw, void *dk_idx,
                            void *workspace, size_t workspace_bytes, void *stream);
 
+/* ------------------------------------------------------------------ backward without a workspace */
+
+/* Size of the library's built-in device scratch used by csa_indexer_bwd_noalloc: 64 MiB. */
+#define CSA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* The same computation as csa_indexer_bwd (same arguments and outputs), for callers that cannot allocate
+ * device memory and so cannot pass a workspace -- for example code running where the host application owns
+ * every device allocation, or a process that must not call cudaMalloc once it is running.  The paper has no
+ * counterpart to this call; it exists only for those callers.
+ *   - Scratch: a fixed device array of CSA_NOALLOC_SCRATCH_BYTES inside the library.  Every GPU on which the
+ *     library's device code is loaded holds it until the process exits.  Nothing is allocated or freed.
+ *   - Limit: returns CSA_ERR_WORKSPACE, without enqueueing anything, when csa_workspace_size(p) exceeds
+ *     CSA_NOALLOC_SCRATCH_BYTES (the bshd_bf16 workload needs about 34 MiB).
+ *   - Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ *     device current; make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps whatever the last call left there; the
+ *     call zeroes what must start at zero (the dK accumulator) itself.  Calls whose work overlaps on the GPU
+ *     (different streams, or different host threads) race on the array and must be serialised by the caller. */
+csa_status csa_indexer_bwd_noalloc(const csa_params *p, const void *q_idx, const float *w, const void *k_idx,
+                                   const void *q, const void *kv, const void *kv_c, const float *sink,
+                                   const int32_t *ids, const float *selscore, const float *teacher_or_null,
+                                   float *loss_out, float *row_loss_out, void *dq_idx, float *dw, void *dk_idx,
+                                   void *stream);
+
 /* ------------------------------------------------------------------ diagnostics */
 
 /* Test aid: the fp32 scores exactly as csa_indexer_fwd computes them, for rows

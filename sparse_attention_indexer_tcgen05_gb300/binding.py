@@ -69,6 +69,8 @@ for _name, _args, _res in [
                          _vp],
      ctypes.c_int),
     ("csa_scores_debug", [_P, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _sz, _vp], ctypes.c_int),
+    ("csa_indexer_bwd_noalloc", [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+     ctypes.c_int),
     ("csa_check_device_status", [_vp], ctypes.c_int),
     ("csa_last_path", [], ctypes.c_char_p),
     ("csa_kernel_launches", [], ctypes.c_uint64),
@@ -80,6 +82,7 @@ for _name, _args, _res in [
 
 EXPORTED = ("csa_topk_width", "csa_key_width", "csa_teacher_width", "csa_rows", "csa_compressed_rows",
             "csa_workspace_size", "csa_indexer_fwd", "csa_teacher", "csa_indexer_bwd", "csa_scores_debug",
+            "csa_indexer_bwd_noalloc",
             "csa_check_device_status", "csa_last_path", "csa_kernel_launches", "csa_status_string")
 
 
@@ -269,6 +272,28 @@ def csa_indexer_bwd(p: Params, q_idx, w, k_idx, q, kv, kv_c, sink, ids, selscore
                                   _ptr(ids), _ptr(selscore), _ptr(teacher), _ptr(loss), _ptr(row_loss), _ptr(dq),
                                   _ptr(dw), _ptr(dk), _ptr(ws), nws, _stream(dev))
     _check(st, "csa_indexer_bwd")
+    return loss, dq, dw, dk
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def csa_indexer_bwd_noalloc(p: Params, q_idx, w, k_idx, q, kv, kv_c, sink, ids, selscore, teacher=None, out=None,
+                            row_loss=None):
+    """csa_indexer_bwd without a workspace, for callers that cannot allocate device memory: the library uses
+    its own fixed 64 MiB device scratch (shared by every call on a device; serialise overlapping calls).
+    Returns (loss, dq_idx, dw, dk_idx); raises CSAError (CSA_ERR_WORKSPACE) if the problem needs more scratch."""
+    dev = q_idx.device
+    rows = p.rows
+    if out is None:
+        out = (torch.empty((), dtype=torch.float32, device=dev), torch.empty_like(q_idx), torch.empty_like(w),
+               torch.empty_like(k_idx))
+    loss, dq, dw, dk = out
+    with _nvtx("csa_indexer_bwd_noalloc"):
+        st = _lib.csa_indexer_bwd_noalloc(p.ref, _ptr(q_idx), _ptr(w), _ptr(k_idx), _ptr(q), _ptr(kv), _ptr(kv_c),
+                                          _ptr(sink), _ptr(ids), _ptr(selscore), _ptr(teacher), _ptr(loss),
+                                          _ptr(row_loss), _ptr(dq), _ptr(dw), _ptr(dk), _stream(dev))
+    _check(st, "csa_indexer_bwd_noalloc")
     return loss, dq, dw, dk
 
 
