@@ -1,0 +1,156 @@
+// tc_ptx.cuh -- inline-PTX building blocks of the sm_103a tensor-core kernels: mbarriers with bounded
+// waits, TMA tile loads, shared-memory matrix descriptors (128-byte swizzle, K-major and MN-major),
+// tcgen05.mma / commit / fences, TMEM loads and named barriers.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace csa {
+namespace ptx {
+
+constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(su32(b)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// make generic-proxy shared-memory writes (st.shared) visible to the tensor core's async proxy
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Bounded wait.  Once any role has given up (abort set), waits return at once so control flow stays
+// uniform and the kernel runs to its end; `err` receives the site code of the first expiry.
+__device__ __forceinline__ void wait_bar(uint64_t *b, uint32_t parity, volatile int *abort_flag, int *err, int site)
+{
+    if (*abort_flag) return;
+    if (mbar_try(b, parity)) return;
+    const long long t0 = clock64();
+    while (!mbar_try(b, parity)) {
+        if (*abort_flag) return;
+        if (clock64() - t0 > kTimeoutCycles) {
+            *abort_flag = 1;
+            atomicExch(err, site);
+            return;
+        }
+    }
+}
+// Timer-only bounded wait, used to drain a kernel's own copies / MMAs even after an abort.
+__device__ __forceinline__ void drain_bar(uint64_t *b, uint32_t parity, int *err)
+{
+    const long long t0 = clock64();
+    while (!mbar_try(b, parity))
+        if (clock64() - t0 > kTimeoutCycles) {
+            atomicExch(err, 99);
+            return;
+        }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+                 ::"r"(su32(dst)), "l"(map), "r"(su32(bar)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+                 ::"r"(su32(dst)), "l"(map), "r"(su32(bar)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, version 1 (bits 46-47), layout SWIZZLE_128B (bits 61-63 = 2).
+//   K-major:  rows of 128 B (64 bf16 of K) per M/N index, 8-row atoms of 1024 B: SBO = 1024 B; LBO unused.
+//   MN-major: 64 consecutive M/N elements per 128-B row, one row per K index, 8-row atoms of 1024 B along K:
+//             SBO = 1024 B (next 8 K), LBO = byte distance between consecutive 64-wide M/N blocks.
+__device__ __forceinline__ uint64_t desc_sw128(const void *p, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    const uint64_t a = su32(p);
+    return ((a & 0x3FFFFull) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ uint64_t desc_kmajor(const void *p) { return desc_sw128(p, 16, 1024); }
+
+// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D: bits 4-5 D fmt (1 = f32), 7-9 A fmt (1 = bf16),
+// 10-12 B fmt (1 = bf16), 15 A major (1 = MN), 16 B major (1 = MN), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t cols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(slot)), "r"(cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols));
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp-collective), waited.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled tile (rows of 128 B, 1024-B aligned)
+__device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk)
+{
+    return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+}  // namespace ptx
+}  // namespace csa
