@@ -45,7 +45,7 @@ struct Plan {
     Geo g;
     int dtype;
     bool dense_rescore;   // dense loss with K below the key width: visible scores go to the workspace
-    size_t off_cu_c, off_teacher, off_g, off_rowloss, off_dk, off_dense, off_tc, total;
+    size_t off_cu_c, off_teacher, off_g, off_rowloss, off_dk, off_dense, off_tc, off_btc, total;
 };
 
 csa_status make_plan(const csa_params *p, Plan *P)
@@ -118,6 +118,8 @@ csa_status make_plan(const csa_params *p, Plan *P)
     off = align_up(off + (P->dense_rescore ? sizeof(float) * (size_t)rows * g.NC : 0));
     P->off_tc = off;
     off = align_up(off + tc_workspace_bytes(g));
+    P->off_btc = off;
+    off = align_up(off + tc_bwd_workspace_bytes(g));
     P->total = off;
     return CSA_OK;
 }
@@ -225,13 +227,25 @@ csa_status run_bwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
     }
     float *gbuf = reinterpret_cast<float *>(ws_at(ws, P.off_g));
     float *row_loss = row_loss_out ? row_loss_out : reinterpret_cast<float *>(ws_at(ws, P.off_rowloss));
-    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, st));
+    const bool tc = tc_bwd_supported(g, sizeof(T) == 2);
+    const int NT = tc_bwd_tiles(g);
+    char *btc = ws_at(ws, P.off_btc);
+    int32_t *toff = (tc && g.sparse)
+                        ? reinterpret_cast<int32_t *>(btc + align_up(sizeof(int) * 2 * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1)))
+                        : nullptr;
+    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, toff, NT, st));
     if (g.key_rows * g.DI > 0)
         CSA_CUDA(cudaMemsetAsync(dk_acc, 0, sizeof(float) * (size_t)g.key_rows * g.DI, st));
-    CSA_TRY(check_smem(grad_generic_smem(g)));
-    t_last_path = "generic";
-    CSA_CUDA(launch_grad_generic<T>(g, (const T *)q_idx, w, (const T *)k_idx, ids, gbuf, (T *)dq_idx, dw, dk_acc,
-                                    st));
+    if (tc) {
+        t_last_path = "tcgen05";
+        CSA_CUDA(launch_bwd_tc(g, (const __nv_bfloat16 *)q_idx, w, (const __nv_bfloat16 *)k_idx, ids, gbuf, toff,
+                               (__nv_bfloat16 *)dq_idx, dw, dk_acc, btc, st));
+    } else {
+        CSA_TRY(check_smem(grad_generic_smem(g)));
+        t_last_path = "generic";
+        CSA_CUDA(launch_grad_generic<T>(g, (const T *)q_idx, w, (const T *)k_idx, ids, gbuf, (T *)dq_idx, dw, dk_acc,
+                                        st));
+    }
     CSA_CUDA(launch_finalize<T>(g, dk_acc, (T *)dk_idx, row_loss, loss, st));
     return CSA_OK;
 }

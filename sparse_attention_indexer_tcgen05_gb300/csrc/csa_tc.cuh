@@ -3,6 +3,8 @@
 
 #include "csa_internal.cuh"
 
+#include <cuda.h>
+
 namespace csa {
 
 // True when the tcgen05 score + top-k kernel takes this shape (bf16 values, H_I = 64, D_I = 128,
@@ -20,6 +22,21 @@ cudaError_t launch_score_topk_tc(const Geo &g, const __nv_bfloat16 *q_idx, const
 cudaError_t launch_score_dump_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w,
                                  const __nv_bfloat16 *k_idx, float *dump, long long row0, long long nrows,
                                  void *ws, cudaStream_t st);
+
+// TMA tensor maps (bf16, 128-byte swizzle): q_idx as [rows][H_I][D_I] with a 64 x H_I x 1 box, and k_idx with a
+// 64 x 128-key box (2D over key rows, or 3D [n_c][B][D_I] for SBHD).
+bool tc_encode_q_map(CUtensorMap *m, const void *q_idx, const Geo &g);
+bool tc_encode_k_map(CUtensorMap *m, const void *k_idx, const Geo &g);
+
+// Tensor-core backward (dQ_idx, dW, dK) for bf16, H_I = 64, D_I = 128, key axis <= 1024.
+bool tc_bwd_supported(const Geo &g, bool bf16);
+int tc_bwd_tiles(const Geo &g);
+size_t tc_bwd_workspace_bytes(const Geo &g);
+// ws: tc_bwd_workspace_bytes(g) bytes; toff: the per-row key-tile slot offsets written by the KL kernel
+cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
+                          const int32_t *ids, const float *gbuf, const int32_t *toff, __nv_bfloat16 *dq, float *dw,
+                          float *dk_acc, void *ws, cudaStream_t st);
+cudaError_t bwd_tc_read_clear_error(int *flag);
 
 // Reads and clears the tensor-core kernels' device error word (set when a kernel gives up a bounded
 // wait on an mbarrier).  Synchronous: call after the stream has drained.

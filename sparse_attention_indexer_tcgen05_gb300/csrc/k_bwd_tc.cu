@@ -1,0 +1,902 @@
+// k_bwd_tc.cu -- the indexer backward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Given g_ts = dloss/dI_ts (from the KL step, zero outside the support C), the gradients of
+// I[t,s] = sum_j w[t,j] max(0, x_tjs), x_tjs = q_idx[t,j] . k_idx[s] are
+//   dQ'[t,j] = sum_s g_ts 1[x_tjs > 0] k_idx[s]           dQ_idx[t,j] = w[t,j] dQ'[t,j]
+//   dW[t,j]  = sum_s g_ts max(0, x_tjs) = q_idx[t,j] . dQ'[t,j]
+//   dK[s]    = sum_t sum_j g_ts w[t,j] 1[x_tjs > 0] q_idx[t,j]
+// ("[Bug] DSV4 unfused CSA indexer loss ..." (Megatron-LM issue #5776), the proposal comment: gradients only
+// for the indexer Q, weights and K; "Megatron-LM PR #8539" item 1: the backward takes global top-k ids.)
+//
+// x is recomputed on the tensor cores over every visible key tile (dense in keys, masked by g), so both
+// kernels stream contiguous k_idx / q_idx tiles by TMA; no per-element global atomics:
+//   * row-owner kernel (dQ_idx, dW): a work item is 2 query rows (N = 128 (row, head) pairs).  Per key tile:
+//     MMA1 X[key, (row,h)] = k . q^T (M 128 keys, K 128), the epilogue forms G'[key, (row,h)] =
+//     g 1[x > 0] in bf16 as an MN-major operand, and MMA2 accumulates dQ'^T... stored as
+//     D[(row,h), d] += sum_key G'[key,(row,h)] k[key, d] in TMEM over all tiles of the item.
+//   * key-owner kernel (dK): a unit is one key tile and a chunk of up to 128 rows that see it.  Per row pair:
+//     MMA1 as above, the epilogue forms G[key, (row,h)] = g w 1[x > 0] (K-major), and MMA3 accumulates
+//     dK[key, d] += sum_(row,h) G q[(row,h), d] in TMEM; the unit flushes its 128 x 128 fp32 partial once.
+// Roles: warp 0 TMA, warp 1 TMEM + MMA issue, warp 2 stages each item's g (and w) into shared memory ahead of
+// use, warps 4..11 epilogue.  Waits are bounded as in the score kernel.
+#include "csa_tc.cuh"
+#include "tc_ptx.cuh"
+
+#include <stdlib.h>
+
+namespace csa {
+
+static __device__ int g_bwd_error = 0;
+
+cudaError_t bwd_tc_read_clear_error(int *flag)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flag, g_bwd_error, sizeof(int));
+    if (e != cudaSuccess || *flag == 0) return e;
+    int zero = 0;
+    return cudaMemcpyToSymbol(g_bwd_error, &zero, sizeof(int));
+}
+
+namespace bwd {
+
+using namespace ptx;
+
+constexpr int HI = 64, DI = 128, NKEY = 128;
+constexpr int RP = 2;                          // query rows per item / row pair
+constexpr int NCMAX = 1024;                    // key axis the row-owner's dense g rows hold
+constexpr int HALF = NKEY * 64 * 2;            // 16 KB: 128 rows x 64 bf16
+constexpr int QBLK = 2 * HALF;                 // 32 KB: 2 rows x 64 heads x 128 d, two K-halves
+constexpr int THREADS = 384;
+constexpr int EPI = 256;
+constexpr int CH = 128;                        // rows per key-owner unit
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC_X = idesc_bf16(128, 128, false, false);   // X = k . q^T
+constexpr uint32_t IDESC_DQ = idesc_bf16(128, 128, true, true);    // dQ' += G'^T k  (both MN-major)
+constexpr uint32_t IDESC_DK = idesc_bf16(128, 128, false, true);   // dK += G q      (B MN-major)
+
+// row-owner shared memory
+constexpr int R_ASTG = 6;
+constexpr int R_OFF_A = 0;
+constexpr int R_OFF_B = R_OFF_A + R_ASTG * HALF;              // 96 KB
+constexpr int R_OFF_G = R_OFF_B + 2 * QBLK;                   // 160 KB
+constexpr int R_OFF_GD = R_OFF_G + QBLK;                      // 192 KB: 2 bufs x 2 rows x NCMAX fp32
+constexpr int R_OFF_W = R_OFF_GD + 2 * RP * NCMAX * 4;        // 208 KB: 2 bufs x 2 rows x 64 fp32
+constexpr int R_OFF_DW = R_OFF_W + 2 * RP * HI * 4;           // 128 fp32
+constexpr int R_OFF_MISC = R_OFF_DW + RP * HI * 4;
+constexpr int R_SMEM = R_OFF_MISC + 1024 + 1024;
+
+// key-owner shared memory
+constexpr int K_BSTG = 3, K_GSTG = 4;
+constexpr int K_OFF_A = 0;                                     // the unit's key tile, 32 KB
+constexpr int K_OFF_B = K_OFF_A + 2 * HALF;                    // 3 q blocks
+constexpr int K_OFF_G = K_OFF_B + K_BSTG * QBLK;               // 2 G buffers
+constexpr int K_OFF_GT = K_OFF_G + 2 * QBLK;                   // g tiles: 4 x 2 rows x 128 fp32
+constexpr int K_OFF_WT = K_OFF_GT + K_GSTG * RP * NKEY * 4;    // w rows: 4 x 2 rows x 64 fp32
+constexpr int K_OFF_MISC = K_OFF_WT + K_GSTG * RP * HI * 4;
+constexpr int K_SMEM = K_OFF_MISC + 1024 + 1024;
+
+struct Args {
+    Geo g;
+    const float *w;
+    const int32_t *ids;      // [rows, K]
+    const float *gbuf;       // [rows, TW] dloss/dI in the teacher's slot layout
+    const int32_t *toff;     // [rows, NT + 1] first slot of each key tile (sparse)
+    int NT;                  // key tiles of the widest key axis
+    __nv_bfloat16 *dq;
+    float *dw;
+    float *dk_acc;           // [key rows, DI] fp32, zeroed by the caller
+    const int *cu_g;         // THD: row-pair items per segment [nseg+1]
+    const int *cu_u;         // THD: key-owner units per segment [nseg+1]
+    int total_items, total_units;     // SBHD/BSHD
+    int units_per_seq;                // SBHD/BSHD
+};
+
+// ------------------------------------------------------------------ geometry
+
+struct Seg {
+    int b, len_phys, len_real, nc;
+    long long gid0;          // global id of local key 0
+    long long key_y;         // TMA row coordinate of local key 0 (2D maps)
+};
+
+__device__ __forceinline__ Seg seg_of(const Geo &g, int b)
+{
+    Seg s;
+    s.b = b;
+    if (g.layout == CSA_THD) {
+        s.len_phys = __ldg(g.cu_q + b + 1) - __ldg(g.cu_q + b);
+        s.len_real = __ldg(g.cu_real + b + 1) - __ldg(g.cu_real + b);
+        s.gid0 = __ldg(g.cu_c + b);
+    } else {
+        s.len_phys = s.len_real = g.S;
+        s.gid0 = (long long)b * g.nc;
+    }
+    s.key_y = s.gid0;
+    int nc = s.len_real / g.ratio;
+    if (nc > g.NC) nc = g.NC;
+    if (g.layout == CSA_THD && s.gid0 + nc > g.key_rows) nc = s.gid0 < g.key_rows ? (int)(g.key_rows - s.gid0) : 0;
+    s.nc = nc;
+    return s;
+}
+
+__device__ __forceinline__ long long row_of(const Geo &g, int b, int s)
+{
+    if (g.layout == CSA_SBHD) return (long long)s * g.B + b;
+    if (g.layout == CSA_BSHD) return (long long)b * g.S + s;
+    return (long long)__ldg(g.cu_q + b) + s;
+}
+
+__device__ __forceinline__ int vis(const Geo &g, const Seg &sg, int s)
+{
+    if (s >= sg.len_real) return 0;
+    int v = (s + 1) / g.ratio;
+    return v < sg.nc ? v : sg.nc;
+}
+
+__device__ __forceinline__ int find_seg(const int *cu, int nseg, int x)
+{
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu + mid) <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// A row-pair item of the row-owner kernel.
+struct Pair {
+    Seg sg;
+    int n;                    // rows present (1..2)
+    long long row0, row1;
+    int v0, v1, vmax;
+};
+
+__device__ Pair decode_pair(const Args &a, int i)
+{
+    const Geo &g = a.g;
+    Pair p;
+    int b, s0;
+    if (g.layout == CSA_THD) {
+        const int total = __ldg(a.cu_g + g.B);
+        const int ir = total - 1 - i;
+        b = find_seg(a.cu_g, g.B, ir);
+        s0 = (ir - __ldg(a.cu_g + b)) * RP;
+    } else {
+        const int groups = (g.S + RP - 1) / RP;
+        b = i % g.B;
+        s0 = (groups - 1 - i / g.B) * RP;
+    }
+    p.sg = seg_of(g, b);
+    p.n = s0 + 1 < p.sg.len_phys ? 2 : 1;
+    p.row0 = row_of(g, b, s0);
+    p.row1 = p.n > 1 ? row_of(g, b, s0 + 1) : p.row0;
+    p.v0 = vis(g, p.sg, s0);
+    p.v1 = p.n > 1 ? vis(g, p.sg, s0 + 1) : 0;
+    p.vmax = p.v0 > p.v1 ? p.v0 : p.v1;
+    return p;
+}
+
+__device__ __forceinline__ int pair_total(const Args &a)
+{
+    return a.g.layout == CSA_THD ? __ldg(a.cu_g + a.g.B) : a.total_items;
+}
+
+// first row position that sees key tile kt, and the number of key-owner units of a segment
+__device__ __forceinline__ int smin_of(const Geo &g, int kt) { return g.ratio * (kt * NKEY + 1) - 1; }
+
+__host__ __device__ inline int units_of_len(int len_real, int nc, int ratio)
+{
+    int u = 0;
+    const int nt = (nc + NKEY - 1) / NKEY;
+    for (int kt = 0; kt < nt; kt++) {
+        const int smin = ratio * (kt * NKEY + 1) - 1;
+        const int rows = len_real - smin;
+        if (rows > 0) u += (rows + CH - 1) / CH;
+    }
+    return u;
+}
+
+struct Unit {
+    Seg sg;
+    int kt;
+    int s_lo, s_hi;           // row positions [s_lo, s_hi)
+    int npairs;
+};
+
+__device__ Unit decode_unit(const Args &a, int u)
+{
+    const Geo &g = a.g;
+    Unit U;
+    int b, lu;
+    if (g.layout == CSA_THD) {
+        b = find_seg(a.cu_u, g.B, u);
+        lu = u - __ldg(a.cu_u + b);
+    } else {
+        b = u % g.B;
+        lu = u / g.B;
+    }
+    U.sg = seg_of(g, b);
+    const int nt = (U.sg.nc + NKEY - 1) / NKEY;
+    U.kt = 0;
+    U.s_lo = U.s_hi = 0;
+    for (int kt = 0; kt < nt; kt++) {
+        const int smin = smin_of(g, kt);
+        const int rows = U.sg.len_real - smin;
+        const int nu = rows > 0 ? (rows + CH - 1) / CH : 0;
+        if (lu < nu) {
+            U.kt = kt;
+            U.s_lo = smin + lu * CH;
+            U.s_hi = min(U.sg.len_real, U.s_lo + CH);
+            break;
+        }
+        lu -= nu;
+    }
+    U.npairs = (U.s_hi - U.s_lo + 1) / RP;
+    return U;
+}
+
+__device__ __forceinline__ int unit_total(const Args &a)
+{
+    return a.g.layout == CSA_THD ? __ldg(a.cu_u + a.g.B) : a.total_units;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&p);
+}
+
+// ------------------------------------------------------------------ row-owner kernel: dQ_idx, dW
+
+__global__ void __launch_bounds__(THREADS, 1)
+dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *sA = smem + R_OFF_A;
+    unsigned char *sB = smem + R_OFF_B;
+    unsigned char *sG = smem + R_OFF_G;
+    float *sGD = reinterpret_cast<float *>(smem + R_OFF_GD);
+    float *sW = reinterpret_cast<float *>(smem + R_OFF_W);
+    float *sDW = reinterpret_cast<float *>(smem + R_OFF_DW);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + R_OFF_MISC);
+    uint64_t *a_full = bars, *a_empty = bars + 6, *b_full = bars + 12, *b_empty = bars + 14;
+    uint64_t *x_full = bars + 16, *x_empty = bars + 18, *g_full = bars + 20, *g_empty = bars + 21;
+    uint64_t *dq_full = bars + 22, *dq_empty = bars + 23, *gd_full = bars + 24, *gd_empty = bars + 26;
+    uint64_t *mma_done = bars + 28;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + R_OFF_MISC + 256);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + R_OFF_MISC + 264);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo &g = a.g;
+    const bool sbhd = g.layout == CSA_SBHD;
+    int *err = &g_bwd_error;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < R_ASTG; i++) { mbar_init(a_full + i, 1); mbar_init(a_empty + i, 1); }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(b_full + i, 1);
+            mbar_init(b_empty + i, 8);
+            mbar_init(x_full + i, 1);
+            mbar_init(x_empty + i, 8);
+            mbar_init(gd_full + i, 1);
+            mbar_init(gd_empty + i, 8);
+        }
+        mbar_init(g_full, 8);
+        mbar_init(g_empty, 1);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_empty, 8);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        init_fence();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tX = tmem, tDQ = tmem + 256;
+    const int total = pair_total(a);
+
+    if (warp == 0) {
+        if (lane == 0) {  // ------------------------------------------------ TMA producer
+            int hs = 0, ai = 0;
+            int last_hs[R_ASTG];
+            int last_ai[2] = {-1, -1};
+            for (int i = 0; i < R_ASTG; i++) last_hs[i] = -1;
+            for (int i = blockIdx.x; i < total; i += gridDim.x) {
+                const Pair p = decode_pair(a, i);
+                if (p.vmax == 0) continue;
+                const int bb = ai & 1;
+                wait_bar(b_empty + bb, ((ai >> 1) & 1) ^ 1, abort_flag, err, 1);
+                mbar_expect_tx(b_full + bb, QBLK);
+                for (int r = 0; r < RP; r++)
+                    for (int kh = 0; kh < 2; kh++)
+                        tma_load_3d(sB + bb * QBLK + kh * HALF + r * (HI * 128), &map_q, b_full + bb, kh * 64, 0,
+                                    (int)(r == 0 ? p.row0 : p.row1));
+                last_ai[bb] = ai;
+                ai++;
+                const int nt = (p.vmax + NKEY - 1) / NKEY;
+                for (int t = 0; t < nt; t++)
+                    for (int kh = 0; kh < 2; kh++) {
+                        const int st = hs % R_ASTG;
+                        wait_bar(a_empty + st, ((hs / R_ASTG) & 1) ^ 1, abort_flag, err, 2);
+                        mbar_expect_tx(a_full + st, HALF);
+                        if (sbhd)
+                            tma_load_3d(sA + st * HALF, &map_k, a_full + st, kh * 64, p.sg.b, t * NKEY);
+                        else
+                            tma_load_2d(sA + st * HALF, &map_k, a_full + st, kh * 64, (int)(p.sg.key_y + t * NKEY));
+                        last_hs[st] = hs;
+                        hs++;
+                    }
+            }
+            for (int st = 0; st < R_ASTG; st++)
+                if (last_hs[st] >= 0) drain_bar(a_full + st, (last_hs[st] / R_ASTG) & 1, err);
+            for (int bb = 0; bb < 2; bb++)
+                if (last_ai[bb] >= 0) drain_bar(b_full + bb, (last_ai[bb] >> 1) & 1, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ------------------------------------------------ MMA issuer
+            int hs = 0, ai = 0, xc = 0, gc = 0, dqc = 0;
+            auto mma2 = [&](int st, bool first) {
+                if (first) {
+                    wait_bar(dq_empty, (dqc & 1) ^ 1, abort_flag, err, 3);
+                    fence_after();
+                }
+                wait_bar(g_full, gc & 1, abort_flag, err, 4);
+                fence_after();
+#pragma unroll
+                for (int s = 0; s < 8; s++)
+                    mma_bf16(tDQ, desc_sw128(sG + s * 2048, HALF, 1024), desc_sw128(sA + st * HALF + s * 2048, HALF, 1024),
+                             IDESC_DQ, (first && s == 0) ? 0u : 1u);
+                mma_commit(g_empty);
+                mma_commit(a_empty + st);
+                mma_commit(a_empty + st + 1);
+                gc++;
+            };
+            for (int i = blockIdx.x; i < total; i += gridDim.x) {
+                const Pair p = decode_pair(a, i);
+                if (p.vmax == 0) continue;
+                const int bb = ai & 1;
+                wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, err, 5);
+                fence_after();
+                const int nt = (p.vmax + NKEY - 1) / NKEY;
+                int st_prev = 0;
+                for (int t = 0; t < nt; t++) {
+                    const int st = hs % R_ASTG;
+                    const int tb = xc & 1;
+                    wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 6);
+                    wait_bar(a_full + st, (hs / R_ASTG) & 1, abort_flag, err, 7);
+                    wait_bar(a_full + st + 1, ((hs + 1) / R_ASTG) & 1, abort_flag, err, 7);
+                    fence_after();
+#pragma unroll
+                    for (int kh = 0; kh < 2; kh++)
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; k4++)
+                            mma_bf16(tX + tb * 128, desc_kmajor(sA + (st + kh) * HALF + k4 * 32),
+                                     desc_kmajor(sB + bb * QBLK + kh * HALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
+                    mma_commit(x_full + tb);
+                    xc++;
+                    if (t > 0) mma2(st_prev, t == 1);
+                    st_prev = st;
+                    hs += 2;
+                }
+                mma2(st_prev, nt == 1);
+                mma_commit(dq_full);
+                dqc++;
+                ai++;
+            }
+            mma_commit(mma_done);
+            drain_bar(mma_done, 0, err);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- g / w stager
+        int ic = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
+            const Pair p = decode_pair(a, i);
+            const int gb = ic & 1;
+            wait_bar(gd_empty + gb, ((ic >> 1) & 1) ^ 1, abort_flag, err, 8);
+            float *gd = sGD + gb * RP * NCMAX;
+            for (int r = 0; r < RP; r++) {
+                const int v = r == 0 ? p.v0 : p.v1;
+                const long long row = r == 0 ? p.row0 : p.row1;
+                float *gr = gd + r * NCMAX;
+                for (int j = lane; j < p.vmax; j += 32) gr[j] = 0.f;
+                sW[gb * RP * HI + r * HI + lane] = (r < p.n) ? __ldg(a.w + row * HI + lane) : 0.f;
+                sW[gb * RP * HI + r * HI + lane + 32] = (r < p.n) ? __ldg(a.w + row * HI + lane + 32) : 0.f;
+                __syncwarp();
+                if (v == 0) continue;
+                if (g.sparse) {
+                    const int32_t *ir = a.ids + row * g.K;
+                    const float *gg = a.gbuf + row * g.TW;
+                    for (int s = lane; s < g.K; s += 32) {
+                        const long long id = __ldg(ir + s);
+                        const long long j = id - p.sg.gid0;
+                        if (id >= 0 && j >= 0 && j < v) gr[j] = __ldg(gg + s);
+                    }
+                } else {
+                    const float *gg = a.gbuf + row * g.TW;
+                    for (int j = lane; j < v; j += 32) gr[j] = __ldg(gg + j);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(gd_full + gb);
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- epilogue
+        const int e = warp - 4, quad = warp & 3, half = e >> 2;
+        int xc = 0, gc = 0, dqc = 0, ai = 0, ic = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
+            const Pair p = decode_pair(a, i);
+            const int gb = ic & 1;
+            wait_bar(gd_full + gb, (ic >> 1) & 1, abort_flag, err, 9);
+            const float *gd = sGD + gb * RP * NCMAX + half * NCMAX;
+            const int v_me = half == 0 ? p.v0 : p.v1;
+            const int nt = (p.vmax + NKEY - 1) / NKEY;
+            const int k = quad * 32 + lane;
+            for (int t = 0; t < nt; t++) {
+                const int tb = xc & 1;
+                wait_bar(x_full + tb, (xc >> 1) & 1, abort_flag, err, 10);
+                fence_after();
+                const int j = t * NKEY + k;
+                const float gk = j < v_me ? gd[j] : 0.f;
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+                    float x[32];
+                    tmem_ld32(tX + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * 128 + half * 64 + c * 32), x);
+#pragma unroll
+                    for (int q2 = 0; q2 < 16; q2++)
+                        pk[c * 16 + q2] = pack_bf16(x[2 * q2] > 0.f ? gk : 0.f, x[2 * q2 + 1] > 0.f ? gk : 0.f);
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_empty + tb);
+                wait_bar(g_empty, (gc & 1) ^ 1, abort_flag, err, 11);
+                unsigned char *dst = sG + half * HALF;
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    *reinterpret_cast<uint4 *>(dst + sw128_off(k, c)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(g_full);
+                xc++;
+                gc++;
+            }
+            // ---- dQ' readout: lane (quad*32 + lane) = (row, head); this warp's 64 of the 128 d
+            const int rh = quad * 32 + lane;
+            const int rr = rh >> 6, h = rh & 63;
+            const bool exists = rr < p.n;
+            const long long row = rr == 0 ? p.row0 : p.row1;
+            float part = 0.f;
+            if (nt > 0) {
+                const int bb = ai & 1;
+                wait_bar(dq_full, dqc & 1, abort_flag, err, 12);
+                fence_after();
+                float vv[64];
+                {
+                    float x[32];
+                    tmem_ld32(tDQ + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64), x);
+#pragma unroll
+                    for (int c = 0; c < 32; c++) vv[c] = x[c];
+                    tmem_ld32(tDQ + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64 + 32), x);
+#pragma unroll
+                    for (int c = 0; c < 32; c++) vv[32 + c] = x[c];
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dq_empty);
+                dqc++;
+                const float wv = sW[gb * RP * HI + rr * HI + h];
+                // q_idx[row, h, half*64 .. +64] from the B tile (K-major, 128-B swizzle)
+                const unsigned char *qb = sB + bb * QBLK + half * HALF;
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const uint4 qv = *reinterpret_cast<const uint4 *>(qb + sw128_off(rh, c));
+                    const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv);
+#pragma unroll
+                    for (int u = 0; u < 4; u++) {
+                        const float2 qf = __bfloat1622float2(q2[u]);
+                        part = fmaf(qf.x, vv[c * 8 + 2 * u], part);
+                        part = fmaf(qf.y, vv[c * 8 + 2 * u + 1], part);
+                    }
+                }
+                if (exists) {
+                    __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + half * 64;
+#pragma unroll
+                    for (int c = 0; c < 8; c++) {
+                        uint4 o;
+                        o.x = pack_bf16(wv * vv[c * 8 + 0], wv * vv[c * 8 + 1]);
+                        o.y = pack_bf16(wv * vv[c * 8 + 2], wv * vv[c * 8 + 3]);
+                        o.z = pack_bf16(wv * vv[c * 8 + 4], wv * vv[c * 8 + 5]);
+                        o.w = pack_bf16(wv * vv[c * 8 + 6], wv * vv[c * 8 + 7]);
+                        *reinterpret_cast<uint4 *>(out + c * 8) = o;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_empty + bb);  // q tile no longer read
+                ai++;
+            } else if (exists) {
+                __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + half * 64;
+                for (int c = 0; c < 8; c++) *reinterpret_cast<uint4 *>(out + c * 8) = make_uint4(0, 0, 0, 0);
+            }
+            // dW = q . dQ' over the two d halves
+            if (half == 1) sDW[rh] = part;
+            named_bar(1, EPI);
+            if (half == 0 && exists) a.dw[row * HI + h] = part + sDW[rh];
+            named_bar(1, EPI);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(gd_empty + gb);
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ key-owner kernel: dK
+
+__global__ void __launch_bounds__(THREADS, 1)
+dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *sA = smem + K_OFF_A;
+    unsigned char *sB = smem + K_OFF_B;
+    unsigned char *sG = smem + K_OFF_G;
+    float *sGT = reinterpret_cast<float *>(smem + K_OFF_GT);
+    float *sWT = reinterpret_cast<float *>(smem + K_OFF_WT);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_OFF_MISC);
+    uint64_t *a_full = bars, *a_empty = bars + 1, *b_full = bars + 2, *b_empty = bars + 5;
+    uint64_t *x_full = bars + 8, *x_empty = bars + 10, *gk_full = bars + 12, *gk_empty = bars + 14;
+    uint64_t *dk_full = bars + 16, *dk_empty = bars + 17, *gt_full = bars + 18, *gt_empty = bars + 22;
+    uint64_t *mma_done = bars + 26;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K_OFF_MISC + 256);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K_OFF_MISC + 264);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo &g = a.g;
+    const bool sbhd = g.layout == CSA_SBHD;
+    int *err = &g_bwd_error;
+
+    if (threadIdx.x == 0) {
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        for (int i = 0; i < K_BSTG; i++) { mbar_init(b_full + i, 1); mbar_init(b_empty + i, 1); }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(x_full + i, 1);
+            mbar_init(x_empty + i, 8);
+            mbar_init(gk_full + i, 8);
+            mbar_init(gk_empty + i, 1);
+        }
+        for (int i = 0; i < K_GSTG; i++) { mbar_init(gt_full + i, 1); mbar_init(gt_empty + i, 8); }
+        mbar_init(dk_full, 1);
+        mbar_init(dk_empty, 8);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        init_fence();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tX = tmem, tDK = tmem + 256;
+    const int total = unit_total(a);
+
+    if (warp == 0) {
+        if (lane == 0) {  // ------------------------------------------------ TMA producer
+            int uc = 0, qs = 0;
+            int last_qs[K_BSTG] = {-1, -1, -1};
+            int last_uc = -1;
+            for (int u = blockIdx.x; u < total; u += gridDim.x) {
+                const Unit U = decode_unit(a, u);
+                if (U.npairs == 0) continue;
+                wait_bar(a_empty, (uc & 1) ^ 1, abort_flag, err, 21);
+                mbar_expect_tx(a_full, 2 * HALF);
+                for (int kh = 0; kh < 2; kh++) {
+                    if (sbhd)
+                        tma_load_3d(sA + kh * HALF, &map_k, a_full, kh * 64, U.sg.b, U.kt * NKEY);
+                    else
+                        tma_load_2d(sA + kh * HALF, &map_k, a_full, kh * 64, (int)(U.sg.key_y + U.kt * NKEY));
+                }
+                last_uc = uc;
+                uc++;
+                for (int pi = 0; pi < U.npairs; pi++) {
+                    const int bs = qs % K_BSTG;
+                    wait_bar(b_empty + bs, ((qs / K_BSTG) & 1) ^ 1, abort_flag, err, 22);
+                    mbar_expect_tx(b_full + bs, QBLK);
+                    const int s0 = U.s_lo + pi * RP;
+                    const long long r0 = row_of(g, U.sg.b, s0);
+                    const long long r1 = s0 + 1 < U.s_hi ? row_of(g, U.sg.b, s0 + 1) : r0;
+                    for (int r = 0; r < RP; r++)
+                        for (int kh = 0; kh < 2; kh++)
+                            tma_load_3d(sB + bs * QBLK + kh * HALF + r * (HI * 128), &map_q, b_full + bs, kh * 64, 0,
+                                        (int)(r == 0 ? r0 : r1));
+                    last_qs[bs] = qs;
+                    qs++;
+                }
+            }
+            if (last_uc >= 0) drain_bar(a_full, last_uc & 1, err);
+            for (int bs = 0; bs < K_BSTG; bs++)
+                if (last_qs[bs] >= 0) drain_bar(b_full + bs, (last_qs[bs] / K_BSTG) & 1, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ------------------------------------------------ MMA issuer
+            int uc = 0, qs = 0, xc = 0, gkc = 0, dkc = 0;
+            auto mma3 = [&](int bs, bool first) {
+                if (first) {
+                    wait_bar(dk_empty, (dkc & 1) ^ 1, abort_flag, err, 23);
+                    fence_after();
+                }
+                const int gkb = gkc & 1;
+                wait_bar(gk_full + gkb, (gkc >> 1) & 1, abort_flag, err, 24);
+                fence_after();
+#pragma unroll
+                for (int s = 0; s < 8; s++)
+                    mma_bf16(tDK, desc_kmajor(sG + gkb * QBLK + (s >> 2) * HALF + (s & 3) * 32),
+                             desc_sw128(sB + bs * QBLK + s * 2048, HALF, 1024), IDESC_DK,
+                             (first && s == 0) ? 0u : 1u);
+                mma_commit(gk_empty + gkb);
+                mma_commit(b_empty + bs);
+                gkc++;
+            };
+            for (int u = blockIdx.x; u < total; u += gridDim.x) {
+                const Unit U = decode_unit(a, u);
+                if (U.npairs == 0) continue;
+                wait_bar(a_full, uc & 1, abort_flag, err, 25);
+                fence_after();
+                int bs_prev = 0;
+                for (int pi = 0; pi < U.npairs; pi++) {
+                    const int bs = qs % K_BSTG;
+                    const int tb = xc & 1;
+                    wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 26);
+                    wait_bar(b_full + bs, (qs / K_BSTG) & 1, abort_flag, err, 27);
+                    fence_after();
+#pragma unroll
+                    for (int kh = 0; kh < 2; kh++)
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; k4++)
+                            mma_bf16(tX + tb * 128, desc_kmajor(sA + kh * HALF + k4 * 32),
+                                     desc_kmajor(sB + bs * QBLK + kh * HALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
+                    mma_commit(x_full + tb);
+                    xc++;
+                    if (pi > 0) mma3(bs_prev, pi == 1);
+                    bs_prev = bs;
+                    qs++;
+                }
+                mma3(bs_prev, U.npairs == 1);
+                mma_commit(dk_full);
+                mma_commit(a_empty);
+                dkc++;
+                uc++;
+            }
+            mma_commit(mma_done);
+            drain_bar(mma_done, 0, err);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- g / w stager (per row pair)
+        int pc = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit U = decode_unit(a, u);
+            const long long key_lo = U.sg.gid0 + (long long)U.kt * NKEY;
+            for (int pi = 0; pi < U.npairs; pi++, pc++) {
+                const int gs = pc % K_GSTG;
+                wait_bar(gt_empty + gs, ((pc / K_GSTG) & 1) ^ 1, abort_flag, err, 28);
+                float *gt = sGT + gs * RP * NKEY;
+                float *wt = sWT + gs * RP * HI;
+                for (int x = lane; x < RP * NKEY; x += 32) gt[x] = 0.f;
+                __syncwarp();
+                for (int r = 0; r < RP; r++) {
+                    const int s = U.s_lo + pi * RP + r;
+                    const bool ok = s < U.s_hi;
+                    const long long row = row_of(g, U.sg.b, ok ? s : U.s_lo);
+                    wt[r * HI + lane] = ok ? __ldg(a.w + row * HI + lane) : 0.f;
+                    wt[r * HI + lane + 32] = ok ? __ldg(a.w + row * HI + lane + 32) : 0.f;
+                    if (!ok) continue;
+                    const int v = vis(g, U.sg, s);
+                    if (g.sparse) {
+                        const int s0 = __ldg(a.toff + row * (a.NT + 1) + U.kt);
+                        const int s1 = __ldg(a.toff + row * (a.NT + 1) + U.kt + 1);
+                        for (int sl = s0 + lane; sl < s1; sl += 32) {
+                            const long long kk = (long long)__ldg(a.ids + row * g.K + sl) - key_lo;
+                            const long long j = kk + (long long)U.kt * NKEY;
+                            if (kk >= 0 && kk < NKEY && j < v) gt[r * NKEY + kk] = __ldg(a.gbuf + row * g.TW + sl);
+                        }
+                    } else {
+                        for (int kk = lane; kk < NKEY; kk += 32) {
+                            const int j = U.kt * NKEY + kk;
+                            if (j < v) gt[r * NKEY + kk] = __ldg(a.gbuf + row * g.TW + j);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gt_full + gs);
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- epilogue
+        const int e = warp - 4, quad = warp & 3, half = e >> 2;
+        const int k = quad * 32 + lane;
+        int xc = 0, gkc = 0, dkc = 0, pc = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit U = decode_unit(a, u);
+            for (int pi = 0; pi < U.npairs; pi++, pc++) {
+                const int gs = pc % K_GSTG;
+                const int tb = xc & 1;
+                wait_bar(gt_full + gs, (pc / K_GSTG) & 1, abort_flag, err, 29);
+                wait_bar(x_full + tb, (xc >> 1) & 1, abort_flag, err, 30);
+                fence_after();
+                const float gk = sGT[gs * RP * NKEY + half * NKEY + k];
+                const float *wr = sWT + gs * RP * HI + half * HI;
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+                    float x[32];
+                    tmem_ld32(tX + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * 128 + half * 64 + c * 32), x);
+#pragma unroll
+                    for (int q2 = 0; q2 < 16; q2++) {
+                        const int hh = c * 32 + 2 * q2;
+                        pk[c * 16 + q2] = pack_bf16(x[2 * q2] > 0.f ? gk * wr[hh] : 0.f,
+                                                    x[2 * q2 + 1] > 0.f ? gk * wr[hh + 1] : 0.f);
+                    }
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(x_empty + tb);
+                    mbar_arrive(gt_empty + gs);
+                }
+                const int gkb = gkc & 1;
+                wait_bar(gk_empty + gkb, ((gkc >> 1) & 1) ^ 1, abort_flag, err, 31);
+                unsigned char *dst = sG + gkb * QBLK + half * HALF;
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    *reinterpret_cast<uint4 *>(dst + sw128_off(k, c)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gk_full + gkb);
+                xc++;
+                gkc++;
+            }
+            if (U.npairs == 0) continue;
+            // ---- flush the unit's dK partial: lane = key, this warp's 64 of the 128 d
+            wait_bar(dk_full, dkc & 1, abort_flag, err, 32);
+            fence_after();
+            float vv[64];
+            {
+                float x[32];
+                tmem_ld32(tDK + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64), x);
+#pragma unroll
+                for (int c = 0; c < 32; c++) vv[c] = x[c];
+                tmem_ld32(tDK + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64 + 32), x);
+#pragma unroll
+                for (int c = 0; c < 32; c++) vv[32 + c] = x[c];
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dk_empty);
+            dkc++;
+            const int j = U.kt * NKEY + k;
+            if (j < U.sg.nc) {
+                const long long gid = U.sg.gid0 + j;
+                const long long kr = g.layout == CSA_SBHD ? (gid % g.nc) * g.B + gid / g.nc : gid;
+                float *dst = a.dk_acc + kr * DI + half * 64;
+#pragma unroll
+                for (int c = 0; c < 16; c++)
+                    atomicAdd(reinterpret_cast<float4 *>(dst + 4 * c),
+                              make_float4(vv[4 * c], vv[4 * c + 1], vv[4 * c + 2], vv[4 * c + 3]));
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// THD: row-pair items and key-owner units per segment
+__global__ void build_bwd_offsets_kernel(Geo g, int *cu_g, int *cu_u)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int ag = 0, au = 0;
+    cu_g[0] = 0;
+    cu_u[0] = 0;
+    for (int b = 0; b < g.B; b++) {
+        const int lp = __ldg(g.cu_q + b + 1) - __ldg(g.cu_q + b);
+        const int lr = __ldg(g.cu_real + b + 1) - __ldg(g.cu_real + b);
+        ag += lp > 0 ? (lp + RP - 1) / RP : 0;
+        const long long gid0 = __ldg(g.cu_c + b);
+        int nc = lr > 0 ? lr / g.ratio : 0;
+        if (nc > g.NC) nc = g.NC;
+        if (gid0 + nc > g.key_rows) nc = gid0 < g.key_rows ? (int)(g.key_rows - gid0) : 0;
+        au += lr > 0 ? units_of_len(lr, nc, g.ratio) : 0;
+        cu_g[b + 1] = ag;
+        cu_u[b + 1] = au;
+    }
+}
+
+}  // namespace bwd
+
+// ------------------------------------------------------------------ host side
+
+bool tc_bwd_supported(const Geo &g, bool bf16)
+{
+    const char *f = getenv("CSA_FORCE_GENERIC");
+    if (f != nullptr && f[0] == '1') return false;
+    return bf16 && g.HI == bwd::HI && g.DI == bwd::DI && g.NC >= 1 && g.NC <= bwd::NCMAX && g.K >= 1 &&
+           g.rows > 0 && g.key_rows > 0;
+}
+
+int tc_bwd_tiles(const Geo &g) { return (g.NC + bwd::NKEY - 1) / bwd::NKEY; }
+
+size_t tc_bwd_workspace_bytes(const Geo &g)
+{
+    const size_t offs = sizeof(int) * 2 * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1);
+    const size_t toff = sizeof(int) * (size_t)g.rows * (size_t)(tc_bwd_tiles(g) + 1);
+    return ((offs + 255) & ~(size_t)255) + toff;
+}
+
+cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
+                          const int32_t *ids, const float *gbuf, const int32_t *toff, __nv_bfloat16 *dq, float *dw,
+                          float *dk_acc, void *ws, cudaStream_t st)
+{
+    using namespace bwd;
+    CUtensorMap mq, mk;
+    if (!tc_encode_q_map(&mq, q_idx, g) || !tc_encode_k_map(&mk, k_idx, g)) return cudaErrorInvalidValue;
+    Args a;
+    a.g = g;
+    a.w = w;
+    a.ids = ids;
+    a.gbuf = gbuf;
+    a.toff = toff;
+    a.NT = tc_bwd_tiles(g);
+    a.dq = dq;
+    a.dw = dw;
+    a.dk_acc = dk_acc;
+    a.cu_g = a.cu_u = nullptr;
+    a.total_items = a.total_units = a.units_per_seq = 0;
+    int upper_items, upper_units;
+    if (g.layout == CSA_THD) {
+        int *cu_g = static_cast<int *>(ws);
+        int *cu_u = cu_g + (g.B + 1);
+        build_bwd_offsets_kernel<<<1, 32, 0, st>>>(g, cu_g, cu_u);
+        note_launches(1);
+        a.cu_g = cu_g;
+        a.cu_u = cu_u;
+        upper_items = (g.rows + RP - 1) / RP + g.B;
+        upper_units = (g.rows + CH - 1) / CH * a.NT + g.B * a.NT;
+    } else {
+        a.total_items = g.B * ((g.S + RP - 1) / RP);
+        a.units_per_seq = units_of_len(g.S, g.nc, g.ratio);
+        a.total_units = g.B * a.units_per_seq;
+        upper_items = a.total_items;
+        upper_units = a.total_units;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dq_dw_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, R_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K_SMEM);
+    if (e != cudaSuccess) return e;
+    const int g1 = upper_items < sms ? (upper_items > 0 ? upper_items : 1) : sms;
+    dq_dw_tc_kernel<<<g1, THREADS, R_SMEM, st>>>(mq, mk, a);
+    note_launches(1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (upper_units > 0) {
+        const int g2 = upper_units < sms ? upper_units : sms;
+        dk_tc_kernel<<<g2, THREADS, K_SMEM, st>>>(mq, mk, a);
+        note_launches(1);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace csa

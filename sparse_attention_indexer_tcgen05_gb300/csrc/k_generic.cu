@@ -372,10 +372,12 @@ cudaError_t launch_teacher_generic(const Geo &g, const T *q, const T *kv, const 
 // One CTA per query row.  p = softmax over C of the scores, L_t = sum t (log(t+eps) - log(p+eps)) and
 // g_s = f * p_s (A - t_s/(p_s+eps)) with A = sum_k t_k p_k/(p_k+eps): the exact derivative of the
 // eps-guarded KL of [BUG] sec. 2 excerpt.  gbuf uses the teacher's slot layout.
+// With toff != nullptr (sparse support, ascending ids), it also records for every key tile kt of 128 keys
+// the first slot whose key lies at or beyond tile kt: toff[row][kt], kt = 0..NT.
 __global__ void __launch_bounds__(kThreads)
 kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ selscore,
           const float *__restrict__ dense_scores, const float *__restrict__ teacher, float *__restrict__ gbuf,
-          float *__restrict__ row_loss)
+          float *__restrict__ row_loss, int32_t *__restrict__ toff, int NT)
 {
     __shared__ float red[kWarps];
     const int tid = threadIdx.x;
@@ -385,6 +387,20 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
         const int32_t *row_ids = ids + r * g.K;
         const float *trow = teacher + r * TW;
         float *grow = gbuf + r * TW;
+        if (toff != nullptr) {
+            const long long lo = key_gid(g, R, 0);
+            for (int kt = tid; kt <= NT; kt += kThreads) {
+                // first slot s with (id_s invalid) or (id_s - lo >= kt * 128); valid ids come first, ascending
+                int a0 = 0, a1 = g.K;
+                while (a0 < a1) {
+                    const int mid = (a0 + a1) >> 1;
+                    const long long id = row_ids[mid];
+                    const bool beyond = id < 0 || id - lo >= (long long)kt * 128;
+                    if (beyond) a1 = mid; else a0 = mid + 1;
+                }
+                toff[r * (NT + 1) + kt] = a0;
+            }
+        }
         // score of support slot s, or -inf when s is not in C
         auto score_of = [&](int s) -> float {
             if (s >= TW) return -INFINITY;
@@ -432,11 +448,11 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
 }
 
 cudaError_t launch_kl(const Geo &g, const int32_t *ids, const float *selscore, const float *dense_scores,
-                      const float *teacher, float *gbuf, float *row_loss, cudaStream_t st)
+                      const float *teacher, float *gbuf, float *row_loss, int32_t *toff, int NT, cudaStream_t st)
 {
     if (g.rows == 0) return cudaSuccess;
     int grid = g.rows < 65535 * 8 ? g.rows : 65535 * 8;
-    kl_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, dense_scores, teacher, gbuf, row_loss);
+    kl_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, toff, NT);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -39,10 +39,17 @@ static __device__ int g_tc_error = 0;
 
 cudaError_t tc_read_clear_error(int *flag)
 {
-    cudaError_t e = cudaMemcpyFromSymbol(flag, g_tc_error, sizeof(int));
-    if (e != cudaSuccess || *flag == 0) return e;
-    int zero = 0;
-    return cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(int));
+    int f1 = 0, f2 = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&f1, g_tc_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    if (f1 != 0) {
+        int zero = 0;
+        e = cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(int));
+        if (e != cudaSuccess) return e;
+    }
+    e = bwd_tc_read_clear_error(&f2);
+    *flag = f1 != 0 ? f1 : f2;
+    return e;
 }
 
 namespace tcs {
@@ -586,29 +593,35 @@ bool tc_score_supported(const Geo &g, bool bf16)
 
 size_t tc_workspace_bytes(const Geo &g) { return sizeof(int) * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1); }
 
+bool tc_encode_q_map(CUtensorMap *m, const void *q_idx, const Geo &g)
+{
+    const cuuint64_t dims[3] = {(cuuint64_t)g.DI, (cuuint64_t)g.HI, (cuuint64_t)g.rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)g.DI * 2, (cuuint64_t)g.HI * g.DI * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)g.HI, 1};
+    return encode(m, q_idx, 3, dims, strides, box);
+}
+
+bool tc_encode_k_map(CUtensorMap *m, const void *k_idx, const Geo &g)
+{
+    if (g.layout == CSA_SBHD) {
+        const cuuint64_t dims[3] = {(cuuint64_t)g.DI, (cuuint64_t)g.B, (cuuint64_t)g.nc};
+        const cuuint64_t strides[2] = {(cuuint64_t)g.DI * 2, (cuuint64_t)g.B * g.DI * 2};
+        const cuuint32_t box[3] = {64, 1, 128};
+        return encode(m, k_idx, 3, dims, strides, box);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)g.DI, (cuuint64_t)g.key_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)g.DI * 2};
+    const cuuint32_t box[2] = {64, 128};
+    return encode(m, k_idx, 2, dims, strides, box);
+}
+
 static cudaError_t launch_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
                              int32_t *ids, float *selscore, float *dump, long long row0, long long nrows, void *ws,
                              cudaStream_t st)
 {
     using namespace tcs;
     CUtensorMap mq, mk;
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)DI, (cuuint64_t)HI, (cuuint64_t)g.rows};
-        const cuuint64_t strides[2] = {(cuuint64_t)DI * 2, (cuuint64_t)HI * DI * 2};
-        const cuuint32_t box[3] = {64, (cuuint32_t)HI, 1};
-        if (!encode(&mq, q_idx, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    }
-    if (g.layout == CSA_SBHD) {
-        const cuuint64_t dims[3] = {(cuuint64_t)DI, (cuuint64_t)g.B, (cuuint64_t)g.nc};
-        const cuuint64_t strides[2] = {(cuuint64_t)DI * 2, (cuuint64_t)g.B * DI * 2};
-        const cuuint32_t box[3] = {64, 1, (cuuint32_t)NKEY};
-        if (!encode(&mk, k_idx, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    } else {
-        const cuuint64_t dims[2] = {(cuuint64_t)DI, (cuuint64_t)g.key_rows};
-        const cuuint64_t strides[1] = {(cuuint64_t)DI * 2};
-        const cuuint32_t box[2] = {64, (cuuint32_t)NKEY};
-        if (!encode(&mk, k_idx, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    }
+    if (!tc_encode_q_map(&mq, q_idx, g) || !tc_encode_k_map(&mk, k_idx, g)) return cudaErrorInvalidValue;
     Args a;
     a.g = g;
     a.w = w;
