@@ -45,7 +45,7 @@ struct Plan {
     Geo g;
     int dtype;
     bool dense_rescore;   // dense loss with K below the key width: visible scores go to the workspace
-    size_t off_cu_c, off_teacher, off_g, off_rowloss, off_dk, off_dense, off_tc, off_btc, total;
+    size_t off_cu_c, off_teacher, off_g, off_rowloss, off_dk, off_dense, off_tc, off_btc, off_ttc, total;
 };
 
 csa_status make_plan(const csa_params *p, Plan *P)
@@ -120,6 +120,8 @@ csa_status make_plan(const csa_params *p, Plan *P)
     off = align_up(off + tc_workspace_bytes(g));
     P->off_btc = off;
     off = align_up(off + tc_bwd_workspace_bytes(g));
+    P->off_ttc = off;
+    off = align_up(off + tc_teacher_workspace_bytes(g));
     P->total = off;
     return CSA_OK;
 }
@@ -196,8 +198,13 @@ csa_status run_fwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
 
 template <typename T>
 csa_status run_teacher(Plan &P, const void *q, const void *kv, const void *kv_c, const float *sink,
-                       const int32_t *ids, float *teacher, cudaStream_t st)
+                       const int32_t *ids, float *teacher, void *ws, cudaStream_t st)
 {
+    if (tc_teacher_supported(P.g, sizeof(T) == 2)) {
+        CSA_CUDA(launch_teacher_tc(P.g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kv,
+                                   (const __nv_bfloat16 *)kv_c, sink, ids, teacher, ws_at(ws, P.off_ttc), st));
+        return CSA_OK;
+    }
     CSA_TRY(check_smem(teacher_generic_smem(P.g, sizeof(T) == 2)));
     CSA_CUDA(launch_teacher_generic<T>(P.g, (const T *)q, (const T *)kv, (const T *)kv_c, sink, ids, teacher, st));
     return CSA_OK;
@@ -214,7 +221,7 @@ csa_status run_bwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
     const float *teacher = teacher_in;
     if (teacher == nullptr) {
         float *tbuf = reinterpret_cast<float *>(ws_at(ws, P.off_teacher));
-        CSA_TRY(run_teacher<T>(P, q, kv, kv_c, sink, ids, tbuf, st));
+        CSA_TRY(run_teacher<T>(P, q, kv, kv_c, sink, ids, tbuf, ws, st));
         teacher = tbuf;
     }
     const float *dense_scores = nullptr;
@@ -350,8 +357,8 @@ csa_status csa_teacher(const csa_params *p, const void *q, const void *kv, const
     if (g.rows == 0 || g.TW == 0) return CSA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     CSA_TRY(prologue(P, workspace, st));
-    if (P.dtype == CSA_BF16) return run_teacher<__nv_bfloat16>(P, q, kv, kv_c, sink, ids, teacher_out, st);
-    return run_teacher<float>(P, q, kv, kv_c, sink, ids, teacher_out, st);
+    if (P.dtype == CSA_BF16) return run_teacher<__nv_bfloat16>(P, q, kv, kv_c, sink, ids, teacher_out, workspace, st);
+    return run_teacher<float>(P, q, kv, kv_c, sink, ids, teacher_out, workspace, st);
 }
 
 csa_status csa_indexer_bwd(const csa_params *p, const void *q_idx, const float *w, const void *k_idx, const void *q,

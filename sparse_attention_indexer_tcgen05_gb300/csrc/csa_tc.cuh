@@ -25,6 +25,8 @@ cudaError_t launch_score_dump_tc(const Geo &g, const __nv_bfloat16 *q_idx, const
 
 // TMA tensor maps (bf16, 128-byte swizzle): q_idx as [rows][H_I][D_I] with a 64 x H_I x 1 box, and k_idx with a
 // 64 x 128-key box (2D over key rows, or 3D [n_c][B][D_I] for SBHD).
+bool tc_encode_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                    const cuuint32_t *box);
 bool tc_encode_q_map(CUtensorMap *m, const void *q_idx, const Geo &g);
 bool tc_encode_k_map(CUtensorMap *m, const void *k_idx, const Geo &g);
 
@@ -37,6 +39,14 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
                           const int32_t *ids, const float *gbuf, const int32_t *toff, __nv_bfloat16 *dq, float *dw,
                           float *dk_acc, void *ws, cudaStream_t st);
 cudaError_t bwd_tc_read_clear_error(int *flag);
+
+// Tensor-core teacher for bf16, H = 64, D in {64, 128, 192}, key axis <= 1024.
+bool tc_teacher_supported(const Geo &g, bool bf16);
+size_t tc_teacher_workspace_bytes(const Geo &g);
+cudaError_t launch_teacher_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *kv,
+                              const __nv_bfloat16 *kv_c, const float *sink, const int32_t *ids, float *teacher,
+                              void *ws, cudaStream_t st);
+cudaError_t teacher_tc_read_clear_error(int *flag);
 
 // Reads and clears the tensor-core kernels' device error word (set when a kernel gives up a bounded
 // wait on an mbarrier).  Synchronous: call after the stream has drained.

@@ -48,7 +48,10 @@ cudaError_t tc_read_clear_error(int *flag)
         if (e != cudaSuccess) return e;
     }
     e = bwd_tc_read_clear_error(&f2);
-    *flag = f1 != 0 ? f1 : f2;
+    if (e != cudaSuccess) return e;
+    int f3 = 0;
+    e = teacher_tc_read_clear_error(&f3);
+    *flag = f1 != 0 ? f1 : (f2 != 0 ? f2 : f3);
     return e;
 }
 
@@ -572,8 +575,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-static bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                   const cuuint32_t *box)
+bool tc_encode_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                    const cuuint32_t *box)
 {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
@@ -598,7 +601,7 @@ bool tc_encode_q_map(CUtensorMap *m, const void *q_idx, const Geo &g)
     const cuuint64_t dims[3] = {(cuuint64_t)g.DI, (cuuint64_t)g.HI, (cuuint64_t)g.rows};
     const cuuint64_t strides[2] = {(cuuint64_t)g.DI * 2, (cuuint64_t)g.HI * g.DI * 2};
     const cuuint32_t box[3] = {64, (cuuint32_t)g.HI, 1};
-    return encode(m, q_idx, 3, dims, strides, box);
+    return tc_encode_bf16(m, q_idx, 3, dims, strides, box);
 }
 
 bool tc_encode_k_map(CUtensorMap *m, const void *k_idx, const Geo &g)
@@ -607,12 +610,12 @@ bool tc_encode_k_map(CUtensorMap *m, const void *k_idx, const Geo &g)
         const cuuint64_t dims[3] = {(cuuint64_t)g.DI, (cuuint64_t)g.B, (cuuint64_t)g.nc};
         const cuuint64_t strides[2] = {(cuuint64_t)g.DI * 2, (cuuint64_t)g.B * g.DI * 2};
         const cuuint32_t box[3] = {64, 1, 128};
-        return encode(m, k_idx, 3, dims, strides, box);
+        return tc_encode_bf16(m, k_idx, 3, dims, strides, box);
     }
     const cuuint64_t dims[2] = {(cuuint64_t)g.DI, (cuuint64_t)g.key_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)g.DI * 2};
     const cuuint32_t box[2] = {64, 128};
-    return encode(m, k_idx, 2, dims, strides, box);
+    return tc_encode_bf16(m, k_idx, 2, dims, strides, box);
 }
 
 static cudaError_t launch_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,

@@ -1,0 +1,498 @@
+// k_teacher_tc.cu -- the full-CSA teacher on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// For query row t and main-attention head h ("[Bug] DSV4 unfused CSA indexer loss ..." (Megatron-LM issue
+// #5776): "Paper reference" equations for Z_h and t_j; sec. 3, the attention shares one denominator over the
+// sliding window, the selected compressed keys and the sink; the proposal comment's factored form):
+//   l_h = log(exp(a_h) + sum_{j in C} exp(c_hj) + sum_{r in W} exp(w_hr)),  c = sigma q.kv_c, w = sigma q.kv
+//   T_j = sum_h exp(c_hj - l_h),   t_j = T_j / max(sum_{k in C} T_k, 1e-10)
+//
+// Mapping (bf16, H = 64 heads, D in {64, 128, 192}).  A work item is 2 consecutive query rows of one sequence.
+// The MMA computes D[(row, h), key] = q[row, h] . key with M = 2 rows x 64 heads = 128 (A = the item's q rows,
+// K-major, resident), N = 128 keys (B = a tile of kv_c or of the window's kv rows, K-major, TMA), K = D.  With
+// (row, head) on TMEM lanes each epilogue thread owns one head of one row, so the per-head log-sum-exp is an
+// in-register online max/sum over the key columns.  The keys are taken densely per tile (every visible
+// compressed key, every window position) and masked by the row's selection and window.
+//   pass 1: window tiles + compressed tiles -> per-(row,h) online max / sum, then l_h with the sink;
+//   pass 2: compressed tiles again -> exp(c - l_h) on selected keys, summed over the 64 heads of a row by a
+//           warp reduce-scatter (31 shuffles per 32 columns) into shared per-key T rows; then the L1
+//           normalisation and the write-out in the id slot order.
+// Roles: warp 0 TMA, warp 1 TMEM + MMA issue, warps 4..11 epilogue (two warps per TMEM lane quadrant, each
+// with half of the 128 key columns).  Waits are bounded as in the other tensor-core kernels.
+#include "csa_tc.cuh"
+#include "tc_ptx.cuh"
+
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+
+namespace csa {
+
+static __device__ int g_teacher_error = 0;
+
+cudaError_t teacher_tc_read_clear_error(int *flag)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flag, g_teacher_error, sizeof(int));
+    if (e != cudaSuccess || *flag == 0) return e;
+    int zero = 0;
+    return cudaMemcpyToSymbol(g_teacher_error, &zero, sizeof(int));
+}
+
+namespace teach {
+
+using namespace ptx;
+
+constexpr int H = 64, RP = 2, M = RP * H, NK = 128;
+constexpr int KB = NK * 64 * 2;                 // 16 KB: one 64-wide K-block of a 128-row tile
+constexpr int MAXKB = 3;                        // D <= 192
+constexpr int QBUF = MAXKB * KB;                // 48 KB: the item's q rows
+constexpr int BSTG = 6;                         // key K-block stages
+constexpr int NCMAX = 1024;
+constexpr int THREADS = 384, EPI = 256;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t IDESC = idesc_bf16(128, 128, false, false);
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_B = OFF_Q + 2 * QBUF;                     // 96 KB
+constexpr int OFF_T = OFF_B + BSTG * KB;                    // 192 KB: 2 rows x NCMAX fp32
+constexpr int OFF_SEL = OFF_T + RP * NCMAX * 4;             // 200 KB: 2 rows x NCMAX bytes
+constexpr int OFF_PART = OFF_SEL + RP * NCMAX;              // 202 KB: 2 halves x 128 x (m, s)
+constexpr int OFF_RED = OFF_PART + 2 * M * 8;               // 8 warps
+constexpr int OFF_MISC = OFF_RED + 64;
+constexpr int SMEM = OFF_MISC + 1024 + 1024;
+
+struct Args {
+    Geo g;
+    const float *sink;
+    const int32_t *ids;
+    float *teacher;
+    const int *cu_g;      // THD: row-pair items per segment [nseg + 1]
+    int total;            // SBHD/BSHD items
+    int nkb;              // D / 64
+};
+
+struct Item {
+    int b, n, s0;
+    long long row0, row1;
+    int v0, v1, vmax;
+    int len_real;
+    long long gid0, key_y;
+    int p_lo, nw, nct;    // window start position, window tiles, compressed tiles
+};
+
+__device__ __forceinline__ int find_seg(const int *cu, int nseg, int x)
+{
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu + mid) <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ long long row_of(const Geo &g, int b, int s)
+{
+    if (g.layout == CSA_SBHD) return (long long)s * g.B + b;
+    if (g.layout == CSA_BSHD) return (long long)b * g.S + s;
+    return (long long)__ldg(g.cu_q + b) + s;
+}
+
+__device__ Item decode(const Args &a, int i, int total)
+{
+    const Geo &g = a.g;
+    Item it;
+    int len_phys;
+    if (g.layout == CSA_THD) {
+        const int ir = total - 1 - i;
+        it.b = find_seg(a.cu_g, g.B, ir);
+        it.s0 = (ir - __ldg(a.cu_g + it.b)) * RP;
+        len_phys = __ldg(g.cu_q + it.b + 1) - __ldg(g.cu_q + it.b);
+        it.len_real = __ldg(g.cu_real + it.b + 1) - __ldg(g.cu_real + it.b);
+        it.gid0 = __ldg(g.cu_c + it.b);
+    } else {
+        const int groups = (g.S + RP - 1) / RP;
+        it.b = i % g.B;
+        it.s0 = (groups - 1 - i / g.B) * RP;
+        len_phys = it.len_real = g.S;
+        it.gid0 = (long long)it.b * g.nc;
+    }
+    it.key_y = it.gid0;
+    int nc = it.len_real / g.ratio;
+    if (nc > g.NC) nc = g.NC;
+    if (g.layout == CSA_THD && it.gid0 + nc > g.key_rows) nc = it.gid0 < g.key_rows ? (int)(g.key_rows - it.gid0) : 0;
+    it.n = it.s0 + 1 < len_phys ? 2 : 1;
+    it.row0 = row_of(g, it.b, it.s0);
+    it.row1 = it.n > 1 ? row_of(g, it.b, it.s0 + 1) : it.row0;
+    auto vis = [&](int s) { int v = s < it.len_real ? (s + 1) / g.ratio : 0; return v < nc ? v : nc; };
+    it.v0 = vis(it.s0);
+    it.v1 = it.n > 1 ? vis(it.s0 + 1) : 0;
+    it.vmax = it.v0 > it.v1 ? it.v0 : it.v1;
+    const int s_last = it.s0 + it.n - 1;
+    it.p_lo = it.s0 - g.window + 1;
+    if (it.p_lo < 0) it.p_lo = 0;
+    it.nw = (it.vmax > 0 && g.window > 0) ? (s_last - it.p_lo + 1 + NK - 1) / NK : 0;
+    it.nct = (it.vmax + NK - 1) / NK;
+    return it;
+}
+
+__device__ __forceinline__ int item_total(const Args &a)
+{
+    return a.g.layout == CSA_THD ? __ldg(a.cu_g + a.g.B) : a.total;
+}
+
+// tile tt of an item: window tiles, then compressed tiles (pass 1), then compressed tiles again (pass 2)
+__device__ __forceinline__ int ntiles(const Item &it) { return it.nw + 2 * it.nct; }
+
+__global__ void __launch_bounds__(THREADS, 1)
+teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
+                  const __grid_constant__ CUtensorMap map_kvc, Args a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *sQ = smem + OFF_Q;
+    unsigned char *sB = smem + OFF_B;
+    float *sT = reinterpret_cast<float *>(smem + OFF_T);
+    unsigned char *sSel = smem + OFF_SEL;
+    float2 *sPart = reinterpret_cast<float2 *>(smem + OFF_PART);
+    float *sRed = reinterpret_cast<float *>(smem + OFF_RED);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
+    uint64_t *b_full = bars, *b_empty = bars + BSTG, *q_full = bars + 12, *q_empty = bars + 14;
+    uint64_t *t_full = bars + 16, *t_empty = bars + 18, *mma_done = bars + 20;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 256);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 264);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo &g = a.g;
+    const bool sbhd = g.layout == CSA_SBHD;
+    const int nkb = a.nkb;
+    int *err = &g_teacher_error;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < BSTG; i++) { mbar_init(b_full + i, 1); mbar_init(b_empty + i, 1); }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(q_full + i, 1);
+            mbar_init(q_empty + i, 1);
+            mbar_init(t_full + i, 1);
+            mbar_init(t_empty + i, 8);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        init_fence();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total = item_total(a);
+
+    if (warp == 0) {
+        if (lane == 0) {  // ------------------------------------------------ TMA producer
+            int hs = 0, ai = 0;
+            int last_hs[BSTG];
+            int last_ai[2] = {-1, -1};
+            for (int i = 0; i < BSTG; i++) last_hs[i] = -1;
+            for (int i = blockIdx.x; i < total; i += gridDim.x) {
+                const Item it = decode(a, i, total);
+                if (it.vmax == 0) continue;
+                const int qb = ai & 1;
+                wait_bar(q_empty + qb, ((ai >> 1) & 1) ^ 1, abort_flag, err, 41);
+                mbar_expect_tx(q_full + qb, (uint32_t)(nkb * KB));
+                for (int r = 0; r < RP; r++)
+                    for (int kb = 0; kb < nkb; kb++)
+                        tma_load_3d(sQ + qb * QBUF + kb * KB + r * (H * 128), &map_q, q_full + qb, kb * 64, 0,
+                                    (int)(r == 0 ? it.row0 : it.row1));
+                last_ai[qb] = ai;
+                ai++;
+                const int nt = ntiles(it);
+                for (int tt = 0; tt < nt; tt++) {
+                    const bool win = tt < it.nw;
+                    const int t = win ? tt : (tt - it.nw) % (it.nct > 0 ? it.nct : 1);
+                    for (int kb = 0; kb < nkb; kb++) {
+                        const int st = hs % BSTG;
+                        wait_bar(b_empty + st, ((hs / BSTG) & 1) ^ 1, abort_flag, err, 42);
+                        mbar_expect_tx(b_full + st, KB);
+                        unsigned char *dst = sB + st * KB;
+                        if (win) {
+                            const int p = it.p_lo + t * NK;
+                            if (sbhd) tma_load_3d(dst, &map_kv, b_full + st, kb * 64, it.b, p);
+                            else tma_load_2d(dst, &map_kv, b_full + st, kb * 64, (int)row_of(g, it.b, p));
+                        } else {
+                            if (sbhd) tma_load_3d(dst, &map_kvc, b_full + st, kb * 64, it.b, t * NK);
+                            else tma_load_2d(dst, &map_kvc, b_full + st, kb * 64, (int)(it.key_y + t * NK));
+                        }
+                        last_hs[st] = hs;
+                        hs++;
+                    }
+                }
+            }
+            for (int st = 0; st < BSTG; st++)
+                if (last_hs[st] >= 0) drain_bar(b_full + st, (last_hs[st] / BSTG) & 1, err);
+            for (int qb = 0; qb < 2; qb++)
+                if (last_ai[qb] >= 0) drain_bar(q_full + qb, (last_ai[qb] >> 1) & 1, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // ------------------------------------------------ MMA issuer
+            int hs = 0, ai = 0, tc = 0;
+            for (int i = blockIdx.x; i < total; i += gridDim.x) {
+                const Item it = decode(a, i, total);
+                if (it.vmax == 0) continue;
+                const int qb = ai & 1;
+                wait_bar(q_full + qb, (ai >> 1) & 1, abort_flag, err, 43);
+                fence_after();
+                const int nt = ntiles(it);
+                for (int tt = 0; tt < nt; tt++) {
+                    const int tb = tc & 1;
+                    wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, err, 44);
+                    fence_after();
+                    for (int kb = 0; kb < nkb; kb++) {
+                        const int st = hs % BSTG;
+                        wait_bar(b_full + st, (hs / BSTG) & 1, abort_flag, err, 45);
+                        fence_after();
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; k4++)
+                            mma_bf16(tmem + tb * NK, desc_kmajor(sQ + qb * QBUF + kb * KB + k4 * 32),
+                                     desc_kmajor(sB + st * KB + k4 * 32), IDESC, (kb | k4) ? 1u : 0u);
+                        mma_commit(b_empty + st);
+                        hs++;
+                    }
+                    mma_commit(t_full + tb);
+                    tc++;
+                }
+                mma_commit(q_empty + qb);
+                ai++;
+            }
+            mma_commit(mma_done);
+            drain_bar(mma_done, 0, err);
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- epilogue
+        const int e = warp - 4, quad = warp & 3, half = e >> 2, et = threadIdx.x - 128;
+        const int rh = quad * 32 + lane;      // (row, head) of this thread's TMEM lane
+        const int i_row = rh >> 6, h = rh & 63;
+        const float sigma = g.scale;
+        int tc = 0;
+        for (int it_i = blockIdx.x; it_i < total; it_i += gridDim.x) {
+            const Item it = decode(a, it_i, total);
+            const int vme = i_row == 0 ? it.v0 : it.v1;
+            const int s_me = it.s0 + i_row;
+            // ---- per-item set-up: selection flags and T rows of both rows
+            named_bar(1, EPI);
+            for (int x = et; x < RP * NCMAX; x += EPI) {
+                sT[x] = 0.f;
+                sSel[x] = 0;
+            }
+            named_bar(1, EPI);
+            if (it.vmax > 0) {
+                for (int r = 0; r < it.n; r++) {
+                    const int v = r == 0 ? it.v0 : it.v1;
+                    const long long row = r == 0 ? it.row0 : it.row1;
+                    if (g.sparse) {
+                        for (int s = et; s < g.K; s += EPI) {
+                            const long long id = __ldg(a.ids + row * g.K + s);
+                            const long long j = id - it.gid0;
+                            if (id >= 0 && j >= 0 && j < v) sSel[r * NCMAX + j] = 1;
+                        }
+                    } else {
+                        for (int j = et; j < v; j += EPI) sSel[r * NCMAX + j] = 1;
+                    }
+                }
+            }
+            named_bar(1, EPI);
+            float m = -INFINITY, ssum = 0.f, ell = 0.f;
+            const int nt = ntiles(it);
+            for (int tt = 0; tt < nt; tt++) {
+                const int tb = tc & 1;
+                wait_bar(t_full + tb, (tc >> 1) & 1, abort_flag, err, 46);
+                fence_after();
+                const bool win = tt < it.nw;
+                const bool pass2 = tt >= it.nw + it.nct;
+                const int t = win ? tt : (tt - it.nw) % it.nct;
+                if (pass2 && tt == it.nw + it.nct) {
+                    // l_h from both column halves (combined in a fixed order) and the sink
+                    sPart[half * M + rh] = make_float2(m, ssum);
+                    named_bar(1, EPI);
+                    const float2 p0 = sPart[rh], p1 = sPart[M + rh];
+                    const float ah = __ldg(a.sink + h);
+                    const float mm = fmaxf(fmaxf(p0.x, p1.x), ah);
+                    float S = 0.f;
+                    if (mm != -INFINITY) {
+                        if (p0.x != -INFINITY) S += p0.y * __expf(p0.x - mm);
+                        if (p1.x != -INFINITY) S += p1.y * __expf(p1.x - mm);
+                        if (ah != -INFINITY) S += __expf(ah - mm);
+                    }
+                    ell = mm + __logf(S);
+                }
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+                    float x[32];
+                    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + half * 64 + c * 32), x);
+                    const int col0 = half * 64 + c * 32;
+                    if (!pass2) {
+                        float cm = -INFINITY;
+#pragma unroll
+                        for (int q = 0; q < 32; q++) {
+                            bool ok;
+                            if (win) {
+                                const int p = it.p_lo + t * NK + col0 + q;
+                                ok = p <= s_me && p > s_me - g.window && s_me < it.len_real;
+                            } else {
+                                const int j = t * NK + col0 + q;
+                                ok = j < vme && sSel[i_row * NCMAX + j];
+                            }
+                            x[q] = ok ? x[q] * sigma : -INFINITY;
+                            cm = fmaxf(cm, x[q]);
+                        }
+                        if (cm != -INFINITY) {
+                            if (cm > m) {
+                                ssum *= __expf(m - cm);
+                                m = cm;
+                            }
+#pragma unroll
+                            for (int q = 0; q < 32; q++) ssum += __expf(x[q] - m);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; q++) {
+                            const int j = t * NK + col0 + q;
+                            const bool ok = j < vme && sSel[i_row * NCMAX + j];
+                            x[q] = ok ? __expf(x[q] * sigma - ell) : 0.f;
+                        }
+                        // sum over the 32 heads of this warp: reduce-scatter, lane l ends with column col0 + l
+#pragma unroll
+                        for (int off = 16; off >= 1; off >>= 1) {
+                            const bool up = (lane & off) != 0;
+#pragma unroll
+                            for (int q = 0; q < off; q++) {
+                                const float send = up ? x[q] : x[q + off];
+                                const float keep = up ? x[q + off] : x[q];
+                                x[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                            }
+                        }
+                        const int j = t * NK + col0 + lane;
+                        if (j < NCMAX && x[0] != 0.f) atomicAdd(sT + i_row * NCMAX + j, x[0]);
+                    }
+                }
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(t_empty + tb);
+                tc++;
+            }
+            named_bar(1, EPI);
+            // ---- L1 normalisation and write-out, one row per 128 threads
+            const int r = et >> 7, rt = et & 127;
+            const int v = r == 0 ? it.v0 : it.v1;
+            float part = 0.f;
+            for (int j = rt; j < v; j += 128) part += sT[r * NCMAX + j];
+            part = warp_sum(part);
+            if (lane == 0) sRed[et >> 5] = part;
+            named_bar(1, EPI);
+            float S = sRed[r * 4] + sRed[r * 4 + 1] + sRed[r * 4 + 2] + sRed[r * 4 + 3];
+            const float inv = 1.f / fmaxf(S, 1e-10f);
+            if (r < it.n) {
+                const long long row = r == 0 ? it.row0 : it.row1;
+                float *trow = a.teacher + row * g.TW;
+                if (g.sparse) {
+                    for (int s = rt; s < g.TW; s += 128) {
+                        const long long id = __ldg(a.ids + row * g.K + s);
+                        const long long j = id - it.gid0;
+                        trow[s] = (id >= 0 && j >= 0 && j < v) ? sT[r * NCMAX + j] * inv : 0.f;
+                    }
+                } else {
+                    for (int j = rt; j < g.TW; j += 128) trow[j] = j < v ? sT[r * NCMAX + j] * inv : 0.f;
+                }
+            }
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+__global__ void build_items_kernel(Geo g, int *cu_g)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int acc = 0;
+    cu_g[0] = 0;
+    for (int b = 0; b < g.B; b++) {
+        const int lp = __ldg(g.cu_q + b + 1) - __ldg(g.cu_q + b);
+        acc += lp > 0 ? (lp + RP - 1) / RP : 0;
+        cu_g[b + 1] = acc;
+    }
+}
+
+}  // namespace teach
+
+// ------------------------------------------------------------------ host side
+
+bool tc_teacher_supported(const Geo &g, bool bf16)
+{
+    const char *f = getenv("CSA_FORCE_GENERIC");
+    if (f != nullptr && f[0] == '1') return false;
+    return bf16 && g.H == teach::H && g.D % 64 == 0 && g.D / 64 >= 1 && g.D / 64 <= teach::MAXKB && g.NC >= 1 &&
+           g.NC <= teach::NCMAX && g.K >= 1 && g.rows > 0 && g.key_rows > 0 && g.TW <= 4096;
+}
+
+size_t tc_teacher_workspace_bytes(const Geo &g) { return sizeof(int) * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1); }
+
+cudaError_t launch_teacher_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *kv,
+                              const __nv_bfloat16 *kv_c, const float *sink, const int32_t *ids, float *teacher,
+                              void *ws, cudaStream_t st)
+{
+    using namespace teach;
+    CUtensorMap mq, mkv, mkc;
+    // q as [rows][H][D] with a 64 x 64 x 1 box
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)g.H, (cuuint64_t)g.rows};
+        const cuuint64_t strides[2] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.H * g.D * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)g.H, 1};
+        if (!tc_encode_bf16(&mq, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    if (g.layout == CSA_SBHD) {
+        const cuuint64_t dkv[3] = {(cuuint64_t)g.D, (cuuint64_t)g.B, (cuuint64_t)g.S};
+        const cuuint64_t skv[2] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.B * g.D * 2};
+        const cuuint64_t dkc[3] = {(cuuint64_t)g.D, (cuuint64_t)g.B, (cuuint64_t)g.nc};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)NK};
+        if (!tc_encode_bf16(&mkv, kv, 3, dkv, skv, box) || !tc_encode_bf16(&mkc, kv_c, 3, dkc, skv, box))
+            return cudaErrorInvalidValue;
+    } else {
+        const cuuint64_t dkv[2] = {(cuuint64_t)g.D, (cuuint64_t)g.rows};
+        const cuuint64_t dkc[2] = {(cuuint64_t)g.D, (cuuint64_t)g.key_rows};
+        const cuuint64_t s1[1] = {(cuuint64_t)g.D * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)NK};
+        if (!tc_encode_bf16(&mkv, kv, 2, dkv, s1, box) || !tc_encode_bf16(&mkc, kv_c, 2, dkc, s1, box))
+            return cudaErrorInvalidValue;
+    }
+    Args a;
+    a.g = g;
+    a.sink = sink;
+    a.ids = ids;
+    a.teacher = teacher;
+    a.cu_g = nullptr;
+    a.total = 0;
+    a.nkb = g.D / 64;
+    int upper;
+    if (g.layout == CSA_THD) {
+        int *cu_g = static_cast<int *>(ws);
+        build_items_kernel<<<1, 32, 0, st>>>(g, cu_g);
+        note_launches(1);
+        a.cu_g = cu_g;
+        upper = (g.rows + RP - 1) / RP + g.B;
+    } else {
+        a.total = g.B * ((g.S + RP - 1) / RP);
+        upper = a.total;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(teacher_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    const int grid = upper < sms ? (upper > 0 ? upper : 1) : sms;
+    teacher_tc_kernel<<<grid, THREADS, SMEM, st>>>(mq, mkv, mkc, a);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace csa
