@@ -390,33 +390,58 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
     } else if (warp == 2) {
         // ---------------------------------------------------------------- g / w stager
+        // Every global load of a row is issued before any is used (one memory latency per chunk of 512 slots),
+        // then scattered into the dense per-row g buffer of the item.
         int ic = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
             const Pair p = decode_pair(a, i);
             const int gb = ic & 1;
             wait_bar(gd_empty + gb, ((ic >> 1) & 1) ^ 1, abort_flag, err, 8);
             float *gd = sGD + gb * RP * NCMAX;
+            for (int j = lane; j < p.vmax; j += 32) {
+                gd[j] = 0.f;
+                gd[NCMAX + j] = 0.f;
+            }
+            float wv[RP][2];
+#pragma unroll
             for (int r = 0; r < RP; r++) {
-                const int v = r == 0 ? p.v0 : p.v1;
                 const long long row = r == 0 ? p.row0 : p.row1;
-                float *gr = gd + r * NCMAX;
-                for (int j = lane; j < p.vmax; j += 32) gr[j] = 0.f;
-                sW[gb * RP * HI + r * HI + lane] = (r < p.n) ? __ldg(a.w + row * HI + lane) : 0.f;
-                sW[gb * RP * HI + r * HI + lane + 32] = (r < p.n) ? __ldg(a.w + row * HI + lane + 32) : 0.f;
-                __syncwarp();
-                if (v == 0) continue;
-                if (g.sparse) {
-                    const int32_t *ir = a.ids + row * g.K;
-                    const float *gg = a.gbuf + row * g.TW;
-                    for (int s = lane; s < g.K; s += 32) {
-                        const long long id = __ldg(ir + s);
-                        const long long j = id - p.sg.gid0;
-                        if (id >= 0 && j >= 0 && j < v) gr[j] = __ldg(gg + s);
+                wv[r][0] = (r < p.n) ? __ldg(a.w + row * HI + lane) : 0.f;
+                wv[r][1] = (r < p.n) ? __ldg(a.w + row * HI + lane + 32) : 0.f;
+            }
+            __syncwarp();
+            constexpr int CHUNK = 16;  // slots per lane per pass
+            const int span = g.sparse ? g.K : p.vmax;
+            for (int base = 0; base < span; base += 32 * CHUNK) {
+                int32_t idv[RP][CHUNK];
+                float gv[RP][CHUNK];
+#pragma unroll
+                for (int r = 0; r < RP; r++) {
+                    const int v = r == 0 ? p.v0 : p.v1;
+                    const long long row = r == 0 ? p.row0 : p.row1;
+#pragma unroll
+                    for (int c = 0; c < CHUNK; c++) {
+                        const int s = base + c * 32 + lane;
+                        const bool ok = v > 0 && s < (g.sparse ? g.K : v);
+                        idv[r][c] = ok ? (g.sparse ? __ldg(a.ids + row * g.K + s) : s) : -1;
+                        gv[r][c] = ok ? __ldg(a.gbuf + row * g.TW + s) : 0.f;
                     }
-                } else {
-                    const float *gg = a.gbuf + row * g.TW;
-                    for (int j = lane; j < v; j += 32) gr[j] = __ldg(gg + j);
                 }
+#pragma unroll
+                for (int r = 0; r < RP; r++) {
+                    const int v = r == 0 ? p.v0 : p.v1;
+#pragma unroll
+                    for (int c = 0; c < CHUNK; c++) {
+                        if (idv[r][c] < 0) continue;
+                        const long long j = g.sparse ? (long long)idv[r][c] - p.sg.gid0 : idv[r][c];
+                        if (j >= 0 && j < v) gd[r * NCMAX + j] = gv[r][c];
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RP; r++) {
+                sW[gb * RP * HI + r * HI + lane] = wv[r][0];
+                sW[gb * RP * HI + r * HI + lane + 32] = wv[r][1];
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(gd_full + gb);
@@ -676,40 +701,73 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             mma_commit(mma_done);
             drain_bar(mma_done, 0, err);
         }
-    } else if (warp == 2) {
-        // ---------------------------------------------------------------- g / w stager (per row pair)
+    } else if (warp == 2 || warp == 3) {
+        // ---------------------------------------------------------------- g / w stagers (per row pair)
+        // Two warps take alternate row pairs; each issues all loads of a pair before using them.
+        const int me = warp - 2;
         int pc = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             const Unit U = decode_unit(a, u);
             const long long key_lo = U.sg.gid0 + (long long)U.kt * NKEY;
             for (int pi = 0; pi < U.npairs; pi++, pc++) {
+                if ((pc & 1) != me) continue;
                 const int gs = pc % K_GSTG;
                 wait_bar(gt_empty + gs, ((pc / K_GSTG) & 1) ^ 1, abort_flag, err, 28);
                 float *gt = sGT + gs * RP * NKEY;
                 float *wt = sWT + gs * RP * HI;
-                for (int x = lane; x < RP * NKEY; x += 32) gt[x] = 0.f;
-                __syncwarp();
+                long long row[RP];
+                bool ok[RP];
+                int v[RP];
+                int t0[RP], t1[RP];
+                float wv[RP][2];
+#pragma unroll
                 for (int r = 0; r < RP; r++) {
                     const int s = U.s_lo + pi * RP + r;
-                    const bool ok = s < U.s_hi;
-                    const long long row = row_of(g, U.sg.b, ok ? s : U.s_lo);
-                    wt[r * HI + lane] = ok ? __ldg(a.w + row * HI + lane) : 0.f;
-                    wt[r * HI + lane + 32] = ok ? __ldg(a.w + row * HI + lane + 32) : 0.f;
-                    if (!ok) continue;
-                    const int v = vis(g, U.sg, s);
-                    if (g.sparse) {
-                        const int s0 = __ldg(a.toff + row * (a.NT + 1) + U.kt);
-                        const int s1 = __ldg(a.toff + row * (a.NT + 1) + U.kt + 1);
-                        for (int sl = s0 + lane; sl < s1; sl += 32) {
-                            const long long kk = (long long)__ldg(a.ids + row * g.K + sl) - key_lo;
-                            const long long j = kk + (long long)U.kt * NKEY;
-                            if (kk >= 0 && kk < NKEY && j < v) gt[r * NKEY + kk] = __ldg(a.gbuf + row * g.TW + sl);
+                    ok[r] = s < U.s_hi;
+                    row[r] = row_of(g, U.sg.b, ok[r] ? s : U.s_lo);
+                    v[r] = ok[r] ? vis(g, U.sg, s) : 0;
+                    wv[r][0] = ok[r] ? __ldg(a.w + row[r] * HI + lane) : 0.f;
+                    wv[r][1] = ok[r] ? __ldg(a.w + row[r] * HI + lane + 32) : 0.f;
+                    t0[r] = (ok[r] && g.sparse) ? __ldg(a.toff + row[r] * (a.NT + 1) + U.kt) : 0;
+                    t1[r] = (ok[r] && g.sparse) ? __ldg(a.toff + row[r] * (a.NT + 1) + U.kt + 1) : 0;
+                }
+#pragma unroll
+                for (int x = 0; x < RP * NKEY / 32; x++) gt[x * 32 + lane] = 0.f;
+                int32_t idv[RP][4];
+                float gv[RP][4];
+#pragma unroll
+                for (int r = 0; r < RP; r++)
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        if (g.sparse) {
+                            const int sl = t0[r] + c * 32 + lane;
+                            const bool in = ok[r] && sl < t1[r];
+                            idv[r][c] = in ? __ldg(a.ids + row[r] * g.K + sl) : -1;
+                            gv[r][c] = in ? __ldg(a.gbuf + row[r] * g.TW + sl) : 0.f;
+                        } else {
+                            const int j = U.kt * NKEY + c * 32 + lane;
+                            const bool in = ok[r] && j < v[r];
+                            idv[r][c] = in ? j : -1;
+                            gv[r][c] = in ? __ldg(a.gbuf + row[r] * g.TW + j) : 0.f;
                         }
-                    } else {
-                        for (int kk = lane; kk < NKEY; kk += 32) {
-                            const int j = U.kt * NKEY + kk;
-                            if (j < v) gt[r * NKEY + kk] = __ldg(a.gbuf + row * g.TW + j);
+                    }
+                __syncwarp();
+#pragma unroll
+                for (int r = 0; r < RP; r++) {
+                    wt[r * HI + lane] = wv[r][0];
+                    wt[r * HI + lane + 32] = wv[r][1];
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        if (idv[r][c] < 0) continue;
+                        long long kk, j;
+                        if (g.sparse) {
+                            kk = (long long)idv[r][c] - key_lo;
+                            j = kk + (long long)U.kt * NKEY;
+                        } else {
+                            j = idv[r][c];
+                            kk = j - (long long)U.kt * NKEY;
                         }
+                        if (kk >= 0 && kk < NKEY && j < v[r]) gt[r * NKEY + kk] = gv[r][c];
                     }
                 }
                 __syncwarp();

@@ -280,16 +280,28 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 sT[x] = 0.f;
                 sSel[x] = 0;
             }
+            // this thread's id slots s = et + 256 q of both rows, loaded together and kept for the write-out
+            constexpr int NQ = NCMAX / EPI;
+            int32_t idr[RP][NQ];
+#pragma unroll
+            for (int r = 0; r < RP; r++) {
+                const long long row = r == 0 ? it.row0 : it.row1;
+#pragma unroll
+                for (int q = 0; q < NQ; q++) {
+                    const int s = et + q * EPI;
+                    idr[r][q] = (g.sparse && it.vmax > 0 && r < it.n && s < g.K) ? __ldg(a.ids + row * g.K + s) : -1;
+                }
+            }
             named_bar(1, EPI);
             if (it.vmax > 0) {
-                for (int r = 0; r < it.n; r++) {
+#pragma unroll
+                for (int r = 0; r < RP; r++) {
                     const int v = r == 0 ? it.v0 : it.v1;
-                    const long long row = r == 0 ? it.row0 : it.row1;
                     if (g.sparse) {
-                        for (int s = et; s < g.K; s += EPI) {
-                            const long long id = __ldg(a.ids + row * g.K + s);
-                            const long long j = id - it.gid0;
-                            if (id >= 0 && j >= 0 && j < v) sSel[r * NCMAX + j] = 1;
+#pragma unroll
+                        for (int q = 0; q < NQ; q++) {
+                            const long long j = (long long)idr[r][q] - it.gid0;
+                            if (idr[r][q] >= 0 && j >= 0 && j < v) sSel[r * NCMAX + j] = 1;
                         }
                     } else {
                         for (int j = et; j < v; j += EPI) sSel[r * NCMAX + j] = 1;
@@ -387,18 +399,29 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             named_bar(1, EPI);
             float S = sRed[r * 4] + sRed[r * 4 + 1] + sRed[r * 4 + 2] + sRed[r * 4 + 3];
             const float inv = 1.f / fmaxf(S, 1e-10f);
-            if (r < it.n) {
+            if (g.sparse) {
+                // write-out with the slot mapping of the set-up: slots et + 256 q of both rows
+                const float S0 = sRed[0] + sRed[1] + sRed[2] + sRed[3];
+                const float S1 = sRed[4] + sRed[5] + sRed[6] + sRed[7];
+#pragma unroll
+                for (int rr = 0; rr < RP; rr++) {
+                    if (rr >= it.n) continue;
+                    const int vr = rr == 0 ? it.v0 : it.v1;
+                    const float ir = 1.f / fmaxf(rr == 0 ? S0 : S1, 1e-10f);
+                    const long long row = rr == 0 ? it.row0 : it.row1;
+                    float *trow = a.teacher + row * g.TW;
+#pragma unroll
+                    for (int q = 0; q < NQ; q++) {
+                        const int s = et + q * EPI;
+                        if (s >= g.TW) continue;
+                        const long long j = (long long)idr[rr][q] - it.gid0;
+                        trow[s] = (idr[rr][q] >= 0 && j >= 0 && j < vr) ? sT[rr * NCMAX + j] * ir : 0.f;
+                    }
+                }
+            } else if (r < it.n) {
                 const long long row = r == 0 ? it.row0 : it.row1;
                 float *trow = a.teacher + row * g.TW;
-                if (g.sparse) {
-                    for (int s = rt; s < g.TW; s += 128) {
-                        const long long id = __ldg(a.ids + row * g.K + s);
-                        const long long j = id - it.gid0;
-                        trow[s] = (id >= 0 && j >= 0 && j < v) ? sT[r * NCMAX + j] * inv : 0.f;
-                    }
-                } else {
-                    for (int j = rt; j < g.TW; j += 128) trow[j] = j < v ? sT[r * NCMAX + j] * inv : 0.f;
-                }
+                for (int j = rt; j < g.TW; j += 128) trow[j] = j < v ? sT[r * NCMAX + j] * inv : 0.f;
             }
         }
     }
