@@ -489,13 +489,19 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         const int half = e >> 2;          // rows {2 half, 2 half + 1}
         const int et = threadIdx.x - 64;  // 0..255
         int tc = 0;
+        // w of this thread's (row, head) for the next item, loaded one item ahead
+        auto w_of = [&](int i) -> float {
+            if (i >= total) return 0.f;
+            const Item nx = decode_item(a, i, total);
+            const int k = et >> 6, h = et & 63;
+            return k < nx.n ? __ldg(a.w + nx.row[k] * HI + h) : 0.f;
+        };
+        float w_next = w_of(blockIdx.x);
         for (int i = blockIdx.x; i < total; i += gridDim.x) {
             const Item it = decode_item(a, i, total);
             named_bar(1, EPI);  // the previous item's selection has finished with sW / sSC
-            {
-                const int k = et >> 6, h = et & 63;
-                sW[et] = k < it.n ? __ldg(a.w + it.row[k] * HI + h) : 0.f;
-            }
+            sW[et] = w_next;
+            w_next = w_of(i + gridDim.x);
             named_bar(1, EPI);
             const int nt = (it.vmax + NKEY - 1) / NKEY;
             for (int t = 0; t < nt; t++) {
@@ -506,15 +512,16 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
 #pragma unroll
                 for (int rr = 0; rr < 2; rr++) {
                     const int k = half * 2 + rr;
-                    float acc = 0.f;
+                    float ac[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums over heads h % 4
 #pragma unroll
                     for (int c = 0; c < 2; c++) {
                         float x[32];
                         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NCOL + k * HI + c * 32), x);
                         const float *wk = sW + k * HI + c * 32;
 #pragma unroll
-                        for (int h = 0; h < 32; h++) acc = fmaf(wk[h], fmaxf(x[h], 0.f), acc);
+                        for (int h = 0; h < 32; h++) ac[h & 3] = fmaf(wk[h], fmaxf(x[h], 0.f), ac[h & 3]);
                     }
+                    const float acc = (ac[0] + ac[1]) + (ac[2] + ac[3]);
                     if (k < it.n && j < it.v[k]) sSC[k * NCMAX + j] = acc;
                 }
                 fence_before();

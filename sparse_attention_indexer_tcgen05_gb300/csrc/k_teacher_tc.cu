@@ -53,7 +53,7 @@ constexpr uint32_t IDESC = idesc_bf16(128, 128, false, false);
 constexpr int OFF_Q = 0;
 constexpr int OFF_B = OFF_Q + 2 * QBUF;                     // 96 KB
 constexpr int OFF_T = OFF_B + BSTG * KB;                    // 192 KB: 2 rows x NCMAX fp32
-constexpr int OFF_SEL = OFF_T + RP * NCMAX * 4;             // 200 KB: 2 rows x NCMAX bytes
+constexpr int OFF_SEL = OFF_T + RP * NCMAX * 4;             // 200 KB: selection bit words, 2 rows x NCMAX bits
 constexpr int OFF_PART = OFF_SEL + RP * NCMAX;              // 202 KB: 2 halves x 128 x (m, s)
 constexpr int OFF_RED = OFF_PART + 2 * M * 8;               // 8 warps
 constexpr int OFF_MISC = OFF_RED + 64;
@@ -77,6 +77,28 @@ struct Item {
     long long gid0, key_y;
     int p_lo, nw, nct;    // window start position, window tiles, compressed tiles
 };
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// bits lo..hi (inclusive) of a 32-bit word, after clamping to 0..31; 0 when the range is empty
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi)
+{
+    if (lo < 0) lo = 0;
+    if (hi > 31) hi = 31;
+    if (hi < lo) return 0u;
+    const uint32_t upto = hi == 31 ? 0xffffffffu : ((1u << (hi + 1)) - 1u);
+    return upto & ~((1u << lo) - 1u);
+}
 
 __device__ __forceinline__ int find_seg(const int *cu, int nseg, int x)
 {
@@ -150,7 +172,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     unsigned char *sQ = smem + OFF_Q;
     unsigned char *sB = smem + OFF_B;
     float *sT = reinterpret_cast<float *>(smem + OFF_T);
-    unsigned char *sSel = smem + OFF_SEL;
+    uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + OFF_SEL);  // [RP][NCMAX / 32]
     float2 *sPart = reinterpret_cast<float2 *>(smem + OFF_PART);
     float *sRed = reinterpret_cast<float *>(smem + OFF_RED);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
@@ -268,7 +290,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int e = warp - 4, quad = warp & 3, half = e >> 2, et = threadIdx.x - 128;
         const int rh = quad * 32 + lane;      // (row, head) of this thread's TMEM lane
         const int i_row = rh >> 6, h = rh & 63;
-        const float sigma = g.scale;
+        const float s2 = g.scale * 1.4426950408889634f;  // logits in log2 units: exp(c) = 2^(x * sigma * log2 e)
         int tc = 0;
         for (int it_i = blockIdx.x; it_i < total; it_i += gridDim.x) {
             const Item it = decode(a, it_i, total);
@@ -276,10 +298,8 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             const int s_me = it.s0 + i_row;
             // ---- per-item set-up: selection flags and T rows of both rows
             named_bar(1, EPI);
-            for (int x = et; x < RP * NCMAX; x += EPI) {
-                sT[x] = 0.f;
-                sSel[x] = 0;
-            }
+            for (int x = et; x < RP * NCMAX; x += EPI) sT[x] = 0.f;
+            if (et < RP * NCMAX / 32) sMask[et] = 0u;
             // this thread's id slots s = et + 256 q of both rows, loaded together and kept for the write-out
             constexpr int NQ = NCMAX / EPI;
             int32_t idr[RP][NQ];
@@ -301,16 +321,18 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
                         for (int q = 0; q < NQ; q++) {
                             const long long j = (long long)idr[r][q] - it.gid0;
-                            if (idr[r][q] >= 0 && j >= 0 && j < v) sSel[r * NCMAX + j] = 1;
+                            if (idr[r][q] >= 0 && j >= 0 && j < v) atomicOr(sMask + r * (NCMAX / 32) + (j >> 5), 1u << (j & 31));
                         }
                     } else {
-                        for (int j = et; j < v; j += EPI) sSel[r * NCMAX + j] = 1;
+                        for (int wd = et; wd < NCMAX / 32; wd += EPI) sMask[r * (NCMAX / 32) + wd] = range_bits(0, v - 1 - wd * 32);
                     }
                 }
             }
             named_bar(1, EPI);
+            // running log2-domain max and sum of this thread's (row, head) over its key columns
             float m = -INFINITY, ssum = 0.f, ell = 0.f;
             const int nt = ntiles(it);
+            const bool row_ok = s_me < it.len_real;
             for (int tt = 0; tt < nt; tt++) {
                 const int tb = tc & 1;
                 wait_bar(t_full + tb, (tc >> 1) & 1, abort_flag, err, 46);
@@ -319,68 +341,82 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const bool pass2 = tt >= it.nw + it.nct;
                 const int t = win ? tt : (tt - it.nw) % it.nct;
                 if (pass2 && tt == it.nw + it.nct) {
-                    // l_h from both column halves (combined in a fixed order) and the sink
+                    // l_h (log2 units) from both column halves, combined in a fixed order, and the sink
                     sPart[half * M + rh] = make_float2(m, ssum);
                     named_bar(1, EPI);
                     const float2 p0 = sPart[rh], p1 = sPart[M + rh];
-                    const float ah = __ldg(a.sink + h);
+                    const float ah = __ldg(a.sink + h) * 1.4426950408889634f;
                     const float mm = fmaxf(fmaxf(p0.x, p1.x), ah);
                     float S = 0.f;
                     if (mm != -INFINITY) {
-                        if (p0.x != -INFINITY) S += p0.y * __expf(p0.x - mm);
-                        if (p1.x != -INFINITY) S += p1.y * __expf(p1.x - mm);
-                        if (ah != -INFINITY) S += __expf(ah - mm);
+                        if (p0.x != -INFINITY) S += p0.y * ex2(p0.x - mm);
+                        if (p1.x != -INFINITY) S += p1.y * ex2(p1.x - mm);
+                        if (ah != -INFINITY) S += ex2(ah - mm);
                     }
-                    ell = mm + __logf(S);
+                    ell = mm + lg2(S);
                 }
+                // mask words of this thread's two 32-column chunks
+                uint32_t mw[2];
 #pragma unroll
                 for (int c = 0; c < 2; c++) {
-                    float x[32];
-                    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + half * 64 + c * 32), x);
                     const int col0 = half * 64 + c * 32;
-                    if (!pass2) {
-                        float cm = -INFINITY;
-#pragma unroll
-                        for (int q = 0; q < 32; q++) {
-                            bool ok;
-                            if (win) {
-                                const int p = it.p_lo + t * NK + col0 + q;
-                                ok = p <= s_me && p > s_me - g.window && s_me < it.len_real;
-                            } else {
-                                const int j = t * NK + col0 + q;
-                                ok = j < vme && sSel[i_row * NCMAX + j];
-                            }
-                            x[q] = ok ? x[q] * sigma : -INFINITY;
-                            cm = fmaxf(cm, x[q]);
-                        }
-                        if (cm != -INFINITY) {
-                            if (cm > m) {
-                                ssum *= __expf(m - cm);
-                                m = cm;
-                            }
-#pragma unroll
-                            for (int q = 0; q < 32; q++) ssum += __expf(x[q] - m);
-                        }
+                    if (win) {
+                        const int pbase = it.p_lo + t * NK + col0;
+                        mw[c] = row_ok ? range_bits(s_me - g.window + 1 - pbase, s_me - pbase) : 0u;
                     } else {
+                        const int j0 = t * NK + col0;
+                        mw[c] = j0 < NCMAX ? (sMask[i_row * (NCMAX / 32) + (j0 >> 5)] & range_bits(0, vme - 1 - j0)) : 0u;
+                    }
+                }
+                float x[2][32];
+#pragma unroll
+                for (int c = 0; c < 2; c++)
+                    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + half * 64 + c * 32), x[c]);
+                if (!pass2) {
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int c = 0; c < 2; c++)
 #pragma unroll
                         for (int q = 0; q < 32; q++) {
-                            const int j = t * NK + col0 + q;
-                            const bool ok = j < vme && sSel[i_row * NCMAX + j];
-                            x[q] = ok ? __expf(x[q] * sigma - ell) : 0.f;
+                            x[c][q] = (mw[c] >> q) & 1u ? x[c][q] * s2 : -INFINITY;
+                            mx[q & 3] = fmaxf(mx[q & 3], x[c][q]);
                         }
-                        // sum over the 32 heads of this warp: reduce-scatter, lane l ends with column col0 + l
+                    const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    if (cm != -INFINITY) {
+                        if (cm > m) {
+                            ssum *= ex2(m - cm);
+                            m = cm;
+                        }
+                        float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int off = 16; off >= 1; off >>= 1) {
-                            const bool up = (lane & off) != 0;
+                        for (int c = 0; c < 2; c++)
 #pragma unroll
-                            for (int q = 0; q < off; q++) {
-                                const float send = up ? x[q] : x[q + off];
-                                const float keep = up ? x[q + off] : x[q];
-                                x[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                            for (int q = 0; q < 32; q++) sm[q & 3] += ex2(x[c][q] - m);
+                        ssum += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 2; c++)
+#pragma unroll
+                        for (int q = 0; q < 32; q++) x[c][q] = (mw[c] >> q) & 1u ? ex2(fmaf(x[c][q], s2, -ell)) : 0.f;
+                    // sum over the 32 heads of this warp, both chunks interleaved: reduce-scatter, lane l ends
+                    // with column (chunk base + l)
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) {
+                        const bool up = (lane & off) != 0;
+#pragma unroll
+                        for (int q = 0; q < off; q++)
+#pragma unroll
+                            for (int c = 0; c < 2; c++) {
+                                const float send = up ? x[c][q] : x[c][q + off];
+                                const float keep = up ? x[c][q + off] : x[c][q];
+                                x[c][q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                             }
-                        }
-                        const int j = t * NK + col0 + lane;
-                        if (j < NCMAX && x[0] != 0.f) atomicAdd(sT + i_row * NCMAX + j, x[0]);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; c++) {
+                        const int j = t * NK + half * 64 + c * 32 + lane;
+                        if (j < NCMAX && x[c][0] != 0.f) atomicAdd(sT + i_row * NCMAX + j, x[c][0]);
                     }
                 }
                 fence_before();
