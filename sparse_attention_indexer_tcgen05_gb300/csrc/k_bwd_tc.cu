@@ -42,6 +42,7 @@ using namespace ptx;
 
 constexpr int HI = 64, DI = 128, NKEY = 128;
 constexpr int RP = 2;                          // query rows per item / row pair
+constexpr int M_PAIRS = RP * 64;               // (row, head) pairs of an item
 constexpr int NCMAX = 1024;                    // key axis the row-owner's dense g rows hold
 constexpr int HALF = NKEY * 64 * 2;            // 16 KB: 128 rows x 64 bf16
 constexpr int QBLK = 2 * HALF;                 // 32 KB: 2 rows x 64 heads x 128 d, two K-halves
@@ -61,7 +62,7 @@ constexpr int R_OFF_G = R_OFF_B + 2 * QBLK;                   // 160 KB
 constexpr int R_OFF_GD = R_OFF_G + QBLK;                      // 192 KB: 2 bufs x 2 rows x NCMAX fp32
 constexpr int R_OFF_W = R_OFF_GD + 2 * RP * NCMAX * 4;        // 208 KB: 2 bufs x 2 rows x 64 fp32
 constexpr int R_OFF_DW = R_OFF_W + 2 * RP * HI * 4;           // 128 fp32
-constexpr int R_OFF_MISC = R_OFF_DW + RP * HI * 4;
+constexpr int R_OFF_MISC = R_OFF_DW + 2 * RP * HI * 4;      // sDW double-buffered by item parity
 constexpr int R_SMEM = R_OFF_MISC + 1024 + 1024;
 
 // key-owner shared memory
@@ -180,18 +181,22 @@ __device__ __forceinline__ int pair_total(const Args &a)
     return a.g.layout == CSA_THD ? __ldg(a.cu_g + a.g.B) : a.total_items;
 }
 
-// first row position that sees key tile kt, and the number of key-owner units of a segment
-__device__ __forceinline__ int smin_of(const Geo &g, int kt) { return g.ratio * (kt * NKEY + 1) - 1; }
+// Key-owner units sit on an absolute grid of CH-row chunks; chunk c of a segment is paired with every key
+// tile its rows can see, key tiles fastest, so the units that read the same q_idx rows run at the same
+// time and share them through L2.
+__host__ __device__ inline int chunk_tiles(int c, int len_real, int nc, int ratio)
+{
+    int last = (c + 1) * CH < len_real ? (c + 1) * CH : len_real;  // one past the chunk's last position
+    int v = last / ratio;                                           // visible keys of its last row
+    if (v > nc) v = nc;
+    return (v + NKEY - 1) / NKEY;
+}
 
 __host__ __device__ inline int units_of_len(int len_real, int nc, int ratio)
 {
     int u = 0;
-    const int nt = (nc + NKEY - 1) / NKEY;
-    for (int kt = 0; kt < nt; kt++) {
-        const int smin = ratio * (kt * NKEY + 1) - 1;
-        const int rows = len_real - smin;
-        if (rows > 0) u += (rows + CH - 1) / CH;
-    }
+    const int nch = (len_real + CH - 1) / CH;
+    for (int c = 0; c < nch; c++) u += chunk_tiles(c, len_real, nc, ratio);
     return u;
 }
 
@@ -215,20 +220,18 @@ __device__ Unit decode_unit(const Args &a, int u)
         lu = u / g.B;
     }
     U.sg = seg_of(g, b);
-    const int nt = (U.sg.nc + NKEY - 1) / NKEY;
     U.kt = 0;
     U.s_lo = U.s_hi = 0;
-    for (int kt = 0; kt < nt; kt++) {
-        const int smin = smin_of(g, kt);
-        const int rows = U.sg.len_real - smin;
-        const int nu = rows > 0 ? (rows + CH - 1) / CH : 0;
-        if (lu < nu) {
-            U.kt = kt;
-            U.s_lo = smin + lu * CH;
+    const int nch = (U.sg.len_real + CH - 1) / CH;
+    for (int c = 0; c < nch; c++) {
+        const int nt = chunk_tiles(c, U.sg.len_real, U.sg.nc, g.ratio);
+        if (lu < nt) {
+            U.kt = lu;
+            U.s_lo = c * CH;
             U.s_hi = min(U.sg.len_real, U.s_lo + CH);
             break;
         }
-        lu -= nu;
+        lu -= nt;
     }
     U.npairs = (U.s_hi - U.s_lo + 1) / RP;
     return U;
@@ -388,19 +391,21 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mma_commit(mma_done);
             drain_bar(mma_done, 0, err);
         }
-    } else if (warp == 2) {
-        // ---------------------------------------------------------------- g / w stager
-        // Every global load of a row is issued before any is used (one memory latency per chunk of 512 slots),
-        // then scattered into the dense per-row g buffer of the item.
+    } else if (warp == 2 || warp == 3) {
+        // ---------------------------------------------------------------- g / w stagers
+        // Warp 2 prepares the even items (buffer 0), warp 3 the odd ones (buffer 1).  Every global load of a
+        // row is issued before any is used, then scattered into the dense per-row g buffer of the item.
+        const int me = warp - 2;
         int ic = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
+            if ((ic & 1) != me) continue;
             const Pair p = decode_pair(a, i);
             const int gb = ic & 1;
             wait_bar(gd_empty + gb, ((ic >> 1) & 1) ^ 1, abort_flag, err, 8);
             float *gd = sGD + gb * RP * NCMAX;
-            for (int j = lane; j < p.vmax; j += 32) {
-                gd[j] = 0.f;
-                gd[NCMAX + j] = 0.f;
+            for (int j4 = lane; j4 * 4 < p.vmax; j4 += 32) {
+                reinterpret_cast<float4 *>(gd)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(gd + NCMAX)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             float wv[RP][2];
 #pragma unroll
@@ -493,7 +498,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const int rr = rh >> 6, h = rh & 63;
             const bool exists = rr < p.n;
             const long long row = rr == 0 ? p.row0 : p.row1;
-            float part = 0.f;
+            float pa[4] = {0.f, 0.f, 0.f, 0.f};
             if (nt > 0) {
                 const int bb = ai & 1;
                 wait_bar(dq_full, dqc & 1, abort_flag, err, 12);
@@ -522,8 +527,8 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
                     for (int u = 0; u < 4; u++) {
                         const float2 qf = __bfloat1622float2(q2[u]);
-                        part = fmaf(qf.x, vv[c * 8 + 2 * u], part);
-                        part = fmaf(qf.y, vv[c * 8 + 2 * u + 1], part);
+                        pa[(2 * u) & 3] = fmaf(qf.x, vv[c * 8 + 2 * u], pa[(2 * u) & 3]);
+                        pa[(2 * u + 1) & 3] = fmaf(qf.y, vv[c * 8 + 2 * u + 1], pa[(2 * u + 1) & 3]);
                     }
                 }
                 if (exists) {
@@ -545,11 +550,12 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + half * 64;
                 for (int c = 0; c < 8; c++) *reinterpret_cast<uint4 *>(out + c * 8) = make_uint4(0, 0, 0, 0);
             }
-            // dW = q . dQ' over the two d halves
-            if (half == 1) sDW[rh] = part;
+            // dW = q . dQ' over the two d halves (sDW alternates by item so one barrier suffices)
+            const float part = (pa[0] + pa[1]) + (pa[2] + pa[3]);
+            float *dwb = sDW + (ic & 1) * M_PAIRS;
+            if (half == 1) dwb[rh] = part;
             named_bar(1, EPI);
-            if (half == 0 && exists) a.dw[row * HI + h] = part + sDW[rh];
-            named_bar(1, EPI);
+            if (half == 0 && exists) a.dw[row * HI + h] = part + dwb[rh];
             __syncwarp();
             if (lane == 0) mbar_arrive(gd_empty + gb);
         }

@@ -388,17 +388,20 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
         const float *trow = teacher + r * TW;
         float *grow = gbuf + r * TW;
         if (toff != nullptr) {
+            // slot s opens key tiles (tile(s-1), tile(s)]: valid ids come first, ascending, so the first slot
+            // of tile kt is where the tile index of consecutive slots steps past kt (invalid slots count as NT)
             const long long lo = key_gid(g, R, 0);
-            for (int kt = tid; kt <= NT; kt += kThreads) {
-                // first slot s with (id_s invalid) or (id_s - lo >= kt * 128); valid ids come first, ascending
-                int a0 = 0, a1 = g.K;
-                while (a0 < a1) {
-                    const int mid = (a0 + a1) >> 1;
-                    const long long id = row_ids[mid];
-                    const bool beyond = id < 0 || id - lo >= (long long)kt * 128;
-                    if (beyond) a1 = mid; else a0 = mid + 1;
-                }
-                toff[r * (NT + 1) + kt] = a0;
+            int32_t *to = toff + r * (NT + 1);
+            auto tile_of = [&](int s) -> int {
+                const long long id = row_ids[s];
+                if (id < 0) return NT;
+                const long long t = (id - lo) >> 7;
+                return t < 0 ? 0 : (t > NT ? NT : (int)t);
+            };
+            for (int s = tid; s <= g.K; s += kThreads) {
+                const int prev = s > 0 ? tile_of(s - 1) : -1;
+                const int cur = s < g.K ? tile_of(s) : NT + 1;
+                for (int kt = prev + 1; kt <= cur && kt <= NT; kt++) to[kt] = s;
             }
         }
         // score of support slot s, or -inf when s is not in C

@@ -267,6 +267,34 @@ __device__ Item decode_item(const Args &a, int i, int total)
     return it;
 }
 
+// memory row of row k (0..3) of item i, or -1 when the item has no such row
+__device__ long long item_row(const Args &a, int i, int total, int k)
+{
+    const Geo &g = a.g;
+    int b, s0, len_phys;
+    if (g.layout == CSA_THD) {
+        const int ir = total - 1 - i;
+        int lo = 0, hi = g.B - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (__ldg(a.cu_g + mid) <= ir) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        s0 = (ir - __ldg(a.cu_g + lo)) * ROWS;
+        len_phys = __ldg(g.cu_q + lo + 1) - __ldg(g.cu_q + lo);
+    } else {
+        const int groups = (g.S + ROWS - 1) / ROWS;
+        b = i % g.B;
+        s0 = (groups - 1 - i / g.B) * ROWS;
+        len_phys = g.S;
+    }
+    const int s = s0 + k;
+    if (s >= len_phys) return -1;
+    if (g.layout == CSA_SBHD) return (long long)s * g.B + b;
+    if (g.layout == CSA_BSHD) return (long long)b * g.S + s;
+    return (long long)__ldg(g.cu_q + b) + s;
+}
+
 // ------------------------------------------------------------------ top-k of one row (a warp pair)
 
 __device__ __forceinline__ int pair_sum(int x, int *slots, int par, int wsel, int bar_id)
@@ -492,9 +520,8 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         // w of this thread's (row, head) for the next item, loaded one item ahead
         auto w_of = [&](int i) -> float {
             if (i >= total) return 0.f;
-            const Item nx = decode_item(a, i, total);
-            const int k = et >> 6, h = et & 63;
-            return k < nx.n ? __ldg(a.w + nx.row[k] * HI + h) : 0.f;
+            const long long row = item_row(a, i, total, et >> 6);
+            return row >= 0 ? __ldg(a.w + row * HI + (et & 63)) : 0.f;
         };
         float w_next = w_of(blockIdx.x);
         for (int i = blockIdx.x; i < total; i += gridDim.x) {
