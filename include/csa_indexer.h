@@ -207,6 +207,10 @@ csa_status csa_check_device_status(void *stream);
  * ("tcgen05", "generic", ...).  Static string. */
 const char *csa_last_path(void);
 
+/* Message of the last CUDA runtime error that ended a call of this library with CSA_ERR_CUDA on this host
+ * thread ("no error" before the first).  Static string; not cleared by later successful calls. */
+const char *csa_last_cuda_error(void);
+
 /* Number of CUDA kernels this library has launched in the process so far (all devices, all threads). */
 uint64_t csa_kernel_launches(void);
 

@@ -73,6 +73,7 @@ for _name, _args, _res in [
      ctypes.c_int),
     ("csa_check_device_status", [_vp], ctypes.c_int),
     ("csa_last_path", [], ctypes.c_char_p),
+    ("csa_last_cuda_error", [], ctypes.c_char_p),
     ("csa_kernel_launches", [], ctypes.c_uint64),
     ("csa_status_string", [ctypes.c_int], ctypes.c_char_p),
 ]:
@@ -83,13 +84,16 @@ for _name, _args, _res in [
 EXPORTED = ("csa_topk_width", "csa_key_width", "csa_teacher_width", "csa_rows", "csa_compressed_rows",
             "csa_workspace_size", "csa_indexer_fwd", "csa_teacher", "csa_indexer_bwd", "csa_scores_debug",
             "csa_indexer_bwd_noalloc",
-            "csa_check_device_status", "csa_last_path", "csa_kernel_launches", "csa_status_string")
+            "csa_check_device_status", "csa_last_path", "csa_last_cuda_error", "csa_kernel_launches",
+            "csa_status_string")
 
 
 class CSAError(RuntimeError):
     def __init__(self, status: int, call: str):
         self.status = status
         msg = _lib.csa_status_string(status).decode()
+        if status == 5:  # CSA_ERR_CUDA
+            msg += " (" + _lib.csa_last_cuda_error().decode() + ")"
         super().__init__(f"{call}: {msg}")
 
 
@@ -317,6 +321,10 @@ def csa_check_device_status(device=None):
 
 def csa_last_path() -> str:
     return _lib.csa_last_path().decode()
+
+
+def csa_last_cuda_error() -> str:
+    return _lib.csa_last_cuda_error().decode()
 
 
 def csa_kernel_launches() -> int:

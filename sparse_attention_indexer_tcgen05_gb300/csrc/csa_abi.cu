@@ -142,9 +142,16 @@ inline csa_status need(const void *ptr, long long elems)
         if (_s != CSA_OK) return _s;                  \
     } while (0)
 
-#define CSA_CUDA(x)                                   \
-    do {                                              \
-        if ((x) != cudaSuccess) return CSA_ERR_CUDA;  \
+thread_local const char *t_last_cuda_error = "no error";
+
+// A failed CUDA call ends the entry point with CSA_ERR_CUDA and leaves its message for csa_last_cuda_error.
+#define CSA_CUDA(x)                                     \
+    do {                                                \
+        const cudaError_t csa_e_ = (x);                 \
+        if (csa_e_ != cudaSuccess) {                    \
+            t_last_cuda_error = cudaGetErrorString(csa_e_); \
+            return CSA_ERR_CUDA;                        \
+        }                                               \
     } while (0)
 
 int g_max_smem = -1;
@@ -403,13 +410,15 @@ csa_status csa_indexer_bwd(const csa_params *p, const void *q_idx, const float *
 csa_status csa_check_device_status(void *stream)
 {
     CSA_TRY(injected_fault());
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
+    CSA_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
     int flag = 0;
-    if (tc_read_clear_error(&flag) != cudaSuccess) return CSA_ERR_CUDA;
+    CSA_CUDA(tc_read_clear_error(&flag));
     return flag != 0 ? CSA_ERR_TIMEOUT : CSA_OK;
 }
 
 const char *csa_last_path(void) { return t_last_path; }
+
+const char *csa_last_cuda_error(void) { return t_last_cuda_error; }
 
 uint64_t csa_kernel_launches(void) { return (uint64_t)g_launches.load(std::memory_order_relaxed); }
 

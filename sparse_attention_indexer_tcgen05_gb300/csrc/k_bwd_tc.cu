@@ -339,21 +339,31 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ------------------------------------------------ MMA issuer
-            int hs = 0, ai = 0, xc = 0, gc = 0, dqc = 0;
-            auto mma2 = [&](int st, bool first) {
-                if (first) {
-                    wait_bar(dq_empty, (dqc & 1) ^ 1, abort_flag, err, 3);
-                    fence_after();
-                }
-                wait_bar(g_full, gc & 1, abort_flag, err, 4);
+            // A half-stage ring: tile t takes stages (st, st + 1), parity aph (R_ASTG is even).  The barriers of
+            // the next group are probed early (mbar_test, all at once) so that their shared-memory round trips
+            // overlap the MMAs issued in between; a probe that comes back false falls back to the bounded waits.
+            int st = 0, ai = 0, xc = 0, gc = 0, dqc = 0;
+            uint32_t aph = 0;
+            bool x_ready = false, g_ready = false;
+            auto probe_x = [&]() -> bool {
+                const bool r0 = mbar_test(x_empty + (xc & 1), ((xc >> 1) & 1) ^ 1);
+                const bool r1 = mbar_test(a_full + st, aph);
+                const bool r2 = mbar_test(a_full + st + 1, aph);
+                return r0 && r1 && r2;
+            };
+            auto mma2 = [&](int sp, bool first) {
+                if (first) wait_bar(dq_empty, (dqc & 1) ^ 1, abort_flag, err, 3);
+                if (!g_ready) wait_bar(g_full, gc & 1, abort_flag, err, 4);
+                x_ready = probe_x();  // the next X group (this item's next tile or the next item's first)
                 fence_after();
+                const unsigned char *pg = sG, *pk = sA + sp * HALF;
 #pragma unroll
                 for (int s = 0; s < 8; s++)
-                    mma_bf16(tDQ, desc_sw128(sG + s * 2048, HALF, 1024), desc_sw128(sA + st * HALF + s * 2048, HALF, 1024),
-                             IDESC_DQ, (first && s == 0) ? 0u : 1u);
+                    mma_bf16(tDQ, desc_sw128(pg + s * 2048, HALF, 1024), desc_sw128(pk + s * 2048, HALF, 1024), IDESC_DQ,
+                             (first && s == 0) ? 0u : 1u);
                 mma_commit(g_empty);
-                mma_commit(a_empty + st);
-                mma_commit(a_empty + st + 1);
+                mma_commit(a_empty + sp);
+                mma_commit(a_empty + sp + 1);
                 gc++;
             };
             for (int i = blockIdx.x; i < total; i += gridDim.x) {
@@ -362,27 +372,39 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const int bb = ai & 1;
                 wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, err, 5);
                 fence_after();
+                const unsigned char *pq = sB + bb * QBLK;
                 const int nt = (p.vmax + NKEY - 1) / NKEY;
                 int st_prev = 0;
                 for (int t = 0; t < nt; t++) {
-                    const int st = hs % R_ASTG;
                     const int tb = xc & 1;
-                    wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 6);
-                    wait_bar(a_full + st, (hs / R_ASTG) & 1, abort_flag, err, 7);
-                    wait_bar(a_full + st + 1, ((hs + 1) / R_ASTG) & 1, abort_flag, err, 7);
+                    if (!x_ready) x_ready = probe_x();
+                    if (!x_ready) {
+                        wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 6);
+                        wait_bar(a_full + st, aph, abort_flag, err, 7);
+                        wait_bar(a_full + st + 1, aph, abort_flag, err, 7);
+                    }
+                    x_ready = false;
+                    g_ready = t > 0 && mbar_test(g_full, gc & 1);  // the dQ group issued right after these MMAs
                     fence_after();
+                    const unsigned char *pk = sA + st * HALF;
 #pragma unroll
                     for (int kh = 0; kh < 2; kh++)
 #pragma unroll
                         for (int k4 = 0; k4 < 4; k4++)
-                            mma_bf16(tX + tb * 128, desc_kmajor(sA + (st + kh) * HALF + k4 * 32),
-                                     desc_kmajor(sB + bb * QBLK + kh * HALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
+                            mma_bf16(tX + tb * 128, desc_kmajor(pk + kh * HALF + k4 * 32), desc_kmajor(pq + kh * HALF + k4 * 32),
+                                     IDESC_X, (kh | k4) ? 1u : 0u);
                     mma_commit(x_full + tb);
                     xc++;
+                    const int st_cur = st;
+                    st += 2;
+                    if (st == R_ASTG) {
+                        st = 0;
+                        aph ^= 1u;
+                    }
                     if (t > 0) mma2(st_prev, t == 1);
-                    st_prev = st;
-                    hs += 2;
+                    st_prev = st_cur;
                 }
+                g_ready = false;
                 mma2(st_prev, nt == 1);
                 mma_commit(dq_full);
                 dqc++;
@@ -656,22 +678,29 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ------------------------------------------------ MMA issuer
-            int uc = 0, qs = 0, xc = 0, gkc = 0, dkc = 0;
-            auto mma3 = [&](int bs, bool first) {
-                if (first) {
-                    wait_bar(dk_empty, (dkc & 1) ^ 1, abort_flag, err, 23);
-                    fence_after();
-                }
+            // q-block ring position (bs, parity bph).  The next group's barriers are probed early, as in the
+            // row-owner kernel.
+            int uc = 0, bs = 0, xc = 0, gkc = 0, dkc = 0;
+            uint32_t bph = 0;
+            bool x_ready = false, g_ready = false;
+            auto probe_x = [&]() -> bool {
+                const bool r0 = mbar_test(x_empty + (xc & 1), ((xc >> 1) & 1) ^ 1);
+                const bool r1 = mbar_test(b_full + bs, bph);
+                return r0 && r1;
+            };
+            auto mma3 = [&](int bp, bool first) {
+                if (first) wait_bar(dk_empty, (dkc & 1) ^ 1, abort_flag, err, 23);
                 const int gkb = gkc & 1;
-                wait_bar(gk_full + gkb, (gkc >> 1) & 1, abort_flag, err, 24);
+                if (!g_ready) wait_bar(gk_full + gkb, (gkc >> 1) & 1, abort_flag, err, 24);
+                x_ready = probe_x();
                 fence_after();
+                const unsigned char *pg = sG + gkb * QBLK, *pq = sB + bp * QBLK;
 #pragma unroll
                 for (int s = 0; s < 8; s++)
-                    mma_bf16(tDK, desc_kmajor(sG + gkb * QBLK + (s >> 2) * HALF + (s & 3) * 32),
-                             desc_sw128(sB + bs * QBLK + s * 2048, HALF, 1024), IDESC_DK,
-                             (first && s == 0) ? 0u : 1u);
+                    mma_bf16(tDK, desc_kmajor(pg + (s >> 2) * HALF + (s & 3) * 32), desc_sw128(pq + s * 2048, HALF, 1024),
+                             IDESC_DK, (first && s == 0) ? 0u : 1u);
                 mma_commit(gk_empty + gkb);
-                mma_commit(b_empty + bs);
+                mma_commit(b_empty + bp);
                 gkc++;
             };
             for (int u = blockIdx.x; u < total; u += gridDim.x) {
@@ -681,23 +710,33 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
                 fence_after();
                 int bs_prev = 0;
                 for (int pi = 0; pi < U.npairs; pi++) {
-                    const int bs = qs % K_BSTG;
                     const int tb = xc & 1;
-                    wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 26);
-                    wait_bar(b_full + bs, (qs / K_BSTG) & 1, abort_flag, err, 27);
+                    if (!x_ready) x_ready = probe_x();
+                    if (!x_ready) {
+                        wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 26);
+                        wait_bar(b_full + bs, bph, abort_flag, err, 27);
+                    }
+                    x_ready = false;
+                    g_ready = pi > 0 && mbar_test(gk_full + (gkc & 1), (gkc >> 1) & 1);
                     fence_after();
+                    const unsigned char *pq = sB + bs * QBLK;
 #pragma unroll
                     for (int kh = 0; kh < 2; kh++)
 #pragma unroll
                         for (int k4 = 0; k4 < 4; k4++)
-                            mma_bf16(tX + tb * 128, desc_kmajor(sA + kh * HALF + k4 * 32),
-                                     desc_kmajor(sB + bs * QBLK + kh * HALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
+                            mma_bf16(tX + tb * 128, desc_kmajor(sA + kh * HALF + k4 * 32), desc_kmajor(pq + kh * HALF + k4 * 32),
+                                     IDESC_X, (kh | k4) ? 1u : 0u);
                     mma_commit(x_full + tb);
                     xc++;
+                    const int bs_cur = bs;
+                    if (++bs == K_BSTG) {
+                        bs = 0;
+                        bph ^= 1u;
+                    }
                     if (pi > 0) mma3(bs_prev, pi == 1);
-                    bs_prev = bs;
-                    qs++;
+                    bs_prev = bs_cur;
                 }
+                g_ready = false;
                 mma3(bs_prev, U.npairs == 1);
                 mma_commit(dk_full);
                 mma_commit(a_empty);

@@ -28,6 +28,7 @@
 // csa_check_device_status), stops waiting (so every role still runs its loops to the end with uniform
 // control flow), drains its own TMA copies and MMAs with timer-bounded waits, frees TMEM and returns.
 #include "csa_tc.cuh"
+#include "tc_ptx.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -57,6 +58,8 @@ cudaError_t tc_read_clear_error(int *flag)
 
 namespace tcs {
 
+using namespace ptx;
+
 constexpr int ROWS = 4;                       // query rows per work item
 constexpr int HI = 64, DI = 128;              // indexer heads / dim taken by this kernel
 constexpr int NKEY = 128;                     // keys per tile (MMA M)
@@ -78,12 +81,7 @@ constexpr int OFF_MISC = OFF_W + ROWS * HI * 4;            // 209 KB
 constexpr int SMEM_BYTES = OFF_MISC + 1024;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;              // slack to align the base to 1024 B
 
-constexpr long long kTimeoutCycles = 4000000000LL;         // ~2 s at 2 GHz
-
-// instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16 (10-12 = 1), both
-// K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NCOL >> 3) << 17) |
-                           ((uint32_t)(NKEY >> 4) << 24);
+constexpr uint32_t IDESC = idesc_bf16(NKEY, NCOL, false, false);  // A, B both K-major
 
 struct Args {
     Geo g;
@@ -95,113 +93,6 @@ struct Args {
     const int *cu_g;     // THD: work-item offsets per segment [nseg+1]
     int total;           // SBHD/BSHD: number of work items (THD: read from cu_g[nseg])
 };
-
-// ------------------------------------------------------------------ PTX wrappers
-
-__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *b)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(su32(b)), "r"(parity)
-                 : "memory");
-    return ok != 0;
-}
-
-// Bounded wait.  Once any role has given up (abort set), waits return at once so that control flow stays
-// uniform and the kernel runs to its end.
-__device__ __forceinline__ void wait_bar(uint64_t *b, uint32_t parity, volatile int *abort_flag, int site)
-{
-    if (*abort_flag) return;
-    if (mbar_try(b, parity)) return;
-    const long long t0 = clock64();
-    while (!mbar_try(b, parity)) {
-        if (*abort_flag) return;
-        if (clock64() - t0 > kTimeoutCycles) {
-            *abort_flag = 1;
-            atomicExch(&g_tc_error, site);
-            return;
-        }
-    }
-}
-
-// Timer-only bounded wait (used to drain our own copies / MMAs even after an abort).
-__device__ __forceinline__ void drain_bar(uint64_t *b, uint32_t parity)
-{
-    const long long t0 = clock64();
-    while (!mbar_try(b, parity))
-        if (clock64() - t0 > kTimeoutCycles) {
-            atomicExch(&g_tc_error, 99);
-            return;
-        }
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y)
-{
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-                 ::"r"(su32(dst)), "l"(map), "r"(su32(bar)), "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z)
-{
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
-                 ::"r"(su32(dst)), "l"(map), "r"(su32(bar)), "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle (8-row atoms of 1024 B, SBO = 1024 B).
-__device__ __forceinline__ uint64_t sdesc(const void *p)
-{
-    const uint64_t a = su32(p);
-    return ((a & 0x3FFFFull) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(IDESC), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_commit(uint64_t *bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
-{
-    uint32_t r[32];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-                 : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 // ------------------------------------------------------------------ work items
 
@@ -443,7 +334,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 const Item it = decode_item(a, i, total);
                 if (it.vmax == 0) continue;
                 const int bb = ai & 1;
-                wait_bar(b_empty + bb, ((ai >> 1) & 1) ^ 1, abort_flag, 1);
+                wait_bar(b_empty + bb, ((ai >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 1);
                 mbar_expect_tx(b_full + bb, B_BUF);
                 for (int k = 0; k < ROWS; k++) {
                     const long long row = k < it.n ? it.row[k] : it.row[0];
@@ -457,7 +348,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 for (int t = 0; t < nt; t++)
                     for (int kh = 0; kh < 2; kh++) {
                         const int st = hs % A_STAGES;
-                        wait_bar(a_empty + st, ((hs / A_STAGES) & 1) ^ 1, abort_flag, 2);
+                        wait_bar(a_empty + st, ((hs / A_STAGES) & 1) ^ 1, abort_flag, &g_tc_error, 2);
                         mbar_expect_tx(a_full + st, A_HALF);
                         if (sbhd)
                             tma_load_3d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, it.b, t * NKEY);
@@ -469,37 +360,48 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             }
             // our own copies must land before the CTA exits
             for (int st = 0; st < A_STAGES; st++)
-                if (last_hs[st] >= 0) drain_bar(a_full + st, (last_hs[st] / A_STAGES) & 1);
+                if (last_hs[st] >= 0) drain_bar(a_full + st, (last_hs[st] / A_STAGES) & 1, &g_tc_error);
             for (int bb = 0; bb < 2; bb++)
-                if (last_ai[bb] >= 0) drain_bar(b_full + bb, (last_ai[bb] >> 1) & 1);
+                if (last_ai[bb] >= 0) drain_bar(b_full + bb, (last_ai[bb] >> 1) & 1, &g_tc_error);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            int hs = 0, ai = 0, tc = 0;
+            // A-stage ring position (st, parity aph).  The full barrier of the next stage and the empty barrier
+            // of the next accumulator are probed early (mbar_test) so that their shared-memory round trips
+            // overlap the MMAs issued in between; a probe that comes back false falls back to the wait.
+            int st = 0, ai = 0, tc = 0;
+            uint32_t aph = 0;
+            bool a_ready = false, t_ready = false;
             for (int i = blockIdx.x; i < total; i += gridDim.x) {
                 const Item it = decode_item(a, i, total);
                 if (it.vmax == 0) continue;
                 const int bb = ai & 1;
-                wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, 3);
+                wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, &g_tc_error, 3);
                 fence_after();
                 const int nt = (it.vmax + NKEY - 1) / NKEY;
+                const unsigned char *pb0 = sB + bb * B_BUF;
                 for (int t = 0; t < nt; t++) {
                     const int tb = tc & 1;
-                    wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, 4);
+                    if (!t_ready) wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 4);
                     fence_after();
                     const uint32_t d = tmem + (uint32_t)(tb * NCOL);
+#pragma unroll
                     for (int kh = 0; kh < 2; kh++) {
-                        const int st = hs % A_STAGES;
-                        wait_bar(a_full + st, (hs / A_STAGES) & 1, abort_flag, 5);
+                        if (!a_ready) wait_bar(a_full + st, aph, abort_flag, &g_tc_error, 5);
+                        const int st1 = st + 1 == A_STAGES ? 0 : st + 1;
+                        const uint32_t ph1 = st1 == 0 ? aph ^ 1u : aph;
+                        a_ready = mbar_test(a_full + st1, ph1);
+                        if (kh == 1) t_ready = mbar_test(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1);
                         fence_after();
                         const unsigned char *pa = sA + st * A_HALF;
-                        const unsigned char *pb = sB + bb * B_BUF + kh * B_HALF;
+                        const unsigned char *pb = pb0 + kh * B_HALF;
 #pragma unroll
                         for (int k = 0; k < 4; k++)
-                            mma_bf16(d, sdesc(pa + k * 32), sdesc(pb + k * 32), (kh | k) != 0);
+                            mma_bf16(d, desc_kmajor(pa + k * 32), desc_kmajor(pb + k * 32), IDESC, (kh | k) != 0);
                         mma_commit(a_empty + st);
-                        hs++;
+                        st = st1;
+                        aph = ph1;
                     }
                     mma_commit(t_full + tb);
                     tc++;
@@ -508,7 +410,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 ai++;
             }
             mma_commit(mma_done);
-            drain_bar(mma_done, 0);
+            drain_bar(mma_done, 0, &g_tc_error);
         }
     } else {
         // ---------------------------------------------------------- epilogue + selection (warps 2..9)
@@ -533,7 +435,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             const int nt = (it.vmax + NKEY - 1) / NKEY;
             for (int t = 0; t < nt; t++) {
                 const int tb = tc & 1;
-                wait_bar(t_full + tb, (tc >> 1) & 1, abort_flag, 6);
+                wait_bar(t_full + tb, (tc >> 1) & 1, abort_flag, &g_tc_error, 6);
                 fence_after();
                 const int j = t * NKEY + quad * 32 + lane;
 #pragma unroll

@@ -8,7 +8,9 @@
 //
 // Mapping (bf16, H = 64 heads, D in {64, 128, 192}).  A work item is 2 consecutive query rows of one sequence.
 // The MMA computes D[(row, h), key] = q[row, h] . key with M = 2 rows x 64 heads = 128 (A = the item's q rows,
-// K-major, resident), N = 128 keys (B = a tile of kv_c or of the window's kv rows, K-major, TMA), K = D.  With
+// K-major, resident), N = 256 keys (B = a tile of kv_c or of the window's kv rows, K-major, TMA), K = D.  N = 256
+// keeps the single issuing thread ahead of the tensor core: one MMA runs 128 cycles, about twice what the thread
+// needs to issue it together with its share of the barrier traffic.  With
 // (row, head) on TMEM lanes each epilogue thread owns one head of one row, so the per-head log-sum-exp is an
 // in-register online max/sum over the key columns.  The keys are taken densely per tile (every visible
 // compressed key, every window position) and masked by the row's selection and window.
@@ -16,8 +18,9 @@
 //   pass 2: compressed tiles again -> exp(c - l_h) on selected keys, summed over the 64 heads of a row by a
 //           warp reduce-scatter (31 shuffles per 32 columns) into shared per-key T rows; then the L1
 //           normalisation and the write-out in the id slot order.
-// Roles: warp 0 TMA, warp 1 TMEM + MMA issue, warps 4..11 epilogue (two warps per TMEM lane quadrant, each
-// with half of the 128 key columns).  Waits are bounded as in the other tensor-core kernels.
+// Roles: warp 0 TMA, warp 1 TMEM (two 256-column accumulators) + MMA issue, warps 2..17 epilogue (four warps
+// per TMEM lane quadrant, each with a quarter of the 256 key columns).  Waits are bounded as in the other
+// tensor-core kernels.
 #include "csa_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -40,22 +43,23 @@ namespace teach {
 
 using namespace ptx;
 
-constexpr int H = 64, RP = 2, M = RP * H, NK = 128;
-constexpr int KB = NK * 64 * 2;                 // 16 KB: one 64-wide K-block of a 128-row tile
+constexpr int H = 64, RP = 2, M = RP * H, NK = 256;
+constexpr int QKB = M * 64 * 2;                 // 16 KB: one 64-wide K-block of the item's 128 (row, head) q rows
+constexpr int KB = NK * 64 * 2;                 // 32 KB: one 64-wide K-block of a 256-key tile
 constexpr int MAXKB = 3;                        // D <= 192
-constexpr int QBUF = MAXKB * KB;                // 48 KB: the item's q rows
-constexpr int BSTG = 6;                         // key K-block stages
+constexpr int QBUF = MAXKB * QKB;               // 48 KB: the item's q rows
+constexpr int BSTG = 3;                         // key K-block stages
 constexpr int NCMAX = 1024;
-constexpr int THREADS = 384, EPI = 256;
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t IDESC = idesc_bf16(128, 128, false, false);
+constexpr int THREADS = 576, EPI = 512;
+constexpr uint32_t TMEM_COLS = 512;             // two 256-column fp32 accumulators
+constexpr uint32_t IDESC = idesc_bf16(128, NK, false, false);
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_B = OFF_Q + 2 * QBUF;                     // 96 KB
 constexpr int OFF_T = OFF_B + BSTG * KB;                    // 192 KB: 2 rows x NCMAX fp32
 constexpr int OFF_SEL = OFF_T + RP * NCMAX * 4;             // 200 KB: selection bit words, 2 rows x NCMAX bits
-constexpr int OFF_PART = OFF_SEL + RP * NCMAX;              // 202 KB: 2 halves x 128 x (m, s)
-constexpr int OFF_RED = OFF_PART + 2 * M * 8;               // 8 warps
+constexpr int OFF_PART = OFF_SEL + RP * NCMAX;              // 4 column quarters x 128 x (m, s)
+constexpr int OFF_RED = OFF_PART + 4 * M * 8;               // 16 epilogue warps
 constexpr int OFF_MISC = OFF_RED + 64;
 constexpr int SMEM = OFF_MISC + 1024 + 1024;
 
@@ -163,6 +167,7 @@ __device__ __forceinline__ int item_total(const Args &a)
 // tile tt of an item: window tiles, then compressed tiles (pass 1), then compressed tiles again (pass 2)
 __device__ __forceinline__ int ntiles(const Item &it) { return it.nw + 2 * it.nct; }
 
+// 18 warps: 5 on some of the SM's four schedulers, whose 16 K-register files then cap a thread at 96 registers
 __global__ void __launch_bounds__(THREADS, 1)
 teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                   const __grid_constant__ CUtensorMap map_kvc, Args a)
@@ -193,7 +198,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             mbar_init(q_full + i, 1);
             mbar_init(q_empty + i, 1);
             mbar_init(t_full + i, 1);
-            mbar_init(t_empty + i, 8);
+            mbar_init(t_empty + i, EPI / 32);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -217,10 +222,10 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 if (it.vmax == 0) continue;
                 const int qb = ai & 1;
                 wait_bar(q_empty + qb, ((ai >> 1) & 1) ^ 1, abort_flag, err, 41);
-                mbar_expect_tx(q_full + qb, (uint32_t)(nkb * KB));
+                mbar_expect_tx(q_full + qb, (uint32_t)(nkb * QKB));
                 for (int r = 0; r < RP; r++)
                     for (int kb = 0; kb < nkb; kb++)
-                        tma_load_3d(sQ + qb * QBUF + kb * KB + r * (H * 128), &map_q, q_full + qb, kb * 64, 0,
+                        tma_load_3d(sQ + qb * QBUF + kb * QKB + r * (H * 128), &map_q, q_full + qb, kb * 64, 0,
                                     (int)(r == 0 ? it.row0 : it.row1));
                 last_ai[qb] = ai;
                 ai++;
@@ -253,28 +258,50 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
     } else if (warp == 1) {
         if (lane == 0) {  // ------------------------------------------------ MMA issuer
-            int hs = 0, ai = 0, tc = 0;
+            // B-stage ring position (st, parity bph).  A barrier probe costs the issuing thread a shared-memory
+            // round trip, so the barriers of a whole tile (its accumulator and its nkb B stages) are probed
+            // together, once per 4 nkb MMAs; only those not yet complete are then waited on.
+            int st = 0, ai = 0, tc = 0;
+            uint32_t bph = 0;
             for (int i = blockIdx.x; i < total; i += gridDim.x) {
                 const Item it = decode(a, i, total);
                 if (it.vmax == 0) continue;
                 const int qb = ai & 1;
                 wait_bar(q_full + qb, (ai >> 1) & 1, abort_flag, err, 43);
                 fence_after();
+                const unsigned char *pq = sQ + qb * QBUF;
                 const int nt = ntiles(it);
                 for (int tt = 0; tt < nt; tt++) {
                     const int tb = tc & 1;
-                    wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, err, 44);
+                    int sk[MAXKB];
+                    uint32_t pk[MAXKB];
+                    bool rk[MAXKB];
+                    const uint32_t tpar = ((tc >> 1) & 1) ^ 1;
+                    const bool rt = mbar_test(t_empty + tb, tpar);
+#pragma unroll
+                    for (int kb = 0; kb < MAXKB; kb++) {
+                        sk[kb] = st;
+                        pk[kb] = bph;
+                        rk[kb] = kb < nkb ? mbar_test(b_full + st, bph) : true;
+                        if (kb < nkb && ++st == BSTG) {
+                            st = 0;
+                            bph ^= 1u;
+                        }
+                    }
+                    if (!rt) wait_bar(t_empty + tb, tpar, abort_flag, err, 44);
+#pragma unroll
+                    for (int kb = 0; kb < MAXKB; kb++)
+                        if (!rk[kb]) wait_bar(b_full + sk[kb], pk[kb], abort_flag, err, 45);
                     fence_after();
-                    for (int kb = 0; kb < nkb; kb++) {
-                        const int st = hs % BSTG;
-                        wait_bar(b_full + st, (hs / BSTG) & 1, abort_flag, err, 45);
-                        fence_after();
+                    const uint32_t d = tmem + tb * NK;
+#pragma unroll
+                    for (int kb = 0; kb < MAXKB; kb++) {
+                        if (kb >= nkb) break;
+                        const unsigned char *pa = pq + kb * QKB, *pb = sB + sk[kb] * KB;
 #pragma unroll
                         for (int k4 = 0; k4 < 4; k4++)
-                            mma_bf16(tmem + tb * NK, desc_kmajor(sQ + qb * QBUF + kb * KB + k4 * 32),
-                                     desc_kmajor(sB + st * KB + k4 * 32), IDESC, (kb | k4) ? 1u : 0u);
-                        mma_commit(b_empty + st);
-                        hs++;
+                            mma_bf16(d, desc_kmajor(pa + k4 * 32), desc_kmajor(pb + k4 * 32), IDESC, (kb | k4) ? 1u : 0u);
+                        mma_commit(b_empty + sk[kb]);
                     }
                     mma_commit(t_full + tb);
                     tc++;
@@ -285,12 +312,16 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             mma_commit(mma_done);
             drain_bar(mma_done, 0, err);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 2) {
         // ---------------------------------------------------------------- epilogue
-        const int e = warp - 4, quad = warp & 3, half = e >> 2, et = threadIdx.x - 128;
+        // 16 warps: four per TMEM lane quadrant (warp % 4), warp cq = (warp - 2) / 4 of a quadrant reads the
+        // 64 key columns [64 cq, 64 cq + 64) of every tile.
+        const int e = warp - 2, quad = warp & 3, cq = e >> 2, et = threadIdx.x - 64;
         const int rh = quad * 32 + lane;      // (row, head) of this thread's TMEM lane
         const int i_row = rh >> 6, h = rh & 63;
         const float s2 = g.scale * 1.4426950408889634f;  // logits in log2 units: exp(c) = 2^(x * sigma * log2 e)
+        const bool s2_pos = s2 > 0.f;  // then max(x s2) = s2 max(x): the scale folds into one FFMA per element
+        const int cb = cq * 64;
         int tc = 0;
         for (int it_i = blockIdx.x; it_i < total; it_i += gridDim.x) {
             const Item it = decode(a, it_i, total);
@@ -300,7 +331,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             named_bar(1, EPI);
             for (int x = et; x < RP * NCMAX; x += EPI) sT[x] = 0.f;
             if (et < RP * NCMAX / 32) sMask[et] = 0u;
-            // this thread's id slots s = et + 256 q of both rows, loaded together and kept for the write-out
+            // this thread's id slots s = et + EPI q of both rows, loaded together and kept for the write-out
             constexpr int NQ = NCMAX / EPI;
             int32_t idr[RP][NQ];
 #pragma unroll
@@ -341,25 +372,29 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const bool pass2 = tt >= it.nw + it.nct;
                 const int t = win ? tt : (tt - it.nw) % it.nct;
                 if (pass2 && tt == it.nw + it.nct) {
-                    // l_h (log2 units) from both column halves, combined in a fixed order, and the sink
-                    sPart[half * M + rh] = make_float2(m, ssum);
+                    // l_h (log2 units) from the four column quarters, combined in a fixed order, and the sink
+                    sPart[cq * M + rh] = make_float2(m, ssum);
                     named_bar(1, EPI);
-                    const float2 p0 = sPart[rh], p1 = sPart[M + rh];
+                    float2 p[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) p[k] = sPart[k * M + rh];
                     const float ah = __ldg(a.sink + h) * 1.4426950408889634f;
-                    const float mm = fmaxf(fmaxf(p0.x, p1.x), ah);
+                    const float mm = fmaxf(fmaxf(fmaxf(p[0].x, p[1].x), fmaxf(p[2].x, p[3].x)), ah);
                     float S = 0.f;
                     if (mm != -INFINITY) {
-                        if (p0.x != -INFINITY) S += p0.y * ex2(p0.x - mm);
-                        if (p1.x != -INFINITY) S += p1.y * ex2(p1.x - mm);
+#pragma unroll
+                        for (int k = 0; k < 4; k++)
+                            if (p[k].x != -INFINITY) S += p[k].y * ex2(p[k].x - mm);
                         if (ah != -INFINITY) S += ex2(ah - mm);
                     }
                     ell = mm + lg2(S);
                 }
-                // mask words of this thread's two 32-column chunks
+                // mask words of this warp's two 32-column chunks; they depend only on the warp's row, so the
+                // skip of an all-masked sub-chunk and the full-word fast paths below are warp-uniform
                 uint32_t mw[2];
 #pragma unroll
                 for (int c = 0; c < 2; c++) {
-                    const int col0 = half * 64 + c * 32;
+                    const int col0 = cb + c * 32;
                     if (win) {
                         const int pbase = it.p_lo + t * NK + col0;
                         mw[c] = row_ok ? range_bits(s_me - g.window + 1 - pbase, s_me - pbase) : 0u;
@@ -368,55 +403,68 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                         mw[c] = j0 < NCMAX ? (sMask[i_row * (NCMAX / 32) + (j0 >> 5)] & range_bits(0, vme - 1 - j0)) : 0u;
                     }
                 }
-                float x[2][32];
+                if ((mw[0] | mw[1]) != 0u) {
+                    if (!pass2) {
+                        // online max / sum, one 32-column chunk at a time
+#pragma unroll 1
+                        for (int c = 0; c < 2; c++) {
+                            if (mw[c] == 0u) continue;
+                            float x[32];
+                            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + cb + c * 32), x);
+                            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                            if (s2_pos) {
+                                if (mw[c] != 0xffffffffu) {
 #pragma unroll
-                for (int c = 0; c < 2; c++)
-                    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + half * 64 + c * 32), x[c]);
-                if (!pass2) {
-                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                                    for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? x[q] : -INFINITY;
+                                }
 #pragma unroll
-                    for (int c = 0; c < 2; c++)
+                                for (int q = 0; q < 32; q++) mx[q & 3] = fmaxf(mx[q & 3], x[q]);
+                            } else {
 #pragma unroll
-                        for (int q = 0; q < 32; q++) {
-                            x[c][q] = (mw[c] >> q) & 1u ? x[c][q] * s2 : -INFINITY;
-                            mx[q & 3] = fmaxf(mx[q & 3], x[c][q]);
-                        }
-                    const float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                    if (cm != -INFINITY) {
-                        if (cm > m) {
-                            ssum *= ex2(m - cm);
-                            m = cm;
-                        }
-                        float sm[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int c = 0; c < 2; c++)
-#pragma unroll
-                            for (int q = 0; q < 32; q++) sm[q & 3] += ex2(x[c][q] - m);
-                        ssum += (sm[0] + sm[1]) + (sm[2] + sm[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 2; c++)
-#pragma unroll
-                        for (int q = 0; q < 32; q++) x[c][q] = (mw[c] >> q) & 1u ? ex2(fmaf(x[c][q], s2, -ell)) : 0.f;
-                    // sum over the 32 heads of this warp, both chunks interleaved: reduce-scatter, lane l ends
-                    // with column (chunk base + l)
-#pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) {
-                        const bool up = (lane & off) != 0;
-#pragma unroll
-                        for (int q = 0; q < off; q++)
-#pragma unroll
-                            for (int c = 0; c < 2; c++) {
-                                const float send = up ? x[c][q] : x[c][q + off];
-                                const float keep = up ? x[c][q + off] : x[c][q];
-                                x[c][q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                for (int q = 0; q < 32; q++) {
+                                    x[q] = (mw[c] >> q) & 1u ? x[q] * s2 : -INFINITY;
+                                    mx[q & 3] = fmaxf(mx[q & 3], x[q]);
+                                }
                             }
-                    }
+                            float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                            if (s2_pos) cm *= s2;
+                            if (cm > m) {  // cm is finite: the chunk holds at least one unmasked column
+                                ssum *= ex2(m - cm);
+                                m = cm;
+                            }
+                            const float sc = s2_pos ? s2 : 1.f;
+                            float sm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int c = 0; c < 2; c++) {
-                        const int j = t * NK + half * 64 + c * 32 + lane;
-                        if (j < NCMAX && x[c][0] != 0.f) atomicAdd(sT + i_row * NCMAX + j, x[c][0]);
+                            for (int q = 0; q < 32; q++) sm[q & 3] += ex2(fmaf(x[q], sc, -m));
+                            ssum += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int c = 0; c < 2; c++) {
+                            if (mw[c] == 0u) continue;
+                            float x[32];
+                            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + cb + c * 32), x);
+                            if (mw[c] == 0xffffffffu) {
+#pragma unroll
+                                for (int q = 0; q < 32; q++) x[q] = ex2(fmaf(x[q], s2, -ell));
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? ex2(fmaf(x[q], s2, -ell)) : 0.f;
+                            }
+                            // sum over the 32 heads of this warp: reduce-scatter, lane l ends with column c0 + l
+#pragma unroll
+                            for (int off = 16; off >= 1; off >>= 1) {
+                                const bool up = (lane & off) != 0;
+#pragma unroll
+                                for (int q = 0; q < off; q++) {
+                                    const float send = up ? x[q] : x[q + off];
+                                    const float keep = up ? x[q + off] : x[q];
+                                    x[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                }
+                            }
+                            const int j = t * NK + cb + c * 32 + lane;
+                            if (j < NCMAX && x[0] != 0.f) atomicAdd(sT + i_row * NCMAX + j, x[0]);
+                        }
                     }
                 }
                 fence_before();
@@ -425,25 +473,29 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 tc++;
             }
             named_bar(1, EPI);
-            // ---- L1 normalisation and write-out, one row per 128 threads
-            const int r = et >> 7, rt = et & 127;
+            // ---- L1 normalisation and write-out, one row per 256 threads (warps 8 r .. 8 r + 7)
+            const int r = et >> 8, rt = et & 255;
             const int v = r == 0 ? it.v0 : it.v1;
             float part = 0.f;
-            for (int j = rt; j < v; j += 128) part += sT[r * NCMAX + j];
+            for (int j = rt; j < v; j += 256) part += sT[r * NCMAX + j];
             part = warp_sum(part);
             if (lane == 0) sRed[et >> 5] = part;
             named_bar(1, EPI);
-            float S = sRed[r * 4] + sRed[r * 4 + 1] + sRed[r * 4 + 2] + sRed[r * 4 + 3];
-            const float inv = 1.f / fmaxf(S, 1e-10f);
+            float Sr[RP];
+#pragma unroll
+            for (int rr = 0; rr < RP; rr++) {
+                float acc = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; k++) acc += sRed[rr * 8 + k];
+                Sr[rr] = acc;
+            }
             if (g.sparse) {
-                // write-out with the slot mapping of the set-up: slots et + 256 q of both rows
-                const float S0 = sRed[0] + sRed[1] + sRed[2] + sRed[3];
-                const float S1 = sRed[4] + sRed[5] + sRed[6] + sRed[7];
+                // write-out with the slot mapping of the set-up: slots et + EPI q of both rows
 #pragma unroll
                 for (int rr = 0; rr < RP; rr++) {
                     if (rr >= it.n) continue;
                     const int vr = rr == 0 ? it.v0 : it.v1;
-                    const float ir = 1.f / fmaxf(rr == 0 ? S0 : S1, 1e-10f);
+                    const float ir = 1.f / fmaxf(Sr[rr], 1e-10f);
                     const long long row = rr == 0 ? it.row0 : it.row1;
                     float *trow = a.teacher + row * g.TW;
 #pragma unroll
@@ -455,13 +507,13 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     }
                 }
             } else if (r < it.n) {
+                const float inv = 1.f / fmaxf(Sr[r], 1e-10f);
                 const long long row = r == 0 ? it.row0 : it.row1;
                 float *trow = a.teacher + row * g.TW;
-                for (int j = rt; j < g.TW; j += 128) trow[j] = j < v ? sT[r * NCMAX + j] * inv : 0.f;
+                for (int j = rt; j < g.TW; j += 256) trow[j] = j < v ? sT[r * NCMAX + j] * inv : 0.f;
             }
         }
     }
-
     fence_before();
     __syncthreads();
     fence_after();

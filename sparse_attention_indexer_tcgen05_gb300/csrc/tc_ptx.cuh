@@ -35,6 +35,18 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity)
                  : "memory");
     return ok != 0;
 }
+// Non-blocking probe of a phase.  Its result is consumed later, so an MMA issuer can overlap the barrier's
+// shared-memory round trip with the tensor work it issues in between.
+__device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(su32(b)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void init_fence()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -44,11 +56,13 @@ __device__ __forceinline__ void init_fence()
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Bounded wait.  Once any role has given up (abort set), waits return at once so control flow stays
-// uniform and the kernel runs to its end; `err` receives the site code of the first expiry.
+// uniform and the kernel runs to its end; `err` receives the site code of the first expiry.  The phase is
+// tried before the abort flag is read: on the fast path the flag's load latency would sit in the MMA
+// issuer's critical path.
 __device__ __forceinline__ void wait_bar(uint64_t *b, uint32_t parity, volatile int *abort_flag, int *err, int site)
 {
-    if (*abort_flag) return;
     if (mbar_try(b, parity)) return;
+    if (*abort_flag) return;
     const long long t0 = clock64();
     while (!mbar_try(b, parity)) {
         if (*abort_flag) return;
