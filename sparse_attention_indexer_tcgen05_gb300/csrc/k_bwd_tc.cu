@@ -50,16 +50,16 @@ constexpr int THREADS = 384;
 constexpr int EPI = 256;
 constexpr int CH = 128;                        // rows per key-owner unit
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC_X = idesc_bf16(128, 128, false, false);   // X = k . q^T
-constexpr uint32_t IDESC_DQ = idesc_bf16(128, 128, true, true);    // dQ' += G'^T k  (both MN-major)
+constexpr uint32_t IDESC_X = idesc_bf16(128, 128, false, false);   // X = k . q^T (key-owner), X^T = q . k^T
+constexpr uint32_t IDESC_DQ = idesc_bf16(128, 128, false, true);   // dQ' += G'^T k  (A in TMEM, B MN-major)
 constexpr uint32_t IDESC_DK = idesc_bf16(128, 128, false, true);   // dK += G q      (B MN-major)
 
 // row-owner shared memory
-constexpr int R_ASTG = 6;
+constexpr int R_ASTG = 8;                                     // k-tile halves: four tiles in flight
+static_assert((2 * R_ASTG + 19) * 8 <= 512, "row-owner barriers overlap the TMEM slot");
 constexpr int R_OFF_A = 0;
-constexpr int R_OFF_B = R_OFF_A + R_ASTG * HALF;              // 96 KB
-constexpr int R_OFF_G = R_OFF_B + 2 * QBLK;                   // 160 KB
-constexpr int R_OFF_GD = R_OFF_G + QBLK;                      // 192 KB: 2 bufs x 2 rows x NCMAX fp32
+constexpr int R_OFF_B = R_OFF_A + R_ASTG * HALF;              // 128 KB: the q tiles of two items
+constexpr int R_OFF_GD = R_OFF_B + 2 * QBLK;                  // 192 KB: 2 bufs x 2 rows x NCMAX fp32
 constexpr int R_OFF_W = R_OFF_GD + 2 * RP * NCMAX * 4;        // 208 KB: 2 bufs x 2 rows x 64 fp32
 constexpr int R_OFF_DW = R_OFF_W + 2 * RP * HI * 4;           // 128 fp32
 constexpr int R_OFF_MISC = R_OFF_DW + 2 * RP * HI * 4;      // sDW double-buffered by item parity
@@ -257,17 +257,16 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem + R_OFF_A;
     unsigned char *sB = smem + R_OFF_B;
-    unsigned char *sG = smem + R_OFF_G;
     float *sGD = reinterpret_cast<float *>(smem + R_OFF_GD);
     float *sW = reinterpret_cast<float *>(smem + R_OFF_W);
     float *sDW = reinterpret_cast<float *>(smem + R_OFF_DW);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + R_OFF_MISC);
-    uint64_t *a_full = bars, *a_empty = bars + 6, *b_full = bars + 12, *b_empty = bars + 14;
-    uint64_t *x_full = bars + 16, *x_empty = bars + 18, *g_full = bars + 20, *g_empty = bars + 21;
-    uint64_t *dq_full = bars + 22, *dq_empty = bars + 23, *gd_full = bars + 24, *gd_empty = bars + 26;
-    uint64_t *mma_done = bars + 28;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + R_OFF_MISC + 256);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + R_OFF_MISC + 264);
+    uint64_t *a_full = bars, *a_empty = bars + R_ASTG, *b_full = bars + 2 * R_ASTG, *b_empty = b_full + 2;
+    uint64_t *x_full = b_full + 4, *x_empty = b_full + 6, *g_full = b_full + 8, *g_empty = b_full + 10;
+    uint64_t *dq_full = b_full + 12, *dq_empty = b_full + 13, *gd_full = b_full + 14, *gd_empty = b_full + 16;
+    uint64_t *mma_done = b_full + 18;                                  // 2 R_ASTG + 19 barriers < 512 B
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + R_OFF_MISC + 512);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + R_OFF_MISC + 520);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geo &g = a.g;
@@ -284,8 +283,10 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             mbar_init(gd_full + i, 1);
             mbar_init(gd_empty + i, 8);
         }
-        mbar_init(g_full, 8);
-        mbar_init(g_empty, 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(g_full + i, 8);
+            mbar_init(g_empty + i, 1);
+        }
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, 8);
         mbar_init(mma_done, 1);
@@ -297,122 +298,157 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tX = tmem, tDQ = tmem + 256;
+    // TMEM: X^T (2 x 128 fp32 columns), G'^T as the A operand of dQ' (2 x 64 columns of bf16 pairs), dQ' (128)
+    const uint32_t tX = tmem, tG = tmem + 256, tDQ = tmem + 384;
     const int total = pair_total(a);
 
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------------ TMA producer
-            int hs = 0, ai = 0;
+            // k tiles stream through the half-stage ring; an item's q tile is requested as soon as its buffer
+            // is free: that buffer is probed before every k-half load of the previous item, and waited for at
+            // the latest when the item starts.
+            int hs = 0, ai = 0, qi = 0;
             int last_hs[R_ASTG];
-            int last_ai[2] = {-1, -1};
+            int last_q[2] = {-1, -1};
             for (int i = 0; i < R_ASTG; i++) last_hs[i] = -1;
-            for (int i = blockIdx.x; i < total; i += gridDim.x) {
-                const Pair p = decode_pair(a, i);
-                if (p.vmax == 0) continue;
-                const int bb = ai & 1;
-                wait_bar(b_empty + bb, ((ai >> 1) & 1) ^ 1, abort_flag, err, 1);
+            auto load_q = [&](const Pair &p) {
+                const int bb = qi & 1;
                 mbar_expect_tx(b_full + bb, QBLK);
                 for (int r = 0; r < RP; r++)
                     for (int kh = 0; kh < 2; kh++)
                         tma_load_3d(sB + bb * QBLK + kh * HALF + r * (HI * 128), &map_q, b_full + bb, kh * 64, 0,
                                     (int)(r == 0 ? p.row0 : p.row1));
-                last_ai[bb] = ai;
-                ai++;
-                const int nt = (p.vmax + NKEY - 1) / NKEY;
+                last_q[bb] = qi;
+                qi++;
+            };
+            // the next item with visible keys after item index i (or total)
+            auto next_item = [&](int i, Pair &np) -> int {
+                for (int j = i + gridDim.x; j < total; j += gridDim.x) {
+                    np = decode_pair(a, j);
+                    if (np.vmax > 0) return j;
+                }
+                return total;
+            };
+            Pair cur;
+            int i = blockIdx.x;
+            if (i < total) {
+                cur = decode_pair(a, i);
+                if (cur.vmax == 0) i = next_item(i, cur);
+            }
+            while (i < total) {
+                Pair nxt;
+                const int inext = next_item(i, nxt);
+                if (qi == ai) {
+                    wait_bar(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, err, 1);
+                    load_q(cur);
+                }
+                const int nt = (cur.vmax + NKEY - 1) / NKEY;
                 for (int t = 0; t < nt; t++)
                     for (int kh = 0; kh < 2; kh++) {
+                        if (qi == ai + 1 && inext < total && mbar_test(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1))
+                            load_q(nxt);
                         const int st = hs % R_ASTG;
                         wait_bar(a_empty + st, ((hs / R_ASTG) & 1) ^ 1, abort_flag, err, 2);
                         mbar_expect_tx(a_full + st, HALF);
                         if (sbhd)
-                            tma_load_3d(sA + st * HALF, &map_k, a_full + st, kh * 64, p.sg.b, t * NKEY);
+                            tma_load_3d(sA + st * HALF, &map_k, a_full + st, kh * 64, cur.sg.b, t * NKEY);
                         else
-                            tma_load_2d(sA + st * HALF, &map_k, a_full + st, kh * 64, (int)(p.sg.key_y + t * NKEY));
+                            tma_load_2d(sA + st * HALF, &map_k, a_full + st, kh * 64, (int)(cur.sg.key_y + t * NKEY));
                         last_hs[st] = hs;
                         hs++;
                     }
+                ai++;
+                i = inext;
+                cur = nxt;
             }
             for (int st = 0; st < R_ASTG; st++)
                 if (last_hs[st] >= 0) drain_bar(a_full + st, (last_hs[st] / R_ASTG) & 1, err);
             for (int bb = 0; bb < 2; bb++)
-                if (last_ai[bb] >= 0) drain_bar(b_full + bb, (last_ai[bb] >> 1) & 1, err);
+                if (last_q[bb] >= 0) drain_bar(b_full + bb, (last_q[bb] >> 1) & 1, err);
         }
     } else if (warp == 1) {
-        if (lane == 0) {  // ------------------------------------------------ MMA issuer
-            // A half-stage ring: tile t takes stages (st, st + 1), parity aph (R_ASTG is even).  The barriers of
-            // the next group are probed early (mbar_test, all at once) so that their shared-memory round trips
-            // overlap the MMAs issued in between; a probe that comes back false falls back to the bounded waits.
-            int st = 0, ai = 0, xc = 0, gc = 0, dqc = 0;
-            uint32_t aph = 0;
-            bool x_ready = false, g_ready = false;
-            auto probe_x = [&]() -> bool {
-                const bool r0 = mbar_test(x_empty + (xc & 1), ((xc >> 1) & 1) ^ 1);
-                const bool r1 = mbar_test(a_full + st, aph);
-                const bool r2 = mbar_test(a_full + st + 1, aph);
-                return r0 && r1 && r2;
-            };
-            auto mma2 = [&](int sp, bool first) {
-                if (first) wait_bar(dq_empty, (dqc & 1) ^ 1, abort_flag, err, 3);
-                if (!g_ready) wait_bar(g_full, gc & 1, abort_flag, err, 4);
-                x_ready = probe_x();  // the next X group (this item's next tile or the next item's first)
-                fence_after();
-                const unsigned char *pg = sG, *pk = sA + sp * HALF;
+        // -------------------------------------------------------------------- MMA issue (whole warp)
+        // The warp runs the loop together so stage indices and descriptors stay warp-uniform; one elected lane
+        // issues each MMA and commit.  Item decoding is lane-parallel: lane l decodes the CTA's item k + l, the
+        // loop reads the tile count of item k by a shuffle.  A half-stage ring: tile t takes stages
+        // (st, st + 1), parity aph (R_ASTG is even).  The next group's barriers are probed together and early
+        // (mbar_test); a probe that comes back false falls back to the bounded waits.
+        //   X^T[(row,h), key] = q . k^T   (A = the item's q tile, B = the k tile, both K-major)
+        //   dQ'[(row,h), d]  += G'^T k    (A = G'^T from TMEM, B = the same k tile read MN-major)
+        int st = 0, ai = 0, xc = 0, gc = 0, dqc = 0, k = 0, nt_lane = 0;
+        uint32_t aph = 0;
+        bool x_ready = false, g_ready = false;
+        auto probe_x = [&]() -> bool {
+            const bool r0 = mbar_test(x_empty + (xc & 1), ((xc >> 1) & 1) ^ 1);
+            const bool r1 = mbar_test(a_full + st, aph);
+            const bool r2 = mbar_test(a_full + st + 1, aph);
+            return r0 && r1 && r2;
+        };
+        auto mma2 = [&](int sp, bool first) {
+            const int gb = gc & 1;
+            if (first) wait_bar(dq_empty, (dqc & 1) ^ 1, abort_flag, err, 3);
+            if (!g_ready) wait_bar(g_full + gb, (gc >> 1) & 1, abort_flag, err, 4);
+            x_ready = probe_x();  // the next X group (this item's next tile or the next item's first)
+            fence_after();
+            const unsigned char *pk = sA + sp * HALF;
 #pragma unroll
-                for (int s = 0; s < 8; s++)
-                    mma_bf16(tDQ, desc_sw128(pg + s * 2048, HALF, 1024), desc_sw128(pk + s * 2048, HALF, 1024), IDESC_DQ,
-                             (first && s == 0) ? 0u : 1u);
-                mma_commit(g_empty);
-                mma_commit(a_empty + sp);
-                mma_commit(a_empty + sp + 1);
-                gc++;
-            };
-            for (int i = blockIdx.x; i < total; i += gridDim.x) {
-                const Pair p = decode_pair(a, i);
-                if (p.vmax == 0) continue;
-                const int bb = ai & 1;
-                wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, err, 5);
-                fence_after();
-                const unsigned char *pq = sB + bb * QBLK;
-                const int nt = (p.vmax + NKEY - 1) / NKEY;
-                int st_prev = 0;
-                for (int t = 0; t < nt; t++) {
-                    const int tb = xc & 1;
-                    if (!x_ready) x_ready = probe_x();
-                    if (!x_ready) {
-                        wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 6);
-                        wait_bar(a_full + st, aph, abort_flag, err, 7);
-                        wait_bar(a_full + st + 1, aph, abort_flag, err, 7);
-                    }
-                    x_ready = false;
-                    g_ready = t > 0 && mbar_test(g_full, gc & 1);  // the dQ group issued right after these MMAs
-                    fence_after();
-                    const unsigned char *pk = sA + st * HALF;
-#pragma unroll
-                    for (int kh = 0; kh < 2; kh++)
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; k4++)
-                            mma_bf16(tX + tb * 128, desc_kmajor(pk + kh * HALF + k4 * 32), desc_kmajor(pq + kh * HALF + k4 * 32),
-                                     IDESC_X, (kh | k4) ? 1u : 0u);
-                    mma_commit(x_full + tb);
-                    xc++;
-                    const int st_cur = st;
-                    st += 2;
-                    if (st == R_ASTG) {
-                        st = 0;
-                        aph ^= 1u;
-                    }
-                    if (t > 0) mma2(st_prev, t == 1);
-                    st_prev = st_cur;
-                }
-                g_ready = false;
-                mma2(st_prev, nt == 1);
-                mma_commit(dq_full);
-                dqc++;
-                ai++;
+            for (int s = 0; s < 8; s++)
+                mma_bf16_ts_w(tDQ, tG + gb * 64 + s * 8, desc_sw128(pk + s * 2048, HALF, 1024), IDESC_DQ,
+                              (first && s == 0) ? 0u : 1u);
+            mma_commit_w(g_empty + gb);
+            mma_commit_w(a_empty + sp);
+            mma_commit_w(a_empty + sp + 1);
+            gc++;
+        };
+        for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
+            if ((k & 31) == 0) {
+                const int il = i + lane * (int)gridDim.x;
+                nt_lane = il < total ? (decode_pair(a, il).vmax + NKEY - 1) / NKEY : 0;
             }
-            mma_commit(mma_done);
-            drain_bar(mma_done, 0, err);
+            const int nt = __shfl_sync(0xffffffffu, nt_lane, k & 31);
+            if (nt == 0) continue;
+            const int bb = ai & 1;
+            wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, err, 5);
+            fence_after();
+            const unsigned char *pq = sB + bb * QBLK;
+            int st_prev = 0;
+            for (int t = 0; t < nt; t++) {
+                const int tb = xc & 1;
+                if (!x_ready) x_ready = probe_x();
+                if (!x_ready) {
+                    wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 6);
+                    wait_bar(a_full + st, aph, abort_flag, err, 7);
+                    wait_bar(a_full + st + 1, aph, abort_flag, err, 7);
+                }
+                x_ready = false;
+                g_ready = t > 0 && mbar_test(g_full + (gc & 1), (gc >> 1) & 1);  // the dQ group issued next
+                fence_after();
+                const unsigned char *pk = sA + st * HALF;
+#pragma unroll
+                for (int kh = 0; kh < 2; kh++)
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; k4++)
+                        mma_bf16_w(tX + tb * 128, desc_kmajor(pq + kh * HALF + k4 * 32), desc_kmajor(pk + kh * HALF + k4 * 32),
+                                   IDESC_X, (kh | k4) ? 1u : 0u);
+                mma_commit_w(x_full + tb);
+                xc++;
+                const int st_cur = st;
+                st += 2;
+                if (st == R_ASTG) {
+                    st = 0;
+                    aph ^= 1u;
+                }
+                if (t > 0) mma2(st_prev, t == 1);
+                st_prev = st_cur;
+            }
+            g_ready = false;
+            mma2(st_prev, nt == 1);
+            mma_commit_w(dq_full);
+            dqc++;
+            ai++;
         }
+        mma_commit_w(mma_done);
+        drain_bar(mma_done, 0, err);
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------------- g / w stagers
         // Warp 2 prepares the even items (buffer 0), warp 3 the odd ones (buffer 1).  Every global load of a
@@ -481,37 +517,47 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const Pair p = decode_pair(a, i);
             const int gb = ic & 1;
             wait_bar(gd_full + gb, (ic >> 1) & 1, abort_flag, err, 9);
-            const float *gd = sGD + gb * RP * NCMAX + half * NCMAX;
-            const int v_me = half == 0 ? p.v0 : p.v1;
+            // X^T / G'^T rows: lane (quad*32 + lane) = (row, head); this warp's 64 of the tile's 128 keys
+            const int er = quad >> 1;
+            const float *gd = sGD + gb * RP * NCMAX + er * NCMAX;
+            const int v_me = er == 0 ? p.v0 : p.v1;
             const int nt = (p.vmax + NKEY - 1) / NKEY;
-            const int k = quad * 32 + lane;
             for (int t = 0; t < nt; t++) {
                 const int tb = xc & 1;
                 wait_bar(x_full + tb, (xc >> 1) & 1, abort_flag, err, 10);
                 fence_after();
-                const int j = t * NKEY + k;
-                const float gk = j < v_me ? gd[j] : 0.f;
+                const int j0 = t * NKEY + half * 64;  // first key of this warp's columns
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 2; c++) {
                     float x[32];
                     tmem_ld32(tX + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * 128 + half * 64 + c * 32), x);
+                    // g of the row for these 32 keys (the same addresses across the warp: broadcast reads)
+                    float gk[32];
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; q4++) {
+                        const int j = j0 + c * 32 + 4 * q4;
+                        const float4 g4 = j + 3 < NCMAX ? *reinterpret_cast<const float4 *>(gd + j)
+                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                        gk[4 * q4] = j < v_me ? g4.x : 0.f;
+                        gk[4 * q4 + 1] = j + 1 < v_me ? g4.y : 0.f;
+                        gk[4 * q4 + 2] = j + 2 < v_me ? g4.z : 0.f;
+                        gk[4 * q4 + 3] = j + 3 < v_me ? g4.w : 0.f;
+                    }
 #pragma unroll
                     for (int q2 = 0; q2 < 16; q2++)
-                        pk[c * 16 + q2] = pack_bf16(x[2 * q2] > 0.f ? gk : 0.f, x[2 * q2 + 1] > 0.f ? gk : 0.f);
+                        pk[c * 16 + q2] = pack_bf16(x[2 * q2] > 0.f ? gk[2 * q2] : 0.f, x[2 * q2 + 1] > 0.f ? gk[2 * q2 + 1] : 0.f);
                 }
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(x_empty + tb);
-                wait_bar(g_empty, (gc & 1) ^ 1, abort_flag, err, 11);
-                unsigned char *dst = sG + half * HALF;
-#pragma unroll
-                for (int c = 0; c < 8; c++)
-                    *reinterpret_cast<uint4 *>(dst + sw128_off(k, c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                fence_async_smem();
+                const int gbuf = gc & 1;
+                wait_bar(g_empty + gbuf, ((gc >> 1) & 1) ^ 1, abort_flag, err, 11);
+                fence_after();
+                tmem_st32(tG + ((uint32_t)(quad * 32) << 16) + (uint32_t)(gbuf * 64 + half * 32), pk);
+                fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(g_full);
+                if (lane == 0) mbar_arrive(g_full + gbuf);
                 xc++;
                 gc++;
             }
@@ -677,75 +723,78 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
                 if (last_qs[bs] >= 0) drain_bar(b_full + bs, (last_qs[bs] / K_BSTG) & 1, err);
         }
     } else if (warp == 1) {
-        if (lane == 0) {  // ------------------------------------------------ MMA issuer
-            // q-block ring position (bs, parity bph).  The next group's barriers are probed early, as in the
-            // row-owner kernel.
-            int uc = 0, bs = 0, xc = 0, gkc = 0, dkc = 0;
-            uint32_t bph = 0;
-            bool x_ready = false, g_ready = false;
-            auto probe_x = [&]() -> bool {
-                const bool r0 = mbar_test(x_empty + (xc & 1), ((xc >> 1) & 1) ^ 1);
-                const bool r1 = mbar_test(b_full + bs, bph);
-                return r0 && r1;
-            };
-            auto mma3 = [&](int bp, bool first) {
-                if (first) wait_bar(dk_empty, (dkc & 1) ^ 1, abort_flag, err, 23);
-                const int gkb = gkc & 1;
-                if (!g_ready) wait_bar(gk_full + gkb, (gkc >> 1) & 1, abort_flag, err, 24);
-                x_ready = probe_x();
-                fence_after();
-                const unsigned char *pg = sG + gkb * QBLK, *pq = sB + bp * QBLK;
+        // -------------------------------------------------------------------- MMA issue (whole warp)
+        // As in the row-owner kernel: warp-uniform loop, elected issue, lane-parallel unit decoding, early
+        // probes of the next group's barriers.  q-block ring position (bs, parity bph).
+        int uc = 0, bs = 0, xc = 0, gkc = 0, dkc = 0, k = 0, np_lane = 0;
+        uint32_t bph = 0;
+        bool x_ready = false, g_ready = false;
+        auto probe_x = [&]() -> bool {
+            const bool r0 = mbar_test(x_empty + (xc & 1), ((xc >> 1) & 1) ^ 1);
+            const bool r1 = mbar_test(b_full + bs, bph);
+            return r0 && r1;
+        };
+        auto mma3 = [&](int bp, bool first) {
+            if (first) wait_bar(dk_empty, (dkc & 1) ^ 1, abort_flag, err, 23);
+            const int gkb = gkc & 1;
+            if (!g_ready) wait_bar(gk_full + gkb, (gkc >> 1) & 1, abort_flag, err, 24);
+            x_ready = probe_x();
+            fence_after();
+            const unsigned char *pg = sG + gkb * QBLK, *pq = sB + bp * QBLK;
 #pragma unroll
-                for (int s = 0; s < 8; s++)
-                    mma_bf16(tDK, desc_kmajor(pg + (s >> 2) * HALF + (s & 3) * 32), desc_sw128(pq + s * 2048, HALF, 1024),
-                             IDESC_DK, (first && s == 0) ? 0u : 1u);
-                mma_commit(gk_empty + gkb);
-                mma_commit(b_empty + bp);
-                gkc++;
-            };
-            for (int u = blockIdx.x; u < total; u += gridDim.x) {
-                const Unit U = decode_unit(a, u);
-                if (U.npairs == 0) continue;
-                wait_bar(a_full, uc & 1, abort_flag, err, 25);
-                fence_after();
-                int bs_prev = 0;
-                for (int pi = 0; pi < U.npairs; pi++) {
-                    const int tb = xc & 1;
-                    if (!x_ready) x_ready = probe_x();
-                    if (!x_ready) {
-                        wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 26);
-                        wait_bar(b_full + bs, bph, abort_flag, err, 27);
-                    }
-                    x_ready = false;
-                    g_ready = pi > 0 && mbar_test(gk_full + (gkc & 1), (gkc >> 1) & 1);
-                    fence_after();
-                    const unsigned char *pq = sB + bs * QBLK;
-#pragma unroll
-                    for (int kh = 0; kh < 2; kh++)
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; k4++)
-                            mma_bf16(tX + tb * 128, desc_kmajor(sA + kh * HALF + k4 * 32), desc_kmajor(pq + kh * HALF + k4 * 32),
-                                     IDESC_X, (kh | k4) ? 1u : 0u);
-                    mma_commit(x_full + tb);
-                    xc++;
-                    const int bs_cur = bs;
-                    if (++bs == K_BSTG) {
-                        bs = 0;
-                        bph ^= 1u;
-                    }
-                    if (pi > 0) mma3(bs_prev, pi == 1);
-                    bs_prev = bs_cur;
-                }
-                g_ready = false;
-                mma3(bs_prev, U.npairs == 1);
-                mma_commit(dk_full);
-                mma_commit(a_empty);
-                dkc++;
-                uc++;
+            for (int s = 0; s < 8; s++)
+                mma_bf16_w(tDK, desc_kmajor(pg + (s >> 2) * HALF + (s & 3) * 32), desc_sw128(pq + s * 2048, HALF, 1024),
+                           IDESC_DK, (first && s == 0) ? 0u : 1u);
+            mma_commit_w(gk_empty + gkb);
+            mma_commit_w(b_empty + bp);
+            gkc++;
+        };
+        for (int u = blockIdx.x; u < total; u += gridDim.x, k++) {
+            if ((k & 31) == 0) {
+                const int ul = u + lane * (int)gridDim.x;
+                np_lane = ul < total ? decode_unit(a, ul).npairs : 0;
             }
-            mma_commit(mma_done);
-            drain_bar(mma_done, 0, err);
+            const int npairs = __shfl_sync(0xffffffffu, np_lane, k & 31);
+            if (npairs == 0) continue;
+            wait_bar(a_full, uc & 1, abort_flag, err, 25);
+            fence_after();
+            int bs_prev = 0;
+            for (int pi = 0; pi < npairs; pi++) {
+                const int tb = xc & 1;
+                if (!x_ready) x_ready = probe_x();
+                if (!x_ready) {
+                    wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 26);
+                    wait_bar(b_full + bs, bph, abort_flag, err, 27);
+                }
+                x_ready = false;
+                g_ready = pi > 0 && mbar_test(gk_full + (gkc & 1), (gkc >> 1) & 1);
+                fence_after();
+                const unsigned char *pq = sB + bs * QBLK;
+#pragma unroll
+                for (int kh = 0; kh < 2; kh++)
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; k4++)
+                        mma_bf16_w(tX + tb * 128, desc_kmajor(sA + kh * HALF + k4 * 32), desc_kmajor(pq + kh * HALF + k4 * 32),
+                                   IDESC_X, (kh | k4) ? 1u : 0u);
+                mma_commit_w(x_full + tb);
+                xc++;
+                const int bs_cur = bs;
+                if (++bs == K_BSTG) {
+                    bs = 0;
+                    bph ^= 1u;
+                }
+                if (pi > 0) mma3(bs_prev, pi == 1);
+                bs_prev = bs_cur;
+            }
+            g_ready = false;
+            mma3(bs_prev, npairs == 1);
+            mma_commit_w(dk_full);
+            mma_commit_w(a_empty);
+            dkc++;
+            uc++;
         }
+        mma_commit_w(mma_done);
+        drain_bar(mma_done, 0, err);
     } else if (warp == 2 || warp == 3) {
         // ---------------------------------------------------------------- g / w stagers (per row pair)
         // Two warps take alternate row pairs; each issues all loads of a pair before using them.

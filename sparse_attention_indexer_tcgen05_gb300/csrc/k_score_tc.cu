@@ -365,53 +365,57 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 if (last_ai[bb] >= 0) drain_bar(b_full + bb, (last_ai[bb] >> 1) & 1, &g_tc_error);
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            // A-stage ring position (st, parity aph).  The full barrier of the next stage and the empty barrier
-            // of the next accumulator are probed early (mbar_test) so that their shared-memory round trips
-            // overlap the MMAs issued in between; a probe that comes back false falls back to the wait.
-            int st = 0, ai = 0, tc = 0;
-            uint32_t aph = 0;
-            bool a_ready = false, t_ready = false;
-            for (int i = blockIdx.x; i < total; i += gridDim.x) {
-                const Item it = decode_item(a, i, total);
-                if (it.vmax == 0) continue;
-                const int bb = ai & 1;
-                wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, &g_tc_error, 3);
-                fence_after();
-                const int nt = (it.vmax + NKEY - 1) / NKEY;
-                const unsigned char *pb0 = sB + bb * B_BUF;
-                for (int t = 0; t < nt; t++) {
-                    const int tb = tc & 1;
-                    if (!t_ready) wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 4);
-                    fence_after();
-                    const uint32_t d = tmem + (uint32_t)(tb * NCOL);
-#pragma unroll
-                    for (int kh = 0; kh < 2; kh++) {
-                        if (!a_ready) wait_bar(a_full + st, aph, abort_flag, &g_tc_error, 5);
-                        const int st1 = st + 1 == A_STAGES ? 0 : st + 1;
-                        const uint32_t ph1 = st1 == 0 ? aph ^ 1u : aph;
-                        a_ready = mbar_test(a_full + st1, ph1);
-                        if (kh == 1) t_ready = mbar_test(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1);
-                        fence_after();
-                        const unsigned char *pa = sA + st * A_HALF;
-                        const unsigned char *pb = pb0 + kh * B_HALF;
-#pragma unroll
-                        for (int k = 0; k < 4; k++)
-                            mma_bf16(d, desc_kmajor(pa + k * 32), desc_kmajor(pb + k * 32), IDESC, (kh | k) != 0);
-                        mma_commit(a_empty + st);
-                        st = st1;
-                        aph = ph1;
-                    }
-                    mma_commit(t_full + tb);
-                    tc++;
-                }
-                mma_commit(b_empty + bb);
-                ai++;
+        // ---------------------------------------------------------- MMA issue (whole warp)
+        // The warp runs the loop together (warp-uniform stage indices and descriptors); one elected lane issues
+        // each MMA and commit.  Items are decoded lane-parallel (lane l: the CTA's item k + l), the loop reads
+        // the tile count of item k by a shuffle.  A-stage ring position (st, parity aph).  The next stage's full
+        // barrier and the next accumulator's empty barrier are probed early (mbar_test) so that their
+        // shared-memory round trips overlap the MMAs issued in between; a probe that comes back false falls back
+        // to the bounded wait.
+        int st = 0, ai = 0, tc = 0, k = 0, nt_lane = 0;
+        uint32_t aph = 0;
+        bool a_ready = false, t_ready = false;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
+            if ((k & 31) == 0) {
+                const int il = i + lane * (int)gridDim.x;
+                nt_lane = il < total ? (decode_item(a, il, total).vmax + NKEY - 1) / NKEY : 0;
             }
-            mma_commit(mma_done);
-            drain_bar(mma_done, 0, &g_tc_error);
+            const int nt = __shfl_sync(0xffffffffu, nt_lane, k & 31);
+            if (nt == 0) continue;
+            const int bb = ai & 1;
+            wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, &g_tc_error, 3);
+            fence_after();
+            const unsigned char *pb0 = sB + bb * B_BUF;
+            for (int t = 0; t < nt; t++) {
+                const int tb = tc & 1;
+                if (!t_ready) wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 4);
+                fence_after();
+                const uint32_t d = tmem + (uint32_t)(tb * NCOL);
+#pragma unroll
+                for (int kh = 0; kh < 2; kh++) {
+                    if (!a_ready) wait_bar(a_full + st, aph, abort_flag, &g_tc_error, 5);
+                    const int st1 = st + 1 == A_STAGES ? 0 : st + 1;
+                    const uint32_t ph1 = st1 == 0 ? aph ^ 1u : aph;
+                    a_ready = mbar_test(a_full + st1, ph1);
+                    if (kh == 1) t_ready = mbar_test(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1);
+                    fence_after();
+                    const unsigned char *pa = sA + st * A_HALF;
+                    const unsigned char *pb = pb0 + kh * B_HALF;
+#pragma unroll
+                    for (int kk = 0; kk < 4; kk++)
+                        mma_bf16_w(d, desc_kmajor(pa + kk * 32), desc_kmajor(pb + kk * 32), IDESC, (kh | kk) != 0);
+                    mma_commit_w(a_empty + st);
+                    st = st1;
+                    aph = ph1;
+                }
+                mma_commit_w(t_full + tb);
+                tc++;
+            }
+            mma_commit_w(b_empty + bb);
+            ai++;
         }
+        mma_commit_w(mma_done);
+        drain_bar(mma_done, 0, &g_tc_error);
     } else {
         // ---------------------------------------------------------- epilogue + selection (warps 2..9)
         const int e = warp - 2;           // 0..7

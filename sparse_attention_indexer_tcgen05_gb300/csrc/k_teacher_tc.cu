@@ -257,61 +257,70 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 if (last_ai[qb] >= 0) drain_bar(q_full + qb, (last_ai[qb] >> 1) & 1, err);
         }
     } else if (warp == 1) {
-        if (lane == 0) {  // ------------------------------------------------ MMA issuer
-            // B-stage ring position (st, parity bph).  A barrier probe costs the issuing thread a shared-memory
-            // round trip, so the barriers of a whole tile (its accumulator and its nkb B stages) are probed
-            // together, once per 4 nkb MMAs; only those not yet complete are then waited on.
-            int st = 0, ai = 0, tc = 0;
-            uint32_t bph = 0;
-            for (int i = blockIdx.x; i < total; i += gridDim.x) {
-                const Item it = decode(a, i, total);
-                if (it.vmax == 0) continue;
-                const int qb = ai & 1;
-                wait_bar(q_full + qb, (ai >> 1) & 1, abort_flag, err, 43);
-                fence_after();
-                const unsigned char *pq = sQ + qb * QBUF;
-                const int nt = ntiles(it);
-                for (int tt = 0; tt < nt; tt++) {
-                    const int tb = tc & 1;
-                    int sk[MAXKB];
-                    uint32_t pk[MAXKB];
-                    bool rk[MAXKB];
-                    const uint32_t tpar = ((tc >> 1) & 1) ^ 1;
-                    const bool rt = mbar_test(t_empty + tb, tpar);
-#pragma unroll
-                    for (int kb = 0; kb < MAXKB; kb++) {
-                        sk[kb] = st;
-                        pk[kb] = bph;
-                        rk[kb] = kb < nkb ? mbar_test(b_full + st, bph) : true;
-                        if (kb < nkb && ++st == BSTG) {
-                            st = 0;
-                            bph ^= 1u;
-                        }
-                    }
-                    if (!rt) wait_bar(t_empty + tb, tpar, abort_flag, err, 44);
-#pragma unroll
-                    for (int kb = 0; kb < MAXKB; kb++)
-                        if (!rk[kb]) wait_bar(b_full + sk[kb], pk[kb], abort_flag, err, 45);
-                    fence_after();
-                    const uint32_t d = tmem + tb * NK;
-#pragma unroll
-                    for (int kb = 0; kb < MAXKB; kb++) {
-                        if (kb >= nkb) break;
-                        const unsigned char *pa = pq + kb * QKB, *pb = sB + sk[kb] * KB;
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; k4++)
-                            mma_bf16(d, desc_kmajor(pa + k4 * 32), desc_kmajor(pb + k4 * 32), IDESC, (kb | k4) ? 1u : 0u);
-                        mma_commit(b_empty + sk[kb]);
-                    }
-                    mma_commit(t_full + tb);
-                    tc++;
+        // -------------------------------------------------------------------- MMA issue (whole warp)
+        // The warp runs the loop together (warp-uniform stage indices and descriptors); one elected lane issues
+        // each MMA and commit.  Items are decoded lane-parallel (lane l: the CTA's item k + l) and the loop reads
+        // the tile count of item k by a shuffle.  B-stage ring position (st, parity bph).  A barrier probe costs
+        // a shared-memory round trip, so the barriers of a whole tile (its accumulator and its nkb B stages) are
+        // probed together, once per 4 nkb MMAs; only those not yet complete are then waited on.
+        int st = 0, ai = 0, tc = 0, k = 0, nt_lane = 0;
+        uint32_t bph = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
+            if ((k & 31) == 0) {
+                const int il = i + lane * (int)gridDim.x;
+                if (il < total) {
+                    const Item itl = decode(a, il, total);
+                    nt_lane = itl.vmax == 0 ? 0 : ntiles(itl);
+                } else {
+                    nt_lane = 0;
                 }
-                mma_commit(q_empty + qb);
-                ai++;
             }
-            mma_commit(mma_done);
-            drain_bar(mma_done, 0, err);
+            const int nt = __shfl_sync(0xffffffffu, nt_lane, k & 31);
+            if (nt == 0) continue;
+            const int qb = ai & 1;
+            wait_bar(q_full + qb, (ai >> 1) & 1, abort_flag, err, 43);
+            fence_after();
+            const unsigned char *pq = sQ + qb * QBUF;
+            for (int tt = 0; tt < nt; tt++) {
+                const int tb = tc & 1;
+                int sk[MAXKB];
+                uint32_t pk[MAXKB];
+                bool rk[MAXKB];
+                const uint32_t tpar = ((tc >> 1) & 1) ^ 1;
+                const bool rt = mbar_test(t_empty + tb, tpar);
+#pragma unroll
+                for (int kb = 0; kb < MAXKB; kb++) {
+                    sk[kb] = st;
+                    pk[kb] = bph;
+                    rk[kb] = kb < nkb ? mbar_test(b_full + st, bph) : true;
+                    if (kb < nkb && ++st == BSTG) {
+                        st = 0;
+                        bph ^= 1u;
+                    }
+                }
+                if (!rt) wait_bar(t_empty + tb, tpar, abort_flag, err, 44);
+#pragma unroll
+                for (int kb = 0; kb < MAXKB; kb++)
+                    if (!rk[kb]) wait_bar(b_full + sk[kb], pk[kb], abort_flag, err, 45);
+                fence_after();
+                const uint32_t d = tmem + tb * NK;
+#pragma unroll
+                for (int kb = 0; kb < MAXKB; kb++) {
+                    if (kb >= nkb) break;
+                    const unsigned char *pa = pq + kb * QKB, *pb = sB + sk[kb] * KB;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; k4++)
+                        mma_bf16_w(d, desc_kmajor(pa + k4 * 32), desc_kmajor(pb + k4 * 32), IDESC, (kb | k4) ? 1u : 0u);
+                    mma_commit_w(b_empty + sk[kb]);
+                }
+                mma_commit_w(t_full + tb);
+                tc++;
+            }
+            mma_commit_w(q_empty + qb);
+            ai++;
         }
+        mma_commit_w(mma_done);
+        drain_bar(mma_done, 0, err);
     } else if (warp >= 2) {
         // ---------------------------------------------------------------- epilogue
         // 16 warps: four per TMEM lane quadrant (warp % 4), warp cq = (warp - 2) / 4 of a quadrant reads the
