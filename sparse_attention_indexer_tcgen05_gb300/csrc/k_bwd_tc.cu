@@ -46,8 +46,10 @@ constexpr int M_PAIRS = RP * 64;               // (row, head) pairs of an item
 constexpr int NCMAX = 1024;                    // key axis the row-owner's dense g rows hold
 constexpr int HALF = NKEY * 64 * 2;            // 16 KB: 128 rows x 64 bf16
 constexpr int QBLK = 2 * HALF;                 // 32 KB: 2 rows x 64 heads x 128 d, two K-halves
-constexpr int THREADS = 384;
-constexpr int EPI = 256;
+constexpr int THREADS = 384;                   // key-owner kernel: 12 warps
+constexpr int EPI = 256;                       //   its epilogue: warps 4..11
+constexpr int R_THREADS = 640;                 // row-owner kernel: 20 warps
+constexpr int R_EPI = 512;                     //   its epilogue: warps 4..19, four per TMEM lane quadrant
 constexpr int CH = 128;                        // rows per key-owner unit
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_X = idesc_bf16(128, 128, false, false);   // X = k . q^T (key-owner), X^T = q . k^T
@@ -61,8 +63,8 @@ constexpr int R_OFF_A = 0;
 constexpr int R_OFF_B = R_OFF_A + R_ASTG * HALF;              // 128 KB: the q tiles of two items
 constexpr int R_OFF_GD = R_OFF_B + 2 * QBLK;                  // 192 KB: 2 bufs x 2 rows x NCMAX fp32
 constexpr int R_OFF_W = R_OFF_GD + 2 * RP * NCMAX * 4;        // 208 KB: 2 bufs x 2 rows x 64 fp32
-constexpr int R_OFF_DW = R_OFF_W + 2 * RP * HI * 4;           // 128 fp32
-constexpr int R_OFF_MISC = R_OFF_DW + 2 * RP * HI * 4;      // sDW double-buffered by item parity
+constexpr int R_OFF_DW = R_OFF_W + 2 * RP * HI * 4;           // dW partials: 2 item parities x 4 d quarters x 128
+constexpr int R_OFF_MISC = R_OFF_DW + 2 * 4 * M_PAIRS * 4;
 constexpr int R_SMEM = R_OFF_MISC + 1024 + 1024;
 
 // key-owner shared memory
@@ -250,7 +252,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 
 // ------------------------------------------------------------------ row-owner kernel: dQ_idx, dW
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(R_THREADS, 1)
 dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -277,18 +279,18 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int i = 0; i < R_ASTG; i++) { mbar_init(a_full + i, 1); mbar_init(a_empty + i, 1); }
         for (int i = 0; i < 2; i++) {
             mbar_init(b_full + i, 1);
-            mbar_init(b_empty + i, 8);
+            mbar_init(b_empty + i, R_EPI / 32);
             mbar_init(x_full + i, 1);
-            mbar_init(x_empty + i, 8);
+            mbar_init(x_empty + i, R_EPI / 32);
             mbar_init(gd_full + i, 1);
-            mbar_init(gd_empty + i, 8);
+            mbar_init(gd_empty + i, R_EPI / 32);
         }
         for (int i = 0; i < 2; i++) {
-            mbar_init(g_full + i, 8);
+            mbar_init(g_full + i, R_EPI / 32);
             mbar_init(g_empty + i, 1);
         }
         mbar_init(dq_full, 1);
-        mbar_init(dq_empty, 8);
+        mbar_init(dq_empty, R_EPI / 32);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         init_fence();
@@ -473,7 +475,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 wv[r][1] = (r < p.n) ? __ldg(a.w + row * HI + lane + 32) : 0.f;
             }
             __syncwarp();
-            constexpr int CHUNK = 16;  // slots per lane per pass
+            constexpr int CHUNK = 8;   // slots per lane per pass
             const int span = g.sparse ? g.K : p.vmax;
             for (int base = 0; base < span; base += 32 * CHUNK) {
                 int32_t idv[RP][CHUNK];
@@ -510,15 +512,18 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             if (lane == 0) mbar_arrive(gd_full + gb);
         }
     } else if (warp >= 4) {
-        // ---------------------------------------------------------------- epilogue
-        const int e = warp - 4, quad = warp & 3, half = e >> 2;
+        // ---------------------------------------------------------------- epilogue (16 warps)
+        // Lane (quad*32 + lane) = (row, head).  Warp qq = (warp - 4) / 4 of a quadrant owns key columns
+        // [32 qq, 32 qq + 32) of every tile and the d quarter [32 qq, 32 qq + 32) of the dQ' readout.
+        const int quad = warp & 3, qq = (warp - 4) >> 2;
+        const int rh = quad * 32 + lane;
+        const int er = rh >> 6, h = rh & 63;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         int xc = 0, gc = 0, dqc = 0, ai = 0, ic = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
             const Pair p = decode_pair(a, i);
             const int gb = ic & 1;
             wait_bar(gd_full + gb, (ic >> 1) & 1, abort_flag, err, 9);
-            // X^T / G'^T rows: lane (quad*32 + lane) = (row, head); this warp's 64 of the tile's 128 keys
-            const int er = quad >> 1;
             const float *gd = sGD + gb * RP * NCMAX + er * NCMAX;
             const int v_me = er == 0 ? p.v0 : p.v1;
             const int nt = (p.vmax + NKEY - 1) / NKEY;
@@ -526,88 +531,81 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 const int tb = xc & 1;
                 wait_bar(x_full + tb, (xc >> 1) & 1, abort_flag, err, 10);
                 fence_after();
-                const int j0 = t * NKEY + half * 64;  // first key of this warp's columns
-                uint32_t pk[32];
+                const int j0 = t * NKEY + qq * 32;  // first key of this warp's columns
+                uint32_t xr[32];
+                tmem_ld32_async(tX + lane_off + (uint32_t)(tb * 128 + qq * 32), xr);
+                // g of the row for these 32 keys (the same addresses across the warp: broadcast reads), fetched
+                // while the TMEM load is in flight; keys at or beyond the row's visible count give 0
+                float gk[32];
 #pragma unroll
-                for (int c = 0; c < 2; c++) {
-                    float x[32];
-                    tmem_ld32(tX + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * 128 + half * 64 + c * 32), x);
-                    // g of the row for these 32 keys (the same addresses across the warp: broadcast reads)
-                    float gk[32];
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; q4++) {
-                        const int j = j0 + c * 32 + 4 * q4;
-                        const float4 g4 = j + 3 < NCMAX ? *reinterpret_cast<const float4 *>(gd + j)
-                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-                        gk[4 * q4] = j < v_me ? g4.x : 0.f;
-                        gk[4 * q4 + 1] = j + 1 < v_me ? g4.y : 0.f;
-                        gk[4 * q4 + 2] = j + 2 < v_me ? g4.z : 0.f;
-                        gk[4 * q4 + 3] = j + 3 < v_me ? g4.w : 0.f;
-                    }
-#pragma unroll
-                    for (int q2 = 0; q2 < 16; q2++)
-                        pk[c * 16 + q2] = pack_bf16(x[2 * q2] > 0.f ? gk[2 * q2] : 0.f, x[2 * q2 + 1] > 0.f ? gk[2 * q2 + 1] : 0.f);
+                for (int q4 = 0; q4 < 8; q4++) {
+                    const int j = j0 + 4 * q4;
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gd + j);
+                    gk[4 * q4] = j < v_me ? g4.x : 0.f;
+                    gk[4 * q4 + 1] = j + 1 < v_me ? g4.y : 0.f;
+                    gk[4 * q4 + 2] = j + 2 < v_me ? g4.z : 0.f;
+                    gk[4 * q4 + 3] = j + 3 < v_me ? g4.w : 0.f;
                 }
+                tmem_wait_ld(xr);
+                uint32_t pk[16];
+#pragma unroll
+                for (int q2 = 0; q2 < 16; q2++)
+                    pk[q2] = pack_bf16(__uint_as_float(xr[2 * q2]) > 0.f ? gk[2 * q2] : 0.f,
+                                       __uint_as_float(xr[2 * q2 + 1]) > 0.f ? gk[2 * q2 + 1] : 0.f);
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(x_empty + tb);
                 const int gbuf = gc & 1;
                 wait_bar(g_empty + gbuf, ((gc >> 1) & 1) ^ 1, abort_flag, err, 11);
                 fence_after();
-                tmem_st32(tG + ((uint32_t)(quad * 32) << 16) + (uint32_t)(gbuf * 64 + half * 32), pk);
+                tmem_st16(tG + lane_off + (uint32_t)(gbuf * 64 + qq * 16), pk);
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(g_full + gbuf);
                 xc++;
                 gc++;
             }
-            // ---- dQ' readout: lane (quad*32 + lane) = (row, head); this warp's 64 of the 128 d
-            const int rh = quad * 32 + lane;
-            const int rr = rh >> 6, h = rh & 63;
-            const bool exists = rr < p.n;
-            const long long row = rr == 0 ? p.row0 : p.row1;
+            // ---- dQ' readout: this warp's 32 of the 128 d of its (row, head)
+            const bool exists = er < p.n;
+            const long long row = er == 0 ? p.row0 : p.row1;
             float pa[4] = {0.f, 0.f, 0.f, 0.f};
             if (nt > 0) {
                 const int bb = ai & 1;
                 wait_bar(dq_full, dqc & 1, abort_flag, err, 12);
                 fence_after();
-                float vv[64];
-                {
-                    float x[32];
-                    tmem_ld32(tDQ + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64), x);
+                uint32_t vr[32];
+                tmem_ld32_async(tDQ + lane_off + (uint32_t)(qq * 32), vr);
+                // q_idx[row, h, 32 qq .. +32] from the q tile (K-major, 128-B swizzle: K-half qq / 2, 16-B chunks
+                // 4 (qq % 2) .. +4 of the row)
+                const unsigned char *qb = sB + bb * QBLK + (qq >> 1) * HALF;
+                uint4 qv[4];
 #pragma unroll
-                    for (int c = 0; c < 32; c++) vv[c] = x[c];
-                    tmem_ld32(tDQ + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64 + 32), x);
-#pragma unroll
-                    for (int c = 0; c < 32; c++) vv[32 + c] = x[c];
-                }
+                for (int c = 0; c < 4; c++) qv[c] = *reinterpret_cast<const uint4 *>(qb + sw128_off(rh, (qq & 1) * 4 + c));
+                tmem_wait_ld(vr);
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dq_empty);
                 dqc++;
-                const float wv = sW[gb * RP * HI + rr * HI + h];
-                // q_idx[row, h, half*64 .. +64] from the B tile (K-major, 128-B swizzle)
-                const unsigned char *qb = sB + bb * QBLK + half * HALF;
+                const float wv = sW[gb * RP * HI + er * HI + h];
 #pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    const uint4 qv = *reinterpret_cast<const uint4 *>(qb + sw128_off(rh, c));
-                    const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv);
+                for (int c = 0; c < 4; c++) {
+                    const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[c]);
 #pragma unroll
                     for (int u = 0; u < 4; u++) {
                         const float2 qf = __bfloat1622float2(q2[u]);
-                        pa[(2 * u) & 3] = fmaf(qf.x, vv[c * 8 + 2 * u], pa[(2 * u) & 3]);
-                        pa[(2 * u + 1) & 3] = fmaf(qf.y, vv[c * 8 + 2 * u + 1], pa[(2 * u + 1) & 3]);
+                        pa[(2 * u) & 3] = fmaf(qf.x, __uint_as_float(vr[c * 8 + 2 * u]), pa[(2 * u) & 3]);
+                        pa[(2 * u + 1) & 3] = fmaf(qf.y, __uint_as_float(vr[c * 8 + 2 * u + 1]), pa[(2 * u + 1) & 3]);
                     }
                 }
                 if (exists) {
-                    __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + half * 64;
+                    __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + qq * 32;
 #pragma unroll
-                    for (int c = 0; c < 8; c++) {
+                    for (int c = 0; c < 4; c++) {
                         uint4 o;
-                        o.x = pack_bf16(wv * vv[c * 8 + 0], wv * vv[c * 8 + 1]);
-                        o.y = pack_bf16(wv * vv[c * 8 + 2], wv * vv[c * 8 + 3]);
-                        o.z = pack_bf16(wv * vv[c * 8 + 4], wv * vv[c * 8 + 5]);
-                        o.w = pack_bf16(wv * vv[c * 8 + 6], wv * vv[c * 8 + 7]);
+                        o.x = pack_bf16(wv * __uint_as_float(vr[c * 8 + 0]), wv * __uint_as_float(vr[c * 8 + 1]));
+                        o.y = pack_bf16(wv * __uint_as_float(vr[c * 8 + 2]), wv * __uint_as_float(vr[c * 8 + 3]));
+                        o.z = pack_bf16(wv * __uint_as_float(vr[c * 8 + 4]), wv * __uint_as_float(vr[c * 8 + 5]));
+                        o.w = pack_bf16(wv * __uint_as_float(vr[c * 8 + 6]), wv * __uint_as_float(vr[c * 8 + 7]));
                         *reinterpret_cast<uint4 *>(out + c * 8) = o;
                     }
                 }
@@ -615,20 +613,20 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (lane == 0) mbar_arrive(b_empty + bb);  // q tile no longer read
                 ai++;
             } else if (exists) {
-                __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + half * 64;
-                for (int c = 0; c < 8; c++) *reinterpret_cast<uint4 *>(out + c * 8) = make_uint4(0, 0, 0, 0);
+                __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + qq * 32;
+                for (int c = 0; c < 4; c++) *reinterpret_cast<uint4 *>(out + c * 8) = make_uint4(0, 0, 0, 0);
             }
-            // dW = q . dQ' over the two d halves (sDW alternates by item so one barrier suffices)
-            const float part = (pa[0] + pa[1]) + (pa[2] + pa[3]);
-            float *dwb = sDW + (ic & 1) * M_PAIRS;
-            if (half == 1) dwb[rh] = part;
-            named_bar(1, EPI);
-            if (half == 0 && exists) a.dw[row * HI + h] = part + dwb[rh];
+            // dW = q . dQ' over the four d quarters, summed in a fixed order (sDW alternates by item parity, so
+            // one barrier per item suffices)
+            float *dwb = sDW + (ic & 1) * 4 * M_PAIRS;
+            dwb[qq * M_PAIRS + rh] = (pa[0] + pa[1]) + (pa[2] + pa[3]);
+            named_bar(1, R_EPI);
+            if (qq == 0 && exists)
+                a.dw[row * HI + h] = (dwb[rh] + dwb[M_PAIRS + rh]) + (dwb[2 * M_PAIRS + rh] + dwb[3 * M_PAIRS + rh]);
             __syncwarp();
             if (lane == 0) mbar_arrive(gd_empty + gb);
         }
     }
-
     fence_before();
     __syncthreads();
     fence_after();
@@ -1039,7 +1037,7 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
     e = cudaFuncSetAttribute(dk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K_SMEM);
     if (e != cudaSuccess) return e;
     const int g1 = upper_items < sms ? (upper_items > 0 ? upper_items : 1) : sms;
-    dq_dw_tc_kernel<<<g1, THREADS, R_SMEM, st>>>(mq, mk, a);
+    dq_dw_tc_kernel<<<g1, R_THREADS, R_SMEM, st>>>(mq, mk, a);
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
