@@ -450,10 +450,114 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
     }
 }
 
+// The same step for the sparse support with K <= 512 slots (teacher width K): one warp per row, the row's
+// ids, scores and teacher values held in registers (slot s = lane + 32 i, coalesced), warp reductions.
+// Key-tile offsets: with valid ids ascending and invalid slots last, the tile index of consecutive slots
+// never decreases, so the first slot of tile kt is the number of slots whose tile lies below kt.
+constexpr int kKlPer = 16;  // slots per lane
+__global__ void __launch_bounds__(kThreads)
+kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ selscore,
+               const float *__restrict__ teacher, float *__restrict__ gbuf, float *__restrict__ row_loss,
+               int32_t *__restrict__ toff, int NT)
+{
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = (long long)gridDim.x * kWarps;
+    const int K = g.K;
+    for (long long r = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5); r < g.rows; r += nwarps) {
+        const Row R = decode_row(g, r);
+        const long long lo = key_gid(g, R, 0);
+        const int32_t *row_ids = ids + r * K;
+        const float *srow = selscore + r * K;
+        const float *trow = teacher + r * K;
+        float *grow = gbuf + r * K;
+        int32_t id[kKlPer];
+        float x[kKlPer], t[kKlPer];
+#pragma unroll
+        for (int i = 0; i < kKlPer; i++) {
+            const int s = lane + 32 * i;
+            const bool in = s < K;
+            id[i] = in ? __ldg(row_ids + s) : -1;
+            x[i] = in ? __ldg(srow + s) : 0.f;
+            t[i] = in ? __ldg(trow + s) : 0.f;
+        }
+        if (toff != nullptr) {
+            int tl[kKlPer];
+#pragma unroll
+            for (int i = 0; i < kKlPer; i++) {
+                const int s = lane + 32 * i;
+                if (s >= K) {
+                    tl[i] = NT + 1;  // beyond the row: below no tile
+                } else if (id[i] < 0) {
+                    tl[i] = NT;
+                } else {
+                    const long long tt = ((long long)id[i] - lo) >> 7;
+                    tl[i] = tt < 0 ? 0 : (tt > NT ? NT : (int)tt);
+                }
+            }
+            int32_t *to = toff + r * (NT + 1);
+            for (int kt = 0; kt <= NT; kt++) {
+                unsigned c = 0;
+#pragma unroll
+                for (int i = 0; i < kKlPer; i++) c += tl[i] < kt ? 1u : 0u;
+                c = __reduce_add_sync(0xffffffffu, c);
+                if (lane == 0) to[kt] = (int32_t)c;
+            }
+        }
+        bool sel[kKlPer];
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kKlPer; i++) {
+            sel[i] = lane + 32 * i < K && id[i] >= lo && id[i] < lo + R.v;
+            if (sel[i]) m = fmaxf(m, x[i]);
+        }
+        m = warp_max(m);
+        if (m == -INFINITY) {  // empty support: no loss, no gradient
+#pragma unroll
+            for (int i = 0; i < kKlPer; i++)
+                if (lane + 32 * i < K) grow[lane + 32 * i] = 0.f;
+            if (lane == 0) row_loss[r] = 0.f;
+            continue;
+        }
+        float z = 0.f;
+#pragma unroll
+        for (int i = 0; i < kKlPer; i++) {
+            x[i] = sel[i] ? __expf(x[i] - m) : 0.f;
+            z += x[i];
+        }
+        z = warp_sum(z);
+        const float inv_z = 1.f / z;
+        float A = 0.f, L = 0.f;
+#pragma unroll
+        for (int i = 0; i < kKlPer; i++) {
+            if (!sel[i]) continue;
+            const float p = x[i] * inv_z;
+            A += t[i] * p / (p + kEps);
+            L += t[i] * (logf(t[i] + kEps) - logf(p + kEps));
+        }
+        A = warp_sum(A);
+        L = warp_sum(L);
+#pragma unroll
+        for (int i = 0; i < kKlPer; i++) {
+            const int s = lane + 32 * i;
+            if (s >= K) continue;
+            const float p = x[i] * inv_z;
+            grow[s] = sel[i] ? g.factor * p * (A - t[i] / (p + kEps)) : 0.f;
+        }
+        if (lane == 0) row_loss[r] = L;
+    }
+}
+
 cudaError_t launch_kl(const Geo &g, const int32_t *ids, const float *selscore, const float *dense_scores,
                       const float *teacher, float *gbuf, float *row_loss, int32_t *toff, int NT, cudaStream_t st)
 {
     if (g.rows == 0) return cudaSuccess;
+    if (g.sparse && dense_scores == nullptr && g.TW == g.K && g.K <= 32 * kKlPer) {
+        const long long blocks = (g.rows + kWarps - 1) / kWarps;
+        const int grid = blocks < 152 * 16 ? (int)blocks : 152 * 16;
+        kl_warp_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, teacher, gbuf, row_loss, toff, NT);
+        note_launches(1);
+        return cudaGetLastError();
+    }
     int grid = g.rows < 65535 * 8 ? g.rows : 65535 * 8;
     kl_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, toff, NT);
     note_launches(1);
