@@ -19,10 +19,11 @@
 //
 // Roles (one CTA per SM, persistent, static round-robin over items ordered heaviest first):
 //   warp 0      TMA producer: B (q_idx rows, 64 KB, 2 buffers) and A (k_idx K-halves, 16 KB, 4 stages)
-//   warp 1      TMEM allocation and the single-thread tcgen05.mma issue
-//   warps 2..9  epilogue (TMEM -> registers -> ReLU.w reduction -> shared score rows), then the top-k:
-//               a warp pair per row finds the exact k-th largest score by a bitwise search on
-//               order-preserving keys and writes the selection by a stable compaction.
+//   warp 1      TMEM allocation and the tcgen05.mma issue (warp-wide loop, one elected lane issues)
+//   warps 2..9  epilogue (TMEM -> registers -> ReLU.w reduction -> shared score rows, two item buffers)
+//   warps 10..13 top-k, one warp per row, on the previous item while the epilogue runs the next one:
+//               the exact k-th largest score by a bitwise search on order-preserving keys held in
+//               registers, then the selection written by a stable ballot compaction.
 //
 // Every mbarrier wait is bounded: on expiry the kernel records an error code (read back by
 // csa_check_device_status), stops waiting (so every role still runs its loops to the end with uniform
@@ -69,17 +70,19 @@ constexpr int A_HALF = NKEY * 64 * 2;         // 16 KB: one 64-wide K-half of a 
 constexpr int A_STAGES = 4;
 constexpr int B_HALF = NCOL * 64 * 2;         // 32 KB
 constexpr int B_BUF = 2 * B_HALF;             // 64 KB
-constexpr int THREADS = 320;
+constexpr int THREADS = 448;                  // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..13 selection
 constexpr int EPI = 256;
+constexpr int SEL_WARP0 = 10;
 constexpr int TMEM_COLS = 512;
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + A_STAGES * A_HALF;           // 64 KB
 constexpr int OFF_SC = OFF_B + 2 * B_BUF;                  // 192 KB
-constexpr int OFF_W = OFF_SC + ROWS * NCMAX * 4;           // 208 KB
+constexpr int OFF_W = OFF_SC + 2 * ROWS * NCMAX * 4;       // 224 KB: score rows of two items
 constexpr int OFF_MISC = OFF_W + ROWS * HI * 4;            // 209 KB
 constexpr int SMEM_BYTES = OFF_MISC + 1024;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;              // slack to align the base to 1024 B
+static_assert(SMEM_ALLOC <= 232448, "score kernel exceeds the 227 KB of shared memory a CTA may use");
 
 constexpr uint32_t IDESC = idesc_bf16(NKEY, NCOL, false, false);  // A, B both K-major
 
@@ -188,93 +191,101 @@ __device__ long long item_row(const Args &a, int i, int total, int k)
 
 // ------------------------------------------------------------------ top-k of one row (a warp pair)
 
-__device__ __forceinline__ int pair_sum(int x, int *slots, int par, int wsel, int bar_id)
+// inverse of score_key (the key of -0.0 is that of +0.0, so -0.0 comes back as +0.0: the same value)
+__device__ __forceinline__ float key_score(uint32_t k)
 {
-    const int s = __reduce_add_sync(0xffffffffu, x);
-    if ((threadIdx.x & 31) == 0) slots[par * 2 + wsel] = s;
-    named_bar(bar_id, 64);
-    return slots[par * 2] + slots[par * 2 + 1];
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// exclusive prefix of x over the 64 threads of the pair (thread order = element order); returns the total
-__device__ __forceinline__ int pair_excl(int x, int *slots, int wsel, int bar_id, int &total)
-{
-    const int lane = threadIdx.x & 31;
-    int inc = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-    }
-    if (lane == 31) slots[4 + wsel] = inc;
-    named_bar(bar_id, 64);
-    const int w0 = slots[4], w1 = slots[5];
-    total = w0 + w1;
-    named_bar(bar_id, 64);
-    return inc - x + (wsel ? w0 : 0);
-}
-
-__device__ void select_row(const Args &a, const Item &it, int k, const float *sc, int pt, int wsel, int bar_id,
-                           int *slots)
+// One warp selects one row: the min(K, v) largest of the row's v scores, ties to the lower key, written in
+// ascending key order.  Lane l holds the keys of slots j = 32 e + l (e = 0..31): conflict-free shared-memory
+// reads, and key order is (e, lane), so a stable compaction takes one ballot per e.  The row's scores are
+// read once into registers; `release` (an mbarrier, arrived by lane 0) is signalled as soon as the shared
+// rows may be overwritten.
+__device__ void select_row(const Args &a, const Item &it, int k, const float *sc, uint64_t *release)
 {
     const Geo &g = a.g;
+    const int lane = threadIdx.x & 31;
     const int v = it.v[k];
     const int K = g.K;
     const int kk = v < K ? v : K;
     const long long r = it.row[k];
     int32_t *orow = a.ids + r * K;
     float *srow = a.selscore + r * K;
+    constexpr int PER = NCMAX / 32;
+    uint32_t key[PER];
+#pragma unroll
+    for (int e = 0; e < PER; e++) {
+        const int j = 32 * e + lane;
+        key[e] = j < v ? score_key(sc[j]) : 0u;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(release);
     if (kk == v) {
         // every visible key is selected: ascending order as is
-        for (int j = pt; j < v; j += 64) {
-            orow[j] = (int32_t)(it.gid0 + j);
-            srow[j] = sc[j];
-        }
-    } else {
-        constexpr int PER = NCMAX / 64;  // 16 consecutive elements per thread
-        uint32_t key[PER];
 #pragma unroll
         for (int e = 0; e < PER; e++) {
-            const int j = pt * PER + e;
-            key[e] = j < v ? score_key(sc[j]) : 0u;
+            const int j = 32 * e + lane;
+            if (j < v) {
+                orow[j] = (int32_t)(it.gid0 + j);
+                srow[j] = key_score(key[e]);
+            }
         }
-        // the k-th largest key: the largest T with #(key >= T) >= kk, built bit by bit
+    } else {
+        // the k-th largest key: the largest T with #(key >= T) >= kk, built bit by bit (keys of absent slots
+        // are 0, below every present score's key); four independent partial counts per round
         uint32_t T = 0u;
         for (int bit = 31; bit >= 0; bit--) {
             const uint32_t cand = T | (1u << bit);
-            int c = 0;
+            unsigned c4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int e = 0; e < PER; e++) c += key[e] >= cand;
-            if (pair_sum(c, slots, bit & 1, wsel, bar_id) >= kk) T = cand;
+            for (int e = 0; e < PER; e++) c4[e & 3] += key[e] >= cand ? 1u : 0u;
+            if ((int)__reduce_add_sync(0xffffffffu, (c4[0] + c4[1]) + (c4[2] + c4[3])) >= kk) T = cand;
         }
-        int gt = 0, eq = 0;
+        unsigned gt4[4] = {0u, 0u, 0u, 0u}, eq4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int e = 0; e < PER; e++) {
-            gt += key[e] > T;
-            eq += key[e] == T;
+            gt4[e & 3] += key[e] > T ? 1u : 0u;
+            eq4[e & 3] += (key[e] == T && key[e] != 0u) ? 1u : 0u;
         }
-        int gt_tot, eq_tot;
-        const int gt_before = pair_excl(gt, slots, wsel, bar_id, gt_tot);
-        const int eq_before = pair_excl(eq, slots, wsel, bar_id, eq_tot);
-        const int need_eq = kk - gt_tot;
-        int er = eq_before;
-        int pos = gt_before + (eq_before < need_eq ? eq_before : need_eq);
+        const int need_eq = kk - (int)__reduce_add_sync(0xffffffffu, (gt4[0] + gt4[1]) + (gt4[2] + gt4[3]));
+        const int eq_tot = (int)__reduce_add_sync(0xffffffffu, (eq4[0] + eq4[1]) + (eq4[2] + eq4[3]));
+        const unsigned lt_mask = (1u << lane) - 1u;
+        int base = 0;
+        if (eq_tot == need_eq) {
+            // no tie is cut: every key >= T is selected
 #pragma unroll
-        for (int e = 0; e < PER; e++) {
-            const int j = pt * PER + e;
-            const bool is_eq = key[e] == T;
-            const bool sel = key[e] > T || (is_eq && er < need_eq);
-            er += is_eq;
-            if (sel && j < v) {
-                orow[pos] = (int32_t)(it.gid0 + j);
-                srow[pos] = sc[j];
-                pos++;
+            for (int e = 0; e < PER; e++) {
+                const bool sel = key[e] >= T && key[e] != 0u;
+                const unsigned msel = __ballot_sync(0xffffffffu, sel);
+                if (sel) {
+                    const int pos = base + __popc(msel & lt_mask);
+                    orow[pos] = (int32_t)(it.gid0 + 32 * e + lane);
+                    srow[pos] = key_score(key[e]);
+                }
+                base += __popc(msel);
+            }
+        } else {
+            int eq_base = 0;
+#pragma unroll
+            for (int e = 0; e < PER; e++) {
+                const bool is_eq = key[e] == T && key[e] != 0u;
+                const unsigned meq = __ballot_sync(0xffffffffu, is_eq);
+                const bool sel = key[e] > T || (is_eq && eq_base + __popc(meq & lt_mask) < need_eq);
+                eq_base += __popc(meq);
+                const unsigned msel = __ballot_sync(0xffffffffu, sel);
+                if (sel) {
+                    const int pos = base + __popc(msel & lt_mask);
+                    orow[pos] = (int32_t)(it.gid0 + 32 * e + lane);
+                    srow[pos] = key_score(key[e]);
+                }
+                base += __popc(msel);
             }
         }
     }
-    for (int s = kk + pt; s < K; s += 64) {
-        orow[s] = -1;
-        srow[s] = -INFINITY;
+    for (int s2 = kk + lane; s2 < K; s2 += 32) {
+        orow[s2] = -1;
+        srow[s2] = -INFINITY;
     }
 }
 
@@ -292,9 +303,9 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
     uint64_t *a_full = bars, *a_empty = bars + 4, *b_full = bars + 8, *b_empty = bars + 10;
     uint64_t *t_full = bars + 12, *t_empty = bars + 14, *mma_done = bars + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 160);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 168);
-    int *pair_slots = reinterpret_cast<int *>(smem + OFF_MISC + 256);  // 4 pairs x 8 ints
+    uint64_t *sc_full = bars + 17, *sc_empty = bars + 19;  // score rows of an item: epilogue -> selection
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 256);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 264);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geo &g = a.g;
@@ -307,6 +318,8 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mbar_init(b_empty + i, 1);
             mbar_init(t_full + i, 1);
             mbar_init(t_empty + i, 8);
+            mbar_init(sc_full + i, EPI / 32);
+            mbar_init(sc_empty + i, ROWS);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -416,13 +429,13 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         }
         mma_commit_w(mma_done);
         drain_bar(mma_done, 0, &g_tc_error);
-    } else {
-        // ---------------------------------------------------------- epilogue + selection (warps 2..9)
+    } else if (warp < SEL_WARP0) {
+        // ---------------------------------------------------------- epilogue (warps 2..9)
         const int e = warp - 2;           // 0..7
         const int quad = warp & 3;        // TMEM lane quadrant this warp may access
         const int half = e >> 2;          // rows {2 half, 2 half + 1}
         const int et = threadIdx.x - 64;  // 0..255
-        int tc = 0;
+        int tc = 0, ic = 0;
         // w of this thread's (row, head) for the next item, loaded one item ahead
         auto w_of = [&](int i) -> float {
             if (i >= total) return 0.f;
@@ -430,12 +443,15 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             return row >= 0 ? __ldg(a.w + row * HI + (et & 63)) : 0.f;
         };
         float w_next = w_of(blockIdx.x);
-        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
             const Item it = decode_item(a, i, total);
-            named_bar(1, EPI);  // the previous item's selection has finished with sW / sSC
+            named_bar(1, EPI);  // every epilogue warp has finished the previous item's tiles (sW)
             sW[et] = w_next;
             w_next = w_of(i + gridDim.x);
             named_bar(1, EPI);
+            // this item's score rows go to buffer ic & 1, free once the selection warps have read item ic - 2
+            float *scb = sSC + (ic & 1) * ROWS * NCMAX;
+            wait_bar(sc_empty + (ic & 1), ((ic >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 7);
             const int nt = (it.vmax + NKEY - 1) / NKEY;
             for (int t = 0; t < nt; t++) {
                 const int tb = tc & 1;
@@ -455,30 +471,40 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                         for (int h = 0; h < 32; h++) ac[h & 3] = fmaf(wk[h], fmaxf(x[h], 0.f), ac[h & 3]);
                     }
                     const float acc = (ac[0] + ac[1]) + (ac[2] + ac[3]);
-                    if (k < it.n && j < it.v[k]) sSC[k * NCMAX + j] = acc;
+                    if (k < it.n && j < it.v[k]) scb[k * NCMAX + j] = acc;
                 }
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(t_empty + tb);
                 tc++;
             }
-            named_bar(1, EPI);  // every score of the item is in shared memory
-            // one warp pair per row: warps e and e + 4
-            const int k = e & 3;
-            const int wsel = e >> 2;
-            const int pt = wsel * 32 + lane;
+            // hand the item's score rows to the selection warps
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sc_full + (ic & 1));
+        }
+    } else {
+        // ---------------------------------------------------------- selection (warps 10..13, one row each)
+        const int k = warp - SEL_WARP0;
+        int ic = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
+            const Item it = decode_item(a, i, total);
+            wait_bar(sc_full + (ic & 1), (ic >> 1) & 1, abort_flag, &g_tc_error, 8);
+            const float *sc = sSC + (ic & 1) * ROWS * NCMAX + k * NCMAX;
             if (k < it.n) {
-                const float *sc = sSC + k * NCMAX;
                 const long long r = it.row[k];
                 if (a.dump != nullptr && r >= a.dump_row0 && r < a.dump_row0 + a.dump_rows) {
                     float *out = a.dump + (r - a.dump_row0) * (long long)g.NC;
-                    for (int jj = pt; jj < g.NC; jj += 64) out[jj] = jj < it.v[k] ? sc[jj] : -INFINITY;
+                    for (int jj = lane; jj < g.NC; jj += 32) out[jj] = jj < it.v[k] ? sc[jj] : -INFINITY;
                 }
-                if (a.ids != nullptr) select_row(a, it, k, sc, pt, wsel, 2 + k, pair_slots + k * 8);
+            }
+            if (k < it.n && a.ids != nullptr) {
+                select_row(a, it, k, sc, sc_empty + (ic & 1));
+            } else {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sc_empty + (ic & 1));
             }
         }
     }
-
     fence_before();
     __syncthreads();
     fence_after();
