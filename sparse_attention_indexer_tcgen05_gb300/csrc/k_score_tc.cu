@@ -18,10 +18,11 @@
 // (double buffer), so the epilogue of one key tile overlaps the MMAs of the next.
 //
 // Roles (one CTA per SM, persistent, static round-robin over items ordered heaviest first):
-//   warp 0      TMA producer: B (q_idx rows, 64 KB, 2 buffers) and A (k_idx K-halves, 16 KB, 4 stages)
+//   warp 0      TMA producer: B (q_idx rows, 64 KB, 2 buffers) and A (k_idx K-halves, 16 KB, 3 stages)
 //   warp 1      TMEM allocation and the tcgen05.mma issue (warp-wide loop, one elected lane issues)
 //   warps 2..9  epilogue (TMEM -> registers -> ReLU.w reduction -> shared score rows, two item buffers)
-//   warps 10..13 top-k, one warp per row, on the previous item while the epilogue runs the next one:
+//   warps 10..17 top-k, one warp per row, two sets taking alternate items (three score buffers), while the
+//               epilogue runs the following items:
 //               the exact k-th largest score by a bitwise search on order-preserving keys held in
 //               registers, then the selection written by a stable ballot compaction.
 //
@@ -67,18 +68,19 @@ constexpr int NKEY = 128;                     // keys per tile (MMA M)
 constexpr int NCOL = ROWS * HI;               // MMA N = 256
 constexpr int NCMAX = 1024;                   // longest key axis held in shared memory
 constexpr int A_HALF = NKEY * 64 * 2;         // 16 KB: one 64-wide K-half of a key tile
-constexpr int A_STAGES = 4;
+constexpr int A_STAGES = 3;
 constexpr int B_HALF = NCOL * 64 * 2;         // 32 KB
 constexpr int B_BUF = 2 * B_HALF;             // 64 KB
-constexpr int THREADS = 448;                  // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..13 selection
+constexpr int THREADS = 576;                  // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..17 selection
 constexpr int EPI = 256;
-constexpr int SEL_WARP0 = 10;
+constexpr int SEL_WARP0 = 10;                 // two sets of four selection warps take alternate items
+constexpr int NSC = 3;                        // item score buffers
 constexpr int TMEM_COLS = 512;
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + A_STAGES * A_HALF;           // 64 KB
 constexpr int OFF_SC = OFF_B + 2 * B_BUF;                  // 192 KB
-constexpr int OFF_W = OFF_SC + 2 * ROWS * NCMAX * 4;       // 224 KB: score rows of two items
+constexpr int OFF_W = OFF_SC + NSC * ROWS * NCMAX * 4;     // score rows of three items
 constexpr int OFF_MISC = OFF_W + ROWS * HI * 4;            // 209 KB
 constexpr int SMEM_BYTES = OFF_MISC + 1024;
 constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;              // slack to align the base to 1024 B
@@ -303,7 +305,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
     uint64_t *a_full = bars, *a_empty = bars + 4, *b_full = bars + 8, *b_empty = bars + 10;
     uint64_t *t_full = bars + 12, *t_empty = bars + 14, *mma_done = bars + 16;
-    uint64_t *sc_full = bars + 17, *sc_empty = bars + 19;  // score rows of an item: epilogue -> selection
+    uint64_t *sc_full = bars + 17, *sc_empty = bars + 17 + NSC;  // score rows of an item: epilogue -> selection
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 256);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 264);
 
@@ -318,6 +320,8 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mbar_init(b_empty + i, 1);
             mbar_init(t_full + i, 1);
             mbar_init(t_empty + i, 8);
+        }
+        for (int i = 0; i < NSC; i++) {
             mbar_init(sc_full + i, EPI / 32);
             mbar_init(sc_empty + i, ROWS);
         }
@@ -341,7 +345,8 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
             int hs = 0, ai = 0;
-            int last_hs[A_STAGES] = {-1, -1, -1, -1};
+            int last_hs[A_STAGES];
+            for (int x = 0; x < A_STAGES; x++) last_hs[x] = -1;
             int last_ai[2] = {-1, -1};
             for (int i = blockIdx.x; i < total; i += gridDim.x) {
                 const Item it = decode_item(a, i, total);
@@ -449,9 +454,10 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             sW[et] = w_next;
             w_next = w_of(i + gridDim.x);
             named_bar(1, EPI);
-            // this item's score rows go to buffer ic & 1, free once the selection warps have read item ic - 2
-            float *scb = sSC + (ic & 1) * ROWS * NCMAX;
-            wait_bar(sc_empty + (ic & 1), ((ic >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 7);
+            // this item's score rows go to buffer ic % NSC, free once the selection warps have read item ic - NSC
+            const int sb = ic % NSC, su = ic / NSC;
+            float *scb = sSC + sb * ROWS * NCMAX;
+            wait_bar(sc_empty + sb, (su & 1) ^ 1, abort_flag, &g_tc_error, 7);
             const int nt = (it.vmax + NKEY - 1) / NKEY;
             for (int t = 0; t < nt; t++) {
                 const int tb = tc & 1;
@@ -480,16 +486,19 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             }
             // hand the item's score rows to the selection warps
             __syncwarp();
-            if (lane == 0) mbar_arrive(sc_full + (ic & 1));
+            if (lane == 0) mbar_arrive(sc_full + sb);
         }
     } else {
-        // ---------------------------------------------------------- selection (warps 10..13, one row each)
-        const int k = warp - SEL_WARP0;
+        // ---------------------------------------------------------- selection (warps 10..17: two sets of four,
+        // alternate items, one row per warp)
+        const int k = (warp - SEL_WARP0) & 3, set = (warp - SEL_WARP0) >> 2;
         int ic = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
+            if ((ic & 1) != set) continue;
             const Item it = decode_item(a, i, total);
-            wait_bar(sc_full + (ic & 1), (ic >> 1) & 1, abort_flag, &g_tc_error, 8);
-            const float *sc = sSC + (ic & 1) * ROWS * NCMAX + k * NCMAX;
+            const int sb = ic % NSC, su = ic / NSC;
+            wait_bar(sc_full + sb, su & 1, abort_flag, &g_tc_error, 8);
+            const float *sc = sSC + sb * ROWS * NCMAX + k * NCMAX;
             if (k < it.n) {
                 const long long r = it.row[k];
                 if (a.dump != nullptr && r >= a.dump_row0 && r < a.dump_row0 + a.dump_rows) {
@@ -498,10 +507,10 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 }
             }
             if (k < it.n && a.ids != nullptr) {
-                select_row(a, it, k, sc, sc_empty + (ic & 1));
+                select_row(a, it, k, sc, sc_empty + sb);
             } else {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sc_empty + (ic & 1));
+                if (lane == 0) mbar_arrive(sc_empty + sb);
             }
         }
     }
