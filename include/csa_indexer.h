@@ -76,6 +76,15 @@ typedef enum {
 typedef enum { CSA_SBHD = 0, CSA_BSHD = 1, CSA_THD = 2 } csa_layout;
 typedef enum { CSA_F32 = 0, CSA_BF16 = 1 } csa_dtype;
 
+/* Which teacher the loss distils ([BUG] "Paper reference" and sec. 3 for the full one; sec. 1, the
+ * compressed-only teacher the issue reports as the bug).
+ *   CSA_TEACHER_FULL: each head's denominator takes the sink, the sliding window and the selected
+ *     compressed keys together (Z_h = e^{a_h} + sum_C e^{c_hj} + sum_W e^{w_hr}).
+ *   CSA_TEACHER_COMPRESSED_ONLY: a per-head softmax over the compressed support alone (no sink, no
+ *     window), i.e. the teacher the issue shows to be wrong; kept as an A/B negative control.  kv and
+ *     sink are still validated but not read. */
+typedef enum { CSA_TEACHER_FULL = 0, CSA_TEACHER_COMPRESSED_ONLY = 1 } csa_teacher_mode;
+
 /* Geometry and flags of one step.  A plain struct read on the host; the two cu_seqlens pointers are
  * device pointers.  Megatron's flags map as: index_topk -> topk, dsa_indexer_use_sparse_loss ->
  * sparse_loss, calculate_per_token_loss -> reduction = 1, dsa_indexer_loss_coeff -> loss_coeff
@@ -101,6 +110,7 @@ typedef struct {
     int32_t sparse_loss;                  /* 1: support C = selected keys.  0: C = every visible key */
     int32_t reduction;                    /* 0: mean over physical rows.  1: sum (per-token loss) */
     float loss_coeff;                     /* multiplies the loss and every gradient */
+    int32_t teacher_mode;                 /* csa_teacher_mode; 0 (full CSA) when zero-initialised */
 } csa_params;
 
 /* ------------------------------------------------------------------ sizes (host only, no CUDA call) */

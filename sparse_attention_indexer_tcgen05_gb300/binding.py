@@ -42,6 +42,10 @@ STATUS = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "C
           4: "CSA_ERR_WORKSPACE", 5: "CSA_ERR_CUDA", 6: "CSA_ERR_TIMEOUT"}
 
 
+# csa_teacher_mode: the full-CSA teacher, or the compressed-only one the issue reports (A/B control)
+TEACHER_MODES = {"full": 0, "compressed_only": 1}
+
+
 class csa_params(ctypes.Structure):
     _fields_ = [
         ("layout", ctypes.c_int32), ("dtype", ctypes.c_int32), ("batch", ctypes.c_int32),
@@ -50,7 +54,7 @@ class csa_params(ctypes.Structure):
         ("window", ctypes.c_int32), ("topk", ctypes.c_int32), ("heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float), ("sparse_loss", ctypes.c_int32), ("reduction", ctypes.c_int32),
-        ("loss_coeff", ctypes.c_float),
+        ("loss_coeff", ctypes.c_float), ("teacher_mode", ctypes.c_int32),
     ]
 
 
@@ -112,7 +116,7 @@ class Params:
 
     def __init__(self, layout, dtype, batch, seqlen, compress_ratio, window, topk, heads, head_dim, idx_heads,
                  idx_dim, softmax_scale, sparse_loss=True, reduction="mean", loss_coeff=1.0, cu_seqlens_q=None,
-                 cu_seqlens_q_unpadded=None, max_seqlen_q=0, key_rows=0):
+                 cu_seqlens_q_unpadded=None, max_seqlen_q=0, key_rows=0, teacher_mode="full"):
         self.cu = cu_seqlens_q
         self.cur = cu_seqlens_q_unpadded
         for t in (self.cu, self.cur):
@@ -126,7 +130,8 @@ class Params:
                             self.cur.data_ptr() if self.cur is not None else None, int(max_seqlen_q), int(key_rows),
                             int(compress_ratio), int(window), int(topk), int(heads), int(head_dim), int(idx_heads),
                             int(idx_dim), float(softmax_scale), 1 if sparse_loss else 0,
-                            0 if reduction in ("mean", 0) else 1, float(loss_coeff))
+                            0 if reduction in ("mean", 0) else 1, float(loss_coeff),
+                            TEACHER_MODES[teacher_mode] if isinstance(teacher_mode, str) else int(teacher_mode))
 
     @property
     def ref(self):

@@ -57,6 +57,7 @@ csa_status make_plan(const csa_params *p, Plan *P)
     if (p->heads < 1 || p->head_dim < 1 || p->idx_heads < 1 || p->idx_dim < 1) return CSA_ERR_INVALID_ARG;
     if (p->sparse_loss != 0 && p->sparse_loss != 1) return CSA_ERR_INVALID_ARG;
     if (p->reduction != 0 && p->reduction != 1) return CSA_ERR_INVALID_ARG;
+    if (p->teacher_mode != CSA_TEACHER_FULL && p->teacher_mode != CSA_TEACHER_COMPRESSED_ONLY) return CSA_ERR_INVALID_ARG;
     if (!isfinite(p->softmax_scale) || !isfinite(p->loss_coeff)) return CSA_ERR_INVALID_ARG;
     if (p->batch < 1 || p->seqlen < 0) return CSA_ERR_INVALID_ARG;
 
@@ -66,7 +67,9 @@ csa_status make_plan(const csa_params *p, Plan *P)
     g.B = p->batch;
     g.S = p->seqlen;
     g.ratio = p->compress_ratio;
-    g.window = p->window;
+    // the compressed-only teacher is the full one with no window and no sink
+    g.window = p->teacher_mode == CSA_TEACHER_COMPRESSED_ONLY ? 0 : p->window;
+    g.no_sink = p->teacher_mode == CSA_TEACHER_COMPRESSED_ONLY ? 1 : 0;
     g.H = p->heads;
     g.D = p->head_dim;
     g.HI = p->idx_heads;

@@ -29,6 +29,7 @@ struct Geo {
     long long key_rows;
     float scale;       // sigma
     int sparse;
+    int no_sink;       // compressed-only teacher: the sink term is dropped (and the window is 0)
     float factor;      // loss_coeff / rows (mean) or loss_coeff (sum)
     const int *cu_q;   // THD physical offsets
     const int *cu_real;// THD unpadded offsets (== cu_q when none given)

@@ -387,7 +387,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     float2 p[4];
 #pragma unroll
                     for (int k = 0; k < 4; k++) p[k] = sPart[k * M + rh];
-                    const float ah = __ldg(a.sink + h) * 1.4426950408889634f;
+                    const float ah = g.no_sink ? -INFINITY : __ldg(a.sink + h) * 1.4426950408889634f;
                     const float mm = fmaxf(fmaxf(fmaxf(p[0].x, p[1].x), fmaxf(p[2].x, p[3].x)), ah);
                     float S = 0.f;
                     if (mm != -INFINITY) {

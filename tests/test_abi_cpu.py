@@ -56,13 +56,20 @@ def test_sizes(B):
 
 @pytest.mark.parametrize("field,value", [("compress_ratio", 0), ("topk", 0), ("window", -1), ("heads", 0),
                                          ("batch", 0), ("seqlen", -5), ("reduction", 2), ("sparse_loss", 3),
-                                         ("layout", 7), ("dtype", 9), ("key_rows", 5)])
+                                         ("layout", 7), ("dtype", 9), ("key_rows", 5), ("teacher_mode", 2)])
 def test_invalid_params_rejected(B, field, value):
     p = _params(B)
     setattr(p.c, field, value)
     assert p.K == -1 and p.workspace_bytes == 0
     st = B._lib.csa_indexer_fwd(p.ref, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 1 << 40, None)
     assert st == 1
+
+
+def test_teacher_mode_accepted(B):
+    """The compressed-only teacher changes no width: it is the same step with the sink and window dropped."""
+    full, comp = _params(B), _params(B, teacher_mode="compressed_only")
+    assert comp.c.teacher_mode == 1 and full.c.teacher_mode == 0
+    assert (comp.K, comp.teacher_width, comp.workspace_bytes) == (full.K, full.teacher_width, full.workspace_bytes)
 
 
 def test_thd_requires_offsets(B):

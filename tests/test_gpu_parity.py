@@ -131,6 +131,41 @@ def test_no_window_no_sink_and_sum_reduction():
     _report("no_window_no_sink_sum", U.check_step(inp))
 
 
+@pytest.mark.parametrize("dtype,wide", [("f32", False), ("bf16", True)])
+def test_compressed_only_teacher_is_a_negative_control(dtype, wide):
+    """teacher_mode="compressed_only" is the teacher the issue reports as the bug (a per-head softmax over the
+    selected compressed keys alone).  It must equal the oracle's teacher with no window and no sink, and be
+    blind to the window values and the sink, both of which move the full-CSA teacher.  wide=True takes the
+    tensor-core teacher (64 heads), wide=False the CUDA-core one."""
+    if wide:
+        cfg = small(dtype=dtype, heads=64, head_dim=64, idx_heads=64, idx_dim=128, seqlen=600, topk=64, window=32)
+    else:
+        cfg = small(dtype=dtype)
+    base = synth.generate(cfg)
+    d_full = workload.to_device(base)
+    d_comp = workload.to_device(base, teacher_mode="compressed_only")
+    ids, _ = B.csa_indexer_fwd(d_full.params, *d_full.indexer)
+    t_full = B.csa_teacher(d_full.params, *d_full.teacher_side, ids).cpu().numpy()
+    t_comp = B.csa_teacher(d_comp.params, *d_comp.teacher_side, ids).cpu().numpy()
+    B.csa_check_device_status()
+    ref = O.Problem.from_inputs(base, window=0).teacher(base.q.values, base.kv.values, base.kv_c.values,
+                                                        np.full(cfg.heads, -np.inf), ids.cpu().numpy())
+    err = U.row_l1(t_comp, ref)
+    assert err <= U.value_tol(dtype), f"compressed-only teacher row L1 error {err}"
+    moved = 0.0
+    for v in (0, 4):  # every window value moved by +-3; one head's sink moved by +3
+        inp = synth.dense_variant(base, v)
+        kv = workload.tensor_to_torch(inp.kv, dtype, "cuda:0")
+        sink = workload.tensor_to_torch(inp.sink, "f32", "cuda:0")
+        t_comp2 = B.csa_teacher(d_comp.params, d_comp.q, kv, d_comp.kv_c, sink, ids).cpu().numpy()
+        t_full2 = B.csa_teacher(d_full.params, d_full.q, kv, d_full.kv_c, sink, ids).cpu().numpy()
+        assert np.array_equal(t_comp2, t_comp), f"variant {v} moved the compressed-only teacher"
+        moved = max(moved, float(np.abs(t_full2 - t_full).sum() / np.abs(t_full).sum()))
+    assert moved > 1e-6, "the full teacher ignored the window and the sink"
+    _report(f"compressed_only_teacher_{dtype}", dict(teacher_err=err, full_teacher_change=moved,
+                                                     path=B.csa_last_path()))
+
+
 def test_window_longer_than_sequence_and_topk_above_keys():
     cfg = small(seqlen=64, window=500, topk=1000)
     _report("window_gt_seq", U.check_step(synth.generate(cfg)))
