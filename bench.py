@@ -63,11 +63,10 @@ def workload_desc(cfg) -> dict:
 
 # ------------------------------------------------------------------ algorithmic work per step
 
-def algorithmic(cfg, inp):
-    """Per-stage algorithmic FLOPs and minimal HBM bytes of one step (exact sums over rows)."""
-    from oracle import oracle as O  # geometry only (key counts per row)
-    P = O.Problem.from_inputs(inp)
-    rows = np.arange(P.rows)
+def algorithmic(cfg, inp, K: int, nrows: int):
+    """Per-stage algorithmic FLOPs, minimal HBM bytes and teacher exponentials of one step (exact sums over
+    rows).  K is the library's top-k width (csa_topk_width); the row geometry follows the layout."""
+    rows = np.arange(nrows)
     if cfg.layout == "thd":
         cu, cur = inp.cu_seqlens_q, inp.cu_seqlens_q_unpadded
         b = np.searchsorted(cu, rows, side="right") - 1
@@ -78,13 +77,12 @@ def algorithmic(cfg, inp):
         s = rows % cfg.seqlen if cfg.layout == "bshd" else rows // cfg.batch
         v = (s + 1) // cfg.ratio
         wn = np.minimum(cfg.window, s + 1)
-    K = P.K
     k = np.minimum(v, K) if cfg.sparse else v
     k = np.where(v > 0, k, 0)
     wn = np.where(v > 0, wn, 0)
     HI, DI, H, D = cfg.idx_heads, cfg.idx_dim, cfg.heads, cfg.head_dim
     eb = 2 if cfg.dtype == "bf16" else 4
-    n = P.rows
+    n = nrows
     nk = inp.k_idx.shape[0] * (inp.k_idx.shape[1] if cfg.layout != "thd" else 1)
     fl = {
         "score_topk": float(np.sum(2.0 * HI * DI * v)),
@@ -99,7 +97,10 @@ def algorithmic(cfg, inp):
         # q_idx, w, ids, selscore read; dq, dw written; k_idx read, dk written
         "kl_grad": n * (2 * HI * DI * eb + 2 * HI * 4 + 2 * K * 4) + 2 * nk * DI * eb,
     }
-    return fl, by
+    # exponentials of the teacher's factored form: the sink, every window and support logit for l_h, then
+    # exp(c - l_h) again for every support logit
+    ex = float(np.sum(np.where(v > 0, H * (1 + wn + 2 * k), 0)))
+    return fl, by, ex
 
 
 # ------------------------------------------------------------------ clocks
@@ -289,7 +290,7 @@ def run_ours(args, cfg):
     path = B.csa_last_path()
 
     # ---- per-stage times (dominant kernel for the roofline), same stream, CUDA events
-    fl, by = algorithmic(cfg, inp)
+    fl, by, exps = algorithmic(cfg, inp, p.K, p.rows)
     teacher_buf = torch.empty((p.rows, p.teacher_width), dtype=torch.float32, device=dev)
     stage_ms = {}
 
@@ -335,6 +336,12 @@ def run_ours(args, cfg):
                 "stage_frac_tensor": {k: fl[k] / (stage_ms[k] / 1e3) / 1e12 / tensor_peak for k in stage_ms},
                 "stage_frac_hbm": {k: by[k] / (stage_ms[k] / 1e3) / 1e9 / hbm_peak for k in stage_ms},
                 "algorithmic_flops": fl, "algorithmic_bytes": by}
+    # the third ceiling of the teacher: its exponentials against the measured MUFU ex2 rate
+    mufu_peak = tr.get("mufu_ex2_per_s") if os.path.exists(tr_path) else None
+    ex_rate = exps / (stage_ms["teacher"] / 1e3)
+    roofline["teacher_mufu"] = {"exps": exps, "achieved_per_s": ex_rate, "peak_per_s": mufu_peak,
+                                "frac": ex_rate / mufu_peak if mufu_peak else None,
+                                "peak_source": "measured (profiles/mufu_ex2_peak.md)" if mufu_peak else None}
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
     host = {n: workload.tensor_to_torch(getattr(inp, n), cfg.dtype if n not in ("w", "sink") else "f32", "cpu",
