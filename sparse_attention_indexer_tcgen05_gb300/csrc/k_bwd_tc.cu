@@ -54,7 +54,7 @@ constexpr int CH = 128;                        // rows per key-owner unit
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC_X = idesc_bf16(128, 128, false, false);   // X = k . q^T (key-owner), X^T = q . k^T
 constexpr uint32_t IDESC_DQ = idesc_bf16(128, 128, false, true);   // dQ' += G'^T k  (A in TMEM, B MN-major)
-constexpr uint32_t IDESC_DK = idesc_bf16(128, 128, false, true);   // dK += G q      (B MN-major)
+constexpr uint32_t IDESC_DK = idesc_bf16(128, 128, false, true);   // dK += G q      (A in TMEM, B MN-major)
 
 // row-owner shared memory
 constexpr int R_ASTG = 8;                                     // k-tile halves: four tiles in flight
@@ -68,14 +68,14 @@ constexpr int R_OFF_MISC = R_OFF_DW + 2 * 4 * M_PAIRS * 4;
 constexpr int R_SMEM = R_OFF_MISC + 1024 + 1024;
 
 // key-owner shared memory
-constexpr int K_BSTG = 3, K_GSTG = 4;
+constexpr int K_BSTG = 5, K_GSTG = 4;
 constexpr int K_OFF_A = 0;                                     // the unit's key tile, 32 KB
-constexpr int K_OFF_B = K_OFF_A + 2 * HALF;                    // 3 q blocks
-constexpr int K_OFF_G = K_OFF_B + K_BSTG * QBLK;               // 2 G buffers
-constexpr int K_OFF_GT = K_OFF_G + 2 * QBLK;                   // g tiles: 4 x 2 rows x 128 fp32
+constexpr int K_OFF_B = K_OFF_A + 2 * HALF;                    // 5 q blocks (G lives in TMEM)
+constexpr int K_OFF_GT = K_OFF_B + K_BSTG * QBLK;              // g tiles: 4 x 2 rows x 128 fp32
 constexpr int K_OFF_WT = K_OFF_GT + K_GSTG * RP * NKEY * 4;    // w rows: 4 x 2 rows x 64 fp32
 constexpr int K_OFF_MISC = K_OFF_WT + K_GSTG * RP * HI * 4;
 constexpr int K_SMEM = K_OFF_MISC + 1024 + 1024;
+static_assert((2 + 2 * K_BSTG + 10 + 2 * K_GSTG + 1) * 8 <= 256, "key-owner barriers overlap the TMEM slot");
 
 struct Args {
     Geo g;
@@ -642,14 +642,13 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem + K_OFF_A;
     unsigned char *sB = smem + K_OFF_B;
-    unsigned char *sG = smem + K_OFF_G;
     float *sGT = reinterpret_cast<float *>(smem + K_OFF_GT);
     float *sWT = reinterpret_cast<float *>(smem + K_OFF_WT);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_OFF_MISC);
-    uint64_t *a_full = bars, *a_empty = bars + 1, *b_full = bars + 2, *b_empty = bars + 5;
-    uint64_t *x_full = bars + 8, *x_empty = bars + 10, *gk_full = bars + 12, *gk_empty = bars + 14;
-    uint64_t *dk_full = bars + 16, *dk_empty = bars + 17, *gt_full = bars + 18, *gt_empty = bars + 22;
-    uint64_t *mma_done = bars + 26;
+    uint64_t *a_full = bars, *a_empty = bars + 1, *b_full = bars + 2, *b_empty = b_full + K_BSTG;
+    uint64_t *x_full = b_empty + K_BSTG, *x_empty = x_full + 2, *gk_full = x_full + 4, *gk_empty = x_full + 6;
+    uint64_t *dk_full = x_full + 8, *dk_empty = x_full + 9, *gt_full = x_full + 10, *gt_empty = gt_full + K_GSTG;
+    uint64_t *mma_done = gt_empty + K_GSTG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K_OFF_MISC + 256);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K_OFF_MISC + 264);
 
@@ -680,13 +679,15 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tX = tmem, tDK = tmem + 256;
+    // TMEM: X (2 x 128 fp32 columns), dK (128), G as the A operand of dK (2 x 64 columns of bf16 pairs)
+    const uint32_t tX = tmem, tDK = tmem + 256, tG = tmem + 384;
     const int total = unit_total(a);
 
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------------ TMA producer
             int uc = 0, qs = 0;
-            int last_qs[K_BSTG] = {-1, -1, -1};
+            int last_qs[K_BSTG];
+            for (int x = 0; x < K_BSTG; x++) last_qs[x] = -1;
             int last_uc = -1;
             for (int u = blockIdx.x; u < total; u += gridDim.x) {
                 const Unit U = decode_unit(a, u);
@@ -738,11 +739,11 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             if (!g_ready) wait_bar(gk_full + gkb, (gkc >> 1) & 1, abort_flag, err, 24);
             x_ready = probe_x();
             fence_after();
-            const unsigned char *pg = sG + gkb * QBLK, *pq = sB + bp * QBLK;
+            const unsigned char *pq = sB + bp * QBLK;
 #pragma unroll
             for (int s = 0; s < 8; s++)
-                mma_bf16_w(tDK, desc_kmajor(pg + (s >> 2) * HALF + (s & 3) * 32), desc_sw128(pq + s * 2048, HALF, 1024),
-                           IDESC_DK, (first && s == 0) ? 0u : 1u);
+                mma_bf16_ts_w(tDK, tG + gkb * 64 + s * 8, desc_sw128(pq + s * 2048, HALF, 1024), IDESC_DK,
+                              (first && s == 0) ? 0u : 1u);
             mma_commit_w(gk_empty + gkb);
             mma_commit_w(b_empty + bp);
             gkc++;
@@ -901,12 +902,10 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
                 }
                 const int gkb = gkc & 1;
                 wait_bar(gk_empty + gkb, ((gkc >> 1) & 1) ^ 1, abort_flag, err, 31);
-                unsigned char *dst = sG + gkb * QBLK + half * HALF;
-#pragma unroll
-                for (int c = 0; c < 8; c++)
-                    *reinterpret_cast<uint4 *>(dst + sw128_off(k, c)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                fence_async_smem();
+                fence_after();
+                // G[key, (row, h)] of this warp's row half: K = (row, h) pairs, columns 32 half .. +32 of buffer gkb
+                tmem_st32(tG + ((uint32_t)(quad * 32) << 16) + (uint32_t)(gkb * 64 + half * 32), pk);
+                fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gk_full + gkb);
                 xc++;
