@@ -58,7 +58,8 @@ constexpr uint32_t IDESC_DK = idesc_bf16(128, 128, false, true);   // dK += G q 
 
 // row-owner shared memory
 constexpr int R_ASTG = 8;                                     // k-tile halves: four tiles in flight
-static_assert((2 * R_ASTG + 19) * 8 <= 512, "row-owner barriers overlap the TMEM slot");
+constexpr int R_XSTG = 3;                                     // X / G' TMEM slots
+static_assert((2 * R_ASTG + 11 + 3 * R_XSTG) * 8 <= 512, "row-owner barriers overlap the TMEM slot");
 constexpr int R_OFF_A = 0;
 constexpr int R_OFF_B = R_OFF_A + R_ASTG * HALF;              // 128 KB: the q tiles of two items
 constexpr int R_OFF_GD = R_OFF_B + 2 * QBLK;                  // 192 KB: 2 bufs x 2 rows x NCMAX fp32
@@ -264,9 +265,9 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     float *sDW = reinterpret_cast<float *>(smem + R_OFF_DW);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + R_OFF_MISC);
     uint64_t *a_full = bars, *a_empty = bars + R_ASTG, *b_full = bars + 2 * R_ASTG, *b_empty = b_full + 2;
-    uint64_t *x_full = b_full + 4, *x_empty = b_full + 6, *g_full = b_full + 8, *g_empty = b_full + 10;
-    uint64_t *dq_full = b_full + 12, *dq_empty = b_full + 13, *gd_full = b_full + 14, *gd_empty = b_full + 16;
-    uint64_t *mma_done = b_full + 18;                                  // 2 R_ASTG + 19 barriers < 512 B
+    uint64_t *x_full = b_full + 4, *x_empty = x_full + R_XSTG, *g_full = x_empty + R_XSTG;
+    uint64_t *dq_full = g_full + R_XSTG, *dq_empty = dq_full + 1, *gd_full = dq_full + 2, *gd_empty = dq_full + 4;
+    uint64_t *mma_done = dq_full + 6;                                  // 2 R_ASTG + 11 + 3 R_XSTG barriers
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + R_OFF_MISC + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + R_OFF_MISC + 520);
 
@@ -280,14 +281,13 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         for (int i = 0; i < 2; i++) {
             mbar_init(b_full + i, 1);
             mbar_init(b_empty + i, R_EPI / 32);
-            mbar_init(x_full + i, 1);
-            mbar_init(x_empty + i, R_EPI / 32);
             mbar_init(gd_full + i, 1);
             mbar_init(gd_empty + i, R_EPI / 32);
         }
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < R_XSTG; i++) {
+            mbar_init(x_full + i, 1);
+            mbar_init(x_empty + i, 1);
             mbar_init(g_full + i, R_EPI / 32);
-            mbar_init(g_empty + i, 1);
         }
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, R_EPI / 32);
@@ -300,8 +300,10 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM: X^T (2 x 128 fp32 columns), G'^T as the A operand of dQ' (2 x 64 columns of bf16 pairs), dQ' (128)
-    const uint32_t tX = tmem, tG = tmem + 256, tDQ = tmem + 384;
+    // TMEM: three slots of 128 columns, each holding one key tile's X^T (fp32) and then, in place, its G'^T as
+    // the A operand of dQ' (bf16 pairs; epilogue warp qq writes its 16 pair columns over the first half of its
+    // own 32 X columns, so key pairs of keys [16 s, 16 s + 16) sit at column 32 (s / 2) + 8 (s % 2)); dQ' (128).
+    const uint32_t tX = tmem, tDQ = tmem + R_XSTG * 128;
     const int total = pair_total(a);
 
     if (warp == 0) {
@@ -377,30 +379,39 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         // (mbar_test); a probe that comes back false falls back to the bounded waits.
         //   X^T[(row,h), key] = q . k^T   (A = the item's q tile, B = the k tile, both K-major)
         //   dQ'[(row,h), d]  += G'^T k    (A = G'^T from TMEM, B = the same k tile read MN-major)
-        int st = 0, ai = 0, xc = 0, gc = 0, dqc = 0, k = 0, nt_lane = 0;
-        uint32_t aph = 0;
-        bool x_ready = false, g_ready = false;
+        // The dQ' group of a tile is issued two tiles behind its X^T (three X / G' slots), so the epilogue's
+        // X -> G' latency is covered by two X^T groups of tensor work.
+        int st = 0, ai = 0, dqc = 0, k = 0, nt_lane = 0;
+        int xb = 0, gb = 0;              // X slot of the next X^T group / of the next dQ' group
+        uint32_t aph = 0, xph = 0, gph = 0;
+        int sd = 0;                      // k-tile stage of the next dQ' group (dQ' groups follow the X order)
+        bool x_ready = false;
         auto probe_x = [&]() -> bool {
-            const bool r0 = mbar_test(x_empty + (xc & 1), ((xc >> 1) & 1) ^ 1);
+            const bool r0 = mbar_test(x_empty + xb, xph ^ 1);
             const bool r1 = mbar_test(a_full + st, aph);
             const bool r2 = mbar_test(a_full + st + 1, aph);
             return r0 && r1 && r2;
         };
-        auto mma2 = [&](int sp, bool first) {
-            const int gb = gc & 1;
+        auto mma2 = [&](bool first) {
             if (first) wait_bar(dq_empty, (dqc & 1) ^ 1, abort_flag, err, 3);
-            if (!g_ready) wait_bar(g_full + gb, (gc >> 1) & 1, abort_flag, err, 4);
+            wait_bar(g_full + gb, gph, abort_flag, err, 4);
             x_ready = probe_x();  // the next X group (this item's next tile or the next item's first)
             fence_after();
+            const int sp = sd;
+            sd = sd + 2 == R_ASTG ? 0 : sd + 2;
             const unsigned char *pk = sA + sp * HALF;
+            const uint32_t tg = tX + gb * 128;
 #pragma unroll
             for (int s = 0; s < 8; s++)
-                mma_bf16_ts_w(tDQ, tG + gb * 64 + s * 8, desc_sw128(pk + s * 2048, HALF, 1024), IDESC_DQ,
+                mma_bf16_ts_w(tDQ, tg + (s >> 1) * 32 + (s & 1) * 8, desc_sw128(pk + s * 2048, HALF, 1024), IDESC_DQ,
                               (first && s == 0) ? 0u : 1u);
-            mma_commit_w(g_empty + gb);
+            mma_commit_w(x_empty + gb);
             mma_commit_w(a_empty + sp);
             mma_commit_w(a_empty + sp + 1);
-            gc++;
+            if (++gb == R_XSTG) {
+                gb = 0;
+                gph ^= 1u;
+            }
         };
         for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
             if ((k & 31) == 0) {
@@ -413,38 +424,35 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, err, 5);
             fence_after();
             const unsigned char *pq = sB + bb * QBLK;
-            int st_prev = 0;
             for (int t = 0; t < nt; t++) {
-                const int tb = xc & 1;
                 if (!x_ready) x_ready = probe_x();
                 if (!x_ready) {
-                    wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 6);
+                    wait_bar(x_empty + xb, xph ^ 1, abort_flag, err, 6);
                     wait_bar(a_full + st, aph, abort_flag, err, 7);
                     wait_bar(a_full + st + 1, aph, abort_flag, err, 7);
                 }
                 x_ready = false;
-                g_ready = t > 0 && mbar_test(g_full + (gc & 1), (gc >> 1) & 1);  // the dQ group issued next
                 fence_after();
                 const unsigned char *pk = sA + st * HALF;
 #pragma unroll
                 for (int kh = 0; kh < 2; kh++)
 #pragma unroll
                     for (int k4 = 0; k4 < 4; k4++)
-                        mma_bf16_w(tX + tb * 128, desc_kmajor(pq + kh * HALF + k4 * 32), desc_kmajor(pk + kh * HALF + k4 * 32),
-                                   IDESC_X, (kh | k4) ? 1u : 0u);
-                mma_commit_w(x_full + tb);
-                xc++;
-                const int st_cur = st;
+                        mma_bf16_w(tX + xb * 128, desc_kmajor(pq + kh * HALF + k4 * 32),
+                                   desc_kmajor(pk + kh * HALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
+                mma_commit_w(x_full + xb);
+                if (++xb == R_XSTG) {
+                    xb = 0;
+                    xph ^= 1u;
+                }
                 st += 2;
                 if (st == R_ASTG) {
                     st = 0;
                     aph ^= 1u;
                 }
-                if (t > 0) mma2(st_prev, t == 1);
-                st_prev = st_cur;
+                if (t >= 2) mma2(t == 2);
             }
-            g_ready = false;
-            mma2(st_prev, nt == 1);
+            for (int t = nt < 2 ? 0 : nt - 2; t < nt; t++) mma2(t == 0);
             mma_commit_w(dq_full);
             dqc++;
             ai++;
@@ -519,7 +527,8 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const int rh = quad * 32 + lane;
         const int er = rh >> 6, h = rh & 63;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        int xc = 0, gc = 0, dqc = 0, ai = 0, ic = 0;
+        int xb = 0, dqc = 0, ai = 0, ic = 0;
+        uint32_t xph = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
             const Pair p = decode_pair(a, i);
             const int gb = ic & 1;
@@ -528,12 +537,12 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const int v_me = er == 0 ? p.v0 : p.v1;
             const int nt = (p.vmax + NKEY - 1) / NKEY;
             for (int t = 0; t < nt; t++) {
-                const int tb = xc & 1;
-                wait_bar(x_full + tb, (xc >> 1) & 1, abort_flag, err, 10);
+                wait_bar(x_full + xb, xph, abort_flag, err, 10);
                 fence_after();
                 const int j0 = t * NKEY + qq * 32;  // first key of this warp's columns
                 uint32_t xr[32];
-                tmem_ld32_async(tX + lane_off + (uint32_t)(tb * 128 + qq * 32), xr);
+                const uint32_t tcol = tX + lane_off + (uint32_t)(xb * 128 + qq * 32);
+                tmem_ld32_async(tcol, xr);
                 // g of the row for these 32 keys (the same addresses across the warp: broadcast reads), fetched
                 // while the TMEM load is in flight; keys at or beyond the row's visible count give 0
                 float gk[32];
@@ -552,18 +561,14 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 for (int q2 = 0; q2 < 16; q2++)
                     pk[q2] = pack_bf16(__uint_as_float(xr[2 * q2]) > 0.f ? gk[2 * q2] : 0.f,
                                        __uint_as_float(xr[2 * q2 + 1]) > 0.f ? gk[2 * q2 + 1] : 0.f);
+                tmem_st16(tcol, pk);  // G' over this warp's own X columns (already read)
                 fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(x_empty + tb);
-                const int gbuf = gc & 1;
-                wait_bar(g_empty + gbuf, ((gc >> 1) & 1) ^ 1, abort_flag, err, 11);
-                fence_after();
-                tmem_st16(tG + lane_off + (uint32_t)(gbuf * 64 + qq * 16), pk);
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(g_full + gbuf);
-                xc++;
-                gc++;
+                if (lane == 0) mbar_arrive(g_full + xb);
+                if (++xb == R_XSTG) {
+                    xb = 0;
+                    xph ^= 1u;
+                }
             }
             // ---- dQ' readout: this warp's 32 of the 128 d of its (row, head)
             const bool exists = er < p.n;
