@@ -245,18 +245,15 @@ csa_status run_bwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
     float *gbuf = reinterpret_cast<float *>(ws_at(ws, P.off_g));
     float *row_loss = row_loss_out ? row_loss_out : reinterpret_cast<float *>(ws_at(ws, P.off_rowloss));
     const bool tc = tc_bwd_supported(g, sizeof(T) == 2);
-    const int NT = tc_bwd_tiles(g);
     char *btc = ws_at(ws, P.off_btc);
-    int32_t *toff = (tc && g.sparse)
-                        ? reinterpret_cast<int32_t *>(btc + align_up(sizeof(int) * 2 * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1)))
-                        : nullptr;
-    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, toff, NT, st));
+    float *gd = tc ? tc_bwd_gd(g, btc) : nullptr;
+    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, gd, tc ? tc_bwd_ncp(g) : 0, st));
     if (g.key_rows * g.DI > 0)
         CSA_CUDA(cudaMemsetAsync(dk_acc, 0, sizeof(float) * (size_t)g.key_rows * g.DI, st));
     if (tc) {
         t_last_path = "tcgen05";
-        CSA_CUDA(launch_bwd_tc(g, (const __nv_bfloat16 *)q_idx, w, (const __nv_bfloat16 *)k_idx, ids, gbuf, toff,
-                               (__nv_bfloat16 *)dq_idx, dw, dk_acc, btc, st));
+        CSA_CUDA(launch_bwd_tc(g, (const __nv_bfloat16 *)q_idx, w, (const __nv_bfloat16 *)k_idx, (__nv_bfloat16 *)dq_idx,
+                               dw, dk_acc, btc, st));
     } else {
         CSA_TRY(check_smem(grad_generic_smem(g)));
         t_last_path = "generic";

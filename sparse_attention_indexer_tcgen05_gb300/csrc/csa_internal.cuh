@@ -152,7 +152,7 @@ template <typename T>
 cudaError_t launch_teacher_generic(const Geo &g, const T *q, const T *kv, const T *kv_c, const float *sink,
                                    const int32_t *ids, float *teacher, cudaStream_t st);
 cudaError_t launch_kl(const Geo &g, const int32_t *ids, const float *selscore, const float *dense_scores,
-                      const float *teacher, float *gbuf, float *row_loss, int32_t *toff, int NT, cudaStream_t st);
+                      const float *teacher, float *gbuf, float *row_loss, float *gd, int ncp, cudaStream_t st);
 template <typename T>
 cudaError_t launch_grad_generic(const Geo &g, const T *q_idx, const float *w, const T *k_idx,
                                 const int32_t *ids, const float *gbuf, T *dq_idx, float *dw, float *dk_acc,

@@ -23,21 +23,27 @@ cudaError_t launch_score_dump_tc(const Geo &g, const __nv_bfloat16 *q_idx, const
                                  const __nv_bfloat16 *k_idx, float *dump, long long row0, long long nrows,
                                  void *ws, cudaStream_t st);
 
-// TMA tensor maps (bf16, 128-byte swizzle): q_idx as [rows][H_I][D_I] with a 64 x H_I x 1 box, and k_idx with a
+// TMA tensor maps (bf16, 128-byte swizzle; rank <= 5): q_idx as [rows][H_I][D_I] with a 64 x H_I x 1 box, and k_idx with a
 // 64 x 128-key box (2D over key rows, or 3D [n_c][B][D_I] for SBHD).
 bool tc_encode_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
                     const cuuint32_t *box);
 bool tc_encode_q_map(CUtensorMap *m, const void *q_idx, const Geo &g);
+// fp32, no swizzle (rank <= 5; strides in bytes, multiples of 16)
+bool tc_encode_f32(CUtensorMap *m, const float *base, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                   const cuuint32_t *box);
 bool tc_encode_k_map(CUtensorMap *m, const void *k_idx, const Geo &g);
 
 // Tensor-core backward (dQ_idx, dW, dK) for bf16, H_I = 64, D_I = 128, key axis <= 1024.
 bool tc_bwd_supported(const Geo &g, bool bf16);
 int tc_bwd_tiles(const Geo &g);
+// Row stride (floats) of the by-key gradient rows gd[rows][ncp] the KL step writes for the backward.
+int tc_bwd_ncp(const Geo &g);
 size_t tc_bwd_workspace_bytes(const Geo &g);
-// ws: tc_bwd_workspace_bytes(g) bytes; toff: the per-row key-tile slot offsets written by the KL kernel
+// Where gd lives inside that workspace.
+float *tc_bwd_gd(const Geo &g, void *ws);
+// ws: tc_bwd_workspace_bytes(g) bytes whose gd rows hold dloss/dI[row][key] for every visible key
 cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
-                          const int32_t *ids, const float *gbuf, const int32_t *toff, __nv_bfloat16 *dq, float *dw,
-                          float *dk_acc, void *ws, cudaStream_t st);
+                          __nv_bfloat16 *dq, float *dw, float *dk_acc, void *ws, cudaStream_t st);
 cudaError_t bwd_tc_read_clear_error(int *flag);
 
 // Tensor-core teacher for bf16, H = 64, D in {64, 128, 192}, key axis <= 1024.

@@ -57,12 +57,13 @@ constexpr uint32_t IDESC_DQ = idesc_bf16(128, 128, false, true);   // dQ' += G'^
 constexpr uint32_t IDESC_DK = idesc_bf16(128, 128, false, true);   // dK += G q      (A in TMEM, B MN-major)
 
 // row-owner shared memory
-constexpr int R_ASTG = 8;                                     // k-tile halves: four tiles in flight
+constexpr int R_ASTG = 4;                                     // k tiles in flight
 constexpr int R_XSTG = 3;                                     // X / G' TMEM slots
 static_assert((2 * R_ASTG + 11 + 3 * R_XSTG) * 8 <= 512, "row-owner barriers overlap the TMEM slot");
+constexpr int KTILE = 2 * HALF;                               // 32 KB: 128 keys x 128 d, two K-halves
 constexpr int R_OFF_A = 0;
-constexpr int R_OFF_B = R_OFF_A + R_ASTG * HALF;              // 128 KB: the q tiles of two items
-constexpr int R_OFF_GD = R_OFF_B + 2 * QBLK;                  // 192 KB: 2 bufs x 2 rows x NCMAX fp32
+constexpr int R_OFF_B = R_OFF_A + R_ASTG * KTILE;             // 128 KB: the q tiles of two items
+constexpr int R_OFF_GD = R_OFF_B + 2 * QBLK;                  // 192 KB: 2 bufs x key tiles x 2 rows x 128 fp32
 constexpr int R_OFF_W = R_OFF_GD + 2 * RP * NCMAX * 4;        // 208 KB: 2 bufs x 2 rows x 64 fp32
 constexpr int R_OFF_DW = R_OFF_W + 2 * RP * HI * 4;           // dW partials: 2 item parities x 4 d quarters x 128
 constexpr int R_OFF_MISC = R_OFF_DW + 2 * 4 * M_PAIRS * 4;
@@ -76,15 +77,11 @@ constexpr int K_OFF_GT = K_OFF_B + K_BSTG * QBLK;              // g tiles: 4 x 2
 constexpr int K_OFF_WT = K_OFF_GT + K_GSTG * RP * NKEY * 4;    // w rows: 4 x 2 rows x 64 fp32
 constexpr int K_OFF_MISC = K_OFF_WT + K_GSTG * RP * HI * 4;
 constexpr int K_SMEM = K_OFF_MISC + 1024 + 1024;
-static_assert((2 + 2 * K_BSTG + 10 + 2 * K_GSTG + 1) * 8 <= 256, "key-owner barriers overlap the TMEM slot");
+constexpr int K_XSTG = 3;                                      // X / G TMEM slots
+static_assert((2 + 2 * K_BSTG + 3 * K_XSTG + 2 + 2 * K_GSTG + 1) * 8 <= 256, "key-owner barriers overlap the TMEM slot");
 
 struct Args {
     Geo g;
-    const float *w;
-    const int32_t *ids;      // [rows, K]
-    const float *gbuf;       // [rows, TW] dloss/dI in the teacher's slot layout
-    const int32_t *toff;     // [rows, NT + 1] first slot of each key tile (sparse)
-    int NT;                  // key tiles of the widest key axis
     __nv_bfloat16 *dq;
     float *dw;
     float *dk_acc;           // [key rows, DI] fp32, zeroed by the caller
@@ -150,6 +147,7 @@ __device__ __forceinline__ int find_seg(const int *cu, int nseg, int x)
 struct Pair {
     Seg sg;
     int n;                    // rows present (1..2)
+    int s0;                   // position of the first row
     long long row0, row1;
     int v0, v1, vmax;
 };
@@ -170,6 +168,7 @@ __device__ Pair decode_pair(const Args &a, int i)
         s0 = (groups - 1 - i / g.B) * RP;
     }
     p.sg = seg_of(g, b);
+    p.s0 = s0;
     p.n = s0 + 1 < p.sg.len_phys ? 2 : 1;
     p.row0 = row_of(g, b, s0);
     p.row1 = p.n > 1 ? row_of(g, b, s0 + 1) : p.row0;
@@ -251,10 +250,31 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&p);
 }
 
+// TMA coordinates of a row pair (positions s0, s0 + 1 of segment b): (y, z) in the pair maps of q_idx and w
+// ([.., rows, 1] for BSHD / THD, [.., B, S] for SBHD), and the pair's first row in the position-major g rows.
+struct PairAt {
+    int y, z, prow;
+};
+__device__ __forceinline__ PairAt pair_at(const Geo &g, int b, int s0, long long row0)
+{
+    PairAt q;
+    if (g.layout == CSA_SBHD) {
+        q.y = b;
+        q.z = s0;
+        q.prow = b * g.S + s0;
+    } else {
+        q.y = (int)row0;
+        q.z = 0;
+        q.prow = (int)row0;
+    }
+    return q;
+}
+
 // ------------------------------------------------------------------ row-owner kernel: dQ_idx, dW
 
 __global__ void __launch_bounds__(R_THREADS, 1)
-dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_w, Args a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -291,7 +311,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, R_EPI / 32);
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);
         *abort_flag = 0;
         init_fence();
     }
@@ -308,23 +328,32 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------------ TMA producer
-            // k tiles stream through the half-stage ring; an item's q tile is requested as soon as its buffer
-            // is free: that buffer is probed before every k-half load of the previous item, and waited for at
-            // the latest when the item starts.
+            // k tiles stream through a four-tile ring (one copy per tile); an item's q tile (one copy for both
+            // rows) is requested as soon as its buffer is free: that buffer is probed before every k-tile load
+            // of the previous item, and waited for at the latest when the item starts.
             int hs = 0, ai = 0, qi = 0;
             int last_hs[R_ASTG];
             int last_q[2] = {-1, -1};
             for (int i = 0; i < R_ASTG; i++) last_hs[i] = -1;
-            auto load_q = [&](const Pair &p) {
+            // the item's g rows over its visible key tiles (one copy of both rows per tile) and its w rows, into
+            // buffer ai & 1
+            auto load_gw = [&](const Pair &p, const PairAt &at) {
+                const int gb = ai & 1;
+                wait_bar(gd_empty + gb, ((ai >> 1) & 1) ^ 1, abort_flag, err, 8);
+                const int nt = (p.vmax + NKEY - 1) / NKEY;
+                mbar_expect_tx(gd_full + gb, (uint32_t)(nt * RP * NKEY * 4 + RP * HI * 4));
+                for (int kt = 0; kt < nt; kt++)
+                    tma_load_2d(sGD + gb * RP * NCMAX + kt * RP * NKEY, &map_g, gd_full + gb, kt * NKEY, at.prow);
+                tma_load_3d(sW + gb * RP * HI, &map_w, gd_full + gb, 0, at.y, at.z);
+            };
+            auto load_q = [&](const PairAt &at) {
                 const int bb = qi & 1;
                 mbar_expect_tx(b_full + bb, QBLK);
-                for (int r = 0; r < RP; r++)
-                    for (int kh = 0; kh < 2; kh++)
-                        tma_load_3d(sB + bb * QBLK + kh * HALF + r * (HI * 128), &map_q, b_full + bb, kh * 64, 0,
-                                    (int)(r == 0 ? p.row0 : p.row1));
+                tma_load_5d(sB + bb * QBLK, &map_q, b_full + bb, 0, 0, at.y, at.z, 0);
                 last_q[bb] = qi;
                 qi++;
             };
+            auto at_of = [&](const Pair &p) { return pair_at(g, p.sg.b, p.s0, p.row0); };
             // the next item with visible keys after item index i (or total)
             auto next_item = [&](int i, Pair &np) -> int {
                 for (int j = i + gridDim.x; j < total; j += gridDim.x) {
@@ -342,25 +371,26 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             while (i < total) {
                 Pair nxt;
                 const int inext = next_item(i, nxt);
+                const PairAt at = at_of(cur);
                 if (qi == ai) {
                     wait_bar(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, err, 1);
-                    load_q(cur);
+                    load_q(at);
                 }
+                load_gw(cur, at);
                 const int nt = (cur.vmax + NKEY - 1) / NKEY;
-                for (int t = 0; t < nt; t++)
-                    for (int kh = 0; kh < 2; kh++) {
-                        if (qi == ai + 1 && inext < total && mbar_test(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1))
-                            load_q(nxt);
-                        const int st = hs % R_ASTG;
-                        wait_bar(a_empty + st, ((hs / R_ASTG) & 1) ^ 1, abort_flag, err, 2);
-                        mbar_expect_tx(a_full + st, HALF);
-                        if (sbhd)
-                            tma_load_3d(sA + st * HALF, &map_k, a_full + st, kh * 64, cur.sg.b, t * NKEY);
-                        else
-                            tma_load_2d(sA + st * HALF, &map_k, a_full + st, kh * 64, (int)(cur.sg.key_y + t * NKEY));
-                        last_hs[st] = hs;
-                        hs++;
-                    }
+                for (int t = 0; t < nt; t++) {
+                    if (qi == ai + 1 && inext < total && mbar_test(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1))
+                        load_q(at_of(nxt));
+                    const int st = hs % R_ASTG;
+                    wait_bar(a_empty + st, ((hs / R_ASTG) & 1) ^ 1, abort_flag, err, 2);
+                    mbar_expect_tx(a_full + st, KTILE);
+                    if (sbhd)
+                        tma_load_4d(sA + st * KTILE, &map_k, a_full + st, 0, cur.sg.b, t * NKEY, 0);
+                    else
+                        tma_load_3d(sA + st * KTILE, &map_k, a_full + st, 0, (int)(cur.sg.key_y + t * NKEY), 0);
+                    last_hs[st] = hs;
+                    hs++;
+                }
                 ai++;
                 i = inext;
                 cur = nxt;
@@ -369,50 +399,23 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 if (last_hs[st] >= 0) drain_bar(a_full + st, (last_hs[st] / R_ASTG) & 1, err);
             for (int bb = 0; bb < 2; bb++)
                 if (last_q[bb] >= 0) drain_bar(b_full + bb, (last_q[bb] >> 1) & 1, err);
+            for (int gb = 0; gb < 2 && gb < ai; gb++) {
+                const int last = ai - 1 - ((ai - 1 - gb) & 1);  // the last item that used buffer gb
+                drain_bar(gd_full + gb, (last >> 1) & 1, err);
+            }
         }
-    } else if (warp == 1) {
-        // -------------------------------------------------------------------- MMA issue (whole warp)
-        // The warp runs the loop together so stage indices and descriptors stay warp-uniform; one elected lane
-        // issues each MMA and commit.  Item decoding is lane-parallel: lane l decodes the CTA's item k + l, the
-        // loop reads the tile count of item k by a shuffle.  A half-stage ring: tile t takes stages
-        // (st, st + 1), parity aph (R_ASTG is even).  The next group's barriers are probed together and early
-        // (mbar_test); a probe that comes back false falls back to the bounded waits.
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------- MMA issue (two warps, whole warp each)
+        // Warp 1 issues the X^T groups, warp 2 the dQ' groups; each commits its own groups, so neither waits on
+        // the other's issue overhead.  Each warp runs its loop together (stage indices and descriptors stay
+        // warp-uniform; one elected lane issues); item decoding is lane-parallel: lane l decodes the CTA's item
+        // k + l, the loop reads the tile count of item k by a shuffle.  k-tile stage st, parity aph; X / G' slot
+        // xb, parity xph.
         //   X^T[(row,h), key] = q . k^T   (A = the item's q tile, B = the k tile, both K-major)
         //   dQ'[(row,h), d]  += G'^T k    (A = G'^T from TMEM, B = the same k tile read MN-major)
-        // The dQ' group of a tile is issued two tiles behind its X^T (three X / G' slots), so the epilogue's
-        // X -> G' latency is covered by two X^T groups of tensor work.
-        int st = 0, ai = 0, dqc = 0, k = 0, nt_lane = 0;
-        int xb = 0, gb = 0;              // X slot of the next X^T group / of the next dQ' group
-        uint32_t aph = 0, xph = 0, gph = 0;
-        int sd = 0;                      // k-tile stage of the next dQ' group (dQ' groups follow the X order)
-        bool x_ready = false;
-        auto probe_x = [&]() -> bool {
-            const bool r0 = mbar_test(x_empty + xb, xph ^ 1);
-            const bool r1 = mbar_test(a_full + st, aph);
-            const bool r2 = mbar_test(a_full + st + 1, aph);
-            return r0 && r1 && r2;
-        };
-        auto mma2 = [&](bool first) {
-            if (first) wait_bar(dq_empty, (dqc & 1) ^ 1, abort_flag, err, 3);
-            wait_bar(g_full + gb, gph, abort_flag, err, 4);
-            x_ready = probe_x();  // the next X group (this item's next tile or the next item's first)
-            fence_after();
-            const int sp = sd;
-            sd = sd + 2 == R_ASTG ? 0 : sd + 2;
-            const unsigned char *pk = sA + sp * HALF;
-            const uint32_t tg = tX + gb * 128;
-#pragma unroll
-            for (int s = 0; s < 8; s++)
-                mma_bf16_ts_w(tDQ, tg + (s >> 1) * 32 + (s & 1) * 8, desc_sw128(pk + s * 2048, HALF, 1024), IDESC_DQ,
-                              (first && s == 0) ? 0u : 1u);
-            mma_commit_w(x_empty + gb);
-            mma_commit_w(a_empty + sp);
-            mma_commit_w(a_empty + sp + 1);
-            if (++gb == R_XSTG) {
-                gb = 0;
-                gph ^= 1u;
-            }
-        };
+        const bool xw = warp == 1;
+        int st = 0, ai = 0, k = 0, nt_lane = 0, xb = 0;
+        uint32_t aph = 0, xph = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
             if ((k & 31) == 0) {
                 const int il = i + lane * (int)gridDim.x;
@@ -421,104 +424,54 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             const int nt = __shfl_sync(0xffffffffu, nt_lane, k & 31);
             if (nt == 0) continue;
             const int bb = ai & 1;
-            wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, err, 5);
-            fence_after();
+            if (xw) {
+                wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, err, 5);
+                fence_after();
+            }
             const unsigned char *pq = sB + bb * QBLK;
             for (int t = 0; t < nt; t++) {
-                if (!x_ready) x_ready = probe_x();
-                if (!x_ready) {
-                    wait_bar(x_empty + xb, xph ^ 1, abort_flag, err, 6);
-                    wait_bar(a_full + st, aph, abort_flag, err, 7);
-                    wait_bar(a_full + st + 1, aph, abort_flag, err, 7);
+                const unsigned char *pk = sA + st * KTILE;
+                if (xw) {
+                    const bool r0 = mbar_test(x_empty + xb, xph ^ 1);
+                    const bool r1 = mbar_test(a_full + st, aph);
+                    if (!(r0 && r1)) {
+                        wait_bar(x_empty + xb, xph ^ 1, abort_flag, err, 6);
+                        wait_bar(a_full + st, aph, abort_flag, err, 7);
+                    }
+                    fence_after();
+#pragma unroll
+                    for (int kh = 0; kh < 2; kh++)
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; k4++)
+                            mma_bf16_w(tX + xb * 128, desc_kmajor(pq + kh * HALF + k4 * 32),
+                                       desc_kmajor(pk + kh * HALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
+                    mma_commit_w(x_full + xb);
+                } else {
+                    if (t == 0) wait_bar(dq_empty, (ai & 1) ^ 1, abort_flag, err, 3);
+                    wait_bar(g_full + xb, xph, abort_flag, err, 4);
+                    fence_after();
+                    const uint32_t tg = tX + xb * 128;
+#pragma unroll
+                    for (int s = 0; s < 8; s++)
+                        mma_bf16_ts_w(tDQ, tg + (s >> 1) * 32 + (s & 1) * 8, desc_sw128(pk + s * 2048, HALF, 1024),
+                                      IDESC_DQ, (t == 0 && s == 0) ? 0u : 1u);
+                    mma_commit_w(x_empty + xb);
+                    mma_commit_w(a_empty + st);
                 }
-                x_ready = false;
-                fence_after();
-                const unsigned char *pk = sA + st * HALF;
-#pragma unroll
-                for (int kh = 0; kh < 2; kh++)
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; k4++)
-                        mma_bf16_w(tX + xb * 128, desc_kmajor(pq + kh * HALF + k4 * 32),
-                                   desc_kmajor(pk + kh * HALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
-                mma_commit_w(x_full + xb);
                 if (++xb == R_XSTG) {
                     xb = 0;
                     xph ^= 1u;
                 }
-                st += 2;
-                if (st == R_ASTG) {
+                if (++st == R_ASTG) {
                     st = 0;
                     aph ^= 1u;
                 }
-                if (t >= 2) mma2(t == 2);
             }
-            for (int t = nt < 2 ? 0 : nt - 2; t < nt; t++) mma2(t == 0);
-            mma_commit_w(dq_full);
-            dqc++;
+            if (!xw) mma_commit_w(dq_full);
             ai++;
         }
         mma_commit_w(mma_done);
         drain_bar(mma_done, 0, err);
-    } else if (warp == 2 || warp == 3) {
-        // ---------------------------------------------------------------- g / w stagers
-        // Warp 2 prepares the even items (buffer 0), warp 3 the odd ones (buffer 1).  Every global load of a
-        // row is issued before any is used, then scattered into the dense per-row g buffer of the item.
-        const int me = warp - 2;
-        int ic = 0;
-        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
-            if ((ic & 1) != me) continue;
-            const Pair p = decode_pair(a, i);
-            const int gb = ic & 1;
-            wait_bar(gd_empty + gb, ((ic >> 1) & 1) ^ 1, abort_flag, err, 8);
-            float *gd = sGD + gb * RP * NCMAX;
-            for (int j4 = lane; j4 * 4 < p.vmax; j4 += 32) {
-                reinterpret_cast<float4 *>(gd)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
-                reinterpret_cast<float4 *>(gd + NCMAX)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            float wv[RP][2];
-#pragma unroll
-            for (int r = 0; r < RP; r++) {
-                const long long row = r == 0 ? p.row0 : p.row1;
-                wv[r][0] = (r < p.n) ? __ldg(a.w + row * HI + lane) : 0.f;
-                wv[r][1] = (r < p.n) ? __ldg(a.w + row * HI + lane + 32) : 0.f;
-            }
-            __syncwarp();
-            constexpr int CHUNK = 8;   // slots per lane per pass
-            const int span = g.sparse ? g.K : p.vmax;
-            for (int base = 0; base < span; base += 32 * CHUNK) {
-                int32_t idv[RP][CHUNK];
-                float gv[RP][CHUNK];
-#pragma unroll
-                for (int r = 0; r < RP; r++) {
-                    const int v = r == 0 ? p.v0 : p.v1;
-                    const long long row = r == 0 ? p.row0 : p.row1;
-#pragma unroll
-                    for (int c = 0; c < CHUNK; c++) {
-                        const int s = base + c * 32 + lane;
-                        const bool ok = v > 0 && s < (g.sparse ? g.K : v);
-                        idv[r][c] = ok ? (g.sparse ? __ldg(a.ids + row * g.K + s) : s) : -1;
-                        gv[r][c] = ok ? __ldg(a.gbuf + row * g.TW + s) : 0.f;
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < RP; r++) {
-                    const int v = r == 0 ? p.v0 : p.v1;
-#pragma unroll
-                    for (int c = 0; c < CHUNK; c++) {
-                        if (idv[r][c] < 0) continue;
-                        const long long j = g.sparse ? (long long)idv[r][c] - p.sg.gid0 : idv[r][c];
-                        if (j >= 0 && j < v) gd[r * NCMAX + j] = gv[r][c];
-                    }
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < RP; r++) {
-                sW[gb * RP * HI + r * HI + lane] = wv[r][0];
-                sW[gb * RP * HI + r * HI + lane + 32] = wv[r][1];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(gd_full + gb);
-        }
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- epilogue (16 warps)
         // Lane (quad*32 + lane) = (row, head).  Warp qq = (warp - 4) / 4 of a quadrant owns key columns
@@ -531,15 +484,16 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         uint32_t xph = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
             const Pair p = decode_pair(a, i);
-            const int gb = ic & 1;
-            wait_bar(gd_full + gb, (ic >> 1) & 1, abort_flag, err, 9);
-            const float *gd = sGD + gb * RP * NCMAX + er * NCMAX;
-            const int v_me = er == 0 ? p.v0 : p.v1;
             const int nt = (p.vmax + NKEY - 1) / NKEY;
+            const int gb = ai & 1;  // g / w buffer of the items with visible keys (as the producer counts them)
+            if (nt > 0) wait_bar(gd_full + gb, (ai >> 1) & 1, abort_flag, err, 9);
+            const float *gd = sGD + gb * RP * NCMAX + er * NKEY;  // [key tile][row][128]
+            const int v_me = er == 0 ? p.v0 : p.v1;
             for (int t = 0; t < nt; t++) {
                 wait_bar(x_full + xb, xph, abort_flag, err, 10);
                 fence_after();
                 const int j0 = t * NKEY + qq * 32;  // first key of this warp's columns
+                const float *gt = gd + t * RP * NKEY + qq * 32;
                 uint32_t xr[32];
                 const uint32_t tcol = tX + lane_off + (uint32_t)(xb * 128 + qq * 32);
                 tmem_ld32_async(tcol, xr);
@@ -549,7 +503,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 #pragma unroll
                 for (int q4 = 0; q4 < 8; q4++) {
                     const int j = j0 + 4 * q4;
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gd + j);
+                    const float4 g4 = *reinterpret_cast<const float4 *>(gt + 4 * q4);
                     gk[4 * q4] = j < v_me ? g4.x : 0.f;
                     gk[4 * q4 + 1] = j + 1 < v_me ? g4.y : 0.f;
                     gk[4 * q4 + 2] = j + 2 < v_me ? g4.z : 0.f;
@@ -629,7 +583,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             if (qq == 0 && exists)
                 a.dw[row * HI + h] = (dwb[rh] + dwb[M_PAIRS + rh]) + (dwb[2 * M_PAIRS + rh] + dwb[3 * M_PAIRS + rh]);
             __syncwarp();
-            if (lane == 0) mbar_arrive(gd_empty + gb);
+            if (nt > 0 && lane == 0) mbar_arrive(gd_empty + gb);
         }
     }
     fence_before();
@@ -641,7 +595,8 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
 // ------------------------------------------------------------------ key-owner kernel: dK
 
 __global__ void __launch_bounds__(THREADS, 1)
-dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+             const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_w, Args a)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -651,8 +606,8 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     float *sWT = reinterpret_cast<float *>(smem + K_OFF_WT);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + K_OFF_MISC);
     uint64_t *a_full = bars, *a_empty = bars + 1, *b_full = bars + 2, *b_empty = b_full + K_BSTG;
-    uint64_t *x_full = b_empty + K_BSTG, *x_empty = x_full + 2, *gk_full = x_full + 4, *gk_empty = x_full + 6;
-    uint64_t *dk_full = x_full + 8, *dk_empty = x_full + 9, *gt_full = x_full + 10, *gt_empty = gt_full + K_GSTG;
+    uint64_t *x_full = b_empty + K_BSTG, *x_empty = x_full + K_XSTG, *gk_full = x_empty + K_XSTG;
+    uint64_t *dk_full = gk_full + K_XSTG, *dk_empty = dk_full + 1, *gt_full = dk_full + 2, *gt_empty = gt_full + K_GSTG;
     uint64_t *mma_done = gt_empty + K_GSTG;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + K_OFF_MISC + 256);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + K_OFF_MISC + 264);
@@ -666,16 +621,15 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         mbar_init(a_full, 1);
         mbar_init(a_empty, 1);
         for (int i = 0; i < K_BSTG; i++) { mbar_init(b_full + i, 1); mbar_init(b_empty + i, 1); }
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < K_XSTG; i++) {
             mbar_init(x_full + i, 1);
-            mbar_init(x_empty + i, 8);
+            mbar_init(x_empty + i, 1);
             mbar_init(gk_full + i, 8);
-            mbar_init(gk_empty + i, 1);
         }
-        for (int i = 0; i < K_GSTG; i++) { mbar_init(gt_full + i, 1); mbar_init(gt_empty + i, 8); }
+        for (int i = 0; i < K_GSTG; i++) { mbar_init(gt_full + i, 1); mbar_init(gt_empty + i, EPI / 32); }
         mbar_init(dk_full, 1);
         mbar_init(dk_empty, 8);
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);
         *abort_flag = 0;
         init_fence();
     }
@@ -684,8 +638,10 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    // TMEM: X (2 x 128 fp32 columns), dK (128), G as the A operand of dK (2 x 64 columns of bf16 pairs)
-    const uint32_t tX = tmem, tDK = tmem + 256, tG = tmem + 384;
+    // TMEM: three slots of 128 columns, each holding one row pair's X (fp32) and then, in place, its G as the A
+    // operand of dK (bf16 pairs; epilogue warp `half` writes its 32 pair columns over the first half of its own
+    // 64 X columns, so the pairs of K indices [16 s, 16 s + 16) sit at column 64 (s / 4) + 8 (s % 4)); dK (128).
+    const uint32_t tX = tmem, tDK = tmem + K_XSTG * 128;
     const int total = unit_total(a);
 
     if (warp == 0) {
@@ -698,61 +654,47 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
                 const Unit U = decode_unit(a, u);
                 if (U.npairs == 0) continue;
                 wait_bar(a_empty, (uc & 1) ^ 1, abort_flag, err, 21);
-                mbar_expect_tx(a_full, 2 * HALF);
-                for (int kh = 0; kh < 2; kh++) {
-                    if (sbhd)
-                        tma_load_3d(sA + kh * HALF, &map_k, a_full, kh * 64, U.sg.b, U.kt * NKEY);
-                    else
-                        tma_load_2d(sA + kh * HALF, &map_k, a_full, kh * 64, (int)(U.sg.key_y + U.kt * NKEY));
-                }
+                mbar_expect_tx(a_full, KTILE);
+                if (sbhd)
+                    tma_load_4d(sA, &map_k, a_full, 0, U.sg.b, U.kt * NKEY, 0);
+                else
+                    tma_load_3d(sA, &map_k, a_full, 0, (int)(U.sg.key_y + U.kt * NKEY), 0);
                 last_uc = uc;
                 uc++;
                 for (int pi = 0; pi < U.npairs; pi++) {
                     const int bs = qs % K_BSTG;
                     wait_bar(b_empty + bs, ((qs / K_BSTG) & 1) ^ 1, abort_flag, err, 22);
                     mbar_expect_tx(b_full + bs, QBLK);
+                    // one copy each: the pair's q rows, its g over this key tile, its w rows (a second row past the
+                    // chunk's end is read but never used)
                     const int s0 = U.s_lo + pi * RP;
-                    const long long r0 = row_of(g, U.sg.b, s0);
-                    const long long r1 = s0 + 1 < U.s_hi ? row_of(g, U.sg.b, s0 + 1) : r0;
-                    for (int r = 0; r < RP; r++)
-                        for (int kh = 0; kh < 2; kh++)
-                            tma_load_3d(sB + bs * QBLK + kh * HALF + r * (HI * 128), &map_q, b_full + bs, kh * 64, 0,
-                                        (int)(r == 0 ? r0 : r1));
+                    const PairAt at = pair_at(g, U.sg.b, s0, row_of(g, U.sg.b, s0));
+                    tma_load_5d(sB + bs * QBLK, &map_q, b_full + bs, 0, 0, at.y, at.z, 0);
                     last_qs[bs] = qs;
+                    const int gs = qs % K_GSTG;
+                    wait_bar(gt_empty + gs, ((qs / K_GSTG) & 1) ^ 1, abort_flag, err, 28);
+                    mbar_expect_tx(gt_full + gs, (uint32_t)(RP * (NKEY + HI) * 4));
+                    tma_load_2d(sGT + gs * RP * NKEY, &map_g, gt_full + gs, U.kt * NKEY, at.prow);
+                    tma_load_3d(sWT + gs * RP * HI, &map_w, gt_full + gs, 0, at.y, at.z);
                     qs++;
                 }
             }
             if (last_uc >= 0) drain_bar(a_full, last_uc & 1, err);
+            for (int q = qs - K_GSTG < 0 ? 0 : qs - K_GSTG; q < qs; q++) drain_bar(gt_full + q % K_GSTG, (q / K_GSTG) & 1, err);
             for (int bs = 0; bs < K_BSTG; bs++)
                 if (last_qs[bs] >= 0) drain_bar(b_full + bs, (last_qs[bs] / K_BSTG) & 1, err);
         }
-    } else if (warp == 1) {
-        // -------------------------------------------------------------------- MMA issue (whole warp)
-        // As in the row-owner kernel: warp-uniform loop, elected issue, lane-parallel unit decoding, early
-        // probes of the next group's barriers.  q-block ring position (bs, parity bph).
-        int uc = 0, bs = 0, xc = 0, gkc = 0, dkc = 0, k = 0, np_lane = 0;
-        uint32_t bph = 0;
-        bool x_ready = false, g_ready = false;
-        auto probe_x = [&]() -> bool {
-            const bool r0 = mbar_test(x_empty + (xc & 1), ((xc >> 1) & 1) ^ 1);
-            const bool r1 = mbar_test(b_full + bs, bph);
-            return r0 && r1;
-        };
-        auto mma3 = [&](int bp, bool first) {
-            if (first) wait_bar(dk_empty, (dkc & 1) ^ 1, abort_flag, err, 23);
-            const int gkb = gkc & 1;
-            if (!g_ready) wait_bar(gk_full + gkb, (gkc >> 1) & 1, abort_flag, err, 24);
-            x_ready = probe_x();
-            fence_after();
-            const unsigned char *pq = sB + bp * QBLK;
-#pragma unroll
-            for (int s = 0; s < 8; s++)
-                mma_bf16_ts_w(tDK, tG + gkb * 64 + s * 8, desc_sw128(pq + s * 2048, HALF, 1024), IDESC_DK,
-                              (first && s == 0) ? 0u : 1u);
-            mma_commit_w(gk_empty + gkb);
-            mma_commit_w(b_empty + bp);
-            gkc++;
-        };
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------- MMA issue (two warps, whole warp each)
+        // Warp 1 issues the X groups, warp 2 the dK groups; each commits its own groups, so neither waits on
+        // the other's issue overhead.  Each warp runs its loop together (stage indices and descriptors stay
+        // warp-uniform; one elected lane issues); unit decoding is lane-parallel: lane l decodes the CTA's unit
+        // k + l, the loop reads the pair count of unit k by a shuffle.
+        //   X[key, (row,h)]  = k . q^T    (A = the unit's key tile, B = the q block, both K-major)
+        //   dK[key, d]      += G q        (A = G from TMEM, B = the same q block read MN-major)
+        const bool xw = warp == 1;
+        int uc = 0, bs = 0, k = 0, np_lane = 0, xb = 0;
+        uint32_t bph = 0, xph = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x, k++) {
             if ((k & 31) == 0) {
                 const int ul = u + lane * (int)gridDim.x;
@@ -760,161 +702,96 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             }
             const int npairs = __shfl_sync(0xffffffffu, np_lane, k & 31);
             if (npairs == 0) continue;
-            wait_bar(a_full, uc & 1, abort_flag, err, 25);
-            fence_after();
-            int bs_prev = 0;
-            for (int pi = 0; pi < npairs; pi++) {
-                const int tb = xc & 1;
-                if (!x_ready) x_ready = probe_x();
-                if (!x_ready) {
-                    wait_bar(x_empty + tb, ((xc >> 1) & 1) ^ 1, abort_flag, err, 26);
-                    wait_bar(b_full + bs, bph, abort_flag, err, 27);
-                }
-                x_ready = false;
-                g_ready = pi > 0 && mbar_test(gk_full + (gkc & 1), (gkc >> 1) & 1);
+            if (xw) {
+                wait_bar(a_full, uc & 1, abort_flag, err, 25);
                 fence_after();
+            }
+            for (int pi = 0; pi < npairs; pi++) {
                 const unsigned char *pq = sB + bs * QBLK;
+                if (xw) {
+                    const bool r0 = mbar_test(x_empty + xb, xph ^ 1);
+                    const bool r1 = mbar_test(b_full + bs, bph);
+                    if (!(r0 && r1)) {
+                        wait_bar(x_empty + xb, xph ^ 1, abort_flag, err, 26);
+                        wait_bar(b_full + bs, bph, abort_flag, err, 27);
+                    }
+                    fence_after();
 #pragma unroll
-                for (int kh = 0; kh < 2; kh++)
+                    for (int kh = 0; kh < 2; kh++)
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; k4++)
-                        mma_bf16_w(tX + tb * 128, desc_kmajor(sA + kh * HALF + k4 * 32), desc_kmajor(pq + kh * HALF + k4 * 32),
-                                   IDESC_X, (kh | k4) ? 1u : 0u);
-                mma_commit_w(x_full + tb);
-                xc++;
-                const int bs_cur = bs;
+                        for (int k4 = 0; k4 < 4; k4++)
+                            mma_bf16_w(tX + xb * 128, desc_kmajor(sA + kh * HALF + k4 * 32),
+                                       desc_kmajor(pq + kh * HALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
+                    mma_commit_w(x_full + xb);
+                    if (pi == npairs - 1) mma_commit_w(a_empty);  // the key tile is read by the X groups only
+                } else {
+                    if (pi == 0) wait_bar(dk_empty, (uc & 1) ^ 1, abort_flag, err, 23);
+                    wait_bar(gk_full + xb, xph, abort_flag, err, 24);
+                    fence_after();
+                    const uint32_t tg = tX + xb * 128;
+#pragma unroll
+                    for (int s = 0; s < 8; s++)
+                        mma_bf16_ts_w(tDK, tg + (s >> 2) * 64 + (s & 3) * 8, desc_sw128(pq + s * 2048, HALF, 1024),
+                                      IDESC_DK, (pi == 0 && s == 0) ? 0u : 1u);
+                    mma_commit_w(x_empty + xb);
+                    mma_commit_w(b_empty + bs);
+                }
+                if (++xb == K_XSTG) {
+                    xb = 0;
+                    xph ^= 1u;
+                }
                 if (++bs == K_BSTG) {
                     bs = 0;
                     bph ^= 1u;
                 }
-                if (pi > 0) mma3(bs_prev, pi == 1);
-                bs_prev = bs_cur;
             }
-            g_ready = false;
-            mma3(bs_prev, npairs == 1);
-            mma_commit_w(dk_full);
-            mma_commit_w(a_empty);
-            dkc++;
+            if (!xw) mma_commit_w(dk_full);
             uc++;
         }
         mma_commit_w(mma_done);
         drain_bar(mma_done, 0, err);
-    } else if (warp == 2 || warp == 3) {
-        // ---------------------------------------------------------------- g / w stagers (per row pair)
-        // Two warps take alternate row pairs; each issues all loads of a pair before using them.
-        const int me = warp - 2;
-        int pc = 0;
-        for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit U = decode_unit(a, u);
-            const long long key_lo = U.sg.gid0 + (long long)U.kt * NKEY;
-            for (int pi = 0; pi < U.npairs; pi++, pc++) {
-                if ((pc & 1) != me) continue;
-                const int gs = pc % K_GSTG;
-                wait_bar(gt_empty + gs, ((pc / K_GSTG) & 1) ^ 1, abort_flag, err, 28);
-                float *gt = sGT + gs * RP * NKEY;
-                float *wt = sWT + gs * RP * HI;
-                long long row[RP];
-                bool ok[RP];
-                int v[RP];
-                int t0[RP], t1[RP];
-                float wv[RP][2];
-#pragma unroll
-                for (int r = 0; r < RP; r++) {
-                    const int s = U.s_lo + pi * RP + r;
-                    ok[r] = s < U.s_hi;
-                    row[r] = row_of(g, U.sg.b, ok[r] ? s : U.s_lo);
-                    v[r] = ok[r] ? vis(g, U.sg, s) : 0;
-                    wv[r][0] = ok[r] ? __ldg(a.w + row[r] * HI + lane) : 0.f;
-                    wv[r][1] = ok[r] ? __ldg(a.w + row[r] * HI + lane + 32) : 0.f;
-                    t0[r] = (ok[r] && g.sparse) ? __ldg(a.toff + row[r] * (a.NT + 1) + U.kt) : 0;
-                    t1[r] = (ok[r] && g.sparse) ? __ldg(a.toff + row[r] * (a.NT + 1) + U.kt + 1) : 0;
-                }
-#pragma unroll
-                for (int x = 0; x < RP * NKEY / 32; x++) gt[x * 32 + lane] = 0.f;
-                int32_t idv[RP][4];
-                float gv[RP][4];
-#pragma unroll
-                for (int r = 0; r < RP; r++)
-#pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        if (g.sparse) {
-                            const int sl = t0[r] + c * 32 + lane;
-                            const bool in = ok[r] && sl < t1[r];
-                            idv[r][c] = in ? __ldg(a.ids + row[r] * g.K + sl) : -1;
-                            gv[r][c] = in ? __ldg(a.gbuf + row[r] * g.TW + sl) : 0.f;
-                        } else {
-                            const int j = U.kt * NKEY + c * 32 + lane;
-                            const bool in = ok[r] && j < v[r];
-                            idv[r][c] = in ? j : -1;
-                            gv[r][c] = in ? __ldg(a.gbuf + row[r] * g.TW + j) : 0.f;
-                        }
-                    }
-                __syncwarp();
-#pragma unroll
-                for (int r = 0; r < RP; r++) {
-                    wt[r * HI + lane] = wv[r][0];
-                    wt[r * HI + lane + 32] = wv[r][1];
-#pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        if (idv[r][c] < 0) continue;
-                        long long kk, j;
-                        if (g.sparse) {
-                            kk = (long long)idv[r][c] - key_lo;
-                            j = kk + (long long)U.kt * NKEY;
-                        } else {
-                            j = idv[r][c];
-                            kk = j - (long long)U.kt * NKEY;
-                        }
-                        if (kk >= 0 && kk < NKEY && j < v[r]) gt[r * NKEY + kk] = gv[r][c];
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(gt_full + gs);
-            }
-        }
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- epilogue
         const int e = warp - 4, quad = warp & 3, half = e >> 2;
         const int k = quad * 32 + lane;
-        int xc = 0, gkc = 0, dkc = 0, pc = 0;
+        int xb = 0, dkc = 0, pc = 0;
+        uint32_t xph = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             const Unit U = decode_unit(a, u);
             for (int pi = 0; pi < U.npairs; pi++, pc++) {
                 const int gs = pc % K_GSTG;
-                const int tb = xc & 1;
+                // this warp's row of the pair: present, and key k of the tile visible to it?
+                const int srow = U.s_lo + pi * RP + half;
+                const bool live = srow < U.s_hi && U.kt * NKEY + k < vis(g, U.sg, srow);
                 wait_bar(gt_full + gs, (pc / K_GSTG) & 1, abort_flag, err, 29);
-                wait_bar(x_full + tb, (xc >> 1) & 1, abort_flag, err, 30);
+                wait_bar(x_full + xb, xph, abort_flag, err, 30);
                 fence_after();
-                const float gk = sGT[gs * RP * NKEY + half * NKEY + k];
+                const float gk = live ? sGT[gs * RP * NKEY + half * NKEY + k] : 0.f;
                 const float *wr = sWT + gs * RP * HI + half * HI;
                 uint32_t pk[32];
+                const uint32_t tcol = tX + ((uint32_t)(quad * 32) << 16) + (uint32_t)(xb * 128 + half * 64);
 #pragma unroll
                 for (int c = 0; c < 2; c++) {
                     float x[32];
-                    tmem_ld32(tX + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * 128 + half * 64 + c * 32), x);
+                    tmem_ld32(tcol + (uint32_t)(c * 32), x);
 #pragma unroll
                     for (int q2 = 0; q2 < 16; q2++) {
                         const int hh = c * 32 + 2 * q2;
-                        pk[c * 16 + q2] = pack_bf16(x[2 * q2] > 0.f ? gk * wr[hh] : 0.f,
-                                                    x[2 * q2 + 1] > 0.f ? gk * wr[hh + 1] : 0.f);
+                        pk[c * 16 + q2] = pack_bf16(live && x[2 * q2] > 0.f ? gk * wr[hh] : 0.f,
+                                                    live && x[2 * q2 + 1] > 0.f ? gk * wr[hh + 1] : 0.f);
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gt_empty + gs);
+                // G[key, (row, h)] of this warp's row half over its own (already read) X columns
+                tmem_st32(tcol, pk);
                 fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(x_empty + tb);
-                    mbar_arrive(gt_empty + gs);
+                if (lane == 0) mbar_arrive(gk_full + xb);
+                if (++xb == K_XSTG) {
+                    xb = 0;
+                    xph ^= 1u;
                 }
-                const int gkb = gkc & 1;
-                wait_bar(gk_empty + gkb, ((gkc >> 1) & 1) ^ 1, abort_flag, err, 31);
-                fence_after();
-                // G[key, (row, h)] of this warp's row half: K = (row, h) pairs, columns 32 half .. +32 of buffer gkb
-                tmem_st32(tG + ((uint32_t)(quad * 32) << 16) + (uint32_t)(gkb * 64 + half * 32), pk);
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(gk_full + gkb);
-                xc++;
-                gkc++;
             }
             if (U.npairs == 0) continue;
             // ---- flush the unit's dK partial: lane = key, this warp's 64 of the 128 d
@@ -988,27 +865,62 @@ bool tc_bwd_supported(const Geo &g, bool bf16)
 
 int tc_bwd_tiles(const Geo &g) { return (g.NC + bwd::NKEY - 1) / bwd::NKEY; }
 
-size_t tc_bwd_workspace_bytes(const Geo &g)
+int tc_bwd_ncp(const Geo &g) { return tc_bwd_tiles(g) * bwd::NKEY; }
+
+static size_t bwd_offsets_bytes(const Geo &g)
 {
     const size_t offs = sizeof(int) * 2 * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1);
-    const size_t toff = sizeof(int) * (size_t)g.rows * (size_t)(tc_bwd_tiles(g) + 1);
-    return ((offs + 255) & ~(size_t)255) + toff;
+    return (offs + 255) & ~(size_t)255;
+}
+
+size_t tc_bwd_workspace_bytes(const Geo &g)
+{
+    return bwd_offsets_bytes(g) + sizeof(float) * (size_t)g.rows * (size_t)tc_bwd_ncp(g);
+}
+
+float *tc_bwd_gd(const Geo &g, void *ws)
+{
+    return reinterpret_cast<float *>(static_cast<char *>(ws) + bwd_offsets_bytes(g));
 }
 
 cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
-                          const int32_t *ids, const float *gbuf, const int32_t *toff, __nv_bfloat16 *dq, float *dw,
-                          float *dk_acc, void *ws, cudaStream_t st)
+                          __nv_bfloat16 *dq, float *dw, float *dk_acc, void *ws, cudaStream_t st)
 {
     using namespace bwd;
-    CUtensorMap mq, mk;
-    if (!tc_encode_q_map(&mq, q_idx, g) || !tc_encode_k_map(&mk, k_idx, g)) return cudaErrorInvalidValue;
+    // Pair maps: a row pair of q_idx (both K-halves: [half][row][head][64 d] in shared memory) and of w in one
+    // copy; a k tile (both K-halves: [half][key][64 d]) in one copy; g rows by position, two rows x 128 keys.
+    const bool sb = g.layout == CSA_SBHD;
+    const cuuint64_t rowb = (cuuint64_t)HI * DI * 2;
+    const cuuint64_t y_n = sb ? (cuuint64_t)g.B : (cuuint64_t)g.rows, z_n = sb ? (cuuint64_t)g.S : 1;
+    const cuuint64_t z_str = sb ? (cuuint64_t)g.B * rowb : (cuuint64_t)g.rows * rowb;
+    const cuuint32_t by = sb ? 1 : 2, bz = sb ? 2 : 1;
+    const cuuint64_t qd[5] = {64, (cuuint64_t)HI, y_n, z_n, 2};
+    const cuuint64_t qs[4] = {(cuuint64_t)DI * 2, rowb, z_str, 128};
+    const cuuint32_t qb[5] = {64, (cuuint32_t)HI, by, bz, 2};
+    const cuuint64_t wd[3] = {(cuuint64_t)HI, y_n, z_n};
+    const cuuint64_t ws_[2] = {(cuuint64_t)HI * 4, sb ? (cuuint64_t)g.B * HI * 4 : (cuuint64_t)g.rows * HI * 4};
+    const cuuint32_t wb[3] = {(cuuint32_t)HI, by, bz};
+    const cuuint64_t gdim[2] = {(cuuint64_t)tc_bwd_ncp(g), (cuuint64_t)g.rows};
+    const cuuint64_t gstr[1] = {(cuuint64_t)tc_bwd_ncp(g) * 4};
+    const cuuint32_t gbox[2] = {NKEY, RP};
+    CUtensorMap mq, mk, mg, mw;
+    bool ok = tc_encode_bf16(&mq, q_idx, 5, qd, qs, qb) && tc_encode_f32(&mg, tc_bwd_gd(g, ws), 2, gdim, gstr, gbox) &&
+              tc_encode_f32(&mw, w, 3, wd, ws_, wb);
+    if (sb) {
+        const cuuint64_t kd[4] = {64, (cuuint64_t)g.B, (cuuint64_t)g.nc, 2};
+        const cuuint64_t ks[3] = {(cuuint64_t)DI * 2, (cuuint64_t)g.B * DI * 2, 128};
+        const cuuint32_t kb[4] = {64, 1, NKEY, 2};
+        ok = ok && tc_encode_bf16(&mk, k_idx, 4, kd, ks, kb);
+    } else {
+        const cuuint64_t kd[3] = {64, (cuuint64_t)g.key_rows, 2};
+        const cuuint64_t ks[2] = {(cuuint64_t)DI * 2, 128};
+        const cuuint32_t kb[3] = {64, NKEY, 2};
+        ok = ok && tc_encode_bf16(&mk, k_idx, 3, kd, ks, kb);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    const int NT = tc_bwd_tiles(g);
     Args a;
     a.g = g;
-    a.w = w;
-    a.ids = ids;
-    a.gbuf = gbuf;
-    a.toff = toff;
-    a.NT = tc_bwd_tiles(g);
     a.dq = dq;
     a.dw = dw;
     a.dk_acc = dk_acc;
@@ -1023,7 +935,7 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
         a.cu_g = cu_g;
         a.cu_u = cu_u;
         upper_items = (g.rows + RP - 1) / RP + g.B;
-        upper_units = (g.rows + CH - 1) / CH * a.NT + g.B * a.NT;
+        upper_units = (g.rows + CH - 1) / CH * NT + g.B * NT;
     } else {
         a.total_items = g.B * ((g.S + RP - 1) / RP);
         a.units_per_seq = units_of_len(g.S, g.nc, g.ratio);
@@ -1041,13 +953,13 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
     e = cudaFuncSetAttribute(dk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K_SMEM);
     if (e != cudaSuccess) return e;
     const int g1 = upper_items < sms ? (upper_items > 0 ? upper_items : 1) : sms;
-    dq_dw_tc_kernel<<<g1, R_THREADS, R_SMEM, st>>>(mq, mk, a);
+    dq_dw_tc_kernel<<<g1, R_THREADS, R_SMEM, st>>>(mq, mk, mg, mw, a);
     note_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (upper_units > 0) {
         const int g2 = upper_units < sms ? upper_units : sms;
-        dk_tc_kernel<<<g2, THREADS, K_SMEM, st>>>(mq, mk, a);
+        dk_tc_kernel<<<g2, THREADS, K_SMEM, st>>>(mq, mk, mg, mw, a);
         note_launches(1);
     }
     return cudaGetLastError();

@@ -372,12 +372,18 @@ cudaError_t launch_teacher_generic(const Geo &g, const T *q, const T *kv, const 
 // One CTA per query row.  p = softmax over C of the scores, L_t = sum t (log(t+eps) - log(p+eps)) and
 // g_s = f * p_s (A - t_s/(p_s+eps)) with A = sum_k t_k p_k/(p_k+eps): the exact derivative of the
 // eps-guarded KL of [BUG] sec. 2 excerpt.  gbuf uses the teacher's slot layout.
-// With toff != nullptr (sparse support, ascending ids), it also records for every key tile kt of 128 keys
-// the first slot whose key lies at or beyond tile kt: toff[row][kt], kt = 0..NT.
+// With gd != nullptr it also writes g by key: gd[prow][j] for the row's visible keys j < v (0 off the support),
+// row stride ncp; what lies beyond v is left as it is.  Rows are ordered by position within each sequence
+// (prow = b S + s for SBHD, the row itself otherwise), so the two rows of a position pair are adjacent.
+__device__ __forceinline__ long long gd_row(const Geo &g, const Row &R, long long r)
+{
+    return g.layout == CSA_SBHD ? (long long)R.b * g.S + R.s : r;
+}
+
 __global__ void __launch_bounds__(kThreads)
 kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ selscore,
           const float *__restrict__ dense_scores, const float *__restrict__ teacher, float *__restrict__ gbuf,
-          float *__restrict__ row_loss, int32_t *__restrict__ toff, int NT)
+          float *__restrict__ row_loss, float *__restrict__ gd, int ncp)
 {
     __shared__ float red[kWarps];
     const int tid = threadIdx.x;
@@ -387,22 +393,10 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
         const int32_t *row_ids = ids + r * g.K;
         const float *trow = teacher + r * TW;
         float *grow = gbuf + r * TW;
-        if (toff != nullptr) {
-            // slot s opens key tiles (tile(s-1), tile(s)]: valid ids come first, ascending, so the first slot
-            // of tile kt is where the tile index of consecutive slots steps past kt (invalid slots count as NT)
-            const long long lo = key_gid(g, R, 0);
-            int32_t *to = toff + r * (NT + 1);
-            auto tile_of = [&](int s) -> int {
-                const long long id = row_ids[s];
-                if (id < 0) return NT;
-                const long long t = (id - lo) >> 7;
-                return t < 0 ? 0 : (t > NT ? NT : (int)t);
-            };
-            for (int s = tid; s <= g.K; s += kThreads) {
-                const int prev = s > 0 ? tile_of(s - 1) : -1;
-                const int cur = s < g.K ? tile_of(s) : NT + 1;
-                for (int kt = prev + 1; kt <= cur && kt <= NT; kt++) to[kt] = s;
-            }
+        float *drow = gd != nullptr ? gd + gd_row(g, R, r) * ncp : nullptr;
+        if (drow != nullptr) {
+            for (int j = tid; j < R.v; j += kThreads) drow[j] = 0.f;
+            __syncthreads();
         }
         // score of support slot s, or -inf when s is not in C
         auto score_of = [&](int s) -> float {
@@ -419,6 +413,7 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
             if (tid == 0) row_loss[r] = 0.f;
             continue;
         }
+        const long long lo = key_gid(g, R, 0);
         float z = 0.f;
         for (int s = tid; s < TW; s += kThreads) {
             float x = score_of(s);
@@ -443,6 +438,7 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
             if (x != -INFINITY) {
                 float p = __expf(x - m) * inv_z;
                 gv = g.factor * p * (A - trow[s] / (p + kEps));
+                if (drow != nullptr) drow[g.sparse ? (int)(row_ids[s] - lo) : s] = gv;
             }
             grow[s] = gv;
         }
@@ -452,13 +448,12 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
 
 // The same step for the sparse support with K <= 512 slots (teacher width K): one warp per row, the row's
 // ids, scores and teacher values held in registers (slot s = lane + 32 i, coalesced), warp reductions.
-// Key-tile offsets: with valid ids ascending and invalid slots last, the tile index of consecutive slots
-// never decreases, so the first slot of tile kt is the number of slots whose tile lies below kt.
+// g by key (gd, as in kl_kernel): the row's visible range is zeroed, then every support slot writes its key.
 constexpr int kKlPer = 16;  // slots per lane
 __global__ void __launch_bounds__(kThreads)
 kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ selscore,
                const float *__restrict__ teacher, float *__restrict__ gbuf, float *__restrict__ row_loss,
-               int32_t *__restrict__ toff, int NT)
+               float *__restrict__ gd, int ncp)
 {
     const int lane = threadIdx.x & 31;
     const long long nwarps = (long long)gridDim.x * kWarps;
@@ -480,28 +475,10 @@ kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__
             x[i] = in ? __ldg(srow + s) : 0.f;
             t[i] = in ? __ldg(trow + s) : 0.f;
         }
-        if (toff != nullptr) {
-            int tl[kKlPer];
-#pragma unroll
-            for (int i = 0; i < kKlPer; i++) {
-                const int s = lane + 32 * i;
-                if (s >= K) {
-                    tl[i] = NT + 1;  // beyond the row: below no tile
-                } else if (id[i] < 0) {
-                    tl[i] = NT;
-                } else {
-                    const long long tt = ((long long)id[i] - lo) >> 7;
-                    tl[i] = tt < 0 ? 0 : (tt > NT ? NT : (int)tt);
-                }
-            }
-            int32_t *to = toff + r * (NT + 1);
-            for (int kt = 0; kt <= NT; kt++) {
-                unsigned c = 0;
-#pragma unroll
-                for (int i = 0; i < kKlPer; i++) c += tl[i] < kt ? 1u : 0u;
-                c = __reduce_add_sync(0xffffffffu, c);
-                if (lane == 0) to[kt] = (int32_t)c;
-            }
+        float *drow = gd != nullptr ? gd + gd_row(g, R, r) * ncp : nullptr;
+        if (drow != nullptr) {  // zero the visible range (16-byte stores: ncp is a multiple of 4)
+            for (int j4 = lane; 4 * j4 < R.v; j4 += 32) reinterpret_cast<float4 *>(drow)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            __syncwarp();
         }
         bool sel[kKlPer];
         float m = -INFINITY;
@@ -541,25 +518,27 @@ kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__
             const int s = lane + 32 * i;
             if (s >= K) continue;
             const float p = x[i] * inv_z;
-            grow[s] = sel[i] ? g.factor * p * (A - t[i] / (p + kEps)) : 0.f;
+            const float gv = sel[i] ? g.factor * p * (A - t[i] / (p + kEps)) : 0.f;
+            grow[s] = gv;
+            if (drow != nullptr && sel[i]) drow[id[i] - lo] = gv;
         }
         if (lane == 0) row_loss[r] = L;
     }
 }
 
 cudaError_t launch_kl(const Geo &g, const int32_t *ids, const float *selscore, const float *dense_scores,
-                      const float *teacher, float *gbuf, float *row_loss, int32_t *toff, int NT, cudaStream_t st)
+                      const float *teacher, float *gbuf, float *row_loss, float *gd, int ncp, cudaStream_t st)
 {
     if (g.rows == 0) return cudaSuccess;
     if (g.sparse && dense_scores == nullptr && g.TW == g.K && g.K <= 32 * kKlPer) {
         const long long blocks = (g.rows + kWarps - 1) / kWarps;
         const int grid = blocks < 152 * 16 ? (int)blocks : 152 * 16;
-        kl_warp_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, teacher, gbuf, row_loss, toff, NT);
+        kl_warp_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, teacher, gbuf, row_loss, gd, ncp);
         note_launches(1);
         return cudaGetLastError();
     }
     int grid = g.rows < 65535 * 8 ? g.rows : 65535 * 8;
-    kl_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, toff, NT);
+    kl_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, gd, ncp);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -97,6 +97,20 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z, int w)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];"
+                 ::"r"(su32(dst)), "l"(map), "r"(su32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z, int w,
+                                            int v)
+{
+    asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+                 ::"r"(su32(dst)), "l"(map), "r"(su32(bar)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
+                 : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle, version 1 (bits 46-47), layout SWIZZLE_128B (bits 61-63 = 2).
 //   K-major:  rows of 128 B (64 bf16 of K) per M/N index, 8-row atoms of 1024 B: SBO = 1024 B; LBO unused.
 //   MN-major: 64 consecutive M/N elements per 128-B row, one row per K index, 8-row atoms of 1024 B along K:
