@@ -760,26 +760,33 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             const Unit U = decode_unit(a, u);
             for (int pi = 0; pi < U.npairs; pi++, pc++) {
                 const int gs = pc % K_GSTG;
-                // this warp's row of the pair: present, and key k of the tile visible to it?
+                // this warp's row of the pair (absent past the chunk's end: its g, w were not loaded) and the
+                // keys of the tile visible to it
                 const int srow = U.s_lo + pi * RP + half;
-                const bool live = srow < U.s_hi && U.kt * NKEY + k < vis(g, U.sg, srow);
+                const bool row_ok = srow < U.s_hi;  // warp-uniform
+                const int vrow = row_ok ? vis(g, U.sg, srow) : 0;
                 wait_bar(gt_full + gs, (pc / K_GSTG) & 1, abort_flag, err, 29);
                 wait_bar(x_full + xb, xph, abort_flag, err, 30);
                 fence_after();
-                const float gk = live ? sGT[gs * RP * NKEY + half * NKEY + k] : 0.f;
+                const float gk = U.kt * NKEY + k < vrow ? sGT[gs * RP * NKEY + half * NKEY + k] : 0.f;
                 const float *wr = sWT + gs * RP * HI + half * HI;
                 uint32_t pk[32];
                 const uint32_t tcol = tX + ((uint32_t)(quad * 32) << 16) + (uint32_t)(xb * 128 + half * 64);
+                if (row_ok) {
 #pragma unroll
-                for (int c = 0; c < 2; c++) {
-                    float x[32];
-                    tmem_ld32(tcol + (uint32_t)(c * 32), x);
+                    for (int c = 0; c < 2; c++) {
+                        float x[32];
+                        tmem_ld32(tcol + (uint32_t)(c * 32), x);
 #pragma unroll
-                    for (int q2 = 0; q2 < 16; q2++) {
-                        const int hh = c * 32 + 2 * q2;
-                        pk[c * 16 + q2] = pack_bf16(live && x[2 * q2] > 0.f ? gk * wr[hh] : 0.f,
-                                                    live && x[2 * q2 + 1] > 0.f ? gk * wr[hh + 1] : 0.f);
+                        for (int q2 = 0; q2 < 16; q2++) {
+                            const int hh = c * 32 + 2 * q2;
+                            pk[c * 16 + q2] = pack_bf16(x[2 * q2] > 0.f ? gk * wr[hh] : 0.f,
+                                                        x[2 * q2 + 1] > 0.f ? gk * wr[hh + 1] : 0.f);
+                        }
                     }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c++) pk[c] = 0u;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gt_empty + gs);
