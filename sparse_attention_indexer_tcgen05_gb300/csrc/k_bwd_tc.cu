@@ -46,8 +46,8 @@ constexpr int M_PAIRS = RP * 64;               // (row, head) pairs of an item
 constexpr int NCMAX = 1024;                    // key axis the row-owner's dense g rows hold
 constexpr int HALF = NKEY * 64 * 2;            // 16 KB: 128 rows x 64 bf16
 constexpr int QBLK = 2 * HALF;                 // 32 KB: 2 rows x 64 heads x 128 d, two K-halves
-constexpr int THREADS = 384;                   // key-owner kernel: 12 warps
-constexpr int EPI = 256;                       //   its epilogue: warps 4..11
+constexpr int THREADS = 640;                   // key-owner kernel: 20 warps
+constexpr int EPI = 512;                       //   its epilogue: warps 4..19
 constexpr int R_THREADS = 640;                 // row-owner kernel: 20 warps
 constexpr int R_EPI = 512;                     //   its epilogue: warps 4..19, four per TMEM lane quadrant
 constexpr int CH = 128;                        // rows per key-owner unit
@@ -624,11 +624,11 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         for (int i = 0; i < K_XSTG; i++) {
             mbar_init(x_full + i, 1);
             mbar_init(x_empty + i, 1);
-            mbar_init(gk_full + i, 8);
+            mbar_init(gk_full + i, EPI / 32);
         }
         for (int i = 0; i < K_GSTG; i++) { mbar_init(gt_full + i, 1); mbar_init(gt_empty + i, EPI / 32); }
         mbar_init(dk_full, 1);
-        mbar_init(dk_empty, 8);
+        mbar_init(dk_empty, EPI / 32);
         mbar_init(mma_done, 2);
         *abort_flag = 0;
         init_fence();
@@ -639,8 +639,9 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     fence_after();
     const uint32_t tmem = *tmem_slot;
     // TMEM: three slots of 128 columns, each holding one row pair's X (fp32) and then, in place, its G as the A
-    // operand of dK (bf16 pairs; epilogue warp `half` writes its 32 pair columns over the first half of its own
-    // 64 X columns, so the pairs of K indices [16 s, 16 s + 16) sit at column 64 (s / 4) + 8 (s % 4)); dK (128).
+    // operand of dK (bf16 pairs; the epilogue warp of X columns [32 c, 32 c + 32) writes its 16 pair columns over
+    // the first half of them, so the pairs of K indices [16 s, 16 s + 16) sit at column 32 (s / 2) + 8 (s % 2));
+    // dK (128).
     const uint32_t tX = tmem, tDK = tmem + K_XSTG * 128;
     const int total = unit_total(a);
 
@@ -731,7 +732,7 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
                     const uint32_t tg = tX + xb * 128;
 #pragma unroll
                     for (int s = 0; s < 8; s++)
-                        mma_bf16_ts_w(tDK, tg + (s >> 2) * 64 + (s & 3) * 8, desc_sw128(pq + s * 2048, HALF, 1024),
+                        mma_bf16_ts_w(tDK, tg + (s >> 1) * 32 + (s & 1) * 8, desc_sw128(pq + s * 2048, HALF, 1024),
                                       IDESC_DK, (pi == 0 && s == 0) ? 0u : 1u);
                     mma_commit_w(x_empty + xb);
                     mma_commit_w(b_empty + bs);
@@ -751,47 +752,60 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         mma_commit_w(mma_done);
         drain_bar(mma_done, 0, err);
     } else if (warp >= 4) {
-        // ---------------------------------------------------------------- epilogue
-        const int e = warp - 4, quad = warp & 3, half = e >> 2;
+        // ---------------------------------------------------------------- epilogue (16 warps)
+        // Lane = key (quad * 32 + lane).  Warp sub = (warp - 4) / 4 of a quadrant owns X columns [32 sub, 32 sub +
+        // 32): the heads [32 (sub % 2), +32) of row `half` = sub / 2 of the pair, and d quarter sub of the flush.
+        const int quad = warp & 3, sub = (warp - 4) >> 2, half = sub >> 1, hq = sub & 1;
         const int k = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         int xb = 0, dkc = 0, pc = 0;
         uint32_t xph = 0;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             const Unit U = decode_unit(a, u);
             for (int pi = 0; pi < U.npairs; pi++, pc++) {
                 const int gs = pc % K_GSTG;
+                const uint32_t gph = (pc / K_GSTG) & 1;
                 // this warp's row of the pair (absent past the chunk's end: its g, w were not loaded) and the
                 // keys of the tile visible to it
                 const int srow = U.s_lo + pi * RP + half;
                 const bool row_ok = srow < U.s_hi;  // warp-uniform
                 const int vrow = row_ok ? vis(g, U.sg, srow) : 0;
-                wait_bar(gt_full + gs, (pc / K_GSTG) & 1, abort_flag, err, 29);
-                wait_bar(x_full + xb, xph, abort_flag, err, 30);
+                const bool r0 = mbar_test(gt_full + gs, gph);
+                const bool r1 = mbar_test(x_full + xb, xph);
+                if (!(r0 && r1)) {
+                    wait_bar(gt_full + gs, gph, abort_flag, err, 29);
+                    wait_bar(x_full + xb, xph, abort_flag, err, 30);
+                }
                 fence_after();
-                const float gk = U.kt * NKEY + k < vrow ? sGT[gs * RP * NKEY + half * NKEY + k] : 0.f;
-                const float *wr = sWT + gs * RP * HI + half * HI;
-                uint32_t pk[32];
-                const uint32_t tcol = tX + ((uint32_t)(quad * 32) << 16) + (uint32_t)(xb * 128 + half * 64);
+                const uint32_t tcol = tX + lane_off + (uint32_t)(xb * 128 + sub * 32);
+                uint32_t pk[16];
                 if (row_ok) {
+                    uint32_t xr[32];
+                    tmem_ld32_async(tcol, xr);
+                    const float gk = U.kt * NKEY + k < vrow ? sGT[gs * RP * NKEY + half * NKEY + k] : 0.f;
+                    const float4 *wr4 = reinterpret_cast<const float4 *>(sWT + gs * RP * HI + half * HI + hq * 32);
+                    float gw[32];
 #pragma unroll
-                    for (int c = 0; c < 2; c++) {
-                        float x[32];
-                        tmem_ld32(tcol + (uint32_t)(c * 32), x);
-#pragma unroll
-                        for (int q2 = 0; q2 < 16; q2++) {
-                            const int hh = c * 32 + 2 * q2;
-                            pk[c * 16 + q2] = pack_bf16(x[2 * q2] > 0.f ? gk * wr[hh] : 0.f,
-                                                        x[2 * q2 + 1] > 0.f ? gk * wr[hh + 1] : 0.f);
-                        }
+                    for (int c = 0; c < 8; c++) {
+                        const float4 w4 = wr4[c];
+                        gw[4 * c] = gk * w4.x;
+                        gw[4 * c + 1] = gk * w4.y;
+                        gw[4 * c + 2] = gk * w4.z;
+                        gw[4 * c + 3] = gk * w4.w;
                     }
+                    tmem_wait_ld(xr);
+#pragma unroll
+                    for (int q2 = 0; q2 < 16; q2++)
+                        pk[q2] = pack_bf16(__uint_as_float(xr[2 * q2]) > 0.f ? gw[2 * q2] : 0.f,
+                                           __uint_as_float(xr[2 * q2 + 1]) > 0.f ? gw[2 * q2 + 1] : 0.f);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 32; c++) pk[c] = 0u;
+                    for (int c = 0; c < 16; c++) pk[c] = 0u;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gt_empty + gs);
-                // G[key, (row, h)] of this warp's row half over its own (already read) X columns
-                tmem_st32(tcol, pk);
+                // G[key, (row, h)] of these heads over this warp's own (already read) X columns
+                tmem_st16(tcol, pk);
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(gk_full + xb);
@@ -801,19 +815,12 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
                 }
             }
             if (U.npairs == 0) continue;
-            // ---- flush the unit's dK partial: lane = key, this warp's 64 of the 128 d
+            // ---- flush the unit's dK partial: lane = key, this warp's d quarter
             wait_bar(dk_full, dkc & 1, abort_flag, err, 32);
             fence_after();
-            float vv[64];
-            {
-                float x[32];
-                tmem_ld32(tDK + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64), x);
-#pragma unroll
-                for (int c = 0; c < 32; c++) vv[c] = x[c];
-                tmem_ld32(tDK + ((uint32_t)(quad * 32) << 16) + (uint32_t)(half * 64 + 32), x);
-#pragma unroll
-                for (int c = 0; c < 32; c++) vv[32 + c] = x[c];
-            }
+            uint32_t vv[32];
+            tmem_ld32_async(tDK + lane_off + (uint32_t)(sub * 32), vv);
+            tmem_wait_ld(vv);
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dk_empty);
@@ -822,11 +829,12 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             if (j < U.sg.nc) {
                 const long long gid = U.sg.gid0 + j;
                 const long long kr = g.layout == CSA_SBHD ? (gid % g.nc) * g.B + gid / g.nc : gid;
-                float *dst = a.dk_acc + kr * DI + half * 64;
+                float *dst = a.dk_acc + kr * DI + sub * 32;
 #pragma unroll
-                for (int c = 0; c < 16; c++)
+                for (int c = 0; c < 8; c++)
                     atomicAdd(reinterpret_cast<float4 *>(dst + 4 * c),
-                              make_float4(vv[4 * c], vv[4 * c + 1], vv[4 * c + 2], vv[4 * c + 3]));
+                              make_float4(__uint_as_float(vv[4 * c]), __uint_as_float(vv[4 * c + 1]),
+                                          __uint_as_float(vv[4 * c + 2]), __uint_as_float(vv[4 * c + 3])));
             }
         }
     }
