@@ -59,7 +59,7 @@ constexpr uint32_t IDESC_DK = idesc_bf16(128, 128, false, true);   // dK += G q 
 // row-owner shared memory
 constexpr int R_ASTG = 4;                                     // k tiles in flight
 constexpr int R_XSTG = 3;                                     // X / G' TMEM slots
-static_assert((2 * R_ASTG + 11 + 3 * R_XSTG) * 8 <= 512, "row-owner barriers overlap the TMEM slot");
+static_assert((2 * R_ASTG + 19 + 3 * R_XSTG) * 8 <= 512, "row-owner barriers overlap the TMEM slot");
 constexpr int KTILE = 2 * HALF;                               // 32 KB: 128 keys x 128 d, two K-halves
 constexpr int R_OFF_A = 0;
 constexpr int R_OFF_B = R_OFF_A + R_ASTG * KTILE;             // 128 KB: the q tiles of two items
@@ -287,7 +287,8 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     uint64_t *a_full = bars, *a_empty = bars + R_ASTG, *b_full = bars + 2 * R_ASTG, *b_empty = b_full + 2;
     uint64_t *x_full = b_full + 4, *x_empty = x_full + R_XSTG, *g_full = x_empty + R_XSTG;
     uint64_t *dq_full = g_full + R_XSTG, *dq_empty = dq_full + 1, *gd_full = dq_full + 2, *gd_empty = dq_full + 4;
-    uint64_t *mma_done = dq_full + 6;                                  // 2 R_ASTG + 11 + 3 R_XSTG barriers
+    uint64_t *mma_done = dq_full + 6;                                  // 2 R_ASTG + 19 + 3 R_XSTG barriers
+    uint64_t *dw_bar = dq_full + 7;                                    // [item parity][quadrant]: dW partials
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + R_OFF_MISC + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + R_OFF_MISC + 520);
 
@@ -312,6 +313,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(dq_full, 1);
         mbar_init(dq_empty, R_EPI / 32);
         mbar_init(mma_done, 2);
+        for (int i = 0; i < 8; i++) mbar_init(dw_bar + i, 4);
         *abort_flag = 0;
         init_fence();
     }
@@ -502,12 +504,15 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 float gk[32];
 #pragma unroll
                 for (int q4 = 0; q4 < 8; q4++) {
-                    const int j = j0 + 4 * q4;
                     const float4 g4 = *reinterpret_cast<const float4 *>(gt + 4 * q4);
-                    gk[4 * q4] = j < v_me ? g4.x : 0.f;
-                    gk[4 * q4 + 1] = j + 1 < v_me ? g4.y : 0.f;
-                    gk[4 * q4 + 2] = j + 2 < v_me ? g4.z : 0.f;
-                    gk[4 * q4 + 3] = j + 3 < v_me ? g4.w : 0.f;
+                    gk[4 * q4] = g4.x;
+                    gk[4 * q4 + 1] = g4.y;
+                    gk[4 * q4 + 2] = g4.z;
+                    gk[4 * q4 + 3] = g4.w;
+                }
+                if (j0 + 32 > v_me) {  // warp-uniform: the row's last visible tile
+#pragma unroll
+                    for (int q = 0; q < 32; q++) gk[q] = j0 + q < v_me ? gk[q] : 0.f;
                 }
                 tmem_wait_ld(xr);
                 uint32_t pk[16];
@@ -577,11 +582,17 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             }
             // dW = q . dQ' over the four d quarters, summed in a fixed order (sDW alternates by item parity, so
             // one barrier per item suffices)
+            // (the four warps of a quadrant meet on an mbarrier; the d-quarter-0 warp adds and writes)
             float *dwb = sDW + (ic & 1) * 4 * M_PAIRS;
             dwb[qq * M_PAIRS + rh] = (pa[0] + pa[1]) + (pa[2] + pa[3]);
-            named_bar(1, R_EPI);
-            if (qq == 0 && exists)
-                a.dw[row * HI + h] = (dwb[rh] + dwb[M_PAIRS + rh]) + (dwb[2 * M_PAIRS + rh] + dwb[3 * M_PAIRS + rh]);
+            __syncwarp();
+            uint64_t *dwq = dw_bar + (ic & 1) * 4 + quad;
+            if (lane == 0) mbar_arrive(dwq);
+            if (qq == 0) {
+                wait_bar(dwq, (ic >> 1) & 1, abort_flag, err, 13);
+                if (exists)
+                    a.dw[row * HI + h] = (dwb[rh] + dwb[M_PAIRS + rh]) + (dwb[2 * M_PAIRS + rh] + dwb[3 * M_PAIRS + rh]);
+            }
             __syncwarp();
             if (nt > 0 && lane == 0) mbar_arrive(gd_empty + gb);
         }
