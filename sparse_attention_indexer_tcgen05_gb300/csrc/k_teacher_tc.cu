@@ -50,18 +50,18 @@ constexpr int MAXKB = 3;                        // D <= 192
 constexpr int QBUF = MAXKB * QKB;               // 48 KB: the item's q rows
 constexpr int BSTG = 3;                         // key K-block stages
 constexpr int NCMAX = 1024;
-constexpr int THREADS = 576, EPI = 512;
+constexpr int THREADS = 640, EPI = 512;          // warps 2..17 epilogue, 18..19 per-item helpers
 constexpr uint32_t TMEM_COLS = 512;             // two 256-column fp32 accumulators
 constexpr uint32_t IDESC = idesc_bf16(128, NK, false, false);
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_B = OFF_Q + 2 * QBUF;                     // 96 KB
-constexpr int OFF_T = OFF_B + BSTG * KB;                    // 192 KB: 2 rows x NCMAX fp32
-constexpr int OFF_SEL = OFF_T + RP * NCMAX * 4;             // 200 KB: selection bit words, 2 rows x NCMAX bits
-constexpr int OFF_PART = OFF_SEL + RP * NCMAX;              // 4 column quarters x 128 x (m, s)
-constexpr int OFF_RED = OFF_PART + 4 * M * 8;               // 16 epilogue warps
-constexpr int OFF_MISC = OFF_RED + 64;
+constexpr int OFF_T = OFF_B + BSTG * KB;                    // 192 KB: 2 item parities x 2 rows x NCMAX fp32
+constexpr int OFF_SEL = OFF_T + 2 * RP * NCMAX * 4;         // 208 KB: selection bit words, 2 x 2 rows x NCMAX bits
+constexpr int OFF_PART = OFF_SEL + 2 * RP * NCMAX / 8;      // 2 item parities x 4 column quarters x 128 x (m, s)
+constexpr int OFF_MISC = OFF_PART + 2 * 4 * M * 8;
 constexpr int SMEM = OFF_MISC + 1024 + 1024;
+static_assert(SMEM <= 232448, "teacher shared memory exceeds the per-block limit");
 
 struct Args {
     Geo g;
@@ -176,13 +176,13 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *sQ = smem + OFF_Q;
     unsigned char *sB = smem + OFF_B;
-    float *sT = reinterpret_cast<float *>(smem + OFF_T);
-    uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + OFF_SEL);  // [RP][NCMAX / 32]
+    float *sT = reinterpret_cast<float *>(smem + OFF_T);                // [2][RP][NCMAX]
+    uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + OFF_SEL);     // [2][RP][NCMAX / 32]
     float2 *sPart = reinterpret_cast<float2 *>(smem + OFF_PART);
-    float *sRed = reinterpret_cast<float *>(smem + OFF_RED);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
     uint64_t *b_full = bars, *b_empty = bars + BSTG, *q_full = bars + 12, *q_empty = bars + 14;
     uint64_t *t_full = bars + 16, *t_empty = bars + 18, *mma_done = bars + 20;
+    uint64_t *mask_full = bars + 22, *t_done = bars + 24;  // [item parity]: helpers -> epilogue, epilogue -> helpers
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 256);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 264);
 
@@ -199,6 +199,8 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             mbar_init(q_empty + i, 1);
             mbar_init(t_full + i, 1);
             mbar_init(t_empty + i, EPI / 32);
+            mbar_init(mask_full + i, 2);
+            mbar_init(t_done + i, EPI / 32);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -321,54 +323,27 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         }
         mma_commit_w(mma_done);
         drain_bar(mma_done, 0, err);
-    } else if (warp >= 2) {
+    } else if (warp < 18) {
         // ---------------------------------------------------------------- epilogue
         // 16 warps: four per TMEM lane quadrant (warp % 4), warp cq = (warp - 2) / 4 of a quadrant reads the
-        // 64 key columns [64 cq, 64 cq + 64) of every tile.
-        const int e = warp - 2, quad = warp & 3, cq = e >> 2, et = threadIdx.x - 64;
+        // 64 key columns [64 cq, 64 cq + 64) of every tile.  The selection masks and the zeroed T rows of an
+        // item come from the helper warps (buffer ic & 1), which also normalise and write the T rows.
+        const int e = warp - 2, quad = warp & 3, cq = e >> 2;
         const int rh = quad * 32 + lane;      // (row, head) of this thread's TMEM lane
         const int i_row = rh >> 6, h = rh & 63;
         const float s2 = g.scale * 1.4426950408889634f;  // logits in log2 units: exp(c) = 2^(x * sigma * log2 e)
         const bool s2_pos = s2 > 0.f;  // then max(x s2) = s2 max(x): the scale folds into one FFMA per element
         const int cb = cq * 64;
         int tc = 0;
-        for (int it_i = blockIdx.x; it_i < total; it_i += gridDim.x) {
+        int ic = 0;
+        for (int it_i = blockIdx.x; it_i < total; it_i += gridDim.x, ic++) {
             const Item it = decode(a, it_i, total);
             const int vme = i_row == 0 ? it.v0 : it.v1;
             const int s_me = it.s0 + i_row;
-            // ---- per-item set-up: selection flags and T rows of both rows
-            named_bar(1, EPI);
-            for (int x = et; x < RP * NCMAX; x += EPI) sT[x] = 0.f;
-            if (et < RP * NCMAX / 32) sMask[et] = 0u;
-            // this thread's id slots s = et + EPI q of both rows, loaded together and kept for the write-out
-            constexpr int NQ = NCMAX / EPI;
-            int32_t idr[RP][NQ];
-#pragma unroll
-            for (int r = 0; r < RP; r++) {
-                const long long row = r == 0 ? it.row0 : it.row1;
-#pragma unroll
-                for (int q = 0; q < NQ; q++) {
-                    const int s = et + q * EPI;
-                    idr[r][q] = (g.sparse && it.vmax > 0 && r < it.n && s < g.K) ? __ldg(a.ids + row * g.K + s) : -1;
-                }
-            }
-            named_bar(1, EPI);
-            if (it.vmax > 0) {
-#pragma unroll
-                for (int r = 0; r < RP; r++) {
-                    const int v = r == 0 ? it.v0 : it.v1;
-                    if (g.sparse) {
-#pragma unroll
-                        for (int q = 0; q < NQ; q++) {
-                            const long long j = (long long)idr[r][q] - it.gid0;
-                            if (idr[r][q] >= 0 && j >= 0 && j < v) atomicOr(sMask + r * (NCMAX / 32) + (j >> 5), 1u << (j & 31));
-                        }
-                    } else {
-                        for (int wd = et; wd < NCMAX / 32; wd += EPI) sMask[r * (NCMAX / 32) + wd] = range_bits(0, v - 1 - wd * 32);
-                    }
-                }
-            }
-            named_bar(1, EPI);
+            const int ib = ic & 1;
+            float *sTb = sT + ib * RP * NCMAX;
+            const uint32_t *sMaskb = sMask + ib * RP * (NCMAX / 32);
+            wait_bar(mask_full + ib, (ic >> 1) & 1, abort_flag, err, 47);
             // running log2-domain max and sum of this thread's (row, head) over its key columns
             float m = -INFINITY, ssum = 0.f, ell = 0.f;
             const int nt = ntiles(it);
@@ -382,11 +357,14 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 const int t = win ? tt : (tt - it.nw) % it.nct;
                 if (pass2 && tt == it.nw + it.nct) {
                     // l_h (log2 units) from the four column quarters, combined in a fixed order, and the sink
-                    sPart[cq * M + rh] = make_float2(m, ssum);
+                    // (sPart alternates by item parity: a warp can reach the next item's combine before a slow
+                    // one has read this one's)
+                    float2 *pp = sPart + ib * 4 * M;
+                    pp[cq * M + rh] = make_float2(m, ssum);
                     named_bar(1, EPI);
                     float2 p[4];
 #pragma unroll
-                    for (int k = 0; k < 4; k++) p[k] = sPart[k * M + rh];
+                    for (int k = 0; k < 4; k++) p[k] = pp[k * M + rh];
                     const float ah = g.no_sink ? -INFINITY : __ldg(a.sink + h) * 1.4426950408889634f;
                     const float mm = fmaxf(fmaxf(fmaxf(p[0].x, p[1].x), fmaxf(p[2].x, p[3].x)), ah);
                     float S = 0.f;
@@ -409,7 +387,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                         mw[c] = row_ok ? range_bits(s_me - g.window + 1 - pbase, s_me - pbase) : 0u;
                     } else {
                         const int j0 = t * NK + col0;
-                        mw[c] = j0 < NCMAX ? (sMask[i_row * (NCMAX / 32) + (j0 >> 5)] & range_bits(0, vme - 1 - j0)) : 0u;
+                        mw[c] = j0 < NCMAX ? (sMaskb[i_row * (NCMAX / 32) + (j0 >> 5)] & range_bits(0, vme - 1 - j0)) : 0u;
                     }
                 }
                 if ((mw[0] | mw[1]) != 0u) {
@@ -472,7 +450,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                                 }
                             }
                             const int j = t * NK + cb + c * 32 + lane;
-                            if (j < NCMAX && x[0] != 0.f) atomicAdd(sT + i_row * NCMAX + j, x[0]);
+                            if (j < NCMAX && x[0] != 0.f) atomicAdd(sTb + i_row * NCMAX + j, x[0]);
                         }
                     }
                 }
@@ -481,47 +459,67 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 if (lane == 0) mbar_arrive(t_empty + tb);
                 tc++;
             }
-            named_bar(1, EPI);
-            // ---- L1 normalisation and write-out, one row per 256 threads (warps 8 r .. 8 r + 7)
-            const int r = et >> 8, rt = et & 255;
+            // this warp's T contributions to buffer ib are in
+            __syncwarp();
+            if (lane == 0) mbar_arrive(t_done + ib);
+        }
+    } else {
+        // ---------------------------------------------------------------- per-item helpers (warps 18, 19)
+        // Warp 18 + r owns row r of every item.  For item ic (buffer ic & 1): zero its T row, build its selection
+        // bit words, signal mask_full; then, once the epilogue has summed item ic - 1 into the other buffer
+        // (t_done), L1-normalise that row and write it out in the id slot order.  Buffer reuse is ordered by the
+        // warp's own program order (item ic - 2's write-out precedes item ic's set-up).
+        const int r = warp - 18;
+        auto writeout = [&](const Item &it, int icw) {
+            const int ib = icw & 1;
+            wait_bar(t_done + ib, (icw >> 1) & 1, abort_flag, err, 48);
+            if (r >= it.n) return;
+            const float *tr = sT + (ib * RP + r) * NCMAX;
             const int v = r == 0 ? it.v0 : it.v1;
             float part = 0.f;
-            for (int j = rt; j < v; j += 256) part += sT[r * NCMAX + j];
-            part = warp_sum(part);
-            if (lane == 0) sRed[et >> 5] = part;
-            named_bar(1, EPI);
-            float Sr[RP];
-#pragma unroll
-            for (int rr = 0; rr < RP; rr++) {
-                float acc = 0.f;
-#pragma unroll
-                for (int k = 0; k < 8; k++) acc += sRed[rr * 8 + k];
-                Sr[rr] = acc;
-            }
+            for (int j = lane; j < v; j += 32) part += tr[j];
+            const float inv = 1.f / fmaxf(warp_sum(part), 1e-10f);
+            const long long row = r == 0 ? it.row0 : it.row1;
+            float *trow = a.teacher + row * g.TW;
             if (g.sparse) {
-                // write-out with the slot mapping of the set-up: slots et + EPI q of both rows
-#pragma unroll
-                for (int rr = 0; rr < RP; rr++) {
-                    if (rr >= it.n) continue;
-                    const int vr = rr == 0 ? it.v0 : it.v1;
-                    const float ir = 1.f / fmaxf(Sr[rr], 1e-10f);
-                    const long long row = rr == 0 ? it.row0 : it.row1;
-                    float *trow = a.teacher + row * g.TW;
-#pragma unroll
-                    for (int q = 0; q < NQ; q++) {
-                        const int s = et + q * EPI;
-                        if (s >= g.TW) continue;
-                        const long long j = (long long)idr[rr][q] - it.gid0;
-                        trow[s] = (idr[rr][q] >= 0 && j >= 0 && j < vr) ? sT[rr * NCMAX + j] * ir : 0.f;
+                for (int s = lane; s < g.TW; s += 32) {
+                    const int32_t id = s < g.K ? __ldg(a.ids + row * g.K + s) : -1;
+                    const long long j = (long long)id - it.gid0;
+                    trow[s] = (id >= 0 && j >= 0 && j < v) ? tr[j] * inv : 0.f;
+                }
+            } else {
+                for (int j = lane; j < g.TW; j += 32) trow[j] = j < v ? tr[j] * inv : 0.f;
+            }
+        };
+        Item prev;
+        int ic = 0;
+        for (int it_i = blockIdx.x; it_i < total; it_i += gridDim.x, ic++) {
+            const Item it = decode(a, it_i, total);
+            const int ib = ic & 1;
+            float4 *tz = reinterpret_cast<float4 *>(sT + (ib * RP + r) * NCMAX);
+            for (int x = lane; x < NCMAX / 4; x += 32) tz[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+            uint32_t *mk = sMask + (ib * RP + r) * (NCMAX / 32);
+            const int v = r == 0 ? it.v0 : it.v1;
+            if (g.sparse) {
+                mk[lane] = 0u;
+                __syncwarp();
+                if (r < it.n && v > 0) {
+                    const long long row = r == 0 ? it.row0 : it.row1;
+                    for (int s = lane; s < g.K; s += 32) {
+                        const int32_t id = __ldg(a.ids + row * g.K + s);
+                        const long long j = (long long)id - it.gid0;
+                        if (id >= 0 && j >= 0 && j < v) atomicOr(mk + (j >> 5), 1u << (j & 31));
                     }
                 }
-            } else if (r < it.n) {
-                const float inv = 1.f / fmaxf(Sr[r], 1e-10f);
-                const long long row = r == 0 ? it.row0 : it.row1;
-                float *trow = a.teacher + row * g.TW;
-                for (int j = rt; j < g.TW; j += 256) trow[j] = j < v ? sT[r * NCMAX + j] * inv : 0.f;
+            } else {
+                mk[lane] = range_bits(0, v - 1 - lane * 32);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mask_full + ib);
+            if (ic > 0) writeout(prev, ic - 1);
+            prev = it;
         }
+        if (ic > 0) writeout(prev, ic - 1);
     }
     fence_before();
     __syncthreads();
