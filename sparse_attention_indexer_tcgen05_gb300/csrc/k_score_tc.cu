@@ -235,14 +235,20 @@ __device__ void select_row(const Args &a, const Item &it, int k, const float *sc
         }
     } else {
         // the k-th largest key: the largest T with #(key >= T) >= kk, built bit by bit (keys of absent slots
-        // are 0, below every present score's key); four independent partial counts per round
+        // are 0, below every present score's key); four independent partial counts per round.  The search
+        // stops early once exactly kk keys lie at or above the candidate: that set is the top kk whatever the
+        // remaining bits, and no tie is cut at T.
         uint32_t T = 0u;
         for (int bit = 31; bit >= 0; bit--) {
             const uint32_t cand = T | (1u << bit);
             unsigned c4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int e = 0; e < PER; e++) c4[e & 3] += key[e] >= cand ? 1u : 0u;
-            if ((int)__reduce_add_sync(0xffffffffu, (c4[0] + c4[1]) + (c4[2] + c4[3])) >= kk) T = cand;
+            const int c = (int)__reduce_add_sync(0xffffffffu, (c4[0] + c4[1]) + (c4[2] + c4[3]));
+            if (c >= kk) {
+                T = cand;
+                if (c == kk) break;
+            }
         }
         unsigned gt4[4] = {0u, 0u, 0u, 0u}, eq4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
