@@ -37,7 +37,7 @@ def gpu_step(d: workload.DeviceInputs, want_teacher=True):
     loss, dq, dw, dk = B.csa_indexer_bwd(p, *d.indexer, *d.teacher_side, ids, sel, row_loss=row_loss)
     torch.cuda.synchronize()
     B.csa_check_device_status()
-    out.update(loss=float(loss), dq=dq, dw=dw, dk=dk, row_loss=row_loss)
+    out.update(loss=float(loss), dq=dq, dw=dw, dk=dk, row_loss=row_loss, bwd_path=B.csa_last_path())
     return out
 
 
@@ -202,7 +202,7 @@ def check_step(inp, d=None, rows=None, full_dk=True, report=None):
     e_dw = rel_l2(dw[same], ref["dw"][same])
     assert e_dq <= GRAD_TOL and e_dw <= GRAD_TOL, f"dq {e_dq} dw {e_dw}"
     out = dict(recall=recall, teacher_err=max(t_err, t_err2), dq_err=e_dq, dw_err=e_dw, rows=len(rws),
-               same_rows=int(same.sum()), path=B.csa_last_path(),
+               same_rows=int(same.sum()), path=B.csa_last_path(), bwd_path=gpu["bwd_path"],
                _oracle_teacher=ref["teacher"], _gpu_teacher_oracle_ids=te_o)
     dk = to_np(gpu["dk"]).reshape(-1, c.idx_dim)
     if rows is None:

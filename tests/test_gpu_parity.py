@@ -112,6 +112,17 @@ def test_tensor_core_shape_multi_tile():
     _report("tc_shape_bshd", U.check_step(synth.generate(cfg)))
 
 
+@pytest.mark.parametrize("layout", ["bshd", "sbhd"])
+def test_tensor_core_shape_odd_length(layout):
+    """The tensor-core shapes (H = 64 teacher heads, H_I = 64, D_I = 128) with an odd sequence length, so the
+    last row pair of each sequence has one row, in both position-major and sequence-major layouts."""
+    cfg = small(layout=layout, seqlen=999, heads=64, head_dim=64, idx_heads=64, idx_dim=128, topk=96, window=40,
+                seed=10)
+    out = U.check_step(synth.generate(cfg))
+    assert out["path"] == "tcgen05" and out["bwd_path"] == "tcgen05", (out["path"], out["bwd_path"])
+    _report(f"tc_shape_odd_{layout}", out)
+
+
 def test_tensor_core_shape_thd():
     cfg = small(layout="thd", seqlen=2600, heads=16, head_dim=64, idx_heads=64, idx_dim=128, topk=128, window=40,
                 doc_len=(300, 1200), seed=9)
