@@ -473,16 +473,18 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
 #pragma unroll
                 for (int rr = 0; rr < 2; rr++) {
                     const int k = half * 2 + rr;
-                    float ac[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums over heads h % 4
+                    // independent partial sums over heads h % 4, two per paired FMA
+                    float2 ac[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
                     for (int c = 0; c < 2; c++) {
                         float x[32];
                         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NCOL + k * HI + c * 32), x);
-                        const float *wk = sW + k * HI + c * 32;
+                        const float2 *wk = reinterpret_cast<const float2 *>(sW + k * HI + c * 32);
 #pragma unroll
-                        for (int h = 0; h < 32; h++) ac[h & 3] = fmaf(wk[h], fmaxf(x[h], 0.f), ac[h & 3]);
+                        for (int h2 = 0; h2 < 16; h2++)
+                            ac[h2 & 1] = fma2(wk[h2], make_float2(fmaxf(x[2 * h2], 0.f), fmaxf(x[2 * h2 + 1], 0.f)), ac[h2 & 1]);
                     }
-                    const float acc = (ac[0] + ac[1]) + (ac[2] + ac[3]);
+                    const float acc = (ac[0].x + ac[0].y) + (ac[1].x + ac[1].y);  // heads (0 + 1) + (2 + 3) mod 4
                     if (k < it.n && j < it.v[k]) scb[k * NCMAX + j] = acc;
                 }
                 fence_before();

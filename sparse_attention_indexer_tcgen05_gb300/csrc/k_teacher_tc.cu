@@ -420,10 +420,14 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                                 m = cm;
                             }
                             const float sc = s2_pos ? s2 : 1.f;
-                            float sm[4] = {0.f, 0.f, 0.f, 0.f};
+                            float2 sm[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // columns q % 4
 #pragma unroll
-                            for (int q = 0; q < 32; q++) sm[q & 3] += ex2(fmaf(x[q], sc, -m));
-                            ssum += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                            for (int q2 = 0; q2 < 16; q2++) {
+                                const float2 arg = fma2(make_float2(x[2 * q2], x[2 * q2 + 1]), make_float2(sc, sc),
+                                                        make_float2(-m, -m));
+                                sm[q2 & 1] = add2(sm[q2 & 1], make_float2(ex2(arg.x), ex2(arg.y)));
+                            }
+                            ssum += (sm[0].x + sm[0].y) + (sm[1].x + sm[1].y);
                         }
                     } else {
 #pragma unroll 1
@@ -433,7 +437,12 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                             tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + cb + c * 32), x);
                             if (mw[c] == 0xffffffffu) {
 #pragma unroll
-                                for (int q = 0; q < 32; q++) x[q] = ex2(fmaf(x[q], s2, -ell));
+                                for (int q2 = 0; q2 < 16; q2++) {
+                                    const float2 arg = fma2(make_float2(x[2 * q2], x[2 * q2 + 1]), make_float2(s2, s2),
+                                                            make_float2(-ell, -ell));
+                                    x[2 * q2] = ex2(arg.x);
+                                    x[2 * q2 + 1] = ex2(arg.y);
+                                }
                             } else {
 #pragma unroll
                                 for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? ex2(fmaf(x[q], s2, -ell)) : 0.f;
