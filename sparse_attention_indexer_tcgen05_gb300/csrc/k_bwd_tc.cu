@@ -799,10 +799,12 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
 #pragma unroll
                     for (int c = 0; c < 8; c++) {
                         const float4 w4 = wr4[c];
-                        gw[4 * c] = gk * w4.x;
-                        gw[4 * c + 1] = gk * w4.y;
-                        gw[4 * c + 2] = gk * w4.z;
-                        gw[4 * c + 3] = gk * w4.w;
+                        const float2 lo = mul2(make_float2(gk, gk), make_float2(w4.x, w4.y));
+                        const float2 hi = mul2(make_float2(gk, gk), make_float2(w4.z, w4.w));
+                        gw[4 * c] = lo.x;
+                        gw[4 * c + 1] = lo.y;
+                        gw[4 * c + 2] = hi.x;
+                        gw[4 * c + 3] = hi.y;
                     }
                     tmem_wait_ld(xr);
 #pragma unroll

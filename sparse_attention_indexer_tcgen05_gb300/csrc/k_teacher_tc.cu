@@ -451,11 +451,21 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
 #pragma unroll
                             for (int off = 16; off >= 1; off >>= 1) {
                                 const bool up = (lane & off) != 0;
+                                if (off >= 2) {  // the adds in pairs
 #pragma unroll
-                                for (int q = 0; q < off; q++) {
-                                    const float send = up ? x[q] : x[q + off];
-                                    const float keep = up ? x[q + off] : x[q];
-                                    x[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                    for (int q = 0; q < off; q += 2) {
+                                        const float s0 = up ? x[q] : x[q + off], s1 = up ? x[q + 1] : x[q + 1 + off];
+                                        const float k0 = up ? x[q + off] : x[q], k1 = up ? x[q + 1 + off] : x[q + 1];
+                                        const float2 r = add2(make_float2(k0, k1),
+                                                              make_float2(__shfl_xor_sync(0xffffffffu, s0, off),
+                                                                          __shfl_xor_sync(0xffffffffu, s1, off)));
+                                        x[q] = r.x;
+                                        x[q + 1] = r.y;
+                                    }
+                                } else {
+                                    const float send = up ? x[0] : x[1];
+                                    const float keep = up ? x[1] : x[0];
+                                    x[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
                                 }
                             }
                             const int j = t * NK + cb + c * 32 + lane;
