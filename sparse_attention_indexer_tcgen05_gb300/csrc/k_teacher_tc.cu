@@ -392,42 +392,52 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 }
                 if ((mw[0] | mw[1]) != 0u) {
                     if (!pass2) {
-                        // online max / sum, one 32-column chunk at a time
+                        // running sum against a reference max, one 32-column chunk at a time: the first chunk
+                        // with columns sets the reference; a later chunk is summed against it directly and only
+                        // re-based on its own max when its sum leaves the safe range (a logit more than ~64
+                        // log2 units above the reference), so the common chunk needs no max pass
 #pragma unroll 1
                         for (int c = 0; c < 2; c++) {
                             if (mw[c] == 0u) continue;
                             float x[32];
                             tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + cb + c * 32), x);
-                            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                             if (s2_pos) {
                                 if (mw[c] != 0xffffffffu) {
 #pragma unroll
                                     for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? x[q] : -INFINITY;
                                 }
-#pragma unroll
-                                for (int q = 0; q < 32; q++) mx[q & 3] = fmaxf(mx[q & 3], x[q]);
                             } else {
 #pragma unroll
-                                for (int q = 0; q < 32; q++) {
-                                    x[q] = (mw[c] >> q) & 1u ? x[q] * s2 : -INFINITY;
-                                    mx[q & 3] = fmaxf(mx[q & 3], x[q]);
-                                }
-                            }
-                            float cm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                            if (s2_pos) cm *= s2;
-                            if (cm > m) {  // cm is finite: the chunk holds at least one unmasked column
-                                ssum *= ex2(m - cm);
-                                m = cm;
+                                for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? x[q] * s2 : -INFINITY;
                             }
                             const float sc = s2_pos ? s2 : 1.f;
-                            float2 sm[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // columns q % 4
+                            auto chunk_max = [&]() -> float {  // finite: the chunk holds an unmasked column
+                                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                            for (int q2 = 0; q2 < 16; q2++) {
-                                const float2 arg = fma2(make_float2(x[2 * q2], x[2 * q2 + 1]), make_float2(sc, sc),
-                                                        make_float2(-m, -m));
-                                sm[q2 & 1] = add2(sm[q2 & 1], make_float2(ex2(arg.x), ex2(arg.y)));
+                                for (int q = 0; q < 32; q++) mx[q & 3] = fmaxf(mx[q & 3], x[q]);
+                                return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+                            };
+                            auto chunk_sum = [&]() -> float {
+                                float2 sm[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // columns q % 4
+#pragma unroll
+                                for (int q2 = 0; q2 < 16; q2++) {
+                                    const float2 arg = fma2(make_float2(x[2 * q2], x[2 * q2 + 1]), make_float2(sc, sc),
+                                                            make_float2(-m, -m));
+                                    sm[q2 & 1] = add2(sm[q2 & 1], make_float2(ex2(arg.x), ex2(arg.y)));
+                                }
+                                return (sm[0].x + sm[0].y) + (sm[1].x + sm[1].y);
+                            };
+                            if (m == -INFINITY) m = chunk_max();
+                            float cs = chunk_sum();
+                            if (!(cs <= 0x1p64f)) {
+                                const float cm = chunk_max();
+                                if (cm > m) {
+                                    ssum *= ex2(m - cm);
+                                    m = cm;
+                                }
+                                cs = chunk_sum();
                             }
-                            ssum += (sm[0].x + sm[0].y) + (sm[1].x + sm[1].y);
+                            ssum += cs;
                         }
                     } else {
 #pragma unroll 1
