@@ -247,7 +247,9 @@ csa_status run_bwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
     const bool tc = tc_bwd_supported(g, sizeof(T) == 2);
     char *btc = ws_at(ws, P.off_btc);
     float *gd = tc ? tc_bwd_gd(g, btc) : nullptr;
-    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, gbuf, row_loss, gd, tc ? tc_bwd_ncp(g) : 0, st));
+    // the tensor-core backward reads g by key only; the slot-layout rows are for the CUDA-core backward
+    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, tc ? nullptr : gbuf, row_loss, gd,
+                       tc ? tc_bwd_ncp(g) : 0, st));
     if (g.key_rows * g.DI > 0)
         CSA_CUDA(cudaMemsetAsync(dk_acc, 0, sizeof(float) * (size_t)g.key_rows * g.DI, st));
     if (tc) {

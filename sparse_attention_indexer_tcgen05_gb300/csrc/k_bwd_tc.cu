@@ -482,59 +482,62 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         const int rh = quad * 32 + lane;
         const int er = rh >> 6, h = rh & 63;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        // An item's dQ' read-out is deferred until the next item's first LAG tiles have been converted, so the
+        // drain of its last dQ' group overlaps useful work (LAG <= R_XSTG: those tiles' X slots were freed by
+        // the previous item's dQ' groups, whose accumulator is the one being read out).
+        constexpr int LAG = 2;
+        static_assert(LAG <= R_XSTG, "deferred read-out would wait on its own X slots");
+        struct Pend {
+            long long row;
+            int gb, ic;       // g / w / q buffer of the item, item index (dW buffer parity)
+            bool tiles, exists, valid;
+        };
         int xb = 0, dqc = 0, ai = 0, ic = 0;
         uint32_t xph = 0;
-        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
-            const Pair p = decode_pair(a, i);
-            const int nt = (p.vmax + NKEY - 1) / NKEY;
-            const int gb = ai & 1;  // g / w buffer of the items with visible keys (as the producer counts them)
-            if (nt > 0) wait_bar(gd_full + gb, (ai >> 1) & 1, abort_flag, err, 9);
-            const float *gd = sGD + gb * RP * NCMAX + er * NKEY;  // [key tile][row][128]
-            const int v_me = er == 0 ? p.v0 : p.v1;
-            for (int t = 0; t < nt; t++) {
-                wait_bar(x_full + xb, xph, abort_flag, err, 10);
-                fence_after();
-                const int j0 = t * NKEY + qq * 32;  // first key of this warp's columns
-                const float *gt = gd + t * RP * NKEY + qq * 32;
-                uint32_t xr[32];
-                const uint32_t tcol = tX + lane_off + (uint32_t)(xb * 128 + qq * 32);
-                tmem_ld32_async(tcol, xr);
-                // g of the row for these 32 keys (the same addresses across the warp: broadcast reads), fetched
-                // while the TMEM load is in flight; keys at or beyond the row's visible count give 0
-                float gk[32];
+        // ---- one key tile: X^T -> G'^T over the warp's own columns
+        auto tile = [&](const float *gd, int v_me, int t) {
+            wait_bar(x_full + xb, xph, abort_flag, err, 10);
+            fence_after();
+            const int j0 = t * NKEY + qq * 32;  // first key of this warp's columns
+            const float *gt = gd + t * RP * NKEY + qq * 32;
+            uint32_t xr[32];
+            const uint32_t tcol = tX + lane_off + (uint32_t)(xb * 128 + qq * 32);
+            tmem_ld32_async(tcol, xr);
+            // g of the row for these 32 keys (the same addresses across the warp: broadcast reads), fetched
+            // while the TMEM load is in flight; keys at or beyond the row's visible count give 0
+            float gk[32];
 #pragma unroll
-                for (int q4 = 0; q4 < 8; q4++) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(gt + 4 * q4);
-                    gk[4 * q4] = g4.x;
-                    gk[4 * q4 + 1] = g4.y;
-                    gk[4 * q4 + 2] = g4.z;
-                    gk[4 * q4 + 3] = g4.w;
-                }
-                if (j0 + 32 > v_me) {  // warp-uniform: the row's last visible tile
-#pragma unroll
-                    for (int q = 0; q < 32; q++) gk[q] = j0 + q < v_me ? gk[q] : 0.f;
-                }
-                tmem_wait_ld(xr);
-                uint32_t pk[16];
-#pragma unroll
-                for (int q2 = 0; q2 < 16; q2++)
-                    pk[q2] = pack_bf16(__uint_as_float(xr[2 * q2]) > 0.f ? gk[2 * q2] : 0.f,
-                                       __uint_as_float(xr[2 * q2 + 1]) > 0.f ? gk[2 * q2 + 1] : 0.f);
-                tmem_st16(tcol, pk);  // G' over this warp's own X columns (already read)
-                fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(g_full + xb);
-                if (++xb == R_XSTG) {
-                    xb = 0;
-                    xph ^= 1u;
-                }
+            for (int q4 = 0; q4 < 8; q4++) {
+                const float4 g4 = *reinterpret_cast<const float4 *>(gt + 4 * q4);
+                gk[4 * q4] = g4.x;
+                gk[4 * q4 + 1] = g4.y;
+                gk[4 * q4 + 2] = g4.z;
+                gk[4 * q4 + 3] = g4.w;
             }
-            // ---- dQ' readout: this warp's 32 of the 128 d of its (row, head)
-            const bool exists = er < p.n;
-            const long long row = er == 0 ? p.row0 : p.row1;
+            if (j0 + 32 > v_me) {  // warp-uniform: the row's last visible tile
+#pragma unroll
+                for (int q = 0; q < 32; q++) gk[q] = j0 + q < v_me ? gk[q] : 0.f;
+            }
+            tmem_wait_ld(xr);
+            uint32_t pk[16];
+#pragma unroll
+            for (int q2 = 0; q2 < 16; q2++)
+                pk[q2] = pack_bf16(__uint_as_float(xr[2 * q2]) > 0.f ? gk[2 * q2] : 0.f,
+                                   __uint_as_float(xr[2 * q2 + 1]) > 0.f ? gk[2 * q2 + 1] : 0.f);
+            tmem_st16(tcol, pk);  // G' over this warp's own X columns (already read)
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(g_full + xb);
+            if (++xb == R_XSTG) {
+                xb = 0;
+                xph ^= 1u;
+            }
+        };
+        // ---- an item's end: dQ' read-out (this warp's 32 of the 128 d of its (row, head)), dW, buffer release
+        auto finish = [&](const Pend &P) {
             float pa[4] = {0.f, 0.f, 0.f, 0.f};
-            if (nt > 0) {
-                const int bb = ai & 1;
+            if (P.tiles) {
+                const int bb = P.gb;
                 wait_bar(dq_full, dqc & 1, abort_flag, err, 12);
                 fence_after();
                 uint32_t vr[32];
@@ -550,7 +553,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(dq_empty);
                 dqc++;
-                const float wv = sW[gb * RP * HI + er * HI + h];
+                const float wv = sW[P.gb * RP * HI + er * HI + h];
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
                     const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[c]);
@@ -561,8 +564,8 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                         pa[(2 * u + 1) & 3] = fmaf(qf.y, __uint_as_float(vr[c * 8 + 2 * u + 1]), pa[(2 * u + 1) & 3]);
                     }
                 }
-                if (exists) {
-                    __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + qq * 32;
+                if (P.exists) {
+                    __nv_bfloat16 *out = a.dq + P.row * (HI * DI) + h * DI + qq * 32;
 #pragma unroll
                     for (int c = 0; c < 4; c++) {
                         uint4 o;
@@ -575,27 +578,58 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_empty + bb);  // q tile no longer read
-                ai++;
-            } else if (exists) {
-                __nv_bfloat16 *out = a.dq + row * (HI * DI) + h * DI + qq * 32;
+            } else if (P.exists) {
+                __nv_bfloat16 *out = a.dq + P.row * (HI * DI) + h * DI + qq * 32;
                 for (int c = 0; c < 4; c++) *reinterpret_cast<uint4 *>(out + c * 8) = make_uint4(0, 0, 0, 0);
             }
-            // dW = q . dQ' over the four d quarters, summed in a fixed order (sDW alternates by item parity, so
-            // one barrier per item suffices)
-            // (the four warps of a quadrant meet on an mbarrier; the d-quarter-0 warp adds and writes)
-            float *dwb = sDW + (ic & 1) * 4 * M_PAIRS;
+            // dW = q . dQ' over the four d quarters, summed in a fixed order (sDW alternates by item parity; the
+            // four warps of a quadrant meet on an mbarrier and the d-quarter-0 warp adds and writes)
+            float *dwb = sDW + (P.ic & 1) * 4 * M_PAIRS;
             dwb[qq * M_PAIRS + rh] = (pa[0] + pa[1]) + (pa[2] + pa[3]);
             __syncwarp();
-            uint64_t *dwq = dw_bar + (ic & 1) * 4 + quad;
+            uint64_t *dwq = dw_bar + (P.ic & 1) * 4 + quad;
             if (lane == 0) mbar_arrive(dwq);
             if (qq == 0) {
-                wait_bar(dwq, (ic >> 1) & 1, abort_flag, err, 13);
-                if (exists)
-                    a.dw[row * HI + h] = (dwb[rh] + dwb[M_PAIRS + rh]) + (dwb[2 * M_PAIRS + rh] + dwb[3 * M_PAIRS + rh]);
+                wait_bar(dwq, (P.ic >> 1) & 1, abort_flag, err, 13);
+                if (P.exists)
+                    a.dw[P.row * HI + h] = (dwb[rh] + dwb[M_PAIRS + rh]) + (dwb[2 * M_PAIRS + rh] + dwb[3 * M_PAIRS + rh]);
             }
             __syncwarp();
-            if (nt > 0 && lane == 0) mbar_arrive(gd_empty + gb);
+            if (P.tiles && lane == 0) mbar_arrive(gd_empty + P.gb);
+        };
+        Pend pend;
+        pend.valid = false;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
+            const Pair p = decode_pair(a, i);
+            const int nt = (p.vmax + NKEY - 1) / NKEY;
+            Pend cur;
+            cur.row = er == 0 ? p.row0 : p.row1;
+            cur.exists = er < p.n;
+            cur.ic = ic;
+            cur.tiles = nt > 0;
+            cur.gb = ai & 1;  // g / w buffer of the items with visible keys (as the producer counts them)
+            cur.valid = true;
+            if (nt == 0) {
+                if (pend.valid) finish(pend);
+                pend.valid = false;
+                finish(cur);
+                continue;
+            }
+            wait_bar(gd_full + cur.gb, (ai >> 1) & 1, abort_flag, err, 9);
+            const float *gd = sGD + cur.gb * RP * NCMAX + er * NKEY;  // [key tile][row][128]
+            const int v_me = er == 0 ? p.v0 : p.v1;
+            for (int t = 0; t < nt; t++) {
+                tile(gd, v_me, t);
+                if (t == LAG - 1 && pend.valid) {
+                    finish(pend);
+                    pend.valid = false;
+                }
+            }
+            if (pend.valid) finish(pend);
+            pend = cur;
+            ai++;
         }
+        if (pend.valid) finish(pend);
     }
     fence_before();
     __syncthreads();

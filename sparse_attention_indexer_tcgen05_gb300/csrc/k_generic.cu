@@ -392,7 +392,7 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
         const Row R = decode_row(g, r);
         const int32_t *row_ids = ids + r * g.K;
         const float *trow = teacher + r * TW;
-        float *grow = gbuf + r * TW;
+        float *grow = gbuf != nullptr ? gbuf + r * TW : nullptr;
         float *drow = gd != nullptr ? gd + gd_row(g, R, r) * ncp : nullptr;
         if (drow != nullptr) {
             for (int j = tid; j < R.v; j += kThreads) drow[j] = 0.f;
@@ -409,7 +409,8 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
         for (int s = tid; s < TW; s += kThreads) m = fmaxf(m, score_of(s));
         m = block_reduce(m, red, true);
         if (m == -INFINITY) {  // empty support: no loss, no gradient
-            for (int s = tid; s < TW; s += kThreads) grow[s] = 0.f;
+            if (grow != nullptr)
+                for (int s = tid; s < TW; s += kThreads) grow[s] = 0.f;
             if (tid == 0) row_loss[r] = 0.f;
             continue;
         }
@@ -440,7 +441,7 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
                 gv = g.factor * p * (A - trow[s] / (p + kEps));
                 if (drow != nullptr) drow[g.sparse ? (int)(row_ids[s] - lo) : s] = gv;
             }
-            grow[s] = gv;
+            if (grow != nullptr) grow[s] = gv;
         }
         if (tid == 0) row_loss[r] = L;
     }
@@ -449,6 +450,8 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
 // The same step for the sparse support with K <= 512 slots (teacher width K): one warp per row, the row's
 // ids, scores and teacher values held in registers (slot s = lane + 32 i, coalesced), warp reductions.
 // g by key (gd, as in kl_kernel): the row's visible range is zeroed, then every support slot writes its key.
+// A lane keeps, per slot, the score, the teacher value and the key offset within the row's visible range
+// (-1 off the support).  gbuf may be null (the tensor-core backward reads gd only).
 constexpr int kKlPer = 16;  // slots per lane
 __global__ void __launch_bounds__(kThreads)
 kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ selscore,
@@ -464,41 +467,45 @@ kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__
         const int32_t *row_ids = ids + r * K;
         const float *srow = selscore + r * K;
         const float *trow = teacher + r * K;
-        float *grow = gbuf + r * K;
-        int32_t id[kKlPer];
+        float *grow = gbuf != nullptr ? gbuf + r * K : nullptr;
+        int jj[kKlPer];
         float x[kKlPer], t[kKlPer];
 #pragma unroll
-        for (int i = 0; i < kKlPer; i++) {
+        for (int i = 0; i < kKlPer; i++) {  // every load issued before any is used
             const int s = lane + 32 * i;
             const bool in = s < K;
-            id[i] = in ? __ldg(row_ids + s) : -1;
+            jj[i] = in ? __ldg(row_ids + s) : -1;
             x[i] = in ? __ldg(srow + s) : 0.f;
             t[i] = in ? __ldg(trow + s) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kKlPer; i++) {
+            const long long j = jj[i] >= 0 ? (long long)jj[i] - lo : -1;
+            jj[i] = (j >= 0 && j < R.v) ? (int)j : -1;
         }
         float *drow = gd != nullptr ? gd + gd_row(g, R, r) * ncp : nullptr;
         if (drow != nullptr) {  // zero the visible range (16-byte stores: ncp is a multiple of 4)
             for (int j4 = lane; 4 * j4 < R.v; j4 += 32) reinterpret_cast<float4 *>(drow)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
             __syncwarp();
         }
-        bool sel[kKlPer];
         float m = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kKlPer; i++) {
-            sel[i] = lane + 32 * i < K && id[i] >= lo && id[i] < lo + R.v;
-            if (sel[i]) m = fmaxf(m, x[i]);
-        }
+        for (int i = 0; i < kKlPer; i++)
+            if (jj[i] >= 0) m = fmaxf(m, x[i]);
         m = warp_max(m);
         if (m == -INFINITY) {  // empty support: no loss, no gradient
+            if (grow != nullptr) {
 #pragma unroll
-            for (int i = 0; i < kKlPer; i++)
-                if (lane + 32 * i < K) grow[lane + 32 * i] = 0.f;
+                for (int i = 0; i < kKlPer; i++)
+                    if (lane + 32 * i < K) grow[lane + 32 * i] = 0.f;
+            }
             if (lane == 0) row_loss[r] = 0.f;
             continue;
         }
         float z = 0.f;
 #pragma unroll
         for (int i = 0; i < kKlPer; i++) {
-            x[i] = sel[i] ? __expf(x[i] - m) : 0.f;
+            x[i] = jj[i] >= 0 ? __expf(x[i] - m) : 0.f;
             z += x[i];
         }
         z = warp_sum(z);
@@ -506,7 +513,7 @@ kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__
         float A = 0.f, L = 0.f;
 #pragma unroll
         for (int i = 0; i < kKlPer; i++) {
-            if (!sel[i]) continue;
+            if (jj[i] < 0) continue;
             const float p = x[i] * inv_z;
             A += t[i] * p / (p + kEps);
             L += t[i] * (logf(t[i] + kEps) - logf(p + kEps));
@@ -518,9 +525,9 @@ kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__
             const int s = lane + 32 * i;
             if (s >= K) continue;
             const float p = x[i] * inv_z;
-            const float gv = sel[i] ? g.factor * p * (A - t[i] / (p + kEps)) : 0.f;
-            grow[s] = gv;
-            if (drow != nullptr && sel[i]) drow[id[i] - lo] = gv;
+            const float gv = jj[i] >= 0 ? g.factor * p * (A - t[i] / (p + kEps)) : 0.f;
+            if (grow != nullptr) grow[s] = gv;
+            if (drow != nullptr && jj[i] >= 0) drow[jj[i]] = gv;
         }
         if (lane == 0) row_loss[r] = L;
     }
