@@ -17,10 +17,10 @@
 //   pass 1: window tiles + compressed tiles -> per-(row,h) online max / sum, then l_h with the sink;
 //   pass 2: compressed tiles again -> exp(c - l_h) on selected keys, summed over the 64 heads of a row by a
 //           warp reduce-scatter (31 shuffles per 32 columns) into shared per-key T rows; then the L1
-//           normalisation and the write-out in the id slot order.
+//           normalisation and the write-out in the id slot order (helper warps).
 // Roles: warp 0 TMA, warp 1 TMEM (two 256-column accumulators) + MMA issue, warps 2..17 epilogue (four warps
-// per TMEM lane quadrant, each with a quarter of the 256 key columns).  Waits are bounded as in the other
-// tensor-core kernels.
+// per TMEM lane quadrant, each with two 32-column chunks of every tile), warps 18..19 per-item helpers.
+// Waits are bounded as in the other tensor-core kernels.
 #include "csa_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -325,15 +325,17 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         drain_bar(mma_done, 0, err);
     } else if (warp < 18) {
         // ---------------------------------------------------------------- epilogue
-        // 16 warps: four per TMEM lane quadrant (warp % 4), warp cq = (warp - 2) / 4 of a quadrant reads the
-        // 64 key columns [64 cq, 64 cq + 64) of every tile.  The selection masks and the zeroed T rows of an
+        // 16 warps: four per TMEM lane quadrant (warp % 4), warp cq = (warp - 2) / 4 of a quadrant reads two
+        // 32-column chunks of every tile (col_of below).  The selection masks and the zeroed T rows of an
         // item come from the helper warps (buffer ic & 1), which also normalise and write the T rows.
         const int e = warp - 2, quad = warp & 3, cq = e >> 2;
         const int rh = quad * 32 + lane;      // (row, head) of this thread's TMEM lane
         const int i_row = rh >> 6, h = rh & 63;
         const float s2 = g.scale * 1.4426950408889634f;  // logits in log2 units: exp(c) = 2^(x * sigma * log2 e)
         const bool s2_pos = s2 > 0.f;  // then max(x s2) = s2 max(x): the scale folds into one FFMA per element
-        const int cb = cq * 64;
+        // chunk c (0, 1) of warp cq covers columns [32 cq + 128 c, +32): the four warps of a quadrant share the
+        // first 128 columns of a tile, so a partly filled tile (the window's, a row's last) keeps them all busy
+        auto col_of = [&](int c) { return cq * 32 + c * 128; };
         int tc = 0;
         int ic = 0;
         for (int it_i = blockIdx.x; it_i < total; it_i += gridDim.x, ic++) {
@@ -381,7 +383,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 uint32_t mw[2];
 #pragma unroll
                 for (int c = 0; c < 2; c++) {
-                    const int col0 = cb + c * 32;
+                    const int col0 = col_of(c);
                     if (win) {
                         const int pbase = it.p_lo + t * NK + col0;
                         mw[c] = row_ok ? range_bits(s_me - g.window + 1 - pbase, s_me - pbase) : 0u;
@@ -400,7 +402,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                         for (int c = 0; c < 2; c++) {
                             if (mw[c] == 0u) continue;
                             float x[32];
-                            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + cb + c * 32), x);
+                            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + col_of(c)), x);
                             if (s2_pos) {
                                 if (mw[c] != 0xffffffffu) {
 #pragma unroll
@@ -444,7 +446,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                         for (int c = 0; c < 2; c++) {
                             if (mw[c] == 0u) continue;
                             float x[32];
-                            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + cb + c * 32), x);
+                            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + col_of(c)), x);
                             if (mw[c] == 0xffffffffu) {
 #pragma unroll
                                 for (int q2 = 0; q2 < 16; q2++) {
@@ -478,7 +480,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                                     x[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
                                 }
                             }
-                            const int j = t * NK + cb + c * 32 + lane;
+                            const int j = t * NK + col_of(c) + lane;
                             if (j < NCMAX && x[0] != 0.f) atomicAdd(sTb + i_row * NCMAX + j, x[0]);
                         }
                     }
