@@ -348,6 +348,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
             wait_bar(mask_full + ib, (ic >> 1) & 1, abort_flag, err, 47);
             // running log2-domain max and sum of this thread's (row, head) over its key columns
             float m = -INFINITY, ssum = 0.f, ell = 0.f;
+            float ell4[4] = {0.f, 0.f, 0.f, 0.f};  // l_h of heads g, g + 8, g + 16, g + 24 of the quadrant
             const int nt = ntiles(it);
             const bool row_ok = s_me < it.len_real;
             for (int tt = 0; tt < nt; tt++) {
@@ -377,6 +378,8 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                         if (ah != -INFINITY) S += ex2(ah - mm);
                     }
                     ell = mm + lg2(S);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; k4++) ell4[k4] = __shfl_sync(0xffffffffu, ell, (lane >> 2) + 8 * k4);
                 }
                 // mask words of this warp's two 32-column chunks; they depend only on the warp's row, so the
                 // skip of an all-masked sub-chunk and the full-word fast paths below are warp-uniform
@@ -442,46 +445,50 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                             ssum += cs;
                         }
                     } else {
+                        // pass 2, read in the 16-lane shape: a thread holds heads g, g + 8, g + 16, g + 24
+                        // (g = lane / 4) of columns 8 p + 2 u + e (u = lane % 4, p = 0..3, e = 0..1); it adds its
+                        // four heads in registers, and the eight threads of a column set reduce-scatter over g,
+                        // leaving thread (g, u) with the 32-head sum of column 8 (g / 2) + 2 u + g % 2
+                        const int u4 = lane & 3, g8 = lane >> 2;
 #pragma unroll 1
                         for (int c = 0; c < 2; c++) {
                             if (mw[c] == 0u) continue;
-                            float x[32];
-                            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + col_of(c)), x);
-                            if (mw[c] == 0xffffffffu) {
+                            const uint32_t ca = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(tb * NK + col_of(c));
+                            uint32_t ra[16], rb[16];
+                            tmem_ld16x256_x4(ca, ra);              // heads g, g + 8
+                            tmem_ld16x256_x4(ca + (16u << 16), rb);  // heads g + 16, g + 24
+                            const bool full = mw[c] == 0xffffffffu;
+                            float s8[8];
 #pragma unroll
-                                for (int q2 = 0; q2 < 16; q2++) {
-                                    const float2 arg = fma2(make_float2(x[2 * q2], x[2 * q2 + 1]), make_float2(s2, s2),
-                                                            make_float2(-ell, -ell));
-                                    x[2 * q2] = ex2(arg.x);
-                                    x[2 * q2 + 1] = ex2(arg.y);
+                            for (int p4 = 0; p4 < 4; p4++) {
+                                const int col = 8 * p4 + 2 * u4;
+                                const bool b0 = full || ((mw[c] >> col) & 1u), b1 = full || ((mw[c] >> (col + 1)) & 1u);
+                                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                                for (int k4 = 0; k4 < 4; k4++) {
+                                    const uint32_t *r = k4 < 2 ? ra : rb;
+                                    const int o = 4 * p4 + 2 * (k4 & 1);
+                                    const float2 arg = fma2(make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])),
+                                                            make_float2(s2, s2), make_float2(-ell4[k4], -ell4[k4]));
+                                    const float e0 = ex2(arg.x), e1 = ex2(arg.y);  // then the mask: no branch
+                                    acc = add2(acc, make_float2(b0 ? e0 : 0.f, b1 ? e1 : 0.f));
                                 }
-                            } else {
-#pragma unroll
-                                for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? ex2(fmaf(x[q], s2, -ell)) : 0.f;
+                                s8[2 * p4] = acc.x;
+                                s8[2 * p4 + 1] = acc.y;
                             }
-                            // sum over the 32 heads of this warp: reduce-scatter, lane l ends with column c0 + l
 #pragma unroll
-                            for (int off = 16; off >= 1; off >>= 1) {
+                            for (int hv = 4; hv >= 1; hv >>= 1) {
+                                const int off = hv * 4;  // the lane bit of g's bit log2(hv)
                                 const bool up = (lane & off) != 0;
-                                if (off >= 2) {  // the adds in pairs
 #pragma unroll
-                                    for (int q = 0; q < off; q += 2) {
-                                        const float s0 = up ? x[q] : x[q + off], s1 = up ? x[q + 1] : x[q + 1 + off];
-                                        const float k0 = up ? x[q + off] : x[q], k1 = up ? x[q + 1 + off] : x[q + 1];
-                                        const float2 r = add2(make_float2(k0, k1),
-                                                              make_float2(__shfl_xor_sync(0xffffffffu, s0, off),
-                                                                          __shfl_xor_sync(0xffffffffu, s1, off)));
-                                        x[q] = r.x;
-                                        x[q + 1] = r.y;
-                                    }
-                                } else {
-                                    const float send = up ? x[0] : x[1];
-                                    const float keep = up ? x[1] : x[0];
-                                    x[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+                                for (int q = 0; q < hv; q++) {
+                                    const float send = up ? s8[q] : s8[q + hv];
+                                    const float keep = up ? s8[q + hv] : s8[q];
+                                    s8[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                                 }
                             }
-                            const int j = t * NK + col_of(c) + lane;
-                            if (j < NCMAX && x[0] != 0.f) atomicAdd(sTb + i_row * NCMAX + j, x[0]);
+                            const int j = t * NK + col_of(c) + 8 * (g8 >> 1) + 2 * u4 + (g8 & 1);
+                            if (j < NCMAX && s8[0] != 0.f) atomicAdd(sTb + i_row * NCMAX + j, s8[0]);
                         }
                     }
                 }
