@@ -350,15 +350,14 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
-            int hs = 0, ai = 0;
+            // An item's q_idx rows are requested as soon as their buffer is free: that buffer is probed before every
+            // k-half load of the previous item, and waited for at the latest when the item starts.
+            int hs = 0, ai = 0, qi = 0;
             int last_hs[A_STAGES];
             for (int x = 0; x < A_STAGES; x++) last_hs[x] = -1;
             int last_ai[2] = {-1, -1};
-            for (int i = blockIdx.x; i < total; i += gridDim.x) {
-                const Item it = decode_item(a, i, total);
-                if (it.vmax == 0) continue;
-                const int bb = ai & 1;
-                wait_bar(b_empty + bb, ((ai >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 1);
+            auto load_q = [&](const Item &it) {
+                const int bb = qi & 1;
                 mbar_expect_tx(b_full + bb, B_BUF);
                 for (int k = 0; k < ROWS; k++) {
                     const long long row = k < it.n ? it.row[k] : it.row[0];
@@ -366,21 +365,48 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                         tma_load_3d(sB + bb * B_BUF + kh * B_HALF + k * (HI * 128), &map_q, b_full + bb, kh * 64, 0,
                                     (int)row);
                 }
-                last_ai[bb] = ai;
-                ai++;
-                const int nt = (it.vmax + NKEY - 1) / NKEY;
+                last_ai[bb] = qi;
+                qi++;
+            };
+            // the next item with visible keys after item index i (or total)
+            auto next_item = [&](int i, Item &nx) -> int {
+                for (int j = i + gridDim.x; j < total; j += gridDim.x) {
+                    nx = decode_item(a, j, total);
+                    if (nx.vmax > 0) return j;
+                }
+                return total;
+            };
+            Item cur;
+            int i = blockIdx.x;
+            if (i < total) {
+                cur = decode_item(a, i, total);
+                if (cur.vmax == 0) i = next_item(i, cur);
+            }
+            while (i < total) {
+                Item nxt;
+                const int inext = next_item(i, nxt);
+                if (qi == ai) {
+                    wait_bar(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 1);
+                    load_q(cur);
+                }
+                const int nt = (cur.vmax + NKEY - 1) / NKEY;
                 for (int t = 0; t < nt; t++)
                     for (int kh = 0; kh < 2; kh++) {
+                        if (qi == ai + 1 && inext < total && mbar_test(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1))
+                            load_q(nxt);
                         const int st = hs % A_STAGES;
                         wait_bar(a_empty + st, ((hs / A_STAGES) & 1) ^ 1, abort_flag, &g_tc_error, 2);
                         mbar_expect_tx(a_full + st, A_HALF);
                         if (sbhd)
-                            tma_load_3d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, it.b, t * NKEY);
+                            tma_load_3d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, cur.b, t * NKEY);
                         else
-                            tma_load_2d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, (int)(it.key_y + t * NKEY));
+                            tma_load_2d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, (int)(cur.key_y + t * NKEY));
                         last_hs[st] = hs;
                         hs++;
                     }
+                ai++;
+                i = inext;
+                cur = nxt;
             }
             // our own copies must land before the CTA exits
             for (int st = 0; st < A_STAGES; st++)
