@@ -276,6 +276,8 @@ __global__ void __launch_bounds__(R_THREADS, 1)
 dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                 const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_w, Args a)
 {
+    // the key-owner kernel reads nothing this one writes: let it take each SM this kernel leaves
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem + R_OFF_A;
@@ -1020,8 +1022,21 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (upper_units > 0) {
+        // launched as a programmatic dependent of the row-owner kernel (which it does not depend on), so its
+        // CTAs start on the SMs the row-owner's last items leave idle
         const int g2 = upper_units < sms ? upper_units : sms;
-        dk_tc_kernel<<<g2, THREADS, K_SMEM, st>>>(mq, mk, mg, mw, a);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(g2);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = K_SMEM;
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, dk_tc_kernel, mq, mk, mg, mw, a);
+        if (e != cudaSuccess) return e;
         note_launches(1);
     }
     return cudaGetLastError();
