@@ -138,6 +138,71 @@ __device__ __forceinline__ float warp_max(float x)
     return x;
 }
 
+// ------------------------------------------------------------------ KL of one row, held by one warp
+// ([BUG] sec. 2 excerpt: p = softmax of the indexer scores over the support C, L = sum t (log(t + eps) -
+// log(p + eps)); g_s = f p_s (A - t_s / (p_s + eps)) with A = sum_k t_k p_k / (p_k + eps), the exact derivative
+// of that eps-guarded KL.)  Slot s = lane + 32 i holds the score x[i], the teacher value t[i] and the key's
+// offset jj[i] within the row's visible range (-1 off the support).  Writes g by slot (grow, may be null) and
+// by key (drow over [0, v), zeroed first; may be null) and returns L (0 for an empty support).
+constexpr int kKlPer = 16;          // slots per lane: K <= 512
+constexpr float kKlEps = 1e-10f;    // [BUG] sec. 2 excerpt: log(x + 1e-10)
+__device__ __forceinline__ float kl_row_warp(const Geo &g, int lane, int K, int v, const int (&jj)[kKlPer],
+                                             float (&x)[kKlPer], const float (&t)[kKlPer], float *grow, float *drow)
+{
+    if (drow != nullptr) {  // zero the visible range (16-byte stores: the row stride is a multiple of 4)
+        for (int j4 = lane; 4 * j4 < v; j4 += 32) reinterpret_cast<float4 *>(drow)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kKlPer; i++)
+        if (jj[i] >= 0) m = fmaxf(m, x[i]);
+    m = warp_max(m);
+    if (m == -INFINITY) {  // empty support: no loss, no gradient
+        if (grow != nullptr) {
+#pragma unroll
+            for (int i = 0; i < kKlPer; i++)
+                if (lane + 32 * i < K) grow[lane + 32 * i] = 0.f;
+        }
+        return 0.f;
+    }
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < kKlPer; i++) {
+        x[i] = jj[i] >= 0 ? __expf(x[i] - m) : 0.f;
+        z += x[i];
+    }
+    z = warp_sum(z);
+    const float inv_z = 1.f / z;
+    float A = 0.f, L = 0.f;
+#pragma unroll
+    for (int i = 0; i < kKlPer; i++) {
+        if (jj[i] < 0) continue;
+        const float p = x[i] * inv_z;
+        A += t[i] * p / (p + kKlEps);
+        L += t[i] * (logf(t[i] + kKlEps) - logf(p + kKlEps));
+    }
+    A = warp_sum(A);
+    L = warp_sum(L);
+#pragma unroll
+    for (int i = 0; i < kKlPer; i++) {
+        const int s = lane + 32 * i;
+        if (s >= K) continue;
+        const float p = x[i] * inv_z;
+        const float gv = jj[i] >= 0 ? g.factor * p * (A - t[i] / (p + kKlEps)) : 0.f;
+        if (grow != nullptr) grow[s] = gv;
+        if (drow != nullptr && jj[i] >= 0) drow[jj[i]] = gv;
+    }
+    return L;
+}
+
+// Row of the by-key gradient rows gd: position-major within each sequence (b S + s for SBHD, the row itself
+// otherwise), so the two rows of a position pair are adjacent.
+__device__ __forceinline__ long long gd_row_of(const Geo &g, int b, int s, long long r)
+{
+    return g.layout == CSA_SBHD ? (long long)b * g.S + s : r;
+}
+
 // Count of kernel launches made by the library in this process (diagnostics; see csa_kernel_launches).
 void note_launches(int n);
 

@@ -375,10 +375,6 @@ cudaError_t launch_teacher_generic(const Geo &g, const T *q, const T *kv, const 
 // With gd != nullptr it also writes g by key: gd[prow][j] for the row's visible keys j < v (0 off the support),
 // row stride ncp; what lies beyond v is left as it is.  Rows are ordered by position within each sequence
 // (prow = b S + s for SBHD, the row itself otherwise), so the two rows of a position pair are adjacent.
-__device__ __forceinline__ long long gd_row(const Geo &g, const Row &R, long long r)
-{
-    return g.layout == CSA_SBHD ? (long long)R.b * g.S + R.s : r;
-}
 
 __global__ void __launch_bounds__(kThreads)
 kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ selscore,
@@ -393,7 +389,7 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
         const int32_t *row_ids = ids + r * g.K;
         const float *trow = teacher + r * TW;
         float *grow = gbuf != nullptr ? gbuf + r * TW : nullptr;
-        float *drow = gd != nullptr ? gd + gd_row(g, R, r) * ncp : nullptr;
+        float *drow = gd != nullptr ? gd + gd_row_of(g, R.b, R.s, r) * ncp : nullptr;
         if (drow != nullptr) {
             for (int j = tid; j < R.v; j += kThreads) drow[j] = 0.f;
             __syncthreads();
@@ -449,10 +445,9 @@ kl_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ sels
 
 // The same step for the sparse support with K <= 512 slots (teacher width K): one warp per row, the row's
 // ids, scores and teacher values held in registers (slot s = lane + 32 i, coalesced), warp reductions.
-// g by key (gd, as in kl_kernel): the row's visible range is zeroed, then every support slot writes its key.
-// A lane keeps, per slot, the score, the teacher value and the key offset within the row's visible range
-// (-1 off the support).  gbuf may be null (the tensor-core backward reads gd only).
-constexpr int kKlPer = 16;  // slots per lane
+// The same step for the sparse support with K <= 512 slots (teacher width K): one warp per row, the row's
+// scores, teacher values and key offsets held in registers (slot s = lane + 32 i, coalesced); the row's
+// arithmetic is kl_row_warp.  gbuf may be null (the tensor-core backward reads gd only).
 __global__ void __launch_bounds__(kThreads)
 kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ selscore,
                const float *__restrict__ teacher, float *__restrict__ gbuf, float *__restrict__ row_loss,
@@ -467,7 +462,6 @@ kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__
         const int32_t *row_ids = ids + r * K;
         const float *srow = selscore + r * K;
         const float *trow = teacher + r * K;
-        float *grow = gbuf != nullptr ? gbuf + r * K : nullptr;
         int jj[kKlPer];
         float x[kKlPer], t[kKlPer];
 #pragma unroll
@@ -483,52 +477,9 @@ kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__
             const long long j = jj[i] >= 0 ? (long long)jj[i] - lo : -1;
             jj[i] = (j >= 0 && j < R.v) ? (int)j : -1;
         }
-        float *drow = gd != nullptr ? gd + gd_row(g, R, r) * ncp : nullptr;
-        if (drow != nullptr) {  // zero the visible range (16-byte stores: ncp is a multiple of 4)
-            for (int j4 = lane; 4 * j4 < R.v; j4 += 32) reinterpret_cast<float4 *>(drow)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
-            __syncwarp();
-        }
-        float m = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kKlPer; i++)
-            if (jj[i] >= 0) m = fmaxf(m, x[i]);
-        m = warp_max(m);
-        if (m == -INFINITY) {  // empty support: no loss, no gradient
-            if (grow != nullptr) {
-#pragma unroll
-                for (int i = 0; i < kKlPer; i++)
-                    if (lane + 32 * i < K) grow[lane + 32 * i] = 0.f;
-            }
-            if (lane == 0) row_loss[r] = 0.f;
-            continue;
-        }
-        float z = 0.f;
-#pragma unroll
-        for (int i = 0; i < kKlPer; i++) {
-            x[i] = jj[i] >= 0 ? __expf(x[i] - m) : 0.f;
-            z += x[i];
-        }
-        z = warp_sum(z);
-        const float inv_z = 1.f / z;
-        float A = 0.f, L = 0.f;
-#pragma unroll
-        for (int i = 0; i < kKlPer; i++) {
-            if (jj[i] < 0) continue;
-            const float p = x[i] * inv_z;
-            A += t[i] * p / (p + kEps);
-            L += t[i] * (logf(t[i] + kEps) - logf(p + kEps));
-        }
-        A = warp_sum(A);
-        L = warp_sum(L);
-#pragma unroll
-        for (int i = 0; i < kKlPer; i++) {
-            const int s = lane + 32 * i;
-            if (s >= K) continue;
-            const float p = x[i] * inv_z;
-            const float gv = jj[i] >= 0 ? g.factor * p * (A - t[i] / (p + kEps)) : 0.f;
-            if (grow != nullptr) grow[s] = gv;
-            if (drow != nullptr && jj[i] >= 0) drow[jj[i]] = gv;
-        }
+        float *grow = gbuf != nullptr ? gbuf + r * K : nullptr;
+        float *drow = gd != nullptr ? gd + gd_row_of(g, R.b, R.s, r) * ncp : nullptr;
+        const float L = kl_row_warp(g, lane, K, R.v, jj, x, t, grow, drow);
         if (lane == 0) row_loss[r] = L;
     }
 }

@@ -205,6 +205,32 @@ def test_thd_single_segment_equals_bshd():
     assert abs(a["loss"] - b["loss"]) <= 1e-5 * abs(a["loss"])
 
 
+@pytest.mark.parametrize("layout", ["bshd", "sbhd", "thd"])
+def test_backward_with_and_without_given_teacher(layout):
+    """The backward that computes the teacher itself and the one given csa_teacher's rows run the same kernels
+    on the same values: the loss, the per-row KL, dQ_idx and dW agree bit for bit; dK_idx sums key-tile
+    partials with fp32 atomics in whatever order the CTAs finish, so it agrees to rounding."""
+    kw = dict(layout=layout, seqlen=999, heads=64, head_dim=64, idx_heads=64, idx_dim=128, topk=96, window=40,
+              seed=15)
+    if layout == "thd":
+        kw.update(seqlen=2600, doc_len=(300, 1200))
+    d = workload.to_device(synth.generate(small(**kw)))
+    p = d.params
+    ids, sel = B.csa_indexer_fwd(p, *d.indexer)
+    outs = []
+    for teacher in (None, B.csa_teacher(p, *d.teacher_side, ids)):
+        rl = torch.empty(p.rows, dtype=torch.float32, device=ids.device)
+        loss, dq, dw, dk = B.csa_indexer_bwd(p, *d.indexer, *d.teacher_side, ids, sel, teacher=teacher, row_loss=rl)
+        torch.cuda.synchronize()
+        B.csa_check_device_status()
+        assert B.csa_last_path() == "tcgen05"
+        outs.append((loss, rl, dq, dw, dk))
+    for a, b in zip(outs[0][:4], outs[1][:4]):
+        assert torch.equal(a, b)
+    dk0, dk1 = outs[0][4].double(), outs[1][4].double()
+    assert float((dk0 - dk1).norm() / dk1.norm()) <= 1e-3
+
+
 def test_batch_split_dk():
     """BSHD b=2 against two b=1 calls scaled for the row mean: the [PR] test plan's dK check (<= 8e-6 there)."""
     cfg = small(batch=2, seqlen=512, idx_heads=64, idx_dim=128, topk=64, seed=13, dtype="f32")
