@@ -188,7 +188,7 @@ csa_status csa_indexer_bwd(const csa_params *p, const void *q_idx, const float *
  *   - Scratch: a fixed device array of CSA_NOALLOC_SCRATCH_BYTES inside the library.  Every GPU on which the
  *     library's device code is loaded holds it until the process exits.  Nothing is allocated or freed.
  *   - Limit: returns CSA_ERR_WORKSPACE, without enqueueing anything, when csa_workspace_size(p) exceeds
- *     CSA_NOALLOC_SCRATCH_BYTES (the bshd_bf16 workload needs about 34 MiB).
+ *     CSA_NOALLOC_SCRATCH_BYTES (the bshd_bf16 workload needs about 49 MiB).
  *   - Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
  *     device current; make that first call before any stream capture.
  *   - Sharing: every call on a device uses the same array, which keeps whatever the last call left there; the

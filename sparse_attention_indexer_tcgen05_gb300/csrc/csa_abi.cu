@@ -111,8 +111,11 @@ csa_status make_plan(const csa_params *p, Plan *P)
     off = align_up(off + sizeof(int) * (size_t)(p->layout == CSA_THD ? p->batch + 1 : 1));
     P->off_teacher = off;
     off = align_up(off + sizeof(float) * (size_t)rows * g.TW);
+    // g by slot for the CUDA-core backward, or g by key (inside the tensor-core backward's region) for the
+    // tensor-core one: only one of the two is sized
+    const bool tc_bwd = tc_bwd_supported(g, p->dtype == CSA_BF16);
     P->off_g = off;
-    off = align_up(off + sizeof(float) * (size_t)rows * g.TW);
+    off = align_up(off + (tc_bwd ? 0 : sizeof(float) * (size_t)rows * g.TW));
     P->off_rowloss = off;
     off = align_up(off + sizeof(float) * (size_t)(rows > 0 ? rows : 1));
     P->off_dk = off;
@@ -122,7 +125,7 @@ csa_status make_plan(const csa_params *p, Plan *P)
     P->off_tc = off;
     off = align_up(off + tc_workspace_bytes(g));
     P->off_btc = off;
-    off = align_up(off + tc_bwd_workspace_bytes(g));
+    off = align_up(off + (tc_bwd ? tc_bwd_workspace_bytes(g) : 0));
     P->off_ttc = off;
     off = align_up(off + tc_teacher_workspace_bytes(g));
     P->total = off;
