@@ -54,6 +54,16 @@ def test_sizes(B):
     assert _params(B, layout="sbhd").compressed_rows == 2048
 
 
+def test_bench_workload_fits_the_no_allocation_scratch(B):
+    """The bshd_bf16 workload (the default bench case) runs through csa_indexer_bwd_noalloc: its workspace
+    (teacher rows, the by-key gradient rows of the tensor-core backward, dK accumulator, per-row loss) stays
+    inside the library's fixed scratch of CSA_NOALLOC_SCRATCH_BYTES."""
+    m = re.search(r"#define CSA_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", open(HEADER).read())
+    scratch = int(m.group(1)) << int(m.group(2))
+    p = _params(B)
+    assert 8192 * 512 * 4 + 8192 * 1024 * 4 <= p.workspace_bytes <= scratch
+
+
 @pytest.mark.parametrize("field,value", [("compress_ratio", 0), ("topk", 0), ("window", -1), ("heads", 0),
                                          ("batch", 0), ("seqlen", -5), ("reduction", 2), ("sparse_loss", 3),
                                          ("layout", 7), ("dtype", 9), ("key_rows", 5), ("teacher_mode", 2)])
