@@ -304,6 +304,82 @@ void orc_teacher(const orc_params *P, const double *q, const double *kv, const d
     }
 }
 
+/* The non-compressed log-sum-exp of the listed rows: for each head,
+ *   u_h = log( exp(a_h) + sum_{r in W} exp(w_hr) ),   w_hr = sigma q[t,h].kv[r]
+ * the sink and window part of the denominator, which [BUG]'s proposal suggests taking from the attention
+ * forward (non_compressed_lse) instead of recomputing it.  -inf when there is neither sink nor window.
+ * out is [nrows][heads]. */
+void orc_noncompressed_lse(const orc_params *P, const double *q, const double *kv, const double *sink,
+                           const int32_t *rows, int nrows, int compact, double *out)
+{
+    const int H = P->heads, D = P->head_dim;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < nrows; i++) {
+        const long r = rows[i];
+        orc_row R = orc_decode(P, r);
+        int p0 = R.s - P->window + 1;
+        if (p0 < 0) p0 = 0;
+        const int nW = (P->window > 0 && !R.pad) ? R.s - p0 + 1 : 0;
+        double *wl = malloc(sizeof(double) * (size_t)(nW > 0 ? nW : 1));
+        for (int h = 0; h < H; h++) {
+            const double *qh = q + (ORC_SRC(i, r) * H + h) * D;
+            double m = sink[h];
+            for (int k = 0; k < nW; k++) {
+                wl[k] = P->scale * orc_dot(qh, kv + orc_qrow(P, &R, p0 + k) * D, D);
+                if (wl[k] > m) m = wl[k];
+            }
+            if (m == -INFINITY) { out[(long)i * H + h] = -INFINITY; continue; }
+            double Z = exp(sink[h] - m);
+            for (int k = 0; k < nW; k++) Z += exp(wl[k] - m);
+            out[(long)i * H + h] = m + log(Z);
+        }
+        free(wl);
+    }
+}
+
+/* The teacher from a given non-compressed log-sum-exp u[nrows][heads] (orc_noncompressed_lse, or the
+ * attention forward's): Z_h = exp(u_h) + sum_{j in C} exp(c_hj), the rest as orc_teacher.  Equal to the
+ * full-CSA teacher when u is the sink-and-window log-sum-exp of the same inputs. */
+void orc_teacher_lse(const orc_params *P, const double *q, const double *kv_c, const double *lse,
+                     const int32_t *ids, const int32_t *rows, int nrows, int compact, double *out)
+{
+    const int H = P->heads, D = P->head_dim, K = orc_topk_width(P), NC = orc_key_width(P);
+    const int TW = orc_teacher_width(P);
+    const int cap = K > NC ? K : NC;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < nrows; i++) {
+        const long r = rows[i];
+        double *t = out + (long)i * TW;
+        for (int k = 0; k < TW; k++) t[k] = 0.0;
+        orc_row R = orc_decode(P, r);
+        if (R.v == 0) continue;
+        int *slot = malloc(sizeof(int) * (size_t)cap);
+        long *gid = malloc(sizeof(long) * (size_t)cap);
+        int nC = orc_support(P, &R, ids + (long)i * K, slot, gid);
+        if (nC == 0) { free(slot); free(gid); continue; }
+        double *c = malloc(sizeof(double) * (size_t)nC);
+        double *T = calloc((size_t)nC, sizeof(double));
+        for (int h = 0; h < H; h++) {
+            const double *qh = q + (ORC_SRC(i, r) * H + h) * D;
+            const double u = lse[(long)i * H + h];
+            double m = u;
+            for (int k = 0; k < nC; k++) {
+                c[k] = P->scale * orc_dot(qh, kv_c + orc_crow(P, gid[k]) * D, D);
+                if (c[k] > m) m = c[k];
+            }
+            if (m == -INFINITY) m = 0.0;
+            double Z = exp(u - m);
+            for (int k = 0; k < nC; k++) Z += exp(c[k] - m);
+            for (int k = 0; k < nC; k++) T[k] += exp(c[k] - m) / Z;
+        }
+        double S = 0.0;
+        for (int k = 0; k < nC; k++) S += T[k];
+        if (S < ORC_EPS) S = ORC_EPS;
+        for (int k = 0; k < nC; k++) t[slot[k]] = T[k] / S;
+        free(c); free(T); free(slot); free(gid);
+    }
+}
+
 /* ---------------------------------------------------------------- step 4: KL */
 
 /* KL(t || p) of one row with p = softmax(I) over the n support entries:

@@ -60,6 +60,8 @@ def _load():
             lib.orc_scores.argtypes = [P, vp, vp, vp, vp, i32, i32, vp]
             lib.orc_topk.argtypes = [P, vp, vp, i32, vp]
             lib.orc_teacher.argtypes = [P, vp, vp, vp, vp, vp, vp, i32, i32, vp]
+            lib.orc_noncompressed_lse.argtypes = [P, vp, vp, vp, vp, i32, i32, vp]
+            lib.orc_teacher_lse.argtypes = [P, vp, vp, vp, vp, vp, i32, i32, vp]
             lib.orc_kl_row.argtypes = [vp, vp, i32, vp, vp]
             lib.orc_kl_row.restype = dbl
             lib.orc_loss_factor.argtypes = [P]
@@ -169,6 +171,26 @@ class Problem:
         out = np.empty((len(rows), self.teacher_width), np.float64)
         self.lib.orc_teacher(ctypes.byref(self.p), _ptr(qq), _ptr(kvv), _ptr(kc), _ptr(sk), _ptr(ids), _ptr(rows),
                              len(rows), int(compact), _ptr(out))
+        return out
+
+    def noncompressed_lse(self, q, kv, sink, rows=None, compact=False) -> np.ndarray:
+        """u [len(rows), heads]: log(exp(a_h) + sum over the window of exp(sigma q.kv)) per row and head."""
+        rows = self._rows(rows)
+        qq, kvv, sk = _f64(q), _f64(kv), _f64(sink)
+        out = np.empty((len(rows), self.p.heads), np.float64)
+        self.lib.orc_noncompressed_lse(ctypes.byref(self.p), _ptr(qq), _ptr(kvv), _ptr(sk), _ptr(rows), len(rows),
+                                       int(compact), _ptr(out))
+        return out
+
+    def teacher_from_lse(self, q, kv_c, lse, ids, rows=None, compact=False) -> np.ndarray:
+        """The teacher [len(rows), teacher_width] from a given non-compressed log-sum-exp lse [len(rows), heads]."""
+        rows = self._rows(rows)
+        qq, kc, ls = _f64(q), _f64(kv_c), _f64(lse)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        assert ids.shape == (len(rows), self.K) and ls.shape == (len(rows), self.p.heads)
+        out = np.empty((len(rows), self.teacher_width), np.float64)
+        self.lib.orc_teacher_lse(ctypes.byref(self.p), _ptr(qq), _ptr(kc), _ptr(ls), _ptr(ids), _ptr(rows),
+                                 len(rows), int(compact), _ptr(out))
         return out
 
     def loss_grads(self, q_idx, w, k_idx, ids, teacher, rows=None, want_dk=True, compact=False):

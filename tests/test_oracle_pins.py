@@ -258,6 +258,39 @@ def test_teacher_factored_lse_form_equals_direct_form():
         np.testing.assert_allclose(t[r, :len(sel)], T / max(T.sum(), 1e-10), rtol=1e-13)
 
 
+def test_noncompressed_lse_is_sink_and_window_logsumexp():
+    """u_h = log(exp(a_h) + sum over the window of exp(sigma q.kv)), by scipy's logsumexp over the logits taken
+    with a library matmul; with no window it is the sink itself, with neither it is -inf."""
+    inp, P, ids = _teacher_case(heads=4, seqlen=64, window=7)
+    u = P.noncompressed_lse(inp.q.values, inp.kv.values, inp.sink.values)
+    assert u.shape == (P.rows, 4)
+    for r in (0, 5, 33, 63, 64 + 2, 64 + 63):
+        b, s = divmod(r, 64)
+        win = inp.kv.values[b, max(0, s - 6):s + 1].astype(np.float64)
+        wl = P.p.scale * inp.q.values[b, s].astype(np.float64) @ win.T
+        ref = logsumexp(np.concatenate([inp.sink.values[:, None].astype(np.float64), wl], axis=1), axis=1)
+        np.testing.assert_allclose(u[r], ref, rtol=1e-13)
+    inp0, P0, _ = _teacher_case(heads=4, seqlen=64, window=0)
+    u0 = P0.noncompressed_lse(inp0.q.values, inp0.kv.values, inp0.sink.values)
+    assert np.array_equal(u0, np.broadcast_to(inp0.sink.values.astype(np.float64), u0.shape))
+    assert np.all(P0.noncompressed_lse(inp0.q.values, inp0.kv.values, np.full(4, -np.inf)) == -np.inf)
+
+
+@pytest.mark.parametrize("layout", ["bshd", "sbhd", "thd"])
+def test_teacher_from_noncompressed_lse_equals_full_teacher(layout):
+    """The teacher from a given u_h (the non-compressed log-sum-exp the proposal would take from the attention
+    forward) equals the full-CSA teacher when u_h is the sink-and-window log-sum-exp of the same inputs, and
+    the compressed-only teacher when u_h = -inf."""
+    inp, P, ids = _teacher_case(layout=layout, heads=4, seqlen=64, window=9)
+    q, kv, kv_c, sink = inp.q.values, inp.kv.values, inp.kv_c.values, inp.sink.values
+    t = P.teacher(q, kv, kv_c, sink, ids)
+    u = P.noncompressed_lse(q, kv, sink)
+    np.testing.assert_allclose(P.teacher_from_lse(q, kv_c, u, ids), t, rtol=1e-12, atol=1e-15)
+    P0 = problem(inp, window=0)
+    t0 = P0.teacher(q, kv, kv_c, np.full(4, -np.inf), ids)
+    np.testing.assert_allclose(P.teacher_from_lse(q, kv_c, np.full_like(u, -np.inf), ids), t0, rtol=1e-12, atol=1e-15)
+
+
 def test_teacher_perturbations():
     """I5: with H > 1, changing only the window values or one head's sink changes the teacher, and leaves
     the selection and the predictor unchanged."""
