@@ -87,6 +87,7 @@ def algorithmic(cfg, inp, K: int, nrows: int):
     fl = {
         "score_topk": float(np.sum(2.0 * HI * DI * v)),
         "teacher": float(np.sum(2.0 * H * D * (k + wn))),
+        "teacher_from_lse": float(np.sum(2.0 * H * D * k)),
         "kl_grad": float(np.sum(6.0 * HI * DI * k)),
     }
     by = {
@@ -94,6 +95,8 @@ def algorithmic(cfg, inp, K: int, nrows: int):
         "score_topk": n * (HI * DI * eb + HI * 4 + 2 * K * 4) + nk * DI * eb,
         # q read, kv window rows and kv_c read once, ids read, teacher kept on chip (bwd) / written (teacher call)
         "teacher": n * (H * D * eb + D * eb + K * 4) + nk * D * eb,
+        # q and the given log-sum-exp read, ids read, kv_c read once, teacher written
+        "teacher_from_lse": n * (H * D * eb + H * 4 + 2 * K * 4) + nk * D * eb,
         # q_idx, w, ids, selscore read; dq, dw written; k_idx read, dk written
         "kl_grad": n * (2 * HI * DI * eb + 2 * HI * 4 + 2 * K * 4) + 2 * nk * DI * eb,
     }
@@ -310,6 +313,11 @@ def run_ours(args, cfg):
     stage_ms["teacher"] = timed(lambda: B.csa_teacher(p, *d.teacher_side, ids, workspace=ws, out=teacher_buf), reps)
     stage_ms["kl_grad"] = timed(lambda: B.csa_indexer_bwd(p, *d.indexer, *d.teacher_side, ids, sel,
                                                          teacher=teacher_buf, workspace=ws, out=outs), reps)
+    # the teacher from a given non-compressed log-sum-exp (no window logits); its input is synthetic
+    lse_nc = torch.randn((p.rows, cfg.heads), generator=torch.Generator(device=dev).manual_seed(cfg.seed),
+                         device=dev, dtype=torch.float32) + float(np.log(cfg.window + 1))
+    stage_ms["teacher_from_lse"] = timed(lambda: B.csa_teacher_from_lse(p, d.q, d.kv_c, lse_nc, ids, workspace=ws,
+                                                                      out=teacher_buf), reps)
     # the roofline is reported for the dominant kernel: of the stages that launch one kernel each
     # (score + top-k, teacher), the slower one; the teacher kernel has the largest share of the launch
     # list (profiles/launch_list_bshd_bf16.md)

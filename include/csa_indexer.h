@@ -157,6 +157,20 @@ csa_status csa_teacher(const csa_params *p, const void *q, const void *kv, const
                        const float *sink, const int32_t *ids, float *teacher_out,
                        void *workspace, size_t workspace_bytes, void *stream);
 
+/* Step 3 from a given non-compressed log-sum-exp ([BUG] follow-up proposal: take u_h, the log-sum-exp of the
+ * sink and the window logits, from the attention forward (non_compressed_lse) instead of recomputing the
+ * window):
+ *   u_h  = lse_nc[t,h] = log(exp(a_h) + sum_W exp(w_hr))          (given; natural log; -inf for neither)
+ *   l_h  = log(exp(u_h) + sum_C exp(c_hj)),  t_j as in csa_teacher
+ *   q [rows, H, D], kv_c [compressed rows, D], lse_nc [rows, H] fp32 (row order of the layout), ids [rows, K]
+ *   -> teacher_out [rows, teacher_width] fp32.
+ * No window logit is computed; p->window and p->teacher_mode are ignored (lse_nc carries the whole
+ * non-compressed part).  Same workspace as csa_teacher; same validation and errors (lse_nc: 16-byte aligned,
+ * non-null when rows > 0). */
+csa_status csa_teacher_from_lse(const csa_params *p, const void *q, const void *kv_c, const float *lse_nc,
+                                const int32_t *ids, float *teacher_out, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
 /* Steps 3-5: teacher (recomputed when teacher_or_null is NULL), KL and the indexer gradients.
  *   p_s   = softmax over C of the scores (selscore from csa_indexer_fwd; dense loss with K below the key
  *           width recomputes the visible scores into the workspace)
@@ -213,8 +227,8 @@ csa_status csa_scores_debug(const csa_params *p, const void *q_idx, const float 
  * gave up a bounded wait).  Returns CSA_ERR_TIMEOUT if it was set, CSA_ERR_CUDA on a CUDA error. */
 csa_status csa_check_device_status(void *stream);
 
-/* Name of the last kernel path csa_indexer_fwd / csa_indexer_bwd chose on this host thread
- * ("tcgen05", "generic", ...).  Static string. */
+/* Name of the last kernel path csa_indexer_fwd, csa_teacher, csa_teacher_from_lse or csa_indexer_bwd chose
+ * on this host thread ("tcgen05", "generic", ...; for csa_indexer_bwd, its backward's).  Static string. */
 const char *csa_last_path(void);
 
 /* Message of the last CUDA runtime error that ended a call of this library with CSA_ERR_CUDA on this host

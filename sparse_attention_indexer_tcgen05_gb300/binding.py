@@ -5,6 +5,7 @@ device memory (outputs and workspace) and the current stream.  The functions kee
 
     csa_indexer_fwd(params, q_idx, w, k_idx)                        -> (ids, selscore)
     csa_teacher(params, q, kv, kv_c, sink, ids)                     -> teacher
+    csa_teacher_from_lse(params, q, kv_c, lse_nc, ids)              -> teacher
     csa_indexer_bwd(params, q_idx, w, k_idx, q, kv, kv_c, sink, ids, selscore[, teacher])
                                                                     -> (loss, dq_idx, dw, dk_idx)
     csa_scores_debug(params, q_idx, w, k_idx, row_begin, row_count) -> scores
@@ -69,6 +70,7 @@ for _name, _args, _res in [
     ("csa_workspace_size", [_P], ctypes.c_size_t),
     ("csa_indexer_fwd", [_P, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     ("csa_teacher", [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
+    ("csa_teacher_from_lse", [_P, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], ctypes.c_int),
     ("csa_indexer_bwd", [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                          _vp],
      ctypes.c_int),
@@ -86,7 +88,8 @@ for _name, _args, _res in [
     _f.restype = _res
 
 EXPORTED = ("csa_topk_width", "csa_key_width", "csa_teacher_width", "csa_rows", "csa_compressed_rows",
-            "csa_workspace_size", "csa_indexer_fwd", "csa_teacher", "csa_indexer_bwd", "csa_scores_debug",
+            "csa_workspace_size", "csa_indexer_fwd", "csa_teacher", "csa_teacher_from_lse", "csa_indexer_bwd",
+            "csa_scores_debug",
             "csa_indexer_bwd_noalloc",
             "csa_check_device_status", "csa_last_path", "csa_last_cuda_error", "csa_kernel_launches",
             "csa_status_string")
@@ -246,6 +249,25 @@ def csa_teacher(p: Params, q, kv, kv_c, sink, ids, workspace=None, out=None):
         st = _lib.csa_teacher(p.ref, _ptr(q), _ptr(kv), _ptr(kv_c), _ptr(sink), _ptr(ids), _ptr(out), _ptr(ws), nws,
                               _stream(dev))
     _check(st, "csa_teacher")
+    return out
+
+
+def csa_teacher_from_lse(p: Params, q, kv_c, lse_nc, ids, workspace=None, out=None):
+    """Step 3 from a given non-compressed log-sum-exp lse_nc [rows, heads] fp32 (natural log of exp(sink) plus
+    the window's exponentials, per row and head).  Returns teacher [rows, teacher_width] fp32."""
+    dev = q.device
+    rows, H, D = p.rows, p.c.heads, p.c.head_dim
+    _check_tensor(q, "q", p.value_dtype, dev, rows * H * D)
+    _check_tensor(kv_c, "kv_c", p.value_dtype, dev, p.compressed_rows * D)
+    _check_tensor(lse_nc, "lse_nc", torch.float32, dev, rows * H)
+    _check_tensor(ids, "ids", torch.int32, dev, rows * p.K)
+    if out is None:
+        out = torch.empty((rows, p.teacher_width), dtype=torch.float32, device=dev)
+    ws, nws = _workspace(p, dev, workspace)
+    with _nvtx("csa_teacher_from_lse"):
+        st = _lib.csa_teacher_from_lse(p.ref, _ptr(q), _ptr(kv_c), _ptr(lse_nc), _ptr(ids), _ptr(out), _ptr(ws), nws,
+                                       _stream(dev))
+    _check(st, "csa_teacher_from_lse")
     return out
 
 

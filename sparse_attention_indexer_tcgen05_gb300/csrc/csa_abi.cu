@@ -214,11 +214,13 @@ csa_status run_teacher(Plan &P, const void *q, const void *kv, const void *kv_c,
                        const int32_t *ids, float *teacher, void *ws, cudaStream_t st)
 {
     if (tc_teacher_supported(P.g, sizeof(T) == 2)) {
+        t_last_path = "tcgen05";
         CSA_CUDA(launch_teacher_tc(P.g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kv,
                                    (const __nv_bfloat16 *)kv_c, sink, ids, teacher, ws_at(ws, P.off_ttc), st));
         return CSA_OK;
     }
     CSA_TRY(check_smem(teacher_generic_smem(P.g, sizeof(T) == 2)));
+    t_last_path = "generic";
     CSA_CUDA(launch_teacher_generic<T>(P.g, (const T *)q, (const T *)kv, (const T *)kv_c, sink, ids, teacher, st));
     return CSA_OK;
 }
@@ -371,6 +373,33 @@ csa_status csa_teacher(const csa_params *p, const void *q, const void *kv, const
     CSA_TRY(prologue(P, workspace, st));
     if (P.dtype == CSA_BF16) return run_teacher<__nv_bfloat16>(P, q, kv, kv_c, sink, ids, teacher_out, workspace, st);
     return run_teacher<float>(P, q, kv, kv_c, sink, ids, teacher_out, workspace, st);
+}
+
+csa_status csa_teacher_from_lse(const csa_params *p, const void *q, const void *kv_c, const float *lse_nc,
+                                const int32_t *ids, float *teacher_out, void *workspace, size_t workspace_bytes,
+                                void *stream)
+{
+    CSA_TRY(injected_fault());
+    Plan P;
+    CSA_TRY(make_plan(p, &P));
+    Geo &g = P.g;
+    CSA_TRY(need(q, (long long)g.rows * g.H * g.D));
+    CSA_TRY(need(kv_c, g.key_rows * g.D));
+    CSA_TRY(need(lse_nc, (long long)g.rows * g.H));
+    CSA_TRY(need(ids, (long long)g.rows * g.K));
+    CSA_TRY(need(teacher_out, (long long)g.rows * g.TW));
+    if (workspace_bytes < P.total || (P.total > 0 && workspace == nullptr)) return CSA_ERR_WORKSPACE;
+    if (g.rows == 0 || g.TW == 0) return CSA_OK;
+    // the given log-sum-exp carries the whole non-compressed part of each head's denominator
+    g.window = 0;
+    g.no_sink = 0;
+    g.lse_nc = lse_nc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CSA_TRY(prologue(P, workspace, st));
+    // kv is never read without a window: kv_c stands in for it
+    if (P.dtype == CSA_BF16)
+        return run_teacher<__nv_bfloat16>(P, q, kv_c, kv_c, nullptr, ids, teacher_out, workspace, st);
+    return run_teacher<float>(P, q, kv_c, kv_c, nullptr, ids, teacher_out, workspace, st);
 }
 
 csa_status csa_indexer_bwd(const csa_params *p, const void *q_idx, const float *w, const void *k_idx, const void *q,

@@ -30,6 +30,8 @@ struct Geo {
     float scale;       // sigma
     int sparse;
     int no_sink;       // compressed-only teacher: the sink term is dropped (and the window is 0)
+    const float *lse_nc; // teacher from a given non-compressed log-sum-exp [rows][H] (natural log): it replaces
+                         // the sink term, and the window is 0; null otherwise
     float factor;      // loss_coeff / rows (mean) or loss_coeff (sum)
     const int *cu_q;   // THD physical offsets
     const int *cu_real;// THD unpadded offsets (== cu_q when none given)

@@ -309,7 +309,7 @@ teacher_generic_kernel(Geo g, const T *__restrict__ q, const T *__restrict__ kv,
         for (int h = tid; h < H; h += kThreads) {
             float m = -INFINITY;
             for (int k = 0; k < kWarps; k++) m = fmaxf(m, st_m[k * H + h]);
-            const float a = g.no_sink ? -INFINITY : sink[h];
+            const float a = g.lse_nc != nullptr ? g.lse_nc[r * H + h] : (g.no_sink ? -INFINITY : sink[h]);
             const float M = fmaxf(m, a);
             float s = 0.f;
             if (M != -INFINITY) {

@@ -368,7 +368,10 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                     float2 p[4];
 #pragma unroll
                     for (int k = 0; k < 4; k++) p[k] = pp[k * M + rh];
-                    const float ah = g.no_sink ? -INFINITY : __ldg(a.sink + h) * 1.4426950408889634f;
+                    // the non-compressed term: the sink, or a given sink-and-window log-sum-exp of this row
+                    const float ah = g.lse_nc != nullptr
+                                         ? __ldg(g.lse_nc + (i_row == 0 ? it.row0 : it.row1) * H + h) * 1.4426950408889634f
+                                         : (g.no_sink ? -INFINITY : __ldg(a.sink + h) * 1.4426950408889634f);
                     const float mm = fmaxf(fmaxf(fmaxf(p[0].x, p[1].x), fmaxf(p[2].x, p[3].x)), ah);
                     float S = 0.f;
                     if (mm != -INFINITY) {
@@ -604,7 +607,20 @@ cudaError_t launch_teacher_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_b
         const cuuint32_t box[3] = {64, (cuuint32_t)g.H, 1};
         if (!tc_encode_bf16(&mq, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    if (g.layout == CSA_SBHD) {
+    if (g.window == 0) {  // no window tile is ever loaded: the kv map is never used
+        if (g.layout == CSA_SBHD) {
+            const cuuint64_t dkc[3] = {(cuuint64_t)g.D, (cuuint64_t)g.B, (cuuint64_t)g.nc};
+            const cuuint64_t skc[2] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.B * g.D * 2};
+            const cuuint32_t box[3] = {64, 1, (cuuint32_t)NK};
+            if (!tc_encode_bf16(&mkc, kv_c, 3, dkc, skc, box)) return cudaErrorInvalidValue;
+        } else {
+            const cuuint64_t dkc[2] = {(cuuint64_t)g.D, (cuuint64_t)g.key_rows};
+            const cuuint64_t s1[1] = {(cuuint64_t)g.D * 2};
+            const cuuint32_t box[2] = {64, (cuuint32_t)NK};
+            if (!tc_encode_bf16(&mkc, kv_c, 2, dkc, s1, box)) return cudaErrorInvalidValue;
+        }
+        mkv = mkc;
+    } else if (g.layout == CSA_SBHD) {
         const cuuint64_t dkv[3] = {(cuuint64_t)g.D, (cuuint64_t)g.B, (cuuint64_t)g.S};
         const cuuint64_t skv[2] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.B * g.D * 2};
         const cuuint64_t dkc[3] = {(cuuint64_t)g.D, (cuuint64_t)g.B, (cuuint64_t)g.nc};

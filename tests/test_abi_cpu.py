@@ -103,6 +103,10 @@ def test_pointer_validation_before_any_launch(B):
     args = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000, 0x9000, None]
     assert bwd(p.ref, *args, None, None, 0xa000, 0xb000, 0xc000, 0xd000, big, None) == 1  # no loss_out
     assert bwd(p.ref, *args, 0xe002, None, 0xa000, 0xb000, 0xc000, 0xd000, big, None) == 3  # misaligned loss
+    tl = B._lib.csa_teacher_from_lse
+    assert tl(p.ref, 0x1000, 0x2000, None, 0x4000, 0x5000, 0x6000, big, None) == 1     # no lse_nc
+    assert tl(p.ref, 0x1000, 0x2000, 0x3004, 0x4000, 0x5000, 0x6000, big, None) == 3   # misaligned lse_nc
+    assert tl(p.ref, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 16, None) == 4    # small workspace
 
 
 def test_no_gpu_is_a_cuda_error_not_a_crash(B):

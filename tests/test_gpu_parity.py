@@ -205,6 +205,38 @@ def test_thd_single_segment_equals_bshd():
     assert abs(a["loss"] - b["loss"]) <= 1e-5 * abs(a["loss"])
 
 
+@pytest.mark.parametrize("dtype,wide,layout", [("f32", False, "bshd"), ("bf16", True, "bshd"), ("bf16", True, "sbhd"),
+                                                ("bf16", True, "thd")])
+def test_teacher_from_noncompressed_lse(dtype, wide, layout):
+    """csa_teacher_from_lse with u_h = the oracle's sink-and-window log-sum-exp equals the oracle's full-CSA
+    teacher (and the GPU's own full teacher) for the GPU's ids, on the CUDA-core (f32) and tensor-core paths."""
+    kw = dict(layout=layout, dtype=dtype, seed=16)
+    if wide:
+        kw.update(seqlen=999, heads=64, head_dim=64, idx_heads=64, idx_dim=128, topk=96, window=40)
+    if layout == "thd":
+        kw.update(seqlen=2600, doc_len=(300, 1200))
+    inp = synth.generate(small(**kw))
+    d = workload.to_device(inp)
+    p = d.params
+    ids, _ = B.csa_indexer_fwd(p, *d.indexer)
+    P = O.Problem.from_inputs(inp)
+    ids_np = ids.cpu().numpy()
+    u = P.noncompressed_lse(inp.q.values, inp.kv.values, inp.sink.values)
+    lse = torch.from_numpy(np.ascontiguousarray(u, dtype=np.float32)).to(d.q.device)
+    got = B.csa_teacher_from_lse(p, d.q, d.kv_c, lse, ids)
+    torch.cuda.synchronize()
+    B.csa_check_device_status()
+    assert B.csa_last_path() == ("tcgen05" if wide else "generic")
+    got = got.cpu().numpy()
+    ref = P.teacher(inp.q.values, inp.kv.values, inp.kv_c.values, inp.sink.values, ids_np)
+    tol = U.value_tol(dtype)
+    err = U.row_l1(got, ref)
+    assert err <= tol, err
+    full = B.csa_teacher(p, *d.teacher_side, ids).cpu().numpy()
+    assert U.row_l1(got, full) <= tol
+    _report(f"teacher_from_lse_{layout}_{dtype}", dict(teacher_err=err, path=B.csa_last_path()))
+
+
 @pytest.mark.parametrize("layout", ["bshd", "sbhd", "thd"])
 def test_backward_with_and_without_given_teacher(layout):
     """The backward that computes the teacher itself and the one given csa_teacher's rows run the same kernels
