@@ -189,6 +189,21 @@ def cpu_oracle_rate(inp, seconds: float):
 
 # ------------------------------------------------------------------ arms
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values, on every rank (the slowest rank's time bounds the job)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(rows_per_rank: int, ms_per_step: float, world: int) -> float:
+    """Whole-job query-tokens/s: every rank runs its own batch (weak scaling) in the slowest rank's time."""
+    return world * rows_per_rank / (ms_per_step / 1e3)
+
+
 def dist_setup(args):
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -282,13 +297,9 @@ def run_ours(args, cfg):
         ev1.record(stream)
         barrier()
     launches = B.csa_kernel_launches() - launches0
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     ms_per_step = ms / args.steps
-    value = world * p.rows / (ms_per_step / 1e3)
+    value = job_rate(p.rows, ms_per_step, world)
     B.csa_check_device_status(dev)
     path = B.csa_last_path()
 
@@ -400,11 +411,7 @@ def run_ours(args, cfg):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
     line = None
     if rank == 0:
@@ -421,7 +428,7 @@ def run_ours(args, cfg):
                        "l2": "inputs exceed L2 (q 201 MB + q_idx 134 MB > 129 MB); no flush",
                        "path": path},
             "roofline": roofline, "cpu_baseline": cpu,
-            "e2e": {"value": world * p.rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_rate(p.rows, e2e_ms, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": 4},
             "gpu_launches": launches, "clocks": clk.summary(),
         }
