@@ -9,16 +9,20 @@
 // for the indexer Q, weights and K; "Megatron-LM PR #8539" item 1: the backward takes global top-k ids.)
 //
 // x is recomputed on the tensor cores over every visible key tile (dense in keys, masked by g), so both
-// kernels stream contiguous k_idx / q_idx tiles by TMA; no per-element global atomics:
-//   * row-owner kernel (dQ_idx, dW): a work item is 2 query rows (N = 128 (row, head) pairs).  Per key tile:
-//     MMA1 X[key, (row,h)] = k . q^T (M 128 keys, K 128), the epilogue forms G'[key, (row,h)] =
-//     g 1[x > 0] in bf16 as an MN-major operand, and MMA2 accumulates dQ'^T... stored as
-//     D[(row,h), d] += sum_key G'[key,(row,h)] k[key, d] in TMEM over all tiles of the item.
+// kernels stream contiguous tiles by TMA; no per-element global atomics.  g arrives by key (the KL step's gd
+// rows, position-major), so a row pair's g over a key tile, its w rows, its q_idx rows and a k tile are one
+// TMA copy each:
+//   * row-owner kernel (dQ_idx, dW): a work item is 2 query rows (M = 128 (row, head) pairs).  Per key tile:
+//     MMA1 X^T[(row,h), key] = q . k^T (N 128 keys, K 128) into one of three TMEM slots, the epilogue forms
+//     G'^T = g 1[x > 0] in bf16 over its own X columns, and MMA2 accumulates dQ'[(row,h), d] += G'^T k
+//     (A from TMEM, B = the k tile read MN-major) over all tiles of the item; the item's dQ' read-out is
+//     deferred behind the next item's first two tiles.
 //   * key-owner kernel (dK): a unit is one key tile and a chunk of up to 128 rows that see it.  Per row pair:
-//     MMA1 as above, the epilogue forms G[key, (row,h)] = g w 1[x > 0] (K-major), and MMA3 accumulates
-//     dK[key, d] += sum_(row,h) G q[(row,h), d] in TMEM; the unit flushes its 128 x 128 fp32 partial once.
-// Roles: warp 0 TMA, warp 1 TMEM + MMA issue, warp 2 stages each item's g (and w) into shared memory ahead of
-// use, warps 4..11 epilogue.  Waits are bounded as in the score kernel.
+//     MMA1 X[key, (row,h)] = k . q^T, the epilogue forms G = g w 1[x > 0] in bf16 over its own X columns, and
+//     MMA3 accumulates dK[key, d] += G q (A from TMEM, B = the q block read MN-major); the unit flushes its
+//     128 x 128 fp32 partial once.  It is launched as a programmatic dependent of the row-owner kernel.
+// Roles (both kernels, 20 warps): warp 0 TMA, warp 1 TMEM + the X MMAs, warp 2 the dQ'/dK MMAs, warp 3 idle,
+// warps 4..19 epilogue.  Waits are bounded as in the score kernel.
 #include "csa_tc.cuh"
 #include "tc_ptx.cuh"
 
