@@ -12,12 +12,13 @@
 // keeps the single issuing thread ahead of the tensor core: one MMA runs 128 cycles, about twice what the thread
 // needs to issue it together with its share of the barrier traffic.  With
 // (row, head) on TMEM lanes each epilogue thread owns one head of one row, so the per-head log-sum-exp is an
-// in-register online max/sum over the key columns.  The keys are taken densely per tile (every visible
+// in-register running sum over the key columns.  The keys are taken densely per tile (every visible
 // compressed key, every window position) and masked by the row's selection and window.
-//   pass 1: window tiles + compressed tiles -> per-(row,h) online max / sum, then l_h with the sink;
-//   pass 2: compressed tiles again -> exp(c - l_h) on selected keys, summed over the 64 heads of a row by a
-//           warp reduce-scatter (31 shuffles per 32 columns) into shared per-key T rows; then the L1
-//           normalisation and the write-out in the id slot order (helper warps).
+//   pass 1: window tiles + compressed tiles -> per-(row,h) sum against a reference maximum, then l_h with the
+//           sink (or with a given sink-and-window log-sum-exp, when there are no window tiles);
+//   pass 2: compressed tiles again, read in the 16-lane TMEM shape -> exp(c - l_h) on selected keys, four heads
+//           added per thread and the rest of the 64 heads of a row by a short reduce-scatter, into shared
+//           per-key T rows; then the L1 normalisation and the write-out in the id slot order (helper warps).
 // Roles: warp 0 TMA, warp 1 TMEM (two 256-column accumulators) + MMA issue, warps 2..17 epilogue (four warps
 // per TMEM lane quadrant, each with two 32-column chunks of every tile), warps 18..19 per-item helpers.
 // Waits are bounded as in the other tensor-core kernels.
@@ -167,7 +168,7 @@ __device__ __forceinline__ int item_total(const Args &a)
 // tile tt of an item: window tiles, then compressed tiles (pass 1), then compressed tiles again (pass 2)
 __device__ __forceinline__ int ntiles(const Item &it) { return it.nw + 2 * it.nct; }
 
-// 18 warps: 5 on some of the SM's four schedulers, whose 16 K-register files then cap a thread at 96 registers
+// 20 warps: 5 on each of the SM's four schedulers, whose 16 K-register files then cap a thread at 96 registers
 __global__ void __launch_bounds__(THREADS, 1)
 teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                   const __grid_constant__ CUtensorMap map_kvc, Args a)
