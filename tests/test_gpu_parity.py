@@ -16,7 +16,9 @@ if torch.cuda.is_available():
     from sparse_attention_indexer_tcgen05_gb300 import workload  # noqa: E402
     import parity_util as U  # noqa: E402
 
-REPORT = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
+# per-case parity figures (errors, recall, path) are appended here as JSON lines
+REPORT = os.environ.get("CSA_PARITY_REPORT_DIR",
+                        os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "parity_reports"))
 
 
 def _report(name, out):
