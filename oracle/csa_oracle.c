@@ -380,6 +380,65 @@ void orc_teacher_lse(const orc_params *P, const double *q, const double *kv_c, c
     }
 }
 
+/* The CSA sparse attention forward of the listed rows, the step right after the path ([BUG] sec. 3: the
+ * attention call takes the query, the window rows and the selected compressed rows as one key/value set
+ * (kv_full) with the sink; reading: the same rows are keys and values, the sink enters the denominator
+ * only):
+ *   l_h    = log(exp(a_h) + sum_{j in C} exp(c_hj) + sum_{r in W} exp(w_hr))
+ *   O[t,h] = sum_{j in C} exp(c_hj - l_h) kv_c[j] + sum_{r in W} exp(w_hr - l_h) kv[r]
+ * out [nrows][heads][head_dim]; lse [nrows][heads] (natural log; -inf with no term at all).  Rows with no
+ * visible compressed key keep their window and sink terms. */
+void orc_attention(const orc_params *P, const double *q, const double *kv, const double *kv_c, const double *sink,
+                   const int32_t *ids, const int32_t *rows, int nrows, int compact, double *out, double *lse)
+{
+    const int H = P->heads, D = P->head_dim, K = orc_topk_width(P), NC = orc_key_width(P);
+    const int cap = K > NC ? K : NC;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < nrows; i++) {
+        const long r = rows[i];
+        orc_row R = orc_decode(P, r);
+        int *slot = malloc(sizeof(int) * (size_t)cap);
+        long *gid = malloc(sizeof(long) * (size_t)cap);
+        const int nC = R.v > 0 ? orc_support(P, &R, ids + (long)i * K, slot, gid) : 0;
+        int p0 = R.s - P->window + 1;
+        if (p0 < 0) p0 = 0;
+        const int nW = (P->window > 0 && !R.pad) ? R.s - p0 + 1 : 0;
+        double *c = malloc(sizeof(double) * (size_t)(nC > 0 ? nC : 1));
+        double *wl = malloc(sizeof(double) * (size_t)(nW > 0 ? nW : 1));
+        for (int h = 0; h < H; h++) {
+            const double *qh = q + (ORC_SRC(i, r) * H + h) * D;
+            double *o = out + ((long)i * H + h) * D;
+            for (int d = 0; d < D; d++) o[d] = 0.0;
+            double m = sink[h];
+            for (int k = 0; k < nC; k++) {
+                c[k] = P->scale * orc_dot(qh, kv_c + orc_crow(P, gid[k]) * D, D);
+                if (c[k] > m) m = c[k];
+            }
+            for (int k = 0; k < nW; k++) {
+                wl[k] = P->scale * orc_dot(qh, kv + orc_qrow(P, &R, p0 + k) * D, D);
+                if (wl[k] > m) m = wl[k];
+            }
+            if (m == -INFINITY) { lse[(long)i * H + h] = -INFINITY; continue; }
+            double Z = exp(sink[h] - m);
+            for (int k = 0; k < nC; k++) Z += exp(c[k] - m);
+            for (int k = 0; k < nW; k++) Z += exp(wl[k] - m);
+            const double l = m + log(Z);
+            lse[(long)i * H + h] = l;
+            for (int k = 0; k < nC; k++) {
+                const double p = exp(c[k] - l);
+                const double *v = kv_c + orc_crow(P, gid[k]) * D;
+                for (int d = 0; d < D; d++) o[d] += p * v[d];
+            }
+            for (int k = 0; k < nW; k++) {
+                const double p = exp(wl[k] - l);
+                const double *v = kv + orc_qrow(P, &R, p0 + k) * D;
+                for (int d = 0; d < D; d++) o[d] += p * v[d];
+            }
+        }
+        free(c); free(wl); free(slot); free(gid);
+    }
+}
+
 /* ---------------------------------------------------------------- step 4: KL */
 
 /* KL(t || p) of one row with p = softmax(I) over the n support entries:

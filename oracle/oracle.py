@@ -62,6 +62,7 @@ def _load():
             lib.orc_teacher.argtypes = [P, vp, vp, vp, vp, vp, vp, i32, i32, vp]
             lib.orc_noncompressed_lse.argtypes = [P, vp, vp, vp, vp, i32, i32, vp]
             lib.orc_teacher_lse.argtypes = [P, vp, vp, vp, vp, vp, i32, i32, vp]
+            lib.orc_attention.argtypes = [P, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp]
             lib.orc_kl_row.argtypes = [vp, vp, i32, vp, vp]
             lib.orc_kl_row.restype = dbl
             lib.orc_loss_factor.argtypes = [P]
@@ -192,6 +193,19 @@ class Problem:
         self.lib.orc_teacher_lse(ctypes.byref(self.p), _ptr(qq), _ptr(kc), _ptr(ls), _ptr(ids), _ptr(rows),
                                  len(rows), int(compact), _ptr(out))
         return out
+
+    def attention(self, q, kv, kv_c, sink, ids, rows=None, compact=False):
+        """The CSA sparse attention forward of the listed rows: (O [len(rows), heads, head_dim], lse [len(rows),
+        heads]) over the sink, the window rows and the selected compressed rows (keys and values alike)."""
+        rows = self._rows(rows)
+        qq, kvv, kc, sk = _f64(q), _f64(kv), _f64(kv_c), _f64(sink)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        assert ids.shape == (len(rows), self.K)
+        out = np.empty((len(rows), self.p.heads, self.p.head_dim), np.float64)
+        lse = np.empty((len(rows), self.p.heads), np.float64)
+        self.lib.orc_attention(ctypes.byref(self.p), _ptr(qq), _ptr(kvv), _ptr(kc), _ptr(sk), _ptr(ids), _ptr(rows),
+                               len(rows), int(compact), _ptr(out), _ptr(lse))
+        return out, lse
 
     def loss_grads(self, q_idx, w, k_idx, ids, teacher, rows=None, want_dk=True, compact=False):
         """(loss, loss_rows, dq[rows,HI,DI], dw[rows,HI], dk[key rows, DI] or None) for the listed rows.

@@ -291,6 +291,51 @@ def test_teacher_from_noncompressed_lse_equals_full_teacher(layout):
     np.testing.assert_allclose(P.teacher_from_lse(q, kv_c, np.full_like(u, -np.inf), ids), t0, rtol=1e-12, atol=1e-15)
 
 
+def test_attention_with_identical_rows_has_closed_form():
+    """Every key/value row equal to one vector v: each of the n = |C| + |W| logits is x = sigma q.v, so
+    l = log(e^a + n e^x) and O = n e^x / (e^a + n e^x) v (the sink takes the rest of the mass)."""
+    inp, P, ids = _teacher_case(heads=3, seqlen=64, window=5)
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal(inp.kv.values.shape[-1])
+    kv = np.broadcast_to(v, inp.kv.values.shape).copy()
+    kv_c = np.broadcast_to(v, inp.kv_c.values.shape).copy()
+    O, lse = P.attention(inp.q.values, kv, kv_c, inp.sink.values, ids)
+    for r in (3, 17, 40, 63, 64 + 30):
+        b, s = divmod(r, 64)
+        n = int((ids[r] >= 0).sum()) + min(5, s + 1)
+        x = P.p.scale * inp.q.values[b, s].astype(np.float64) @ v          # [H]
+        a = inp.sink.values.astype(np.float64)
+        ell = np.logaddexp(a, np.log(n) + x)
+        np.testing.assert_allclose(lse[r], ell, rtol=1e-13)
+        np.testing.assert_allclose(O[r], (np.exp(np.log(n) + x - ell))[:, None] * v[None, :], rtol=1e-12, atol=1e-15)
+
+
+def test_attention_single_key_no_sink_no_window_returns_its_value():
+    """One visible compressed key, no window, no sink: the attention puts all mass on it, O = kv_c[key]."""
+    inp, P, ids = _teacher_case(heads=2, seqlen=64, window=0)
+    O, lse = P.attention(inp.q.values, inp.kv.values, inp.kv_c.values, np.full(2, -np.inf), ids)
+    kvc = inp.kv_c.values.reshape(-1, inp.kv_c.values.shape[-1]).astype(np.float64)
+    for r in (3, 4, 5, 6, 64 + 5):                     # positions 4..7: exactly one visible key (ratio 4)
+        sel = ids[r][ids[r] >= 0]
+        assert len(sel) == 1
+        np.testing.assert_allclose(O[r], np.broadcast_to(kvc[sel[0]], O[r].shape), rtol=1e-14)
+    assert np.all(lse[:3] == -np.inf) and np.all(O[:3] == 0.0)   # no key, no window, no sink
+
+
+def test_attention_lse_reproduces_the_teacher():
+    """The attention's l_h is the teacher's denominator: T_j = sum_h exp(c_hj - l_h), normalised, is the
+    full-CSA teacher of the same inputs."""
+    inp, P, ids = _teacher_case(heads=4, seqlen=64, window=9)
+    t = P.teacher(inp.q.values, inp.kv.values, inp.kv_c.values, inp.sink.values, ids)
+    _, lse = P.attention(inp.q.values, inp.kv.values, inp.kv_c.values, inp.sink.values, ids)
+    for r in (10, 33, 63, 64 + 63):
+        b, s = divmod(r, 64)
+        sel = ids[r][ids[r] >= 0]
+        c = _logits(inp, (b, s), sel, P.p.scale)                     # [H, n]
+        T = np.exp(c - lse[r][:, None]).sum(axis=0)
+        np.testing.assert_allclose(t[r, :len(sel)], T / T.sum(), rtol=1e-12)
+
+
 def test_teacher_perturbations():
     """I5: with H > 1, changing only the window values or one head's sink changes the teacher, and leaves
     the selection and the predictor unchanged."""
