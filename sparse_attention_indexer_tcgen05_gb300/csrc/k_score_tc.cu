@@ -7,8 +7,10 @@
 //   I[t,s] = sum_j w[t,j] * max(0, q_idx[t,j] . k_idx[s]) for the keys s < i_t / r, then the K largest per row
 //   (ties to the lower key), written as ascending global ids with their fp32 scores.
 //
-// Shape taken: bf16 values, H_I = 64 indexer heads, D_I = 128, key axis <= 1024 (the score rows of one work
-// item live in shared memory).  Other shapes use the CUDA-core kernels.
+// Shape taken: bf16 values, H_I = 64 indexer heads, D_I = 128.  Key axes up to 1024 keep an item's score rows
+// whole in shared memory (score_topk_tc_kernel); longer ones (up to 65535 keys, K <= 3840) stream the score
+// tiles into per-row candidate buffers (score_topk_long_tc_kernel, below).  Other shapes and fp32 values take
+// the CUDA-core kernels.
 //
 // Mapping.  A work item is 4 consecutive query positions of one sequence (or THD segment).  The MMA computes
 // D[key, (row, head)] = k_idx[key] . q_idx[row, head] with M = 128 keys (A = a k_idx tile, K-major, streamed
@@ -25,6 +27,8 @@
 //               epilogue runs the following items:
 //               the exact k-th largest score by a bitwise search on order-preserving keys held in
 //               registers, then the selection written by a stable ballot compaction.
+//   (long key axis: warps 10..13, one per row, follow the epilogue tile by tile through a four-tile ring; each
+//    keeps the row's current best candidates and cuts them back to the top K with an 8-bit radix select.)
 //
 // Every mbarrier wait is bounded: on expiry the kernel records an error code (read back by
 // csa_check_device_status), stops waiting (so every role still runs its loops to the end with uniform
@@ -52,9 +56,11 @@ cudaError_t tc_read_clear_error(int *flag)
     }
     e = bwd_tc_read_clear_error(&f2);
     if (e != cudaSuccess) return e;
-    int f3 = 0;
+    int f3 = 0, f4 = 0;
     e = teacher_tc_read_clear_error(&f3);
-    *flag = f1 != 0 ? f1 : (f2 != 0 ? f2 : f3);
+    if (e != cudaSuccess) return e;
+    e = teacher_h128_read_clear_error(&f4);
+    *flag = f1 != 0 ? f1 : (f2 != 0 ? f2 : (f3 != 0 ? f3 : f4));
     return e;
 }
 
@@ -66,25 +72,56 @@ constexpr int ROWS = 4;                       // query rows per work item
 constexpr int HI = 64, DI = 128;              // indexer heads / dim taken by this kernel
 constexpr int NKEY = 128;                     // keys per tile (MMA M)
 constexpr int NCOL = ROWS * HI;               // MMA N = 256
-constexpr int NCMAX = 1024;                   // longest key axis held in shared memory
+constexpr int NCMAX = 1024;                   // longest key axis whose score rows are held whole in shared memory
 constexpr int A_HALF = NKEY * 64 * 2;         // 16 KB: one 64-wide K-half of a key tile
 constexpr int A_STAGES = 3;
 constexpr int B_HALF = NCOL * 64 * 2;         // 32 KB
 constexpr int B_BUF = 2 * B_HALF;             // 64 KB
-constexpr int THREADS = 576;                  // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..17 selection
 constexpr int EPI = 256;
-constexpr int SEL_WARP0 = 10;                 // two sets of four selection warps take alternate items
-constexpr int NSC = 3;                        // item score buffers
+constexpr int SEL_WARP0 = 10;
 constexpr int TMEM_COLS = 512;
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + A_STAGES * A_HALF;           // 64 KB
-constexpr int OFF_SC = OFF_B + 2 * B_BUF;                  // 192 KB
-constexpr int OFF_W = OFF_SC + NSC * ROWS * NCMAX * 4;     // score rows of three items
-constexpr int OFF_MISC = OFF_W + ROWS * HI * 4;            // 209 KB
-constexpr int SMEM_BYTES = OFF_MISC + 1024;
-constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;              // slack to align the base to 1024 B
-static_assert(SMEM_ALLOC <= 232448, "score kernel exceeds the 227 KB of shared memory a CTA may use");
+// Two instantiations of one kernel body:
+//   short key axis (<= NCMAX keys): an item's score rows are kept whole in shared memory (three item buffers)
+//     and each row is selected by one warp once the item is done; two sets of four selection warps take
+//     alternate items; the q_idx rows of two items are resident (double buffer).
+//   long key axis: the score rows stream through a ring of key tiles; the selection warp of each row keeps a
+//     candidate buffer of at most CAP (key, index) entries in ascending key order, admits a new key only when
+//     it beats the row's current K-th best (strictly: a later key loses a tie), and cuts the buffer back to
+//     exactly K entries (the current top K, ties to the lower key) whenever the next tile might not fit, and
+//     once more at the row's end.  One set of four selection warps; one q_idx buffer.
+template <bool LONG> struct SC;
+template <> struct SC<false> {
+    static constexpr int THREADS = 576;       // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..17 selection
+    static constexpr int NB = 2;              // q_idx item buffers
+    static constexpr int NSC = 3;             // item score buffers
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + A_STAGES * A_HALF;        // 48 KB
+    static constexpr int OFF_SC = OFF_B + NB * B_BUF;              // 176 KB
+    static constexpr int OFF_W = OFF_SC + NSC * ROWS * NCMAX * 4;  // score rows of three items
+    static constexpr int OFF_MISC = OFF_W + ROWS * HI * 4;
+    static constexpr int SMEM_ALLOC = OFF_MISC + 1024 + 1024;      // slack to align the base to 1024 B
+};
+template <> struct SC<true> {
+    static constexpr int THREADS = 448;       // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..13 selection
+    static constexpr int NB = 1;
+    static constexpr int NRING = 4;           // score tiles in flight between epilogue and selection
+    static constexpr int CAP = 4096;          // candidate entries per row
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + A_STAGES * A_HALF;        // 48 KB
+    static constexpr int OFF_RING = OFF_B + NB * B_BUF;            // 112 KB
+    static constexpr int OFF_W = OFF_RING + NRING * ROWS * NKEY * 4;
+    static constexpr int OFF_CK = OFF_W + ROWS * HI * 4;           // candidate keys [ROWS][CAP] u32
+    static constexpr int OFF_CI = OFF_CK + ROWS * CAP * 4;         // candidate indices [ROWS][CAP] u16
+    static constexpr int OFF_HIST = OFF_CI + ROWS * CAP * 2;       // radix histograms [ROWS][256] u32
+    static constexpr int OFF_MISC = OFF_HIST + ROWS * 256 * 4;
+    static constexpr int SMEM_ALLOC = OFF_MISC + 1024 + 1024;
+};
+static_assert(SC<false>::SMEM_ALLOC <= 232448, "score kernel exceeds the 227 KB of shared memory a CTA may use");
+static_assert(SC<true>::SMEM_ALLOC <= 232448, "long score kernel exceeds the 227 KB of shared memory a CTA may use");
+// largest K the long kernel takes: a cut leaves K entries and must leave room for one more tile
+constexpr int LONG_KMAX = SC<true>::CAP - 2 * NKEY;
+constexpr int LONG_NCMAX = 65535;             // candidate indices are 16-bit
 
 constexpr uint32_t IDESC = idesc_bf16(NKEY, NCOL, false, false);  // A, B both K-major
 
@@ -297,23 +334,122 @@ __device__ void select_row(const Args &a, const Item &it, int k, const float *sc
     }
 }
 
+// ------------------------------------------------------------------ long key axis: candidate buffers
+
+// The K-th largest of the n keys ck[0..n) (K <= n), one warp, by an 8-bit radix walk from the top byte with a
+// 256-bin histogram per pass.  Returns that key; `need_eq` receives how many entries equal to it belong to the
+// top K (the rest of the top K lies strictly above it).
+__device__ uint32_t kth_largest(const uint32_t *ck, int n, int K, uint32_t *hist, int &need_eq)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t prefix = 0u, pmask = 0u;
+    int need = K;  // rank of the wanted entry among those matching the prefix, counted from the top
+#pragma unroll 1
+    for (int shift = 24; shift >= 0; shift -= 8) {
+#pragma unroll
+        for (int q = 0; q < 8; q++) hist[lane * 8 + q] = 0u;
+        __syncwarp();
+        for (int e = lane; e < n; e += 32) {
+            const uint32_t k = ck[e];
+            if ((k & pmask) == prefix) atomicAdd(hist + ((k >> shift) & 255u), 1u);
+        }
+        __syncwarp();
+        // lane l owns bins 255 - 8 l .. 248 - 8 l (descending); an inclusive scan over lanes counts the entries
+        // in bins at or above each lane's lowest bin
+        uint32_t c[8], tot = 0u;
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            c[q] = hist[255 - 8 * lane - q];
+            tot += c[q];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t before = incl - tot;
+        const bool mine = before < (uint32_t)need && (uint32_t)need <= incl;
+        const unsigned who = __ballot_sync(0xffffffffu, mine);
+        int bin = 0;
+        uint32_t above = 0u;
+        if (mine) {
+            uint32_t acc = before;
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                if (bin == 0 && acc + c[q] >= (uint32_t)need) bin = 256 + 255 - 8 * lane - q;  // +256: found
+                if (bin == 0) acc += c[q];
+            }
+            above = acc;
+            bin -= 256;
+        }
+        const int src = __ffs(who) - 1;
+        bin = __shfl_sync(0xffffffffu, bin, src);
+        above = __shfl_sync(0xffffffffu, above, src);
+        prefix |= (uint32_t)bin << shift;
+        pmask |= 255u << shift;
+        need -= (int)above;
+        __syncwarp();
+    }
+    need_eq = need;
+    return prefix;
+}
+
+// Cuts the candidate buffer (ascending key index) to its top K (K < n), ties to the lower index, keeping the
+// ascending order (stable in-place compaction).  Returns the new count (K) and the K-th largest key in `thr`.
+__device__ int cut_to_topk(uint32_t *ck, uint16_t *ci, int n, int K, uint32_t *hist, uint32_t &thr)
+{
+    const int lane = threadIdx.x & 31;
+    int need_eq = 0;
+    const uint32_t T = kth_largest(ck, n, K, hist, need_eq);
+    const unsigned lt = (1u << lane) - 1u;
+    int base = 0, eq_seen = 0;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int e = c0 + lane;
+        uint32_t k = 0u;
+        uint16_t ix = 0;
+        if (e < n) {
+            k = ck[e];
+            ix = ci[e];
+        }
+        const bool eq = e < n && k == T;
+        const unsigned meq = __ballot_sync(0xffffffffu, eq);
+        const bool keep = e < n && (k > T || (eq && eq_seen + __popc(meq & lt) < need_eq));
+        eq_seen += __popc(meq);
+        const unsigned mk = __ballot_sync(0xffffffffu, keep);
+        __syncwarp();  // every lane has read its entry before any is overwritten (writes land at or below c0 + 31)
+        if (keep) {
+            const int pos = base + __popc(mk & lt);
+            ck[pos] = k;
+            ci[pos] = ix;
+        }
+        base += __popc(mk);
+        __syncwarp();
+    }
+    thr = T;
+    return base;
+}
+
 // ------------------------------------------------------------------ the kernel
 
-__global__ void __launch_bounds__(THREADS, 1)
-score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+template <bool LONG>
+__device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUtensorMap *map_k, const Args &a)
 {
+    using C = SC<LONG>;
+    constexpr int NB = C::NB;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *sA = smem + OFF_A;
-    unsigned char *sB = smem + OFF_B;
-    float *sSC = reinterpret_cast<float *>(smem + OFF_SC);
-    float *sW = reinterpret_cast<float *>(smem + OFF_W);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
+    unsigned char *sA = smem + C::OFF_A;
+    unsigned char *sB = smem + C::OFF_B;
+    float *sW = reinterpret_cast<float *>(smem + C::OFF_W);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_MISC);
     uint64_t *a_full = bars, *a_empty = bars + 4, *b_full = bars + 8, *b_empty = bars + 10;
     uint64_t *t_full = bars + 12, *t_empty = bars + 14, *mma_done = bars + 16;
-    uint64_t *sc_full = bars + 17, *sc_empty = bars + 17 + NSC;  // score rows of an item: epilogue -> selection
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 256);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 264);
+    // short axis: score rows of an item, epilogue -> selection (sc_full / sc_empty, NSC each);
+    // long axis: score tiles (ring_full / ring_empty, NRING each)
+    uint64_t *x_full = bars + 17, *x_empty = bars + 17 + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC + 256);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 264);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geo &g = a.g;
@@ -327,9 +463,16 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             mbar_init(t_full + i, 1);
             mbar_init(t_empty + i, 8);
         }
-        for (int i = 0; i < NSC; i++) {
-            mbar_init(sc_full + i, EPI / 32);
-            mbar_init(sc_empty + i, ROWS);
+        if constexpr (LONG) {
+            for (int i = 0; i < C::NRING; i++) {
+                mbar_init(x_full + i, EPI / 32);
+                mbar_init(x_empty + i, ROWS);
+            }
+        } else {
+            for (int i = 0; i < C::NSC; i++) {
+                mbar_init(x_full + i, EPI / 32);
+                mbar_init(x_empty + i, ROWS);
+            }
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -350,22 +493,23 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
-            // An item's q_idx rows are requested as soon as their buffer is free: that buffer is probed before every
-            // k-half load of the previous item, and waited for at the latest when the item starts.
+            // With two q_idx buffers an item's rows are requested as soon as their buffer is free: that buffer is
+            // probed before every k-half load of the previous item, and waited for at the latest when the item
+            // starts.  With one buffer they are requested when the previous item's MMAs have read it.
             int hs = 0, ai = 0, qi = 0;
             int last_hs[A_STAGES];
             for (int x = 0; x < A_STAGES; x++) last_hs[x] = -1;
-            int last_ai[2] = {-1, -1};
+            int last_qi[2] = {-1, -1};
             auto load_q = [&](const Item &it) {
-                const int bb = qi & 1;
+                const int bb = qi % NB;
                 mbar_expect_tx(b_full + bb, B_BUF);
                 for (int k = 0; k < ROWS; k++) {
                     const long long row = k < it.n ? it.row[k] : it.row[0];
                     for (int kh = 0; kh < 2; kh++)
-                        tma_load_3d(sB + bb * B_BUF + kh * B_HALF + k * (HI * 128), &map_q, b_full + bb, kh * 64, 0,
+                        tma_load_3d(sB + bb * B_BUF + kh * B_HALF + k * (HI * 128), map_q, b_full + bb, kh * 64, 0,
                                     (int)row);
                 }
-                last_ai[bb] = qi;
+                last_qi[bb] = qi;
                 qi++;
             };
             // the next item with visible keys after item index i (or total)
@@ -386,21 +530,22 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 Item nxt;
                 const int inext = next_item(i, nxt);
                 if (qi == ai) {
-                    wait_bar(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1, abort_flag, &g_tc_error, 1);
+                    wait_bar(b_empty + qi % NB, ((qi / NB) & 1) ^ 1, abort_flag, &g_tc_error, 1);
                     load_q(cur);
                 }
                 const int nt = (cur.vmax + NKEY - 1) / NKEY;
                 for (int t = 0; t < nt; t++)
                     for (int kh = 0; kh < 2; kh++) {
-                        if (qi == ai + 1 && inext < total && mbar_test(b_empty + (qi & 1), ((qi >> 1) & 1) ^ 1))
+                        if (NB > 1 && qi == ai + 1 && inext < total &&
+                            mbar_test(b_empty + qi % NB, ((qi / NB) & 1) ^ 1))
                             load_q(nxt);
                         const int st = hs % A_STAGES;
                         wait_bar(a_empty + st, ((hs / A_STAGES) & 1) ^ 1, abort_flag, &g_tc_error, 2);
                         mbar_expect_tx(a_full + st, A_HALF);
                         if (sbhd)
-                            tma_load_3d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, cur.b, t * NKEY);
+                            tma_load_3d(sA + st * A_HALF, map_k, a_full + st, kh * 64, cur.b, t * NKEY);
                         else
-                            tma_load_2d(sA + st * A_HALF, &map_k, a_full + st, kh * 64, (int)(cur.key_y + t * NKEY));
+                            tma_load_2d(sA + st * A_HALF, map_k, a_full + st, kh * 64, (int)(cur.key_y + t * NKEY));
                         last_hs[st] = hs;
                         hs++;
                     }
@@ -411,8 +556,8 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             // our own copies must land before the CTA exits
             for (int st = 0; st < A_STAGES; st++)
                 if (last_hs[st] >= 0) drain_bar(a_full + st, (last_hs[st] / A_STAGES) & 1, &g_tc_error);
-            for (int bb = 0; bb < 2; bb++)
-                if (last_ai[bb] >= 0) drain_bar(b_full + bb, (last_ai[bb] >> 1) & 1, &g_tc_error);
+            for (int bb = 0; bb < NB; bb++)
+                if (last_qi[bb] >= 0) drain_bar(b_full + bb, (last_qi[bb] / NB) & 1, &g_tc_error);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issue (whole warp)
@@ -432,8 +577,8 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             }
             const int nt = __shfl_sync(0xffffffffu, nt_lane, k & 31);
             if (nt == 0) continue;
-            const int bb = ai & 1;
-            wait_bar(b_full + bb, (ai >> 1) & 1, abort_flag, &g_tc_error, 3);
+            const int bb = ai % NB;
+            wait_bar(b_full + bb, (ai / NB) & 1, abort_flag, &g_tc_error, 3);
             fence_after();
             const unsigned char *pb0 = sB + bb * B_BUF;
             for (int t = 0; t < nt; t++) {
@@ -486,16 +631,22 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
             sW[et] = w_next;
             w_next = w_of(i + gridDim.x);
             named_bar(1, EPI);
-            // this item's score rows go to buffer ic % NSC, free once the selection warps have read item ic - NSC
-            const int sb = ic % NSC, su = ic / NSC;
-            float *scb = sSC + sb * ROWS * NCMAX;
-            wait_bar(sc_empty + sb, (su & 1) ^ 1, abort_flag, &g_tc_error, 7);
+            float *scb = nullptr;
+            int sb = 0;
+            if constexpr (!LONG) {
+                // this item's score rows go to buffer ic % NSC, free once the selection warps have read item ic - NSC
+                sb = ic % C::NSC;
+                const int su = ic / C::NSC;
+                scb = reinterpret_cast<float *>(smem + C::OFF_SC) + sb * ROWS * NCMAX;
+                wait_bar(x_empty + sb, (su & 1) ^ 1, abort_flag, &g_tc_error, 7);
+            }
             const int nt = (it.vmax + NKEY - 1) / NKEY;
             for (int t = 0; t < nt; t++) {
                 const int tb = tc & 1;
                 wait_bar(t_full + tb, (tc >> 1) & 1, abort_flag, &g_tc_error, 6);
                 fence_after();
                 const int j = t * NKEY + quad * 32 + lane;
+                float accs[2];
 #pragma unroll
                 for (int rr = 0; rr < 2; rr++) {
                     const int k = half * 2 + rr;
@@ -510,28 +661,44 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                         for (int h2 = 0; h2 < 16; h2++)
                             ac[h2 & 1] = fma2(wk[h2], make_float2(fmaxf(x[2 * h2], 0.f), fmaxf(x[2 * h2 + 1], 0.f)), ac[h2 & 1]);
                     }
-                    const float acc = (ac[0].x + ac[0].y) + (ac[1].x + ac[1].y);  // heads (0 + 1) + (2 + 3) mod 4
-                    if (k < it.n && j < it.v[k]) scb[k * NCMAX + j] = acc;
+                    accs[rr] = (ac[0].x + ac[0].y) + (ac[1].x + ac[1].y);  // heads (0 + 1) + (2 + 3) mod 4
+                    if constexpr (!LONG) {
+                        if (k < it.n && j < it.v[k]) scb[k * NCMAX + j] = accs[rr];
+                    }
                 }
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(t_empty + tb);
+                if constexpr (LONG) {
+                    // the tile's scores of rows 2 half, 2 half + 1 into ring slot tc % NRING (keys past a row's
+                    // visible count are written too; the selection masks them)
+                    const int slot = tc % C::NRING;
+                    wait_bar(x_empty + slot, ((tc / C::NRING) & 1) ^ 1, abort_flag, &g_tc_error, 7);
+                    float *ring = reinterpret_cast<float *>(smem + C::OFF_RING) + slot * ROWS * NKEY;
+                    ring[(half * 2) * NKEY + quad * 32 + lane] = accs[0];
+                    ring[(half * 2 + 1) * NKEY + quad * 32 + lane] = accs[1];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(x_full + slot);
+                }
                 tc++;
             }
-            // hand the item's score rows to the selection warps
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sc_full + sb);
+            if constexpr (!LONG) {
+                // hand the item's score rows to the selection warps
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_full + sb);
+            }
         }
-    } else {
+    } else if constexpr (!LONG) {
         // ---------------------------------------------------------- selection (warps 10..17: two sets of four,
         // alternate items, one row per warp)
         const int k = (warp - SEL_WARP0) & 3, set = (warp - SEL_WARP0) >> 2;
+        float *sSC = reinterpret_cast<float *>(smem + C::OFF_SC);
         int ic = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
             if ((ic & 1) != set) continue;
             const Item it = decode_item(a, i, total);
-            const int sb = ic % NSC, su = ic / NSC;
-            wait_bar(sc_full + sb, su & 1, abort_flag, &g_tc_error, 8);
+            const int sb = ic % C::NSC, su = ic / C::NSC;
+            wait_bar(x_full + sb, su & 1, abort_flag, &g_tc_error, 8);
             const float *sc = sSC + sb * ROWS * NCMAX + k * NCMAX;
             if (k < it.n) {
                 const long long r = it.row[k];
@@ -541,17 +708,101 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
                 }
             }
             if (k < it.n && a.ids != nullptr) {
-                select_row(a, it, k, sc, sc_empty + sb);
+                select_row(a, it, k, sc, x_empty + sb);
             } else {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sc_empty + sb);
+                if (lane == 0) mbar_arrive(x_empty + sb);
             }
+        }
+    } else {
+        // ---------------------------------------------------------- selection, long key axis (warps 10..13, one
+        // row each): consume the score tiles of every item in order; keep the row's candidates in shared memory
+        const int k = warp - SEL_WARP0;
+        uint32_t *ck = reinterpret_cast<uint32_t *>(smem + C::OFF_CK) + k * C::CAP;
+        uint16_t *ci = reinterpret_cast<uint16_t *>(smem + C::OFF_CI) + k * C::CAP;
+        uint32_t *hist = reinterpret_cast<uint32_t *>(smem + C::OFF_HIST) + k * 256;
+        const float *ringb = reinterpret_cast<const float *>(smem + C::OFF_RING);
+        const int K = g.K;
+        const unsigned lt = (1u << lane) - 1u;
+        int tc = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+            const Item it = decode_item(a, i, total);
+            const int nt = (it.vmax + NKEY - 1) / NKEY;
+            const bool present = k < it.n;
+            const int v = present ? it.v[k] : 0;
+            const long long r = present ? it.row[k] : -1;
+            float *dump_row = (present && a.dump != nullptr && r >= a.dump_row0 && r < a.dump_row0 + a.dump_rows)
+                                  ? a.dump + (r - a.dump_row0) * (long long)g.NC
+                                  : nullptr;
+            const bool select = present && a.ids != nullptr;
+            int n = 0;
+            uint32_t thr = 0u;  // a key enters only above this (0: every score, before the first cut)
+            for (int t = 0; t < nt; t++, tc++) {
+                const int slot = tc % C::NRING;
+                wait_bar(x_full + slot, (tc / C::NRING) & 1, abort_flag, &g_tc_error, 8);
+                float s[4];
+#pragma unroll
+                for (int c = 0; c < 4; c++) s[c] = ringb[(slot * ROWS + k) * NKEY + 32 * c + lane];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_empty + slot);
+                if (dump_row != nullptr) {
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        const int j = t * NKEY + 32 * c + lane;
+                        if (j < g.NC) dump_row[j] = j < v ? s[c] : -INFINITY;
+                    }
+                }
+                if (!select) continue;
+                if (n + NKEY > C::CAP) n = cut_to_topk(ck, ci, n, K, hist, thr);
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int j = t * NKEY + 32 * c + lane;
+                    const uint32_t key = score_key(s[c]);
+                    const bool in = j < v && key > thr;
+                    const unsigned m = __ballot_sync(0xffffffffu, in);
+                    if (in) {
+                        const int pos = n + __popc(m & lt);
+                        ck[pos] = key;
+                        ci[pos] = (uint16_t)j;
+                    }
+                    n += __popc(m);
+                }
+                __syncwarp();
+            }
+            if (dump_row != nullptr)
+                for (int j = nt * NKEY + lane; j < g.NC; j += 32) dump_row[j] = -INFINITY;
+            if (!select) continue;
+            if (n > K) n = cut_to_topk(ck, ci, n, K, hist, thr);
+            __syncwarp();
+            int32_t *orow = a.ids + r * K;
+            float *srow = a.selscore + r * K;
+            for (int s2 = lane; s2 < n; s2 += 32) {
+                orow[s2] = (int32_t)(it.gid0 + ci[s2]);
+                srow[s2] = key_score(ck[s2]);
+            }
+            for (int s2 = n + lane; s2 < K; s2 += 32) {
+                orow[s2] = -1;
+                srow[s2] = -INFINITY;
+            }
+            __syncwarp();
         }
     }
     fence_before();
     __syncthreads();
     fence_after();
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+}
+
+__global__ void __launch_bounds__(SC<false>::THREADS, 1)
+score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+{
+    score_body<false>(&map_q, &map_k, a);
+}
+
+__global__ void __launch_bounds__(SC<true>::THREADS, 1)
+score_topk_long_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+{
+    score_body<true>(&map_q, &map_k, a);
 }
 
 // THD: work-item offsets per segment, cu_g[b+1] = cu_g[b] + ceil(physical length / 4)
@@ -610,8 +861,10 @@ bool tc_score_supported(const Geo &g, bool bf16)
 {
     const char *f = getenv("CSA_FORCE_GENERIC");
     if (f != nullptr && f[0] == '1') return false;
-    return bf16 && g.HI == tcs::HI && g.DI == tcs::DI && g.NC >= 1 && g.NC <= tcs::NCMAX && g.K >= 1 &&
-           g.rows > 0 && g.key_rows > 0;
+    if (!(bf16 && g.HI == tcs::HI && g.DI == tcs::DI && g.NC >= 1 && g.K >= 1 && g.rows > 0 && g.key_rows > 0))
+        return false;
+    // short key axis: whole score rows in shared memory; long: streamed tiles and candidate buffers
+    return g.NC <= tcs::NCMAX || (g.NC <= tcs::LONG_NCMAX && g.K <= tcs::LONG_KMAX);
 }
 
 size_t tc_workspace_bytes(const Geo &g) { return sizeof(int) * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1); }
@@ -645,7 +898,7 @@ static cudaError_t launch_tc(const Geo &g, const __nv_bfloat16 *q_idx, const flo
     using namespace tcs;
     CUtensorMap mq, mk;
     if (!tc_encode_q_map(&mq, q_idx, g) || !tc_encode_k_map(&mk, k_idx, g)) return cudaErrorInvalidValue;
-    Args a;
+    Args a = {};  // every field set below; zero first so none is ever left unset
     a.g = g;
     a.w = w;
     a.ids = ids;
@@ -671,10 +924,17 @@ static cudaError_t launch_tc(const Geo &g, const __nv_bfloat16 *q_idx, const flo
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(score_topk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
     const int grid = upper < sms ? (upper > 0 ? upper : 1) : sms;
-    score_topk_tc_kernel<<<grid, THREADS, SMEM_ALLOC, st>>>(mq, mk, a);
+    if (g.NC <= NCMAX) {
+        e = cudaFuncSetAttribute(score_topk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SC<false>::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        score_topk_tc_kernel<<<grid, SC<false>::THREADS, SC<false>::SMEM_ALLOC, st>>>(mq, mk, a);
+    } else {
+        e = cudaFuncSetAttribute(score_topk_long_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SC<true>::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        score_topk_long_tc_kernel<<<grid, SC<true>::THREADS, SC<true>::SMEM_ALLOC, st>>>(mq, mk, a);
+    }
     note_launches(1);
     return cudaGetLastError();
 }
