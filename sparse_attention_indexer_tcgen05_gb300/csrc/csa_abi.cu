@@ -111,11 +111,12 @@ csa_status make_plan(const csa_params *p, Plan *P)
     off = align_up(off + sizeof(int) * (size_t)(p->layout == CSA_THD ? p->batch + 1 : 1));
     P->off_teacher = off;
     off = align_up(off + sizeof(float) * (size_t)rows * g.TW);
-    // g by slot for the CUDA-core backward, or g by key (inside the tensor-core backward's region) for the
-    // tensor-core one: only one of the two is sized
+    // g by slot for the CUDA-core backward and the tensor-core one on long key axes, or g by key (inside the
+    // tensor-core backward's region) for the tensor-core one on short key axes
     const bool tc_bwd = tc_bwd_supported(g, p->dtype == CSA_BF16);
+    const bool by_key = tc_bwd && !tc_bwd_long(g);
     P->off_g = off;
-    off = align_up(off + (tc_bwd ? 0 : sizeof(float) * (size_t)rows * g.TW));
+    off = align_up(off + (by_key ? 0 : sizeof(float) * (size_t)rows * g.TW));
     P->off_rowloss = off;
     off = align_up(off + sizeof(float) * (size_t)(rows > 0 ? rows : 1));
     P->off_dk = off;
@@ -219,6 +220,12 @@ csa_status run_teacher(Plan &P, const void *q, const void *kv, const void *kv_c,
                                    (const __nv_bfloat16 *)kv_c, sink, ids, teacher, ws_at(ws, P.off_ttc), st));
         return CSA_OK;
     }
+    if (tc_teacher_h128_supported(P.g, sizeof(T) == 2)) {
+        t_last_path = "tcgen05";
+        CSA_CUDA(launch_teacher_h128_tc(P.g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kv,
+                                        (const __nv_bfloat16 *)kv_c, sink, ids, teacher, st));
+        return CSA_OK;
+    }
     CSA_TRY(check_smem(teacher_generic_smem(P.g, sizeof(T) == 2)));
     t_last_path = "generic";
     CSA_CUDA(launch_teacher_generic<T>(P.g, (const T *)q, (const T *)kv, (const T *)kv_c, sink, ids, teacher, st));
@@ -250,17 +257,19 @@ csa_status run_bwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
     float *gbuf = reinterpret_cast<float *>(ws_at(ws, P.off_g));
     float *row_loss = row_loss_out ? row_loss_out : reinterpret_cast<float *>(ws_at(ws, P.off_rowloss));
     const bool tc = tc_bwd_supported(g, sizeof(T) == 2);
+    const bool by_key = tc && !tc_bwd_long(g);
     char *btc = ws_at(ws, P.off_btc);
-    float *gd = tc ? tc_bwd_gd(g, btc) : nullptr;
-    // the tensor-core backward reads g by key only; the slot-layout rows are for the CUDA-core backward
-    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, tc ? nullptr : gbuf, row_loss, gd,
-                       tc ? tc_bwd_ncp(g) : 0, st));
+    float *gd = by_key ? tc_bwd_gd(g, btc) : nullptr;
+    // the tensor-core backward on short key axes reads g by key only; the slot-layout rows serve the CUDA-core
+    // backward and the tensor-core one on long key axes
+    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, by_key ? nullptr : gbuf, row_loss, gd,
+                       by_key ? tc_bwd_ncp(g) : 0, st));
     if (g.key_rows * g.DI > 0)
         CSA_CUDA(cudaMemsetAsync(dk_acc, 0, sizeof(float) * (size_t)g.key_rows * g.DI, st));
     if (tc) {
         t_last_path = "tcgen05";
         CSA_CUDA(launch_bwd_tc(g, (const __nv_bfloat16 *)q_idx, w, (const __nv_bfloat16 *)k_idx, (__nv_bfloat16 *)dq_idx,
-                               dw, dk_acc, btc, st));
+                               dw, dk_acc, btc, ids, gbuf, st));
     } else {
         CSA_TRY(check_smem(grad_generic_smem(g)));
         t_last_path = "generic";

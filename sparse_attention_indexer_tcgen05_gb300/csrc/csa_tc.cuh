@@ -33,17 +33,22 @@ bool tc_encode_f32(CUtensorMap *m, const float *base, int rank, const cuuint64_t
                    const cuuint32_t *box);
 bool tc_encode_k_map(CUtensorMap *m, const void *k_idx, const Geo &g);
 
-// Tensor-core backward (dQ_idx, dW, dK) for bf16, H_I = 64, D_I = 128, key axis <= 1024.
+// Tensor-core backward (dQ_idx, dW, dK) for bf16, H_I = 64, D_I = 128: any key axis with the sparse loss, key
+// axes up to 1024 with the dense loss.
 bool tc_bwd_supported(const Geo &g, bool bf16);
+// Long key axis (more than 1024 keys): g stays in the KL step's slot layout and the kernels build g tiles.
+bool tc_bwd_long(const Geo &g);
 int tc_bwd_tiles(const Geo &g);
-// Row stride (floats) of the by-key gradient rows gd[rows][ncp] the KL step writes for the backward.
+// Row stride (floats) of the by-key gradient rows gd[rows][ncp] the KL step writes for the backward (short axis).
 int tc_bwd_ncp(const Geo &g);
 size_t tc_bwd_workspace_bytes(const Geo &g);
-// Where gd lives inside that workspace.
+// Where gd (short axis) or the per-row tile offsets (long axis) live inside that workspace.
 float *tc_bwd_gd(const Geo &g, void *ws);
-// ws: tc_bwd_workspace_bytes(g) bytes whose gd rows hold dloss/dI[row][key] for every visible key
+// ws: tc_bwd_workspace_bytes(g) bytes; short axis: its gd rows hold dloss/dI[row][key] for every visible key;
+// long axis: gslot [rows][K] holds dloss/dI by slot of the ascending ids.
 cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
-                          __nv_bfloat16 *dq, float *dw, float *dk_acc, void *ws, cudaStream_t st);
+                          __nv_bfloat16 *dq, float *dw, float *dk_acc, void *ws, const int32_t *ids,
+                          const float *gslot, cudaStream_t st);
 cudaError_t bwd_tc_read_clear_error(int *flag);
 
 // Tensor-core teacher for bf16, H = 64, D in {64, 128, 192}, key axis <= 1024.
@@ -53,6 +58,14 @@ cudaError_t launch_teacher_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_b
                               const __nv_bfloat16 *kv_c, const float *sink, const int32_t *ids, float *teacher,
                               void *ws, cudaStream_t st);
 cudaError_t teacher_tc_read_clear_error(int *flag);
+
+// Tensor-core teacher for bf16, H = 128, D a multiple of 64 up to 512, teacher rows up to 2048 wide: one query
+// row per work item, q in TMEM, the selected compressed keys gathered (sparse loss) or tiled (dense loss).
+bool tc_teacher_h128_supported(const Geo &g, bool bf16);
+cudaError_t launch_teacher_h128_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *kv,
+                                   const __nv_bfloat16 *kv_c, const float *sink, const int32_t *ids, float *teacher,
+                                   cudaStream_t st);
+cudaError_t teacher_h128_read_clear_error(int *flag);
 
 // Reads and clears the tensor-core kernels' device error word (set when a kernel gives up a bounded
 // wait on an mbarrier).  Synchronous: call after the stream has drained.

@@ -9,9 +9,12 @@
 // for the indexer Q, weights and K; "Megatron-LM PR #8539" item 1: the backward takes global top-k ids.)
 //
 // x is recomputed on the tensor cores over every visible key tile (dense in keys, masked by g), so both
-// kernels stream contiguous tiles by TMA; no per-element global atomics.  g arrives by key (the KL step's gd
-// rows, position-major), so a row pair's g over a key tile, its w rows, its q_idx rows and a k tile are one
-// TMA copy each:
+// kernels stream contiguous tiles by TMA; no per-element global atomics.  On key axes up to 1024 keys g arrives
+// by key (the KL step's gd rows, position-major), so a row pair's g over a key tile, its w rows, its q_idx rows
+// and a k tile are one TMA copy each.  On longer key axes g stays in the KL step's slot layout ([rows][K], the
+// row's ascending ids) and a builder warp assembles each row's 128-key g tile in shared memory: the row-owner's
+// walks the row's slots with a cursor, the key-owner's reads the tile's slot range from a per-row table of tile
+// offsets (tile_offsets_kernel), so no [rows][keys] array is ever written.
 //   * row-owner kernel (dQ_idx, dW): a work item is 2 query rows (M = 128 (row, head) pairs).  Per key tile:
 //     MMA1 X^T[(row,h), key] = q . k^T (N 128 keys, K 128) into one of three TMEM slots, the epilogue forms
 //     G'^T = g 1[x > 0] in bf16 over its own X columns, and MMA2 accumulates dQ'[(row,h), d] += G'^T k
@@ -21,8 +24,8 @@
 //     MMA1 X[key, (row,h)] = k . q^T, the epilogue forms G = g w 1[x > 0] in bf16 over its own X columns, and
 //     MMA3 accumulates dK[key, d] += G q (A from TMEM, B = the q block read MN-major); the unit flushes its
 //     128 x 128 fp32 partial once.  It is launched as a programmatic dependent of the row-owner kernel.
-// Roles (both kernels, 20 warps): warp 0 TMA, warp 1 TMEM + the X MMAs, warp 2 the dQ'/dK MMAs, warp 3 idle,
-// warps 4..19 epilogue.  Waits are bounded as in the score kernel.
+// Roles (both kernels, 20 warps): warp 0 TMA, warp 1 TMEM + the X MMAs, warp 2 the dQ'/dK MMAs, warp 3 the g-tile
+// builder on long key axes (idle otherwise), warps 4..19 epilogue.  Waits are bounded as in the score kernel.
 #include "csa_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -47,7 +50,8 @@ using namespace ptx;
 constexpr int HI = 64, DI = 128, NKEY = 128;
 constexpr int RP = 2;                          // query rows per item / row pair
 constexpr int M_PAIRS = RP * 64;               // (row, head) pairs of an item
-constexpr int NCMAX = 1024;                    // key axis the row-owner's dense g rows hold
+constexpr int NCMAX = 1024;                    // key axis the row-owner's dense g rows hold (longer: g tiles built)
+constexpr int GR = 8;                          // long key axis: row-owner g tiles in flight (2 rows x 128 keys each)
 constexpr int HALF = NKEY * 64 * 2;            // 16 KB: 128 rows x 64 bf16
 constexpr int QBLK = 2 * HALF;                 // 32 KB: 2 rows x 64 heads x 128 d, two K-halves
 constexpr int THREADS = 640;                   // key-owner kernel: 20 warps
@@ -63,7 +67,7 @@ constexpr uint32_t IDESC_DK = idesc_bf16(128, 128, false, true);   // dK += G q 
 // row-owner shared memory
 constexpr int R_ASTG = 4;                                     // k tiles in flight
 constexpr int R_XSTG = 3;                                     // X / G' TMEM slots
-static_assert((2 * R_ASTG + 19 + 3 * R_XSTG) * 8 <= 512, "row-owner barriers overlap the TMEM slot");
+static_assert((2 * R_ASTG + 19 + 3 * R_XSTG + 2 * GR) * 8 <= 512, "row-owner barriers overlap the TMEM slot");
 constexpr int KTILE = 2 * HALF;                               // 32 KB: 128 keys x 128 d, two K-halves
 constexpr int R_OFF_A = 0;
 constexpr int R_OFF_B = R_OFF_A + R_ASTG * KTILE;             // 128 KB: the q tiles of two items
@@ -79,7 +83,8 @@ constexpr int K_OFF_A = 0;                                     // the unit's key
 constexpr int K_OFF_B = K_OFF_A + 2 * HALF;                    // 5 q blocks (G lives in TMEM)
 constexpr int K_OFF_GT = K_OFF_B + K_BSTG * QBLK;              // g tiles: 4 x 2 rows x 128 fp32
 constexpr int K_OFF_WT = K_OFF_GT + K_GSTG * RP * NKEY * 4;    // w rows: 4 x 2 rows x 64 fp32
-constexpr int K_OFF_MISC = K_OFF_WT + K_GSTG * RP * HI * 4;
+constexpr int K_OFF_RNG = K_OFF_WT + K_GSTG * RP * HI * 4;      // long key axis: a unit's slot ranges, CH x 2 int
+constexpr int K_OFF_MISC = K_OFF_RNG + CH * 2 * 4;
 constexpr int K_SMEM = K_OFF_MISC + 1024 + 1024;
 constexpr int K_XSTG = 3;                                      // X / G TMEM slots
 static_assert((2 + 2 * K_BSTG + 3 * K_XSTG + 2 + 2 * K_GSTG + 1) * 8 <= 256, "key-owner barriers overlap the TMEM slot");
@@ -93,6 +98,12 @@ struct Args {
     const int *cu_u;         // THD: key-owner units per segment [nseg+1]
     int total_items, total_units;     // SBHD/BSHD
     int units_per_seq;                // SBHD/BSHD
+    // long key axis: g by slot [rows][K], the ids, and per row the first slot of each key tile [rows][NT + 1]
+    bool lng;
+    const float *gslot;
+    const int32_t *ids;
+    const int *toff;
+    int NT;
 };
 
 // ------------------------------------------------------------------ geometry
@@ -295,6 +306,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     uint64_t *dq_full = g_full + R_XSTG, *dq_empty = dq_full + 1, *gd_full = dq_full + 2, *gd_empty = dq_full + 4;
     uint64_t *mma_done = dq_full + 6;                                  // 2 R_ASTG + 19 + 3 R_XSTG barriers
     uint64_t *dw_bar = dq_full + 7;                                    // [item parity][quadrant]: dW partials
+    uint64_t *gr_full = dq_full + 15, *gr_empty = gr_full + GR;        // long key axis: built g tiles
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + R_OFF_MISC + 512);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + R_OFF_MISC + 520);
 
@@ -320,6 +332,10 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         mbar_init(dq_empty, R_EPI / 32);
         mbar_init(mma_done, 2);
         for (int i = 0; i < 8; i++) mbar_init(dw_bar + i, 4);
+        for (int i = 0; i < GR; i++) {
+            mbar_init(gr_full + i, 1);
+            mbar_init(gr_empty + i, R_EPI / 32);
+        }
         *abort_flag = 0;
         init_fence();
     }
@@ -345,10 +361,11 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             for (int i = 0; i < R_ASTG; i++) last_hs[i] = -1;
             // the item's g rows over its visible key tiles (one copy of both rows per tile) and its w rows, into
             // buffer ai & 1
+            // (long key axis: the w rows only; the builder warp assembles the g tiles)
             auto load_gw = [&](const Pair &p, const PairAt &at) {
                 const int gb = ai & 1;
                 wait_bar(gd_empty + gb, ((ai >> 1) & 1) ^ 1, abort_flag, err, 8);
-                const int nt = (p.vmax + NKEY - 1) / NKEY;
+                const int nt = a.lng ? 0 : (p.vmax + NKEY - 1) / NKEY;
                 mbar_expect_tx(gd_full + gb, (uint32_t)(nt * RP * NKEY * 4 + RP * HI * 4));
                 for (int kt = 0; kt < nt; kt++)
                     tma_load_2d(sGD + gb * RP * NCMAX + kt * RP * NKEY, &map_g, gd_full + gb, kt * NKEY, at.prow);
@@ -480,6 +497,66 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
         }
         mma_commit_w(mma_done);
         drain_bar(mma_done, 0, err);
+    } else if (warp == 3 && a.lng) {
+        // ---------------------------------------------------------------- g-tile builder (long key axis)
+        // Half-warp r builds row r of the item: for each key tile, in order, 128 floats of g by key (zero off the
+        // row's selection) from the row's slots, whose ids ascend.  It walks the slots with a cursor over chunks of
+        // 16 (chunk A being placed, chunk B loaded ahead); a chunk advances once all its keys lie below the tile's
+        // end.  Keys outside the tile or the row's visible range are never placed.
+        const int half = lane >> 4, hl = lane & 15;
+        const unsigned hmask = 0xffffu << (16 * half);
+        const int K = g.K;
+        float *sG = sGD;  // [GR][RP][NKEY]
+        int tcnt = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+            const Pair p = decode_pair(a, i);
+            const int nt = (p.vmax + NKEY - 1) / NKEY;
+            if (nt == 0) continue;
+            const bool present = half < p.n;
+            const long long row = half == 0 ? p.row0 : p.row1;
+            const int v_me = half == 0 ? p.v0 : p.v1;
+            const int32_t *rid = a.ids + row * K;
+            const float *rg = a.gslot + row * K;
+            auto load = [&](int sl, int &j, float &gv) {  // key (INT_MAX when unusable) and g of slot sl
+                j = 0x7fffffff;
+                gv = 0.f;
+                if (present && sl < K) {
+                    const int32_t id = __ldg(rid + sl);
+                    const long long jj = (long long)id - p.sg.gid0;
+                    if (id >= 0 && jj >= 0 && jj < v_me) {
+                        j = (int)jj;
+                        gv = __ldg(rg + sl);
+                    }
+                }
+            };
+            int cur = 0, ja, jb;
+            float ga, gb_;
+            load(hl, ja, ga);
+            load(16 + hl, jb, gb_);
+            for (int t = 0; t < nt; t++, tcnt++) {
+                const int slot = tcnt % GR;
+                wait_bar(gr_empty + slot, ((tcnt / GR) & 1) ^ 1, abort_flag, err, 14);
+                float *dst = sG + slot * RP * NKEY + half * NKEY;
+                reinterpret_cast<float4 *>(dst)[2 * hl] = make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(dst)[2 * hl + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                __syncwarp();
+                const int t0 = t * NKEY, t1 = t0 + NKEY;
+                while (true) {
+                    if (ja >= t0 && ja < t1) dst[ja - t0] = ga;
+                    const unsigned below = __ballot_sync(0xffffffffu, ja < t1);
+                    const bool adv = present && (below & hmask) == hmask;
+                    if (!__any_sync(0xffffffffu, adv)) break;
+                    if (adv) {
+                        ja = jb;
+                        ga = gb_;
+                        cur += 16;
+                        load(cur + 16 + hl, jb, gb_);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gr_full + slot);
+            }
+        }
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- epilogue (16 warps)
         // Lane (quad*32 + lane) = (row, head).  Warp qq = (warp - 4) / 4 of a quadrant owns key columns
@@ -498,7 +575,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             int gb, ic;       // g / w / q buffer of the item, item index (dW buffer parity)
             bool tiles, exists, valid;
         };
-        int xb = 0, dqc = 0, ai = 0, ic = 0;
+        int xb = 0, dqc = 0, ai = 0, ic = 0, gcnt = 0;
         uint32_t xph = 0;
         // ---- one key tile: X^T -> G'^T over the warp's own columns
         auto tile = [&](const float *gd, int v_me, int t) {
@@ -506,6 +583,11 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
             fence_after();
             const int j0 = t * NKEY + qq * 32;  // first key of this warp's columns
             const float *gt = gd + t * RP * NKEY + qq * 32;
+            const int gslot = gcnt % GR;
+            if (a.lng) {  // the builder's tile (rows x 128 keys) of this key tile
+                wait_bar(gr_full + gslot, (gcnt / GR) & 1, abort_flag, err, 15);
+                gt = sGD + gslot * RP * NKEY + er * NKEY + qq * 32;
+            }
             uint32_t xr[32];
             const uint32_t tcol = tX + lane_off + (uint32_t)(xb * 128 + qq * 32);
             tmem_ld32_async(tcol, xr);
@@ -519,6 +601,11 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
                 gk[4 * q4 + 1] = g4.y;
                 gk[4 * q4 + 2] = g4.z;
                 gk[4 * q4 + 3] = g4.w;
+            }
+            if (a.lng) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gr_empty + gslot);
+                gcnt++;
             }
             if (j0 + 32 > v_me) {  // warp-uniform: the row's last visible tile
 #pragma unroll
@@ -677,7 +764,8 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             mbar_init(x_empty + i, 1);
             mbar_init(gk_full + i, EPI / 32);
         }
-        for (int i = 0; i < K_GSTG; i++) { mbar_init(gt_full + i, 1); mbar_init(gt_empty + i, EPI / 32); }
+        // long key axis: a g/w slot is full once the w copy has landed and the builder has written the g tile
+        for (int i = 0; i < K_GSTG; i++) { mbar_init(gt_full + i, a.lng ? 2 : 1); mbar_init(gt_empty + i, EPI / 32); }
         mbar_init(dk_full, 1);
         mbar_init(dk_empty, EPI / 32);
         mbar_init(mma_done, 2);
@@ -725,8 +813,8 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
                     last_qs[bs] = qs;
                     const int gs = qs % K_GSTG;
                     wait_bar(gt_empty + gs, ((qs / K_GSTG) & 1) ^ 1, abort_flag, err, 28);
-                    mbar_expect_tx(gt_full + gs, (uint32_t)(RP * (NKEY + HI) * 4));
-                    tma_load_2d(sGT + gs * RP * NKEY, &map_g, gt_full + gs, U.kt * NKEY, at.prow);
+                    mbar_expect_tx(gt_full + gs, (uint32_t)(RP * ((a.lng ? 0 : NKEY) + HI) * 4));
+                    if (!a.lng) tma_load_2d(sGT + gs * RP * NKEY, &map_g, gt_full + gs, U.kt * NKEY, at.prow);
                     tma_load_3d(sWT + gs * RP * HI, &map_w, gt_full + gs, 0, at.y, at.z);
                     qs++;
                 }
@@ -802,6 +890,52 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         }
         mma_commit_w(mma_done);
         drain_bar(mma_done, 0, err);
+    } else if (warp == 3 && a.lng) {
+        // ---------------------------------------------------------------- g-tile builder (long key axis)
+        // Per unit: the slot range [lo, hi) of the unit's key tile in each of its rows, from the tile-offset rows;
+        // then per row pair, into the pair's g/w slot: half-warp r zeroes row r's 128 keys and places the g of its
+        // slots lo .. hi - 1 (keys outside the tile are never placed).
+        const int half = lane >> 4, hl = lane & 15;
+        const int K = g.K;
+        int *sRng = reinterpret_cast<int *>(smem + K_OFF_RNG);  // [CH][2]
+        int pc = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit U = decode_unit(a, u);
+            if (U.npairs == 0) continue;
+            const int nrow = U.s_hi - U.s_lo;
+            __syncwarp();
+            for (int r = lane; r < nrow; r += 32) {
+                const int *o = a.toff + row_of(g, U.sg.b, U.s_lo + r) * (long long)(a.NT + 1);
+                int lo = __ldg(o + U.kt), hi = __ldg(o + U.kt + 1);
+                lo = lo < 0 ? 0 : (lo > K ? K : lo);
+                hi = hi < lo ? lo : (hi > K ? K : hi);
+                sRng[2 * r] = lo;
+                sRng[2 * r + 1] = hi;
+            }
+            __syncwarp();
+            const long long k0 = U.sg.gid0 + (long long)U.kt * NKEY;
+            for (int pi = 0; pi < U.npairs; pi++, pc++) {
+                const int gs = pc % K_GSTG;
+                wait_bar(gt_empty + gs, ((pc / K_GSTG) & 1) ^ 1, abort_flag, err, 33);
+                float *dst = sGT + gs * RP * NKEY + half * NKEY;
+                reinterpret_cast<float4 *>(dst)[2 * hl] = make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(dst)[2 * hl + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                __syncwarp();
+                const int r = pi * RP + half;
+                if (r < nrow) {
+                    const long long row = row_of(g, U.sg.b, U.s_lo + r);
+                    const int32_t *rid = a.ids + row * K;
+                    const float *rg = a.gslot + row * K;
+                    const int hi = sRng[2 * r + 1];
+                    for (int sl = sRng[2 * r] + hl; sl < hi; sl += 16) {
+                        const long long j = (long long)__ldg(rid + sl) - k0;
+                        if (j >= 0 && j < NKEY) dst[j] = __ldg(rg + sl);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gt_full + gs);
+            }
+        }
     } else if (warp >= 4) {
         // ---------------------------------------------------------------- epilogue (16 warps)
         // Lane = key (quad * 32 + lane).  Warp sub = (warp - 4) / 4 of a quadrant owns X columns [32 sub, 32 sub +
@@ -898,6 +1032,36 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// Long key axis: toff[r][b] = the first slot of row r whose key (id minus the row's first key) lies at or above
+// 128 b, b = 0 .. NT (the slots hold ascending valid ids, then -1 pads; a pad or an invalid id counts as past the
+// last tile, and a virtual slot K closes the remaining boundaries).  One warp per row.
+__global__ void tile_offsets_kernel(Geo g, const int32_t *__restrict__ ids, int *__restrict__ toff, int NT)
+{
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < g.rows; r += nwarps) {
+        const Row R = decode_row(g, r);
+        const long long gid0 = key_gid(g, R, 0);
+        int *o = toff + r * (long long)(NT + 1);
+        const int32_t *rid = ids + r * (long long)g.K;
+        int prev = -1;  // tile of the slot before this chunk
+        for (int s0 = 0; s0 <= g.K; s0 += 32) {
+            const int sl = s0 + lane;
+            int ts = NT;
+            if (sl < g.K) {
+                const int32_t id = __ldg(rid + sl);
+                const long long j = (long long)id - gid0;
+                if (id >= 0 && j >= 0 && j < R.v) ts = (int)(j >> 7) < NT ? (int)(j >> 7) : NT;
+            }
+            int tp = __shfl_up_sync(0xffffffffu, ts, 1);
+            if (lane == 0) tp = prev;
+            if (sl <= g.K)
+                for (int b = tp + 1; b <= ts; b++) o[b] = sl;
+            prev = __shfl_sync(0xffffffffu, ts, 31);
+        }
+    }
+}
+
 // THD: row-pair items and key-owner units per segment
 __global__ void build_bwd_offsets_kernel(Geo g, int *cu_g, int *cu_u)
 {
@@ -927,9 +1091,12 @@ bool tc_bwd_supported(const Geo &g, bool bf16)
 {
     const char *f = getenv("CSA_FORCE_GENERIC");
     if (f != nullptr && f[0] == '1') return false;
-    return bf16 && g.HI == bwd::HI && g.DI == bwd::DI && g.NC >= 1 && g.NC <= bwd::NCMAX && g.K >= 1 &&
-           g.rows > 0 && g.key_rows > 0;
+    // long key axes take the sparse loss (g by slot, assembled from the ascending ids)
+    return bf16 && g.HI == bwd::HI && g.DI == bwd::DI && g.NC >= 1 && (g.NC <= bwd::NCMAX || g.sparse) &&
+           g.K >= 1 && g.rows > 0 && g.key_rows > 0;
 }
+
+bool tc_bwd_long(const Geo &g) { return g.NC > bwd::NCMAX; }
 
 int tc_bwd_tiles(const Geo &g) { return (g.NC + bwd::NKEY - 1) / bwd::NKEY; }
 
@@ -943,6 +1110,7 @@ static size_t bwd_offsets_bytes(const Geo &g)
 
 size_t tc_bwd_workspace_bytes(const Geo &g)
 {
+    if (tc_bwd_long(g)) return bwd_offsets_bytes(g) + sizeof(int) * (size_t)g.rows * (size_t)(tc_bwd_tiles(g) + 1);
     return bwd_offsets_bytes(g) + sizeof(float) * (size_t)g.rows * (size_t)tc_bwd_ncp(g);
 }
 
@@ -952,9 +1120,11 @@ float *tc_bwd_gd(const Geo &g, void *ws)
 }
 
 cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
-                          __nv_bfloat16 *dq, float *dw, float *dk_acc, void *ws, cudaStream_t st)
+                          __nv_bfloat16 *dq, float *dw, float *dk_acc, void *ws, const int32_t *ids,
+                          const float *gslot, cudaStream_t st)
 {
     using namespace bwd;
+    const bool lng = tc_bwd_long(g);
     // Pair maps: a row pair of q_idx (both K-halves: [half][row][head][64 d] in shared memory) and of w in one
     // copy; a k tile (both K-halves: [half][key][64 d]) in one copy; g rows by position, two rows x 128 keys.
     const bool sb = g.layout == CSA_SBHD;
@@ -972,8 +1142,9 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
     const cuuint64_t gstr[1] = {(cuuint64_t)tc_bwd_ncp(g) * 4};
     const cuuint32_t gbox[2] = {NKEY, RP};
     CUtensorMap mq, mk, mg, mw;
-    bool ok = tc_encode_bf16(&mq, q_idx, 5, qd, qs, qb) && tc_encode_f32(&mg, tc_bwd_gd(g, ws), 2, gdim, gstr, gbox) &&
-              tc_encode_f32(&mw, w, 3, wd, ws_, wb);
+    bool ok = tc_encode_bf16(&mq, q_idx, 5, qd, qs, qb) && tc_encode_f32(&mw, w, 3, wd, ws_, wb);
+    if (lng) mg = mw;  // no by-key g rows: the map is never used
+    else ok = ok && tc_encode_f32(&mg, tc_bwd_gd(g, ws), 2, gdim, gstr, gbox);
     if (sb) {
         const cuuint64_t kd[4] = {64, (cuuint64_t)g.B, (cuuint64_t)g.nc, 2};
         const cuuint64_t ks[3] = {(cuuint64_t)DI * 2, (cuuint64_t)g.B * DI * 2, 128};
@@ -987,13 +1158,18 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
     }
     if (!ok) return cudaErrorInvalidValue;
     const int NT = tc_bwd_tiles(g);
-    Args a;
+    Args a = {};  // every field set below; zero first so none is ever left unset
     a.g = g;
     a.dq = dq;
     a.dw = dw;
     a.dk_acc = dk_acc;
     a.cu_g = a.cu_u = nullptr;
     a.total_items = a.total_units = a.units_per_seq = 0;
+    a.lng = lng;
+    a.gslot = gslot;
+    a.ids = ids;
+    a.NT = NT;
+    a.toff = lng ? reinterpret_cast<const int *>(tc_bwd_gd(g, ws)) : nullptr;
     int upper_items, upper_units;
     if (g.layout == CSA_THD) {
         int *cu_g = static_cast<int *>(ws);
@@ -1020,6 +1196,14 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K_SMEM);
     if (e != cudaSuccess) return e;
+    if (lng) {
+        const long long blocks = ((long long)g.rows + 7) / 8;
+        tile_offsets_kernel<<<(int)(blocks < sms * 16 ? blocks : sms * 16), 256, 0, st>>>(
+            g, ids, const_cast<int *>(a.toff), NT);
+        note_launches(1);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const int g1 = upper_items < sms ? (upper_items > 0 ? upper_items : 1) : sms;
     dq_dw_tc_kernel<<<g1, R_THREADS, R_SMEM, st>>>(mq, mk, mg, mw, a);
     note_launches(1);

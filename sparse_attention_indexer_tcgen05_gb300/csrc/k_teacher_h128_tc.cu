@@ -1,0 +1,633 @@
+// k_teacher_h128_tc.cu -- the full-CSA teacher for 128 main-attention heads on the 5th-generation tensor cores
+// (tcgen05 + TMEM), with the selected compressed keys gathered from L2.
+//
+// For query row t and head h ("[Bug] DSV4 unfused CSA indexer loss ..." (Megatron-LM issue #5776): "Paper
+// reference" equations for Z_h and t_j; sec. 3, one denominator over the sliding window, the selected compressed
+// keys and the sink; the proposal comment's factored form):
+//   l_h = log(exp(a_h) + sum_{j in C} exp(c_hj) + sum_{r in W} exp(w_hr)),  c = sigma q.kv_c, w = sigma q.kv
+//   T_j = sum_h exp(c_hj - l_h),   t_j = T_j / max(sum_{k in C} T_k, 1e-10)
+//
+// Mapping (bf16, H = 128, D = 64 .. 512 in steps of 64).  A work item is one query row: its 128 heads fill the
+// MMA's M = 128 lanes.  The row's q is the A operand and lives in TMEM (D / 2 columns, at most 256), so shared
+// memory holds only key tiles: D[h, key] = q[h] . key with N = 128 keys per tile (two 128-column fp32
+// accumulators next to q), K = D in 64-wide K-blocks, one 16 KB shared-memory stage per K-block.
+//   * one ring of twelve 16 KB stages carries, in order, each row's q, its window tiles and its compressed
+//     tiles (both passes); q, the window's original-KV rows and (dense loss) the contiguous compressed keys come
+//     by TMA tile loads;
+//   * the selected compressed keys (sparse loss) are gathered by four producer warps with 16-byte cp.async
+//     copies, each written to its place in the 128-byte-swizzled K-major tile.  (TMA's gather4 moves 512 bytes
+//     per instruction and measured about a tenth of the tile-load rate from L2, too slow for 2048 keys of 1 KB
+//     per row.)
+//   pass 1: window tiles + compressed tiles -> per-head running sum against a reference maximum, then l_h with
+//           the sink (or a given sink-and-window log-sum-exp);
+//   pass 2: compressed tiles again -> exp(c - l_h) summed over the 128 heads into shared per-slot T;
+//   the helper warp then L1-normalises the row and writes it out.
+// Between rows the epilogue warps copy the next row's q from its ring stages into TMEM once the current row's
+// last MMAs have completed (the accumulators are double-buffered, the q columns are not).
+// Roles: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2..9 epilogue (two per TMEM lane quadrant), warp 10
+// per-row helper, warps 11..14 cp.async producers.  Waits are bounded as in the other tensor-core kernels.
+#include "csa_tc.cuh"
+#include "tc_ptx.cuh"
+
+#include <stdlib.h>
+
+namespace csa {
+
+static __device__ int g_teacher_h128_error = 0;
+
+cudaError_t teacher_h128_read_clear_error(int *flag)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flag, g_teacher_h128_error, sizeof(int));
+    if (e != cudaSuccess || *flag == 0) return e;
+    int zero = 0;
+    return cudaMemcpyToSymbol(g_teacher_h128_error, &zero, sizeof(int));
+}
+
+namespace tw {
+
+using namespace ptx;
+
+constexpr int H = 128, NK = 128;
+constexpr int MAXKB = 8;                        // D <= 512
+constexpr int STG = NK * 64 * 2;                // 16 KB: one K-block of a 128-key tile (or of the row's q)
+constexpr int NSTG = 12;                        // ring stages
+constexpr int TWMAX = 2048;                     // teacher row width held in shared memory
+constexpr int THREADS = 480;                    // 15 warps
+constexpr int EPI = 256;                        // warps 2..9
+constexpr int EPI_WARP0 = 2, HELPER_WARP = 10, PROD_WARP0 = 11, NPROD = 128;
+constexpr int DEPTH = 6;                        // cp.async stages a producer thread keeps in flight (< NSTG)
+constexpr uint32_t TMEM_COLS = 512;             // q (<= 256 columns) + two 128-column accumulators
+constexpr uint32_t ACC0 = 256;
+constexpr uint32_t IDESC = idesc_bf16(128, NK, false, false);  // A (q, TMEM) and B (keys) K-major
+
+constexpr int OFF_RING = 0;                                     // NSTG stages
+constexpr int OFF_T = OFF_RING + NSTG * STG;                    // 192 KB: per-slot T, 2 item parities
+constexpr int OFF_MASK = OFF_T + 2 * TWMAX * 4;                 // slot-validity words, 2 x TWMAX / 32
+constexpr int OFF_PART = OFF_MASK + 2 * (TWMAX / 32) * 4;       // (m, s) partials: 2 parities x 2 halves x 128
+constexpr int OFF_MISC = OFF_PART + 2 * 2 * H * 8;
+constexpr int SMEM = OFF_MISC + 1024 + 1024;
+static_assert(SMEM <= 232448, "teacher shared memory exceeds the per-block limit");
+
+struct Args {
+    Geo g;
+    const float *sink;
+    const int32_t *ids;
+    const __nv_bfloat16 *kv_c;   // cp.async gather source
+    float *teacher;
+    int nkb;                     // D / 64
+};
+
+struct Item {
+    long long row;
+    int b, s, v;
+    long long gid0, key_y;
+    int wcount, p_lo;            // window positions [p_lo, p_lo + wcount)
+    int nw, ncs, nct;            // window tiles, compressed slots / keys, compressed tiles
+};
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// bits lo..hi (inclusive) of a 32-bit word, after clamping to 0..31; 0 when the range is empty
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi)
+{
+    if (lo < 0) lo = 0;
+    if (hi > 31) hi = 31;
+    if (hi < lo) return 0u;
+    const uint32_t upto = hi == 31 ? 0xffffffffu : ((1u << (hi + 1)) - 1u);
+    return upto & ~((1u << lo) - 1u);
+}
+
+// Items are the query rows in reverse memory order (the latest positions, with the most keys, first).
+__device__ Item decode(const Args &a, int i)
+{
+    const Geo &g = a.g;
+    Item it;
+    it.row = (long long)g.rows - 1 - i;
+    const Row R = decode_row(g, it.row);
+    it.b = R.b;
+    it.s = R.s;
+    it.v = R.v;
+    it.gid0 = key_gid(g, R, 0);
+    it.key_y = it.gid0;
+    it.wcount = (R.v > 0 && g.window > 0) ? (R.s + 1 < g.window ? R.s + 1 : g.window) : 0;
+    it.p_lo = R.s - it.wcount + 1;
+    it.nw = (it.wcount + NK - 1) / NK;
+    it.ncs = g.sparse ? (R.v < g.K ? R.v : g.K) : R.v;
+    it.nct = (it.ncs + NK - 1) / NK;
+    return it;
+}
+
+// tiles of a row: window, then compressed (pass 1), then compressed again (pass 2)
+__device__ __forceinline__ int ntiles(const Item &it) { return it.v > 0 ? it.nw + 2 * it.nct : 0; }
+// ring stages of a row: q, window tiles, both passes of the compressed tiles (one stage per K-block)
+__device__ __forceinline__ int row_stages(const Args &a, const Item &it) { return a.nkb * (1 + it.nw + 2 * it.nct); }
+// slot s of the row holds a usable key: a valid id of the row's segment within its visible range
+__device__ __forceinline__ long long slot_key_row(const Args &a, const Item &it, int s, bool &ok)
+{
+    const Geo &g = a.g;
+    ok = false;
+    if (s >= g.K) return 0;
+    const int32_t id = __ldg(a.ids + it.row * g.K + s);
+    const long long j = (long long)id - it.gid0;
+    if (id < 0 || j < 0 || j >= it.v) return 0;
+    ok = true;
+    return key_row(g, (long long)id);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
+                       const __grid_constant__ CUtensorMap map_kvc, Args a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *ring = smem + OFF_RING;
+    float *sT = reinterpret_cast<float *>(smem + OFF_T);             // [2][TWMAX]
+    uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + OFF_MASK); // [2][TWMAX / 32]
+    float2 *sPart = reinterpret_cast<float2 *>(smem + OFF_PART);     // [2][2][H]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
+    // full: one arrival per stage (a TMA load's expect_tx, or one producer thread once a gathered stage's copies are
+    // visible); empty: the MMA's commit, or the epilogue once it has copied a q stage
+    uint64_t *full = bars, *empty = bars + NSTG;
+    uint64_t *t_full = bars + 2 * NSTG, *t_empty = t_full + 2, *q_ready = t_full + 4, *mma_done = t_full + 5;
+    uint64_t *mask_full = t_full + 6, *t_done = t_full + 8;          // [item parity]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 512);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 520);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo &g = a.g;
+    const bool sbhd = g.layout == CSA_SBHD;
+    const int nkb = a.nkb;
+    int *err = &g_teacher_h128_error;
+    const int total = g.rows;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTG; i++) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(t_full + i, 1);
+            mbar_init(t_empty + i, EPI / 32);
+            mbar_init(mask_full + i, 1);
+            mbar_init(t_done + i, EPI / 32);
+        }
+        mbar_init(q_ready, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        init_fence();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ------------------------------------------------ TMA producer
+            // walks every stage of the stream, loading q, window and dense-loss tiles and skipping gathered ones;
+            // tma_slot[st] remembers whether a slot's last stage was one of this thread's loads (to drain it)
+            int x = 0;
+            bool tma_slot[NSTG];
+            for (int st = 0; st < NSTG; st++) tma_slot[st] = false;
+            auto stage = [&]() -> unsigned char * {
+                const int st = x % NSTG;
+                wait_bar(empty + st, ((x / NSTG) & 1) ^ 1, abort_flag, err, 61);
+                mbar_expect_tx(full + st, STG);
+                tma_slot[st] = true;
+                return ring + st * STG;
+            };
+            for (int i = blockIdx.x; i < total; i += gridDim.x) {
+                const Item it = decode(a, i);
+                if (ntiles(it) == 0) continue;
+                for (int kb = 0; kb < nkb; kb++, x++)
+                    tma_load_3d(stage(), &map_q, full + x % NSTG, kb * 64, 0, (int)it.row);
+                for (int t = 0; t < it.nw; t++) {
+                    const int p = it.p_lo + t * NK;
+                    for (int kb = 0; kb < nkb; kb++, x++) {
+                        unsigned char *dst = stage();
+                        if (sbhd) tma_load_3d(dst, &map_kv, full + x % NSTG, kb * 64, it.b, p);
+                        else tma_load_2d(dst, &map_kv, full + x % NSTG, kb * 64, (int)(it.row - it.s + p));
+                    }
+                }
+                for (int pass = 0; pass < 2; pass++)
+                    for (int t = 0; t < it.nct; t++)
+                        for (int kb = 0; kb < nkb; kb++, x++) {
+                            if (g.sparse) {  // gathered by the cp.async producers
+                                tma_slot[x % NSTG] = false;
+                                continue;
+                            }
+                            unsigned char *dst = stage();
+                            if (sbhd) tma_load_3d(dst, &map_kvc, full + x % NSTG, kb * 64, it.b, t * NK);
+                            else tma_load_2d(dst, &map_kvc, full + x % NSTG, kb * 64, (int)(it.key_y + t * NK));
+                        }
+            }
+            // our own copies must land before the CTA exits (a slot whose last stage was gathered held an earlier
+            // load of ours only if that load was consumed, i.e. had landed)
+            for (int y = x - NSTG < 0 ? 0 : x - NSTG; y < x; y++)
+                if (tma_slot[y % NSTG]) drain_bar(full + y % NSTG, (y / NSTG) & 1, err);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------------------- MMA issue (whole warp)
+        // Rows are decoded lane-parallel (lane l: the CTA's row k + l) and the loop reads the tile count of row k
+        // by a shuffle.  Per row: skip its q stages (the epilogue copies them into TMEM), wait for q in
+        // TMEM, then per tile and K-block four MMAs of K = 16 with A = q's columns of that K-block.
+        int x = 0, tc = 0, rc = 0, k = 0, nt_lane = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
+            if ((k & 31) == 0) {
+                const int il = i + lane * (int)gridDim.x;
+                nt_lane = il < total ? ntiles(decode(a, il)) : 0;
+            }
+            const int nt = __shfl_sync(0xffffffffu, nt_lane, k & 31);
+            if (nt == 0) continue;
+            x += nkb;
+            wait_bar(q_ready, rc & 1, abort_flag, err, 62);
+            fence_after();
+            for (int tt = 0; tt < nt; tt++) {
+                const int tb = tc & 1;
+                wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, err, 63);
+                fence_after();
+                const uint32_t d = tmem + ACC0 + (uint32_t)(tb * NK);
+                for (int kb = 0; kb < nkb; kb++, x++) {
+                    const int st = x % NSTG;
+                    wait_bar(full + st, (x / NSTG) & 1, abort_flag, err, 64);
+                    fence_after();
+                    const unsigned char *pb = ring + st * STG;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; k4++)
+                        mma_bf16_ts_w(d, tmem + (uint32_t)(kb * 32 + k4 * 8), desc_kmajor(pb + k4 * 32), IDESC,
+                                      (kb | k4) ? 1u : 0u);
+                    mma_commit_w(empty + st);
+                }
+                mma_commit_w(t_full + tb);
+                tc++;
+            }
+            rc++;
+        }
+        mma_commit_w(mma_done);
+        drain_bar(mma_done, 0, err);
+    } else if (warp < HELPER_WARP) {
+        // ---------------------------------------------------------------- epilogue (8 warps)
+        // Two warps per TMEM lane quadrant (warp % 4); warp half cq = (warp - 2) / 4 reads the 32-column chunks at
+        // columns 32 cq and 32 cq + 64 of every tile, and copies q's K-blocks kb = cq (mod 2) into TMEM.
+        const int quad = warp & 3, cq = (warp - EPI_WARP0) >> 2;
+        const int h = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const float s2 = g.scale * 1.4426950408889634f;  // logits in log2 units: exp(c) = 2^(x * sigma * log2 e)
+        const bool s2_pos = s2 > 0.f;
+        auto col_of = [&](int c) { return cq * 32 + c * 64; };
+        // copy the q of the row whose stages start at x0 into TMEM, release those stages, signal the MMA
+        auto copy_q = [&](int x0) {
+            for (int kb = cq; kb < nkb; kb += 2) {
+                const int x = x0 + kb, st = x % NSTG;
+                wait_bar(full + st, (x / NSTG) & 1, abort_flag, err, 66);
+                const unsigned char *src = ring + st * STG;
+                uint32_t v[32];
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const uint4 q4 = *reinterpret_cast<const uint4 *>(src + sw128_off((uint32_t)h, (uint32_t)c));
+                    v[4 * c] = q4.x;
+                    v[4 * c + 1] = q4.y;
+                    v[4 * c + 2] = q4.z;
+                    v[4 * c + 3] = q4.w;
+                }
+                tmem_st32(tmem + lane_off + (uint32_t)(kb * 32), v);
+            }
+            fence_before();
+            named_bar(2, EPI);
+            if (threadIdx.x == EPI_WARP0 * 32) {
+                for (int kb = 0; kb < nkb; kb++) mbar_arrive(empty + (x0 + kb) % NSTG);
+                mbar_arrive(q_ready);
+            }
+        };
+        int tc = 0, ic = 0, x = 0;  // x: first stage of the current row
+        bool first = true;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
+            const Item it = decode(a, i);
+            const int nt = ntiles(it);
+            const int ib = ic & 1;
+            float *sTb = sT + ib * TWMAX;
+            const uint32_t *sMaskb = sMask + ib * (TWMAX / 32);
+            wait_bar(mask_full + ib, (ic >> 1) & 1, abort_flag, err, 67);
+            if (nt > 0) {
+                if (first) {
+                    copy_q(x);
+                    first = false;
+                }
+                const int x_next = x + row_stages(a, it);
+                float m = -INFINITY, ssum = 0.f, ell = 0.f;
+                float ell4[4] = {0.f, 0.f, 0.f, 0.f};  // l_h of heads g, g + 8, g + 16, g + 24 of the quadrant
+                for (int tt = 0; tt < nt; tt++) {
+                    const int tb = tc & 1;
+                    wait_bar(t_full + tb, (tc >> 1) & 1, abort_flag, err, 68);
+                    fence_after();
+                    if (tt == nt - 1) {
+                        // every MMA of this row has completed: the next row's q may replace it in TMEM
+                        for (int j = i + gridDim.x; j < total; j += gridDim.x)
+                            if (ntiles(decode(a, j)) > 0) {
+                                copy_q(x_next);
+                                break;
+                            }
+                    }
+                    const bool win = tt < it.nw;
+                    const bool pass2 = tt >= it.nw + it.nct;
+                    const int t = win ? tt : (tt - it.nw) % it.nct;
+                    if (pass2 && tt == it.nw + it.nct) {
+                        // l_h (log2 units) from the two column halves, combined in a fixed order, and the sink
+                        float2 *pp = sPart + ib * 2 * H;
+                        pp[cq * H + h] = make_float2(m, ssum);
+                        named_bar(1, EPI);
+                        const float2 p0 = pp[h], p1 = pp[H + h];
+                        const float ah = g.lse_nc != nullptr ? __ldg(g.lse_nc + it.row * H + h) * 1.4426950408889634f
+                                                             : (g.no_sink ? -INFINITY : __ldg(a.sink + h) * 1.4426950408889634f);
+                        const float mm = fmaxf(fmaxf(p0.x, p1.x), ah);
+                        float S = 0.f;
+                        if (mm != -INFINITY) {
+                            if (p0.x != -INFINITY) S += p0.y * ex2(p0.x - mm);
+                            if (p1.x != -INFINITY) S += p1.y * ex2(p1.x - mm);
+                            if (ah != -INFINITY) S += ex2(ah - mm);
+                        }
+                        ell = mm + lg2(S);
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; k4++) ell4[k4] = __shfl_sync(0xffffffffu, ell, (lane >> 2) + 8 * k4);
+                    }
+                    uint32_t mw[2];
+#pragma unroll
+                    for (int c = 0; c < 2; c++) {
+                        const int c0 = t * NK + col_of(c);
+                        if (win) mw[c] = range_bits(0, it.wcount - 1 - c0);
+                        else if (g.sparse) mw[c] = c0 < it.ncs ? sMaskb[c0 >> 5] & range_bits(0, it.ncs - 1 - c0) : 0u;
+                        else mw[c] = range_bits(0, it.ncs - 1 - c0);
+                    }
+                    if ((mw[0] | mw[1]) != 0u) {
+                        if (!pass2) {
+                            // running sum against a reference max, one 32-column chunk at a time; a chunk is re-based
+                            // on its own max only when its sum leaves the safe range
+#pragma unroll 1
+                            for (int c = 0; c < 2; c++) {
+                                if (mw[c] == 0u) continue;
+                                float x[32];
+                                tmem_ld32(tmem + lane_off + ACC0 + (uint32_t)(tb * NK + col_of(c)), x);
+                                if (s2_pos) {
+                                    if (mw[c] != 0xffffffffu) {
+#pragma unroll
+                                        for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? x[q] : -INFINITY;
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? x[q] * s2 : -INFINITY;
+                                }
+                                const float sc = s2_pos ? s2 : 1.f;
+                                auto chunk_max = [&]() -> float {
+                                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                                    for (int q = 0; q < 32; q++) mx[q & 3] = fmaxf(mx[q & 3], x[q]);
+                                    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+                                };
+                                auto chunk_sum = [&]() -> float {
+                                    float2 sm[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                                    for (int q2 = 0; q2 < 16; q2++) {
+                                        const float2 arg = fma2(make_float2(x[2 * q2], x[2 * q2 + 1]), make_float2(sc, sc),
+                                                                make_float2(-m, -m));
+                                        sm[q2 & 1] = add2(sm[q2 & 1], make_float2(ex2(arg.x), ex2(arg.y)));
+                                    }
+                                    return (sm[0].x + sm[0].y) + (sm[1].x + sm[1].y);
+                                };
+                                if (m == -INFINITY) m = chunk_max();
+                                float cs = chunk_sum();
+                                if (!(cs <= 0x1p64f)) {
+                                    const float cm = chunk_max();
+                                    if (cm > m) {
+                                        ssum *= ex2(m - cm);
+                                        m = cm;
+                                    }
+                                    cs = chunk_sum();
+                                }
+                                ssum += cs;
+                            }
+                        } else {
+                            // pass 2 in the 16-lane shape: a thread holds heads g, g + 8, g + 16, g + 24 (g = lane / 4)
+                            // of columns 8 p + 2 u + e (u = lane % 4); four heads are added in registers and the eight
+                            // threads of a column set reduce-scatter over g
+                            const int u4 = lane & 3, g8 = lane >> 2;
+#pragma unroll 1
+                            for (int c = 0; c < 2; c++) {
+                                if (mw[c] == 0u) continue;
+                                const uint32_t ca = tmem + lane_off + ACC0 + (uint32_t)(tb * NK + col_of(c));
+                                uint32_t ra[16], rb[16];
+                                tmem_ld16x256_x4(ca, ra);
+                                tmem_ld16x256_x4(ca + (16u << 16), rb);
+                                const bool full = mw[c] == 0xffffffffu;
+                                float s8[8];
+#pragma unroll
+                                for (int p4 = 0; p4 < 4; p4++) {
+                                    const int col = 8 * p4 + 2 * u4;
+                                    const bool b0 = full || ((mw[c] >> col) & 1u), b1 = full || ((mw[c] >> (col + 1)) & 1u);
+                                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                                    for (int k4 = 0; k4 < 4; k4++) {
+                                        const uint32_t *r = k4 < 2 ? ra : rb;
+                                        const int o = 4 * p4 + 2 * (k4 & 1);
+                                        const float2 arg = fma2(make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])),
+                                                                make_float2(s2, s2), make_float2(-ell4[k4], -ell4[k4]));
+                                        const float e0 = ex2(arg.x), e1 = ex2(arg.y);
+                                        acc = add2(acc, make_float2(b0 ? e0 : 0.f, b1 ? e1 : 0.f));
+                                    }
+                                    s8[2 * p4] = acc.x;
+                                    s8[2 * p4 + 1] = acc.y;
+                                }
+#pragma unroll
+                                for (int hv = 4; hv >= 1; hv >>= 1) {
+                                    const int off = hv * 4;
+                                    const bool up = (lane & off) != 0;
+#pragma unroll
+                                    for (int q = 0; q < hv; q++) {
+                                        const float send = up ? s8[q] : s8[q + hv];
+                                        const float keep = up ? s8[q + hv] : s8[q];
+                                        s8[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                    }
+                                }
+                                const int j = t * NK + col_of(c) + 8 * (g8 >> 1) + 2 * u4 + (g8 & 1);
+                                if (j < TWMAX && s8[0] != 0.f) atomicAdd(sTb + j, s8[0]);
+                            }
+                        }
+                    }
+                    fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(t_empty + tb);
+                    tc++;
+                }
+                x = x_next;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(t_done + ib);
+        }
+    } else if (warp == HELPER_WARP) {
+        // ---------------------------------------------------------------- per-row helper
+        // For row ic (buffer ic & 1): zero its T row, build its slot-validity words (sparse loss), signal
+        // mask_full; then, once the epilogue has summed row ic - 1 into the other buffer (t_done), L1-normalise
+        // that row and write it out.  Buffer reuse is ordered by this warp's program order.
+        auto writeout = [&](const Item &it, int icw) {
+            const int ib = icw & 1;
+            wait_bar(t_done + ib, (icw >> 1) & 1, abort_flag, err, 69);
+            const float *tr = sT + ib * TWMAX;
+            float part = 0.f;
+            for (int j = lane; j < it.ncs; j += 32) part += tr[j];
+            const float inv = 1.f / fmaxf(warp_sum(part), 1e-10f);
+            float *trow = a.teacher + it.row * g.TW;
+            for (int j = lane; j < g.TW; j += 32) trow[j] = j < it.ncs ? tr[j] * inv : 0.f;
+        };
+        Item prev;
+        int ic = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ic++) {
+            const Item it = decode(a, i);
+            const int ib = ic & 1;
+            float4 *tz = reinterpret_cast<float4 *>(sT + ib * TWMAX);
+            const int nz = (it.ncs + 3) / 4;
+            for (int x = lane; x < nz; x += 32) tz[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (g.sparse && ntiles(it) > 0) {
+                uint32_t *mk = sMask + ib * (TWMAX / 32);
+                for (int w0 = 0; w0 < it.ncs; w0 += 32) {
+                    bool ok;
+                    slot_key_row(a, it, w0 + lane, ok);
+                    const unsigned bits = __ballot_sync(0xffffffffu, ok && w0 + lane < it.ncs);
+                    if (lane == 0) mk[w0 >> 5] = bits;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mask_full + ib);
+            if (ic > 0) writeout(prev, ic - 1);
+            prev = it;
+        }
+        if (ic > 0) writeout(prev, ic - 1);
+    } else if (warp >= PROD_WARP0 && g.sparse) {
+        // ---------------------------------------------------------------- gather producers
+        // Thread n copies key slot n of every gathered tile: per K-block, its 128-byte row in eight 16-byte cp.async
+        // copies, each to its chunk of the 128-byte-swizzled row n.  A stage is handed to the MMA once every
+        // producer thread's copies for it have completed and been made visible to the async proxy (cp.async.wait,
+        // proxy fence, then the four warps meet on a named barrier and one thread arrives).  Each thread keeps
+        // DEPTH stages in flight within a row's run of gathered stages, so it signals stage x - DEPTH after issuing
+        // stage x, and flushes at the run's end (the next run starts behind the next row's q and window stages).
+        const int n = threadIdx.x - PROD_WARP0 * 32;
+        const int D = g.D;
+        int x = 0;
+        auto signal = [&](int y0, int y1) {  // stages [y0, y1): this thread's copies are complete and fenced
+            fence_proxy_async();
+            named_bar(3, NPROD);
+            if (n == 0)
+                for (int y = y0; y < y1; y++) mbar_arrive(full + y % NSTG);
+        };
+        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+            const Item it = decode(a, i);
+            if (ntiles(it) == 0) continue;
+            x += nkb * (1 + it.nw);  // q and window stages (TMA)
+            const int run0 = x;
+            for (int pass = 0; pass < 2; pass++)
+                for (int t = 0; t < it.nct; t++) {
+                    bool ok;
+                    const long long kr = slot_key_row(a, it, t * NK + n, ok);
+                    const __nv_bfloat16 *src = a.kv_c + kr * D;
+                    for (int kb = 0; kb < nkb; kb++, x++) {
+                        const int st = x % NSTG;
+                        wait_bar(empty + st, ((x / NSTG) & 1) ^ 1, abort_flag, err, 70);
+                        unsigned char *dst = ring + st * STG + n * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; c++) cp_async16(dst + ((c ^ (n & 7)) << 4), src + kb * 64 + c * 8);
+                        cp_async_commit();
+                        if (x - run0 >= DEPTH) {
+                            cp_async_wait<DEPTH>();
+                            signal(x - DEPTH, x - DEPTH + 1);
+                        }
+                    }
+                }
+            cp_async_wait<0>();
+            signal(x - DEPTH > run0 ? x - DEPTH : run0, x);
+        }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace tw
+
+// ------------------------------------------------------------------ host side
+
+bool tc_teacher_h128_supported(const Geo &g, bool bf16)
+{
+    const char *f = getenv("CSA_FORCE_GENERIC");
+    if (f != nullptr && f[0] == '1') return false;
+    return bf16 && g.H == tw::H && g.D % 64 == 0 && g.D / 64 >= 1 && g.D / 64 <= tw::MAXKB && g.NC >= 1 &&
+           g.K >= 1 && g.TW <= tw::TWMAX && g.rows > 0 && g.key_rows > 0;
+}
+
+cudaError_t launch_teacher_h128_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *kv,
+                                   const __nv_bfloat16 *kv_c, const float *sink, const int32_t *ids, float *teacher,
+                                   cudaStream_t st)
+{
+    using namespace tw;
+    CUtensorMap mq, mkv, mkc;
+    // q as [rows][H][D] with a 64 x 128 x 1 box (one K-block of a row's 128 heads)
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)g.D, (cuuint64_t)g.H, (cuuint64_t)g.rows};
+        const cuuint64_t strides[2] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.H * g.D * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)g.H, 1};
+        if (!tc_encode_bf16(&mq, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    // kv_c as tiles of 128 keys (dense loss); kv as tiles of 128 positions (window)
+    if (g.layout == CSA_SBHD) {
+        const cuuint64_t dkc[3] = {(cuuint64_t)g.D, (cuuint64_t)g.B, (cuuint64_t)g.nc};
+        const cuuint64_t skc[2] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.B * g.D * 2};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)NK};
+        if (!tc_encode_bf16(&mkc, kv_c, 3, dkc, skc, box)) return cudaErrorInvalidValue;
+    } else {
+        const cuuint64_t dkc[2] = {(cuuint64_t)g.D, (cuuint64_t)g.key_rows};
+        const cuuint64_t s1[1] = {(cuuint64_t)g.D * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)NK};
+        if (!tc_encode_bf16(&mkc, kv_c, 2, dkc, s1, box)) return cudaErrorInvalidValue;
+    }
+    if (g.window == 0) {  // no window tile is ever loaded: the kv map is never used
+        mkv = mkc;
+    } else if (g.layout == CSA_SBHD) {
+        const cuuint64_t dkv[3] = {(cuuint64_t)g.D, (cuuint64_t)g.B, (cuuint64_t)g.S};
+        const cuuint64_t skv[2] = {(cuuint64_t)g.D * 2, (cuuint64_t)g.B * g.D * 2};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)NK};
+        if (!tc_encode_bf16(&mkv, kv, 3, dkv, skv, box)) return cudaErrorInvalidValue;
+    } else {
+        const cuuint64_t dkv[2] = {(cuuint64_t)g.D, (cuuint64_t)g.rows};
+        const cuuint64_t s1[1] = {(cuuint64_t)g.D * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)NK};
+        if (!tc_encode_bf16(&mkv, kv, 2, dkv, s1, box)) return cudaErrorInvalidValue;
+    }
+    Args a = {};  // every field set below; zero first so none is ever left unset
+    a.g = g;
+    a.sink = sink;
+    a.ids = ids;
+    a.kv_c = kv_c;
+    a.teacher = teacher;
+    a.nkb = g.D / 64;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(teacher_h128_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    const int grid = g.rows < sms ? g.rows : sms;
+    teacher_h128_tc_kernel<<<grid, THREADS, SMEM, st>>>(mq, mkv, mkc, a);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace csa

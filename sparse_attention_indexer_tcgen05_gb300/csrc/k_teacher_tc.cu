@@ -636,7 +636,7 @@ cudaError_t launch_teacher_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_b
         if (!tc_encode_bf16(&mkv, kv, 2, dkv, s1, box) || !tc_encode_bf16(&mkc, kv_c, 2, dkc, s1, box))
             return cudaErrorInvalidValue;
     }
-    Args a;
+    Args a = {};  // every field set below; zero first so none is ever left unset
     a.g = g;
     a.sink = sink;
     a.ids = ids;
