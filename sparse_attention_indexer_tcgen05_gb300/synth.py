@@ -8,10 +8,12 @@ sides read the same bytes.
 
 Recipe (one stream per tensor, so every tensor is reproducible on its own):
   * generator: numpy PCG64 seeded with SeedSequence([config_seed, tensor_id]);
-  * q, kv, kv_c, q_idx, k_idx ~ N(0, 1) / sqrt(own last dim);
+  * q, kv, kv_c, q_idx, k_idx ~ N(0, 1) / sqrt(own last dim) (q, kv, kv_c optionally ~ N(0, qk_std^2),
+    used with qk_std = 1 for a teacher-sensitivity input whose attention logits are of order one);
   * w ~ U(0, 1) (the indexer weights as passed, i.e. with the indexer softmax
     scale already folded in);
-  * sink ~ N(0, sink_std^2), one logit per main-attention head;
+  * sink ~ N(sink_mean, sink_std^2), one logit per main-attention head (sink_mean = 0 except for the
+    teacher-sensitivity input);
   * bf16 tensors are rounded from float32 on the host with round-to-nearest-even;
   * THD document lengths ~ U{lo..hi} drawn while the running total fits; the rest
     of the token budget is padding absorbed into the last segment.
@@ -57,6 +59,8 @@ class Config:
     seed: int = 0
     doc_len: tuple = (512, 4096)  # THD only: inclusive range of document lengths
     softmax_scale: Optional[float] = None  # default 1/sqrt(head_dim)
+    qk_std: Optional[float] = None  # std of q, kv and kv_c (default 1/sqrt(head_dim)); 1.0 gives logits of order one
+    sink_mean: float = 0.0
 
     @property
     def scale(self) -> float:
@@ -239,9 +243,10 @@ def generate(cfg: Config, skip=()) -> Inputs:
 
     q_idx = normal_tensor("q_idx", cq + (cfg.idx_heads, cfg.idx_dim), 1.0 / math.sqrt(cfg.idx_dim))
     k_idx = normal_tensor("k_idx", cc + (cfg.idx_dim,), 1.0 / math.sqrt(cfg.idx_dim))
-    q = normal_tensor("q", cq + (cfg.heads, cfg.head_dim), 1.0 / math.sqrt(cfg.head_dim))
-    kv = normal_tensor("kv", cq + (cfg.head_dim,), 1.0 / math.sqrt(cfg.head_dim))
-    kv_c = normal_tensor("kv_c", cc + (cfg.head_dim,), 1.0 / math.sqrt(cfg.head_dim))
+    main_std = cfg.qk_std if cfg.qk_std is not None else 1.0 / math.sqrt(cfg.head_dim)
+    q = normal_tensor("q", cq + (cfg.heads, cfg.head_dim), main_std)
+    kv = normal_tensor("kv", cq + (cfg.head_dim,), main_std)
+    kv_c = normal_tensor("kv_c", cc + (cfg.head_dim,), main_std)
     if "w" in skip:
         w = Tensor(np.zeros((0,), np.float32))
     else:
@@ -253,7 +258,8 @@ def generate(cfg: Config, skip=()) -> Inputs:
 
         _blocks(n, fill)
         w = Tensor(wv.reshape(cq + (cfg.idx_heads,)), lead=nlead)
-    sink = Tensor(_rng(cfg.seed, "sink").standard_normal(cfg.heads, dtype=np.float32) * np.float32(cfg.sink_std))
+    sink = Tensor(_rng(cfg.seed, "sink").standard_normal(cfg.heads, dtype=np.float32) * np.float32(cfg.sink_std)
+                  + np.float32(cfg.sink_mean))
 
     inp = Inputs(cfg, q_idx, w, k_idx, q, kv, kv_c, sink, cu, cur, max_len)
     if cfg.layout == "sbhd":

@@ -30,9 +30,10 @@ def gpu_step(d: workload.DeviceInputs, want_teacher=True):
     """The natural pipeline through the C ABI: fwd -> teacher -> bwd (teacher recomputed inside bwd)."""
     p = d.params
     ids, sel = B.csa_indexer_fwd(p, *d.indexer)
-    out = dict(ids=ids, sel=sel)
+    out = dict(ids=ids, sel=sel, fwd_path=B.csa_last_path())
     if want_teacher:
         out["teacher"] = B.csa_teacher(p, *d.teacher_side, ids)
+        out["teacher_path"] = B.csa_last_path()
     row_loss = torch.empty(p.rows, dtype=torch.float32, device=ids.device)
     loss, dq, dw, dk = B.csa_indexer_bwd(p, *d.indexer, *d.teacher_side, ids, sel, row_loss=row_loss)
     torch.cuda.synchronize()
@@ -202,8 +203,10 @@ def check_step(inp, d=None, rows=None, full_dk=True, report=None):
     e_dw = rel_l2(dw[same], ref["dw"][same])
     assert e_dq <= GRAD_TOL and e_dw <= GRAD_TOL, f"dq {e_dq} dw {e_dw}"
     out = dict(recall=recall, teacher_err=max(t_err, t_err2), dq_err=e_dq, dw_err=e_dw, rows=len(rws),
-               same_rows=int(same.sum()), path=B.csa_last_path(), bwd_path=gpu["bwd_path"],
-               _oracle_teacher=ref["teacher"], _gpu_teacher_oracle_ids=te_o)
+               same_rows=int(same.sum()), path=gpu["fwd_path"], fwd_path=gpu["fwd_path"],
+               teacher_path=gpu["teacher_path"], bwd_path=gpu["bwd_path"],
+               _oracle_teacher=ref["teacher"], _gpu_teacher_oracle_ids=te_o,
+               _oracle_loss_rows=ref["loss_rows"], _gpu_loss_rows=rl)
     dk = to_np(gpu["dk"]).reshape(-1, c.idx_dim)
     if rows is None:
         e_dk = rel_l2(dk, ref["dk"])
@@ -211,12 +214,39 @@ def check_step(inp, d=None, rows=None, full_dk=True, report=None):
         out["dk_err"] = e_dk
         out["loss_err"] = loss_err
     else:
-        # sum_s k_s . dK_s == sum_t sum_j q_tj . dQ_tj (both equal sum_t sum_s g_ts I_ts)
-        lhs = float((d.k_idx.float().reshape(-1, c.idx_dim) * gpu["dk"].float().reshape(-1, c.idx_dim)).double().sum())
-        rhs = float((d.q_idx.float() * gpu["dq"].float().reshape(d.q_idx.shape)).double().sum())
-        inv = abs(lhs - rhs) / max(abs(rhs), 1e-30)
-        assert inv <= GRAD_TOL, f"dk invariant {lhs} vs {rhs}"
-        out["dk_invariant_err"] = inv
+        out.update(check_sampled_dk(inp, d, P, rws, gpu["ids"]))
     if report is not None:
         report.update(out)
     return out
+
+
+def check_sampled_dk(inp, d, P, rws, ids_gpu):
+    """dK element by element on a row sample: the GPU step is run again with w zeroed on every row outside the
+    sample.  Those rows then score every key 0 and, since dK takes each row's contribution through w, add nothing
+    to dK (dK_s = sum_t sum_j g_ts w_tj 1[x_tjs > 0] q_tj), while the sampled rows keep their scores, ids, teacher
+    and gradient.  The oracle computes the sampled rows' dK from the same ids (the GPU's), with its own teacher and
+    float64 scores.  Also compares the sampled rows' summed loss."""
+    c = inp.cfg
+    p = d.params
+    keep = torch.zeros(p.rows, dtype=torch.bool, device=d.w.device)
+    keep[torch.from_numpy(np.asarray(rws, np.int64)).to(d.w.device)] = True
+    w_m = torch.where(keep.view((p.rows,) + (1,) * 1), d.w.reshape(p.rows, -1), torch.zeros((), device=d.w.device))
+    w_m = w_m.reshape(d.w.shape).contiguous()
+    dm = workload.DeviceInputs(p, d.q_idx, w_m, d.k_idx, d.q, d.kv, d.kv_c, d.sink, d.cu, d.cur)
+    ids_m, sel_m = B.csa_indexer_fwd(p, *dm.indexer)
+    rl = torch.empty(p.rows, dtype=torch.float32, device=ids_m.device)
+    _, _, _, dk_m = B.csa_indexer_bwd(p, *dm.indexer, *dm.teacher_side, ids_m, sel_m, row_loss=rl)
+    torch.cuda.synchronize()
+    B.csa_check_device_status()
+    ids_s = ids_m.cpu().numpy()[rws]
+    assert np.array_equal(ids_s, ids_gpu.cpu().numpy()[rws]), "masking other rows changed the sampled rows' ids"
+    qq = inp.q.rows_f32(rws)
+    te_s = P.teacher(qq, inp.kv.values, inp.kv_c.values, inp.sink.values, ids_s, rws, compact=True)
+    qi, ww = inp.q_idx.rows_f32(rws), inp.w.rows_f32(rws)
+    loss_o, lr_o, _, _, dk_o = P.loss_grads(qi, ww, inp.k_idx.values, ids_s, te_s, rws, want_dk=True, compact=True)
+    e_dk = rel_l2(to_np(dk_m).reshape(-1, c.idx_dim), dk_o)
+    assert e_dk <= GRAD_TOL, f"dk (sampled rows) {e_dk}"
+    loss_g = float(rl.cpu().numpy()[rws].astype(np.float64).sum()) * P.loss_factor
+    e_loss = abs(loss_g - loss_o) / max(abs(loss_o), 1e-30)
+    assert e_loss <= value_tol(c.dtype), f"sampled-row loss {loss_g} vs {loss_o}"
+    return dict(dk_err=e_dk, sampled_loss_err=e_loss)
