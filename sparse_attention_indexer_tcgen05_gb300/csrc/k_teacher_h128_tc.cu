@@ -12,20 +12,19 @@
 // memory holds only key tiles: D[h, key] = q[h] . key with N = 128 keys per tile (two 128-column fp32
 // accumulators next to q), K = D in 64-wide K-blocks, one 16 KB shared-memory stage per K-block.
 //   * one ring of twelve 16 KB stages carries, in order, each row's q, its window tiles and its compressed
-//     tiles (both passes); q, the window's original-KV rows and (dense loss) the contiguous compressed keys come
-//     by TMA tile loads;
-//   * the selected compressed keys (sparse loss) are gathered by four producer warps with 16-byte cp.async
-//     copies, each written to its place in the 128-byte-swizzled K-major tile.  (TMA's gather4 moves 512 bytes
-//     per instruction and measured about a tenth of the tile-load rate from L2, too slow for 2048 keys of 1 KB
-//     per row.)
+//     tiles (both passes), filled by one group of four producer warps: q, the window's original-KV rows and
+//     (dense loss) the contiguous compressed keys by TMA tile loads, the selected compressed keys (sparse loss)
+//     gathered with 16-byte cp.async copies, each written to its place in the 128-byte-swizzled K-major tile.
+//     (TMA's gather4 moves 512 bytes per instruction and measured about a tenth of the tile-load rate from L2,
+//     too slow for 2048 keys of 1 KB per row.)
 //   pass 1: window tiles + compressed tiles -> per-head running sum against a reference maximum, then l_h with
 //           the sink (or a given sink-and-window log-sum-exp);
 //   pass 2: compressed tiles again -> exp(c - l_h) summed over the 128 heads into shared per-slot T;
 //   the helper warp then L1-normalises the row and writes it out.
 // Between rows the epilogue warps copy the next row's q from its ring stages into TMEM once the current row's
 // last MMAs have completed (the accumulators are double-buffered, the q columns are not).
-// Roles: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2..9 epilogue (two per TMEM lane quadrant), warp 10
-// per-row helper, warps 11..14 cp.async producers.  Waits are bounded as in the other tensor-core kernels.
+// Roles: warp 1 TMEM + MMA issue, warps 2..9 epilogue (two per TMEM lane quadrant), warp 10 per-row helper,
+// warps 11..14 producers (warp 0 has no role).  Waits are bounded as in the other tensor-core kernels.
 #include "csa_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -155,7 +154,7 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
     uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + OFF_MASK); // [2][TWMAX / 32]
     float2 *sPart = reinterpret_cast<float2 *>(smem + OFF_PART);     // [2][2][H]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_MISC);
-    // full: one arrival per stage (a TMA load's expect_tx, or one producer thread once a gathered stage's copies are
+    // full: one arrival per stage (producer thread 0: a TMA load's expect_tx, or once a gathered stage's copies are
     // visible); empty: the MMA's commit, or the epilogue once it has copied a q stage
     uint64_t *full = bars, *empty = bars + NSTG;
     uint64_t *t_full = bars + 2 * NSTG, *t_empty = t_full + 2, *q_ready = t_full + 4, *mma_done = t_full + 5;
@@ -192,51 +191,7 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
     fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) {  // ------------------------------------------------ TMA producer
-            // walks every stage of the stream, loading q, window and dense-loss tiles and skipping gathered ones;
-            // tma_slot[st] remembers whether a slot's last stage was one of this thread's loads (to drain it)
-            int x = 0;
-            bool tma_slot[NSTG];
-            for (int st = 0; st < NSTG; st++) tma_slot[st] = false;
-            auto stage = [&]() -> unsigned char * {
-                const int st = x % NSTG;
-                wait_bar(empty + st, ((x / NSTG) & 1) ^ 1, abort_flag, err, 61);
-                mbar_expect_tx(full + st, STG);
-                tma_slot[st] = true;
-                return ring + st * STG;
-            };
-            for (int i = blockIdx.x; i < total; i += gridDim.x) {
-                const Item it = decode(a, i);
-                if (ntiles(it) == 0) continue;
-                for (int kb = 0; kb < nkb; kb++, x++)
-                    tma_load_3d(stage(), &map_q, full + x % NSTG, kb * 64, 0, (int)it.row);
-                for (int t = 0; t < it.nw; t++) {
-                    const int p = it.p_lo + t * NK;
-                    for (int kb = 0; kb < nkb; kb++, x++) {
-                        unsigned char *dst = stage();
-                        if (sbhd) tma_load_3d(dst, &map_kv, full + x % NSTG, kb * 64, it.b, p);
-                        else tma_load_2d(dst, &map_kv, full + x % NSTG, kb * 64, (int)(it.row - it.s + p));
-                    }
-                }
-                for (int pass = 0; pass < 2; pass++)
-                    for (int t = 0; t < it.nct; t++)
-                        for (int kb = 0; kb < nkb; kb++, x++) {
-                            if (g.sparse) {  // gathered by the cp.async producers
-                                tma_slot[x % NSTG] = false;
-                                continue;
-                            }
-                            unsigned char *dst = stage();
-                            if (sbhd) tma_load_3d(dst, &map_kvc, full + x % NSTG, kb * 64, it.b, t * NK);
-                            else tma_load_2d(dst, &map_kvc, full + x % NSTG, kb * 64, (int)(it.key_y + t * NK));
-                        }
-            }
-            // our own copies must land before the CTA exits (a slot whose last stage was gathered held an earlier
-            // load of ours only if that load was consumed, i.e. had landed)
-            for (int y = x - NSTG < 0 ? 0 : x - NSTG; y < x; y++)
-                if (tma_slot[y % NSTG]) drain_bar(full + y % NSTG, (y / NSTG) & 1, err);
-        }
-    } else if (warp == 1) {
+    if (warp == 1) {
         // -------------------------------------------------------------------- MMA issue (whole warp)
         // Rows are decoded lane-parallel (lane l: the CTA's row k + l) and the loop reads the tile count of row k
         // by a shuffle.  Per row: skip its q stages (the epilogue copies them into TMEM), wait for q in
@@ -275,7 +230,7 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         }
         mma_commit_w(mma_done);
         drain_bar(mma_done, 0, err);
-    } else if (warp < HELPER_WARP) {
+    } else if (warp >= EPI_WARP0 && warp < HELPER_WARP) {
         // ---------------------------------------------------------------- epilogue (8 warps)
         // Two warps per TMEM lane quadrant (warp % 4); warp half cq = (warp - 2) / 4 reads the 32-column chunks at
         // columns 32 cq and 32 cq + 64 of every tile, and copies q's K-blocks kb = cq (mod 2) into TMEM.
@@ -510,48 +465,97 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
             prev = it;
         }
         if (ic > 0) writeout(prev, ic - 1);
-    } else if (warp >= PROD_WARP0 && g.sparse) {
-        // ---------------------------------------------------------------- gather producers
-        // Thread n copies key slot n of every gathered tile: per K-block, its 128-byte row in eight 16-byte cp.async
-        // copies, each to its chunk of the 128-byte-swizzled row n.  A stage is handed to the MMA once every
-        // producer thread's copies for it have completed and been made visible to the async proxy (cp.async.wait,
-        // proxy fence, then the four warps meet on a named barrier and one thread arrives).  Each thread keeps
-        // DEPTH stages in flight within a row's run of gathered stages, so it signals stage x - DEPTH after issuing
-        // stage x, and flushes at the run's end (the next run starts behind the next row's q and window stages).
+    } else if (warp >= PROD_WARP0) {
+        // ---------------------------------------------------------------- producers (one group, the whole stream)
+        // The four producer warps walk every stage of the stream in order and are its only producer, so each empty
+        // barrier has one waiter that sees every one of its phases (a barrier tested by parity must never be two
+        // phases away from its waiter, which two producers sharing the ring and skipping each other's stages
+        // cannot guarantee).  q, the window tiles and the dense loss's compressed tiles are TMA tile loads issued
+        // by thread 0 (their full barrier completes with the copy's bytes); a gathered tile of the sparse loss is
+        // copied by all 128 threads: thread n takes key slot n and, per K-block, copies its 128-byte row in eight
+        // 16-byte cp.async copies, each to its chunk of the 128-byte-swizzled row n.  A gathered stage is handed to
+        // the MMA once every thread's copies for it have completed and been made visible to the async proxy
+        // (cp.async.wait, proxy fence, a named barrier of the four warps, one arrival); each thread keeps DEPTH
+        // stages in flight within a row's run of gathered stages, signalling stage x - DEPTH after issuing stage x,
+        // and flushes at the run's end.  With the dense loss only thread 0 works.
         const int n = threadIdx.x - PROD_WARP0 * 32;
-        const int D = g.D;
-        int x = 0;
-        auto signal = [&](int y0, int y1) {  // stages [y0, y1): this thread's copies are complete and fenced
-            fence_proxy_async();
-            named_bar(3, NPROD);
-            if (n == 0)
-                for (int y = y0; y < y1; y++) mbar_arrive(full + y % NSTG);
-        };
-        for (int i = blockIdx.x; i < total; i += gridDim.x) {
-            const Item it = decode(a, i);
-            if (ntiles(it) == 0) continue;
-            x += nkb * (1 + it.nw);  // q and window stages (TMA)
-            const int run0 = x;
-            for (int pass = 0; pass < 2; pass++)
-                for (int t = 0; t < it.nct; t++) {
-                    bool ok;
-                    const long long kr = slot_key_row(a, it, t * NK + n, ok);
-                    const __nv_bfloat16 *src = a.kv_c + kr * D;
+        if (g.sparse || n == 0) {
+            const int D = g.D;
+            int x = 0;
+            bool tma_slot[NSTG];  // whether a slot's last stage was a TMA load of thread 0 (drained at the end)
+            for (int st = 0; st < NSTG; st++) tma_slot[st] = false;
+            auto wait_slot = [&]() { wait_bar(empty + x % NSTG, ((x / NSTG) & 1) ^ 1, abort_flag, err, 61); };
+            // a TMA stage: thread 0 arms the stage's full barrier with its bytes and returns the destination
+            auto tma_dst = [&]() -> unsigned char * {
+                const int st = x % NSTG;
+                tma_slot[st] = true;
+                if (n != 0) return nullptr;
+                mbar_expect_tx(full + st, STG);
+                return ring + st * STG;
+            };
+            auto signal = [&](int y0, int y1) {  // gathered stages [y0, y1): this thread's copies are complete
+                fence_proxy_async();
+                named_bar(3, NPROD);
+                if (n == 0)
+                    for (int y = y0; y < y1; y++) mbar_arrive(full + y % NSTG);
+            };
+            for (int i = blockIdx.x; i < total; i += gridDim.x) {
+                const Item it = decode(a, i);
+                if (ntiles(it) == 0) continue;
+                for (int kb = 0; kb < nkb; kb++, x++) {
+                    wait_slot();
+                    if (unsigned char *dst = tma_dst()) tma_load_3d(dst, &map_q, full + x % NSTG, kb * 64, 0, (int)it.row);
+                }
+                for (int t = 0; t < it.nw; t++) {
+                    const int p = it.p_lo + t * NK;
                     for (int kb = 0; kb < nkb; kb++, x++) {
-                        const int st = x % NSTG;
-                        wait_bar(empty + st, ((x / NSTG) & 1) ^ 1, abort_flag, err, 70);
-                        unsigned char *dst = ring + st * STG + n * 128;
-#pragma unroll
-                        for (int c = 0; c < 8; c++) cp_async16(dst + ((c ^ (n & 7)) << 4), src + kb * 64 + c * 8);
-                        cp_async_commit();
-                        if (x - run0 >= DEPTH) {
-                            cp_async_wait<DEPTH>();
-                            signal(x - DEPTH, x - DEPTH + 1);
+                        wait_slot();
+                        if (unsigned char *dst = tma_dst()) {
+                            if (sbhd) tma_load_3d(dst, &map_kv, full + x % NSTG, kb * 64, it.b, p);
+                            else tma_load_2d(dst, &map_kv, full + x % NSTG, kb * 64, (int)(it.row - it.s + p));
                         }
                     }
                 }
-            cp_async_wait<0>();
-            signal(x - DEPTH > run0 ? x - DEPTH : run0, x);
+                if (!g.sparse) {
+                    for (int pass = 0; pass < 2; pass++)
+                        for (int t = 0; t < it.nct; t++)
+                            for (int kb = 0; kb < nkb; kb++, x++) {
+                                wait_slot();
+                                if (unsigned char *dst = tma_dst()) {
+                                    if (sbhd) tma_load_3d(dst, &map_kvc, full + x % NSTG, kb * 64, it.b, t * NK);
+                                    else tma_load_2d(dst, &map_kvc, full + x % NSTG, kb * 64, (int)(it.key_y + t * NK));
+                                }
+                            }
+                    continue;
+                }
+                const int run0 = x;
+                for (int pass = 0; pass < 2; pass++)
+                    for (int t = 0; t < it.nct; t++) {
+                        bool ok;
+                        const long long kr = slot_key_row(a, it, t * NK + n, ok);
+                        const __nv_bfloat16 *src = a.kv_c + kr * D;
+                        for (int kb = 0; kb < nkb; kb++, x++) {
+                            wait_slot();
+                            const int st = x % NSTG;
+                            tma_slot[st] = false;
+                            unsigned char *dst = ring + st * STG + n * 128;
+#pragma unroll
+                            for (int c = 0; c < 8; c++) cp_async16(dst + ((c ^ (n & 7)) << 4), src + kb * 64 + c * 8);
+                            cp_async_commit();
+                            if (x - run0 >= DEPTH) {
+                                cp_async_wait<DEPTH>();
+                                signal(x - DEPTH, x - DEPTH + 1);
+                            }
+                        }
+                    }
+                cp_async_wait<0>();
+                signal(x - DEPTH > run0 ? x - DEPTH : run0, x);
+            }
+            // thread 0's TMA loads must land before the CTA exits (a slot whose last stage was gathered held an
+            // earlier load only if that load was consumed, i.e. had landed)
+            if (n == 0)
+                for (int y = x - NSTG < 0 ? 0 : x - NSTG; y < x; y++)
+                    if (tma_slot[y % NSTG]) drain_bar(full + y % NSTG, (y / NSTG) & 1, err);
         }
     }
     fence_before();
