@@ -2,8 +2,9 @@
 
 One step = the whole hot path on one batch of synthetic input already resident in HBM:
 csa_indexer_fwd (scores + top-k) then csa_indexer_bwd (full-CSA teacher, KL, dQ_idx / dW / dK_idx).
-Workload: the BSHD bf16 configuration (b=2, sq=4096, ratio 4, H=64, D=192, H_I=64, D_I=128, topk 512,
-window 128).  Prints one JSON line (rank 0).
+Default workload: the long-context BSHD bf16 configuration (b=1, sq=65536, ratio 4 -> 16384 compressed keys,
+H=128, D=512, H_I=64, D_I=128, topk 2048, window 128, sink ~ N(0, 2^2)); --workload picks another of the five
+(tiny_fp32, bshd_bf16, thd_bf16, long_bf16, dense_bf16).  Prints one JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
@@ -36,19 +37,31 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="bshd_bf16")
+    ap.add_argument("--workload", default="long_bf16")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="repeat the timed K-step loop until this much time has passed (median repetition reported)")
     ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="target seconds of the oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-whole-step-s", type=float, default=15.0,
+                    help="reference arm: time whole oracle steps when one is estimated to take at most this long")
+    ap.add_argument("--ref-step-s", type=float, default=5.0, help="reference arm: seconds of each sampled step")
     return ap.parse_args()
 
 
-def _kernel_sha1(stage: str) -> str:
-    """Hash of the sources a stage's kernel is built from; ncu traffic figures count only while it matches."""
+def stage_kernels(cfg, key_width: int) -> dict:
+    """The one kernel each single-kernel stage launches for this workload, and the source file it is built from."""
+    score = ("score_topk_long_tc_kernel" if key_width > 1024 else "score_topk_tc_kernel", "k_score_tc.cu")
+    teacher = (("teacher_h128_tc_kernel", "k_teacher_h128_tc.cu") if cfg.heads == 128
+               else ("teacher_tc_kernel", "k_teacher_tc.cu"))
+    return {"score_topk": score, "teacher": teacher}
+
+
+def _kernel_sha1(source: str) -> str:
+    """Hash of the sources a kernel is built from; ncu traffic figures count only while it matches."""
     import hashlib
     src = os.path.join(ROOT, "sparse_attention_indexer_tcgen05_gb300", "csrc")
-    files = {"score_topk": "k_score_tc.cu", "teacher": "k_teacher_tc.cu"}[stage]
     m = hashlib.sha1()
-    for f in (files, "tc_ptx.cuh", "csa_internal.cuh"):
+    for f in (source, "tc_ptx.cuh", "csa_internal.cuh"):
         with open(os.path.join(src, f), "rb") as fh:
             m.update(fh.read())
     return m.hexdigest()[:12]
@@ -216,6 +229,10 @@ def dist_setup(args):
 
 
 def run_reference(args, cfg):
+    """The reference arm: the float64 CPU oracle, as it stands, on the machine's host cores.  Whole steps when one
+    takes at most --ref-whole-step-s seconds (timed, median reported); otherwise each step is a stratified row
+    sample of about --ref-step-s seconds and the full step's time is extrapolated from the sample's per-row rate
+    (labelled as such)."""
     # under torchrun only rank 0 runs the CPU baseline; the other ranks exit without work
     if int(os.environ.get("RANK", "0")) != 0:
         return
@@ -224,29 +241,41 @@ def run_reference(args, cfg):
     inp = synth.generate(cfg)
     P = O.Problem.from_inputs(inp)
     n = P.rows
-    # each step: a bounded stratified sample of the workload's rows (offset per step)
-    per_step = max(16, min(n, 256))
+    probe = np.unique(np.linspace(0, n - 1, min(n, 64)).astype(np.int32))
+    t0 = time.perf_counter()
+    P.step(inp, rows=probe, want_dk=True)
+    dt = time.perf_counter() - t0
+    est_full = dt * n / len(probe)
+    whole = est_full <= args.ref_whole_step_s
+    per_step = n if whole else int(max(16, min(n, len(probe) * args.ref_step_s / max(dt, 1e-6))))
     times = []
     for it in range(args.warmup + args.steps):
-        off = it % 7
-        rows = np.unique(np.clip(np.linspace(off, n - 1, per_step).astype(np.int32), 0, n - 1))
+        rows = None if whole else np.unique(
+            np.clip(np.linspace(it % 7, n - 1, per_step).astype(np.int32), 0, n - 1))
         t0 = time.perf_counter()
         P.step(inp, rows=rows, want_dk=True)
         dt = time.perf_counter() - t0
         if it >= args.warmup:
-            times.append((len(rows), dt))
-    rows_done = sum(r for r, _ in times)
-    secs = sum(t for _, t in times)
-    value = rows_done / secs
-    ms_per_step = 1e3 * n / value  # time the oracle would take for one full step
+            times.append((n if whole else len(rows), dt))
+    if whole:
+        ms_per_step = 1e3 * statistics.median(t for _, t in times)
+        value = n / (ms_per_step / 1e3)
+        sample = f"whole steps ({n} rows each), median of {len(times)}, full step work (scores, top-k, teacher, KL, gradients)"
+        kind = "measured whole steps"
+    else:
+        rows_done = sum(r for r, _ in times)
+        secs = sum(t for _, t in times)
+        value = rows_done / secs
+        ms_per_step = 1e3 * n / value  # extrapolated: the full step at the sample's per-row rate
+        sample = (f"{per_step} stratified rows of {n} per step ({secs / len(times):.1f} s each), full step work per "
+                  f"row; ms_per_step extrapolated to all rows")
+        kind = "extrapolated from stratified row samples"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_kind": kind,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_desc(cfg),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle",
-                         "sample": f"{per_step} stratified rows of {n} per step, full step work per row "
-                                   f"(scores, top-k, teacher, KL, gradients incl. dK contributions)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -286,18 +315,26 @@ def run_ours(args, cfg):
     barrier()
     B.csa_check_device_status(dev)
 
-    # ---- timed region: K steps, inputs resident in HBM (inputs exceed L2, so no flush between steps)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- timed region: K steps, inputs resident in HBM (inputs exceed L2, so no flush between steps).  The K-step
+    # loop is repeated, each repetition bracketed by a barrier and a synchronize, until --min-timed-s has passed, so
+    # the clock sampler sees the timed work; the median repetition is reported.
     launches0 = B.csa_kernel_launches()
+    rep_ms = []
     with ClockSampler(local) as clk:
-        barrier()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        barrier()
-    launches = B.csa_kernel_launches() - launches0
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+        t_begin = time.perf_counter()
+        while True:
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier()
+            ev0.record(stream)
+            for _ in range(args.steps):
+                step()
+            ev1.record(stream)
+            barrier()
+            rep_ms.append(ev0.elapsed_time(ev1))
+            if time.perf_counter() - t_begin >= args.min_timed_s:
+                break
+    launches = (B.csa_kernel_launches() - launches0) // len(rep_ms)
+    ms = max_over_ranks(statistics.median(rep_ms), world, dev)
     ms_per_step = ms / args.steps
     value = job_rate(p.rows, ms_per_step, world)
     B.csa_check_device_status(dev)
@@ -330,9 +367,9 @@ def run_ours(args, cfg):
     stage_ms["teacher_from_lse"] = timed(lambda: B.csa_teacher_from_lse(p, d.q, d.kv_c, lse_nc, ids, workspace=ws,
                                                                       out=teacher_buf), reps)
     # the roofline is reported for the dominant kernel: of the stages that launch one kernel each
-    # (score + top-k, teacher), the slower one; the teacher kernel has the largest share of the launch
-    # list (profiles/launch_list_bshd_bf16.md)
-    single_kernel = {"score_topk": "score_topk_tc_kernel", "teacher": "teacher_tc_kernel"}
+    # (score + top-k, teacher), the slower one (the launch lists under profiles/ give every kernel's share)
+    kernels = stage_kernels(cfg, p.key_width)
+    single_kernel = {k: v[0] for k, v in kernels.items()}
     dom = max(single_kernel, key=stage_ms.get)
     import json as _j
     peaks = _j.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
@@ -343,11 +380,11 @@ def run_ours(args, cfg):
     achieved_tf = fl[dom] / (stage_ms[dom] / 1e3) / 1e12
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        tr = _j.load(open(tr_path))
-        if (tr.get("path") == path and tr.get("workload") == cfg.name and dom in tr.get("per_launch_bytes", {})
-                and tr.get("kernel_source_sha1", {}).get(dom) == _kernel_sha1(dom)):
-            traffic = tr["per_launch_bytes"][dom]
+    tr = _j.load(open(tr_path)) if os.path.exists(tr_path) else {}
+    rec = tr.get("workloads", {}).get(cfg.name, {})
+    kname, ksrc = kernels[dom]
+    if kname in rec.get("per_launch_bytes", {}) and rec.get("kernel_source_sha1", {}).get(kname) == _kernel_sha1(ksrc):
+        traffic = rec["per_launch_bytes"][kname]
     roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": achieved_tf / tensor_peak, "traffic": traffic, "kernel": single_kernel[dom], "stage": dom,
                 "peak_source": peak_src,
@@ -356,7 +393,7 @@ def run_ours(args, cfg):
                 "stage_frac_hbm": {k: by[k] / (stage_ms[k] / 1e3) / 1e9 / hbm_peak for k in stage_ms},
                 "algorithmic_flops": fl, "algorithmic_bytes": by}
     # the third ceiling of the teacher: its exponentials against the measured MUFU ex2 rate
-    mufu_peak = tr.get("mufu_ex2_per_s") if os.path.exists(tr_path) else None
+    mufu_peak = tr.get("mufu_ex2_per_s")
     ex_rate = exps / (stage_ms["teacher"] / 1e3)
     roofline["teacher_mufu"] = {"exps": exps, "achieved_per_s": ex_rate, "peak_per_s": mufu_peak,
                                 "frac": ex_rate / mufu_peak if mufu_peak else None,
@@ -414,6 +451,7 @@ def run_ours(args, cfg):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
 
     line = None
+    clocks = clk.summary()
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
@@ -425,12 +463,15 @@ def run_ours(args, cfg):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
             "config": {**workload_desc(cfg), "parallelism": f"replicas{world}" if world > 1 else "single",
-                       "l2": "inputs exceed L2 (q 201 MB + q_idx 134 MB > 129 MB); no flush",
+                       "l2": f"inputs exceed L2 (q {d.q.numel() * d.q.element_size() / 1e6:.0f} MB + q_idx "
+                             f"{d.q_idx.numel() * d.q_idx.element_size() / 1e6:.0f} MB > 129 MB); no flush",
                        "path": path},
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": job_rate(p.rows, e2e_ms, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": 4},
-            "gpu_launches": launches, "clocks": clk.summary(),
+            "gpu_launches": launches, "clocks": clocks,
+            "timed": {"repetitions": len(rep_ms), "ms_per_repetition": rep_ms,
+                      "sm_cycles_per_step": (ms_per_step * clocks["sm_mhz"] * 1e3) if clocks.get("sm_mhz") else None},
         }
         print(json.dumps(line), flush=True)
     if world > 1:
