@@ -472,8 +472,9 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         // phases away from its waiter, which two producers sharing the ring and skipping each other's stages
         // cannot guarantee).  q, the window tiles and the dense loss's compressed tiles are TMA tile loads issued
         // by thread 0 (their full barrier completes with the copy's bytes); a gathered tile of the sparse loss is
-        // copied by all 128 threads: thread n takes key slot n and, per K-block, copies its 128-byte row in eight
-        // 16-byte cp.async copies, each to its chunk of the 128-byte-swizzled row n.  A gathered stage is handed to
+        // copied by all 128 threads with 16-byte cp.async copies, each to its chunk of the 128-byte-swizzled row of
+        // its key slot: thread n takes chunk n % 8 of the slots n / 8 + 16 i (i = 0..7), so the eight consecutive
+        // threads of a slot read its whole 128-byte row and one warp instruction reads four rows.  A gathered stage is handed to
         // the MMA once every thread's copies for it have completed and been made visible to the async proxy
         // (cp.async.wait, proxy fence, a named barrier of the four warps, one arrival); each thread keeps DEPTH
         // stages in flight within a row's run of gathered stages, signalling stage x - DEPTH after issuing stage x,
@@ -529,18 +530,23 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                     continue;
                 }
                 const int run0 = x;
+                const int cc = n & 7, kq = n >> 3;
                 for (int pass = 0; pass < 2; pass++)
                     for (int t = 0; t < it.nct; t++) {
-                        bool ok;
-                        const long long kr = slot_key_row(a, it, t * NK + n, ok);
-                        const __nv_bfloat16 *src = a.kv_c + kr * D;
+                        const __nv_bfloat16 *src[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i++) {
+                            bool ok;
+                            src[i] = a.kv_c + slot_key_row(a, it, t * NK + kq + 16 * i, ok) * D + cc * 8;
+                        }
                         for (int kb = 0; kb < nkb; kb++, x++) {
                             wait_slot();
                             const int st = x % NSTG;
                             tma_slot[st] = false;
-                            unsigned char *dst = ring + st * STG + n * 128;
+                            // row kq + 16 i, chunk cc; (kq + 16 i) & 7 == kq & 7
+                            unsigned char *dst = ring + st * STG + kq * 128 + ((cc ^ (kq & 7)) << 4);
 #pragma unroll
-                            for (int c = 0; c < 8; c++) cp_async16(dst + ((c ^ (n & 7)) << 4), src + kb * 64 + c * 8);
+                            for (int i = 0; i < 8; i++) cp_async16(dst + i * 16 * 128, src[i] + kb * 64);
                             cp_async_commit();
                             if (x - run0 >= DEPTH) {
                                 cp_async_wait<DEPTH>();
