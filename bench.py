@@ -42,6 +42,8 @@ def parse():
                     help="repeat the timed K-step loop until this much time has passed (median repetition reported)")
     ap.add_argument("--cpu-sample-s", type=float, default=12.0, help="target seconds of the oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="override the workload's sequence length (a reduced case for profiling; named in config)")
     ap.add_argument("--ref-whole-step-s", type=float, default=15.0,
                     help="reference arm: time whole oracle steps when one is estimated to take at most this long")
     ap.add_argument("--ref-step-s", type=float, default=5.0, help="reference arm: seconds of each sampled step")
@@ -484,6 +486,8 @@ def main():
     args = parse()
     from sparse_attention_indexer_tcgen05_gb300 import synth
     cfg = synth.CONFIGS[args.workload]
+    if args.seqlen is not None:
+        cfg = cfg.replace(name=f"{cfg.name}@sq{args.seqlen}", seqlen=args.seqlen)
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

@@ -111,6 +111,10 @@ typedef struct {
     int32_t reduction;                    /* 0: mean over physical rows.  1: sum (per-token loss) */
     float loss_coeff;                     /* multiplies the loss and every gradient */
     int32_t teacher_mode;                 /* csa_teacher_mode; 0 (full CSA) when zero-initialised */
+    int32_t require_tensor_cores;         /* 1: a call that the tcgen05 kernels do not take (fp32 values, or a
+                                             shape outside their limits) returns CSA_ERR_UNSUPPORTED instead of
+                                             running the CUDA-core kernels.  0 (default): it runs them, and
+                                             csa_last_path reports "generic". */
 } csa_params;
 
 /* ------------------------------------------------------------------ sizes (host only, no CUDA call) */
@@ -208,6 +212,9 @@ csa_status csa_indexer_bwd(const csa_params *p, const void *q_idx, const float *
  *   - Sharing: every call on a device uses the same array, which keeps whatever the last call left there; the
  *     call zeroes what must start at zero (the dK accumulator) itself.  Calls whose work overlaps on the GPU
  *     (different streams, or different host threads) race on the array and must be serialised by the caller. */
+/*   - Device resets: the looked-up address belongs to the device's primary context; after cudaDeviceReset (or
+ *     anything else that destroys that context) the library would keep using the old address, so do not call
+ *     csa_indexer_bwd_noalloc again on a device that was reset in the same process. */
 csa_status csa_indexer_bwd_noalloc(const csa_params *p, const void *q_idx, const float *w, const void *k_idx,
                                    const void *q, const void *kv, const void *kv_c, const float *sink,
                                    const int32_t *ids, const float *selscore, const float *teacher_or_null,
@@ -226,6 +233,13 @@ csa_status csa_scores_debug(const csa_params *p, const void *q_idx, const float 
 /* Synchronises `stream`, then reads and clears the library's device error word (set by a kernel that
  * gave up a bounded wait).  Returns CSA_ERR_TIMEOUT if it was set, CSA_ERR_CUDA on a CUDA error. */
 csa_status csa_check_device_status(void *stream);
+
+/* Test aid for the device-side timeout reporting: enqueues one tiny kernel that waits, with the same bounded
+ * wait the tensor-core kernels use but a limit of about 1 ms, on a barrier nothing arrives on.  The wait runs
+ * out, the kernel records the expiry in the library's device error word and returns; no copy or MMA is in
+ * flight.  The next csa_check_device_status on the stream returns CSA_ERR_TIMEOUT (and clears the word); the
+ * CUDA context stays usable.  The pages have no counterpart to this call. */
+csa_status csa_selftest_bounded_wait(void *stream);
 
 /* Name of the last kernel path csa_indexer_fwd, csa_teacher, csa_teacher_from_lse or csa_indexer_bwd chose
  * on this host thread ("tcgen05", "generic", ...; for csa_indexer_bwd, its backward's).  Static string. */

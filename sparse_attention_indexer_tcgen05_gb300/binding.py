@@ -56,6 +56,7 @@ class csa_params(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float), ("sparse_loss", ctypes.c_int32), ("reduction", ctypes.c_int32),
         ("loss_coeff", ctypes.c_float), ("teacher_mode", ctypes.c_int32),
+        ("require_tensor_cores", ctypes.c_int32),
     ]
 
 
@@ -78,6 +79,7 @@ for _name, _args, _res in [
     ("csa_indexer_bwd_noalloc", [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
      ctypes.c_int),
     ("csa_check_device_status", [_vp], ctypes.c_int),
+    ("csa_selftest_bounded_wait", [_vp], ctypes.c_int),
     ("csa_last_path", [], ctypes.c_char_p),
     ("csa_last_cuda_error", [], ctypes.c_char_p),
     ("csa_kernel_launches", [], ctypes.c_uint64),
@@ -91,7 +93,8 @@ EXPORTED = ("csa_topk_width", "csa_key_width", "csa_teacher_width", "csa_rows", 
             "csa_workspace_size", "csa_indexer_fwd", "csa_teacher", "csa_teacher_from_lse", "csa_indexer_bwd",
             "csa_scores_debug",
             "csa_indexer_bwd_noalloc",
-            "csa_check_device_status", "csa_last_path", "csa_last_cuda_error", "csa_kernel_launches",
+            "csa_check_device_status", "csa_selftest_bounded_wait", "csa_last_path", "csa_last_cuda_error",
+            "csa_kernel_launches",
             "csa_status_string")
 
 
@@ -119,7 +122,8 @@ class Params:
 
     def __init__(self, layout, dtype, batch, seqlen, compress_ratio, window, topk, heads, head_dim, idx_heads,
                  idx_dim, softmax_scale, sparse_loss=True, reduction="mean", loss_coeff=1.0, cu_seqlens_q=None,
-                 cu_seqlens_q_unpadded=None, max_seqlen_q=0, key_rows=0, teacher_mode="full"):
+                 cu_seqlens_q_unpadded=None, max_seqlen_q=0, key_rows=0, teacher_mode="full",
+                 require_tensor_cores=False):
         self.cu = cu_seqlens_q
         self.cur = cu_seqlens_q_unpadded
         for t in (self.cu, self.cur):
@@ -134,7 +138,8 @@ class Params:
                             int(compress_ratio), int(window), int(topk), int(heads), int(head_dim), int(idx_heads),
                             int(idx_dim), float(softmax_scale), 1 if sparse_loss else 0,
                             0 if reduction in ("mean", 0) else 1, float(loss_coeff),
-                            TEACHER_MODES[teacher_mode] if isinstance(teacher_mode, str) else int(teacher_mode))
+                            TEACHER_MODES[teacher_mode] if isinstance(teacher_mode, str) else int(teacher_mode),
+                            1 if require_tensor_cores else 0)
 
     @property
     def ref(self):

@@ -44,6 +44,7 @@ csa_status injected_fault()
 struct Plan {
     Geo g;
     int dtype;
+    bool require_tc;      // refuse the CUDA-core kernels of the score, teacher and backward steps
     bool dense_rescore;   // dense loss with K below the key width: visible scores go to the workspace
     size_t off_cu_c, off_teacher, off_g, off_rowloss, off_dk, off_dense, off_tc, off_btc, off_ttc, total;
 };
@@ -58,6 +59,7 @@ csa_status make_plan(const csa_params *p, Plan *P)
     if (p->sparse_loss != 0 && p->sparse_loss != 1) return CSA_ERR_INVALID_ARG;
     if (p->reduction != 0 && p->reduction != 1) return CSA_ERR_INVALID_ARG;
     if (p->teacher_mode != CSA_TEACHER_FULL && p->teacher_mode != CSA_TEACHER_COMPRESSED_ONLY) return CSA_ERR_INVALID_ARG;
+    if (p->require_tensor_cores != 0 && p->require_tensor_cores != 1) return CSA_ERR_INVALID_ARG;
     if (!isfinite(p->softmax_scale) || !isfinite(p->loss_coeff)) return CSA_ERR_INVALID_ARG;
     if (p->batch < 1 || p->seqlen < 0) return CSA_ERR_INVALID_ARG;
 
@@ -105,6 +107,7 @@ csa_status make_plan(const csa_params *p, Plan *P)
 
     P->g = g;
     P->dtype = p->dtype;
+    P->require_tc = p->require_tensor_cores != 0;
     P->dense_rescore = !g.sparse && g.K < g.NC;
     size_t off = 0;
     P->off_cu_c = off;
@@ -174,6 +177,19 @@ csa_status check_smem(size_t bytes)
 }
 
 char *ws_at(void *ws, size_t off) { return static_cast<char *>(ws) + off; }
+
+// With require_tensor_cores set: CSA_ERR_UNSUPPORTED, before anything is enqueued, when a step of the call would run
+// a CUDA-core kernel for its contraction (the score, the teacher, or the backward, including the dense loss's
+// rescoring of the visible keys).
+csa_status check_required_tc(const Plan &P, bool fwd, bool teacher, bool bwd)
+{
+    if (!P.require_tc) return CSA_OK;
+    const bool bf16 = P.dtype == CSA_BF16;
+    if (fwd && !tc_score_supported(P.g, bf16)) return CSA_ERR_UNSUPPORTED;
+    if (teacher && !tc_teacher_supported(P.g, bf16) && !tc_teacher_h128_supported(P.g, bf16)) return CSA_ERR_UNSUPPORTED;
+    if (bwd && (!tc_bwd_supported(P.g, bf16) || P.dense_rescore)) return CSA_ERR_UNSUPPORTED;
+    return CSA_OK;
+}
 
 // Per-call prologue shared by the three calls: THD compressed offsets into the workspace.
 csa_status prologue(Plan &P, void *ws, cudaStream_t st)
@@ -334,6 +350,7 @@ csa_status csa_indexer_fwd(const csa_params *p, const void *q_idx, const float *
     CSA_TRY(need(ids_out, (long long)g.rows * g.K));
     CSA_TRY(need(selscore_out, (long long)g.rows * g.K));
     if (workspace_bytes < P.total || (P.total > 0 && workspace == nullptr)) return CSA_ERR_WORKSPACE;
+    CSA_TRY(check_required_tc(P, true, false, false));
     if (g.rows == 0) return CSA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (P.dtype == CSA_BF16)
@@ -355,6 +372,7 @@ csa_status csa_scores_debug(const csa_params *p, const void *q_idx, const float 
     CSA_TRY(need(k_idx, g.key_rows * g.DI));
     CSA_TRY(need(scores_out, row_count * g.NC));
     if (workspace_bytes < P.total || (P.total > 0 && workspace == nullptr)) return CSA_ERR_WORKSPACE;
+    CSA_TRY(check_required_tc(P, true, false, false));
     if (row_count == 0 || g.NC == 0) return CSA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (P.dtype == CSA_BF16)
@@ -377,6 +395,7 @@ csa_status csa_teacher(const csa_params *p, const void *q, const void *kv, const
     CSA_TRY(need(ids, (long long)g.rows * g.K));
     CSA_TRY(need(teacher_out, (long long)g.rows * g.TW));
     if (workspace_bytes < P.total || (P.total > 0 && workspace == nullptr)) return CSA_ERR_WORKSPACE;
+    CSA_TRY(check_required_tc(P, false, true, false));
     if (g.rows == 0 || g.TW == 0) return CSA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     CSA_TRY(prologue(P, workspace, st));
@@ -398,6 +417,7 @@ csa_status csa_teacher_from_lse(const csa_params *p, const void *q, const void *
     CSA_TRY(need(ids, (long long)g.rows * g.K));
     CSA_TRY(need(teacher_out, (long long)g.rows * g.TW));
     if (workspace_bytes < P.total || (P.total > 0 && workspace == nullptr)) return CSA_ERR_WORKSPACE;
+    CSA_TRY(check_required_tc(P, false, true, false));
     if (g.rows == 0 || g.TW == 0) return CSA_OK;
     // the given log-sum-exp carries the whole non-compressed part of each head's denominator
     g.window = 0;
@@ -441,6 +461,7 @@ csa_status csa_indexer_bwd(const csa_params *p, const void *q_idx, const float *
     CSA_TRY(need(dw, (long long)g.rows * g.HI));
     CSA_TRY(need(dk_idx, g.key_rows * g.DI));
     if (workspace_bytes < P.total || (P.total > 0 && workspace == nullptr)) return CSA_ERR_WORKSPACE;
+    CSA_TRY(check_required_tc(P, false, teacher_or_null == nullptr, true));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     float *dk_acc = reinterpret_cast<float *>(ws_at(workspace, P.off_dk));
     if (P.dtype == CSA_BF16)
@@ -454,9 +475,17 @@ csa_status csa_check_device_status(void *stream)
 {
     CSA_TRY(injected_fault());
     CSA_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
-    int flag = 0;
+    int flag = 0, flag2 = 0;
     CSA_CUDA(tc_read_clear_error(&flag));
-    return flag != 0 ? CSA_ERR_TIMEOUT : CSA_OK;
+    CSA_CUDA(selftest_read_clear_error(&flag2));
+    return (flag != 0 || flag2 != 0) ? CSA_ERR_TIMEOUT : CSA_OK;
+}
+
+csa_status csa_selftest_bounded_wait(void *stream)
+{
+    CSA_TRY(injected_fault());
+    CSA_CUDA(launch_bounded_wait_selftest(static_cast<cudaStream_t>(stream)));
+    return CSA_OK;
 }
 
 const char *csa_last_path(void) { return t_last_path; }

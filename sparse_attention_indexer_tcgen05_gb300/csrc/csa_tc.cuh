@@ -67,6 +67,11 @@ cudaError_t launch_teacher_h128_tc(const Geo &g, const __nv_bfloat16 *q, const _
                                    cudaStream_t st);
 cudaError_t teacher_h128_read_clear_error(int *flag);
 
+// One tiny kernel whose bounded wait (about 1 ms) on a barrier nothing arrives on runs out (k_selftest.cu), and
+// the read-and-clear of the word it sets.
+cudaError_t launch_bounded_wait_selftest(cudaStream_t st);
+cudaError_t selftest_read_clear_error(int *flag);
+
 // Reads and clears the tensor-core kernels' device error word (set when a kernel gives up a bounded
 // wait on an mbarrier).  Synchronous: call after the stream has drained.
 cudaError_t tc_read_clear_error(int *flag);

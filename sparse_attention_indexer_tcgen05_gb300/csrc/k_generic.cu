@@ -2,7 +2,8 @@
 //
 // These are the correct-first path: one CTA per query row, fp32 arithmetic on CUDA cores, shared
 // memory for the row's operands.  They serve every shape the tensor-core kernels do not take (fp32
-// mode, small or odd head counts) and are the reference the faster kernels are tested against.
+// mode, small or odd head counts), unless the caller sets csa_params.require_tensor_cores.  Both paths
+// are tested against the float64 oracle.
 //
 // Sources, by page title and section:
 //   [BUG] "[Bug] DSV4 unfused CSA indexer loss uses a compressed-only teacher instead of the full CSA

@@ -58,19 +58,24 @@ __device__ __forceinline__ void init_fence()
 // uniform and the kernel runs to its end; `err` receives the site code of the first expiry.  The phase is
 // tried before the abort flag is read: on the fast path the flag's load latency would sit in the MMA
 // issuer's critical path.
-__device__ __forceinline__ void wait_bar(uint64_t *b, uint32_t parity, volatile int *abort_flag, int *err, int site)
+__device__ __forceinline__ void wait_bar_for(uint64_t *b, uint32_t parity, volatile int *abort_flag, int *err, int site,
+                                             long long limit_cycles)
 {
     if (mbar_try(b, parity)) return;
     if (*abort_flag) return;
     const long long t0 = clock64();
     while (!mbar_try(b, parity)) {
         if (*abort_flag) return;
-        if (clock64() - t0 > kTimeoutCycles) {
+        if (clock64() - t0 > limit_cycles) {
             *abort_flag = 1;
             atomicExch(err, site);
             return;
         }
     }
+}
+__device__ __forceinline__ void wait_bar(uint64_t *b, uint32_t parity, volatile int *abort_flag, int *err, int site)
+{
+    wait_bar_for(b, parity, abort_flag, err, site, kTimeoutCycles);
 }
 // Timer-only bounded wait, used to drain a kernel's own copies / MMAs even after an abort.
 __device__ __forceinline__ void drain_bar(uint64_t *b, uint32_t parity, int *err)

@@ -10,6 +10,14 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "csa_indexer.h")
 
 
+def _no_gpu():
+    """Tests that hand made-up device addresses to the library run only where no GPU exists: on a GPU machine a
+    regression in the host-side validation would otherwise launch kernels on those addresses."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("passes made-up device addresses: run only where no GPU exists")
+
+
 @pytest.fixture(scope="module")
 def B():
     from sparse_attention_indexer_tcgen05_gb300 import build
@@ -68,6 +76,7 @@ def test_bench_workload_fits_the_no_allocation_scratch(B):
                                          ("batch", 0), ("seqlen", -5), ("reduction", 2), ("sparse_loss", 3),
                                          ("layout", 7), ("dtype", 9), ("key_rows", 5), ("teacher_mode", 2)])
 def test_invalid_params_rejected(B, field, value):
+    _no_gpu()
     p = _params(B)
     setattr(p.c, field, value)
     assert p.K == -1 and p.workspace_bytes == 0
@@ -92,6 +101,7 @@ def test_thd_requires_offsets(B):
 
 
 def test_pointer_validation_before_any_launch(B):
+    _no_gpu()
     p = _params(B)
     big = 1 << 40
     f = B._lib.csa_indexer_fwd
@@ -121,12 +131,39 @@ def test_no_gpu_is_a_cuda_error_not_a_crash(B):
 @pytest.mark.parametrize("site,status", [("invalid_arg", 1), ("unsupported", 2), ("alignment", 3),
                                          ("workspace", 4), ("cuda", 5), ("timeout", 6)])
 def test_fault_injection(B, monkeypatch, site, status):
+    _no_gpu()
     monkeypatch.setenv("CSA_FAULT", site)
     p = _params(B)
     assert B._lib.csa_indexer_fwd(p.ref, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 1 << 40, None) == status
     assert B._lib.csa_check_device_status(None) == status
     err = B.CSAError(status, "csa_indexer_fwd")
     assert B.STATUS[status] in str(err)
+
+
+def test_noalloc_rejects_problems_beyond_the_scratch(B):
+    """The 64k long-context shape needs far more than the fixed scratch of csa_indexer_bwd_noalloc: refused with
+    CSA_ERR_WORKSPACE by the host-side size check, before anything is enqueued."""
+    _no_gpu()
+    p = B.Params("bshd", "bf16", 1, 65536, 4, 128, 2048, 128, 512, 64, 128, 0.044)
+    assert p.workspace_bytes > B.NOALLOC_SCRATCH_BYTES
+    fake = [0x10000 * (i + 1) for i in range(13)]
+    # q_idx, w, k_idx, q, kv, kv_c, sink, ids, selscore | teacher | loss | row_loss | dq_idx, dw, dk_idx | stream
+    st = B._lib.csa_indexer_bwd_noalloc(p.ref, *fake[:9], None, fake[9], None, fake[10], fake[11], fake[12], None)
+    assert st == 4  # CSA_ERR_WORKSPACE
+
+
+def test_require_tensor_cores_refuses_the_cuda_core_kernels(B):
+    """With require_tensor_cores set, a call whose shape the tensor-core kernels do not take (here 8 indexer
+    heads) returns CSA_ERR_UNSUPPORTED before anything is enqueued; fp32 values are refused the same way."""
+    _no_gpu()
+    big = 1 << 40
+    args = (0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, big, None)
+    p = _params(B, idx_heads=8, require_tensor_cores=True)
+    assert p.c.require_tensor_cores == 1
+    assert B._lib.csa_indexer_fwd(p.ref, *args) == 2
+    assert B._lib.csa_indexer_fwd(_params(B, dtype="f32", require_tensor_cores=True).ref, *args) == 2
+    # without the flag the same call gets past the path choice (and fails only for want of a GPU)
+    assert B._lib.csa_indexer_fwd(_params(B, idx_heads=8).ref, *args) == 5
 
 
 def test_status_strings(B):

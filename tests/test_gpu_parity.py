@@ -429,6 +429,35 @@ def test_autograd_function():
     assert q.grad is None  # no gradient to the teacher side
 
 
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    """A device-side bounded wait that runs out (csa_selftest_bounded_wait: the tensor-core kernels' wait, limited
+    to about 1 ms, on a barrier nothing arrives on) is reported on the host as CSA_ERR_TIMEOUT by the next
+    csa_check_device_status, which clears it; the CUDA context stays usable and the next step is correct."""
+    stream = torch.cuda.current_stream().cuda_stream
+    assert B._lib.csa_selftest_bounded_wait(stream) == 0
+    assert B._lib.csa_check_device_status(stream) == 6      # CSA_ERR_TIMEOUT
+    assert B._lib.csa_check_device_status(stream) == 0      # read and cleared
+    out = U.check_step(synth.generate(small(idx_heads=64, idx_dim=128, heads=64, seed=17)))
+    assert out["fwd_path"] == "tcgen05"
+    _report("after_timeout", out)
+
+
+def test_require_tensor_cores_runs_every_step_on_tcgen05():
+    """With require_tensor_cores set, a shape the tcgen05 kernels take runs as usual; one they do not take (8
+    indexer heads) is refused with CSA_ERR_UNSUPPORTED and nothing runs."""
+    inp = synth.generate(small(idx_heads=64, idx_dim=128, heads=64, seed=18))
+    d = workload.to_device(inp, require_tensor_cores=True)
+    ids, sel = B.csa_indexer_fwd(d.params, *d.indexer)
+    B.csa_indexer_bwd(d.params, *d.indexer, *d.teacher_side, ids, sel)
+    torch.cuda.synchronize()
+    assert B.csa_last_path() == "tcgen05"
+    d8 = workload.to_device(synth.generate(small(seed=18)), require_tensor_cores=True)
+    with pytest.raises(B.CSAError) as e:
+        B.csa_indexer_fwd(d8.params, *d8.indexer)
+    assert e.value.status == 2
+    B.csa_check_device_status()
+
+
 def test_errors_fail_closed():
     cfg = small()
     d = workload.to_device(synth.generate(cfg))
