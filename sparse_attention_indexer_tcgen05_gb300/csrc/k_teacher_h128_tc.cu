@@ -54,7 +54,7 @@ constexpr int TWMAX = 2048;                     // teacher row width held in sha
 constexpr int THREADS = 480;                    // 15 warps
 constexpr int EPI = 256;                        // warps 2..9
 constexpr int EPI_WARP0 = 2, HELPER_WARP = 10, PROD_WARP0 = 11, NPROD = 128;
-constexpr int DEPTH = 6;                        // cp.async stages a producer thread keeps in flight (< NSTG)
+constexpr int GRP = 4;                          // gathered stages committed and handed over together
 constexpr uint32_t TMEM_COLS = 512;             // q (<= 256 columns) + two 128-column accumulators
 constexpr uint32_t ACC0 = 256;
 constexpr uint32_t IDESC = idesc_bf16(128, NK, false, false);  // A (q, TMEM) and B (keys) K-major
@@ -476,9 +476,10 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         // its key slot: thread n takes chunk n % 8 of the slots n / 8 + 16 i (i = 0..7), so the eight consecutive
         // threads of a slot read its whole 128-byte row and one warp instruction reads four rows.  A gathered stage is handed to
         // the MMA once every thread's copies for it have completed and been made visible to the async proxy
-        // (cp.async.wait, proxy fence, a named barrier of the four warps, one arrival); each thread keeps DEPTH
-        // stages in flight within a row's run of gathered stages, signalling stage x - DEPTH after issuing stage x,
-        // and flushes at the run's end.  With the dense loss only thread 0 works.
+        // (cp.async.wait, proxy fence, a named barrier of the four warps, one arrival per stage).  The stages of a
+        // row's run of gathered stages go in groups of GRP, one commit group each; group j is handed over after
+        // group j + 1 has been issued (at most 2 GRP stages unsignalled, well inside the ring), and the run's last
+        // groups at its end.  With the dense loss only thread 0 works.
         const int n = threadIdx.x - PROD_WARP0 * 32;
         if (g.sparse || n == 0) {
             const int D = g.D;
@@ -529,8 +530,9 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                             }
                     continue;
                 }
-                const int run0 = x;
                 const int cc = n & 7, kq = n >> 3;
+                int grp0 = x;              // first stage of the group being issued
+                int pend0 = -1, pend1 = -1;  // the issued group not yet handed over, [pend0, pend1)
                 for (int pass = 0; pass < 2; pass++)
                     for (int t = 0; t < it.nct; t++) {
                         const __nv_bfloat16 *src[8];
@@ -539,7 +541,7 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                             bool ok;
                             src[i] = a.kv_c + slot_key_row(a, it, t * NK + kq + 16 * i, ok) * D + cc * 8;
                         }
-                        for (int kb = 0; kb < nkb; kb++, x++) {
+                        for (int kb = 0; kb < nkb; kb++) {
                             wait_slot();
                             const int st = x % NSTG;
                             tma_slot[st] = false;
@@ -547,15 +549,23 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                             unsigned char *dst = ring + st * STG + kq * 128 + ((cc ^ (kq & 7)) << 4);
 #pragma unroll
                             for (int i = 0; i < 8; i++) cp_async16(dst + i * 16 * 128, src[i] + kb * 64);
-                            cp_async_commit();
-                            if (x - run0 >= DEPTH) {
-                                cp_async_wait<DEPTH>();
-                                signal(x - DEPTH, x - DEPTH + 1);
+                            x++;
+                            if (x - grp0 == GRP) {  // the group is complete: commit it, hand over the previous one
+                                cp_async_commit();
+                                if (pend0 >= 0) {
+                                    cp_async_wait<1>();
+                                    signal(pend0, pend1);
+                                }
+                                pend0 = grp0;
+                                pend1 = x;
+                                grp0 = x;
                             }
                         }
                     }
+                if (grp0 < x) cp_async_commit();  // a last, partial group
                 cp_async_wait<0>();
-                signal(x - DEPTH > run0 ? x - DEPTH : run0, x);
+                if (pend0 >= 0) signal(pend0, pend1);
+                if (grp0 < x) signal(grp0, x);
             }
             // thread 0's TMA loads must land before the CTA exits (a slot whose last stage was gathered held an
             // earlier load only if that load was consumed, i.e. had landed)
