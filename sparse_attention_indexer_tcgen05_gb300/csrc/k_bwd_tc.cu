@@ -1204,10 +1204,15 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const int g1 = upper_items < sms ? (upper_items > 0 ? upper_items : 1) : sms;
-    dq_dw_tc_kernel<<<g1, R_THREADS, R_SMEM, st>>>(mq, mk, mg, mw, a);
-    note_launches(1);
-    e = cudaGetLastError();
+    if (lng) {
+        // long key axis: the row-owner over each row's selected keys only
+        e = launch_dq_dw_gather_tc(g, q_idx, w, k_idx, ids, gslot, dq, dw, st);
+    } else {
+        const int g1 = upper_items < sms ? (upper_items > 0 ? upper_items : 1) : sms;
+        dq_dw_tc_kernel<<<g1, R_THREADS, R_SMEM, st>>>(mq, mk, mg, mw, a);
+        note_launches(1);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     if (upper_units > 0) {
         // launched as a programmatic dependent of the row-owner kernel (which it does not depend on), so its

@@ -56,11 +56,13 @@ cudaError_t tc_read_clear_error(int *flag)
     }
     e = bwd_tc_read_clear_error(&f2);
     if (e != cudaSuccess) return e;
-    int f3 = 0, f4 = 0;
+    int f3 = 0, f4 = 0, f5 = 0;
     e = teacher_tc_read_clear_error(&f3);
     if (e != cudaSuccess) return e;
     e = teacher_h128_read_clear_error(&f4);
-    *flag = f1 != 0 ? f1 : (f2 != 0 ? f2 : (f3 != 0 ? f3 : f4));
+    if (e != cudaSuccess) return e;
+    e = bwd_gather_read_clear_error(&f5);
+    *flag = f1 != 0 ? f1 : (f2 != 0 ? f2 : (f3 != 0 ? f3 : (f4 != 0 ? f4 : f5)));
     return e;
 }
 
