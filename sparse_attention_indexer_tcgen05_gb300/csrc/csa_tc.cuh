@@ -51,9 +51,10 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
                           const float *gslot, cudaStream_t st);
 cudaError_t bwd_tc_read_clear_error(int *flag);
 // Long key axes: the row-owner backward (dQ_idx, dW) over each row's selected keys only (k_bwd_gather_tc.cu);
-// gslot [rows][K] holds dloss/dI by slot of the ascending ids.
+// gslot [rows][K] holds dloss/dI by slot of the ascending ids; sgn [rows][K] receives the signs of x per slot.
 cudaError_t launch_dq_dw_gather_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
-                                   const int32_t *ids, const float *gslot, __nv_bfloat16 *dq, float *dw, cudaStream_t st);
+                                   const int32_t *ids, const float *gslot, __nv_bfloat16 *dq, float *dw,
+                                   unsigned long long *sgn, cudaStream_t st);
 cudaError_t bwd_gather_read_clear_error(int *flag);
 
 // Tensor-core teacher for bf16, H = 64, D in {64, 128, 192}, key axis <= 1024.

@@ -16,6 +16,8 @@
 //   MMA2  dQ'^T[d, h] += k^T . G'     M = 128 d (A: the same k tile read MN-major), N = 64 heads (B: G'), K = 128
 //                                      keys; fp32 in TMEM (64 columns), accumulated over the row's tiles;
 // and at the row's end the epilogue reads dQ'^T (lane = d), writes dQ_idx = w dQ' and reduces dW = q . dQ' over d.
+// The epilogue also stores, per (row, slot), the 64 signs of x (bit h: x[key, h] > 0) for the key-owner kernel,
+// which then forms its G = g w 1[x > 0] without recomputing x.
 // The k rows of a tile are gathered by four producer warps with 16-byte cp.async copies (16 threads per 256-byte
 // row, coalesced), each chunk written to its place in the swizzled tile; tiles are handed to the MMA one tile late
 // (after the next tile's copies are issued) once every thread's copies have completed and been made visible to
@@ -76,6 +78,7 @@ struct Args {
     const float *gslot;           // dloss/dI by slot [rows][K]
     __nv_bfloat16 *dq;
     float *dw;
+    unsigned long long *sgn;      // [rows][K]: bit h set when x > 0 for head h (0 for slots without a key)
 };
 
 struct Item {
@@ -283,6 +286,13 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
                 fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(x_empty + xb);
+                const int sl = t * NKEY + r_lane;
+                if (sl < K) {
+                    unsigned long long m = 0ull;
+#pragma unroll
+                    for (int h = 0; h < HI; h++) m |= (unsigned long long)(__uint_as_float(xr[h]) > 0.f) << h;
+                    a.sgn[row * K + sl] = gk != 0.f ? m : 0ull;
+                }
                 // G' of this key over the 64 heads into buffer xb, row r_lane of the MN-major tile
                 wait_bar(g_empty + xb, ((xc / NX) & 1) ^ 1, abort_flag, err, 54);
                 unsigned char *gt = sG + xb * GT + r_lane * 128;
@@ -408,7 +418,8 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
 // ------------------------------------------------------------------ host side
 
 cudaError_t launch_dq_dw_gather_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w, const __nv_bfloat16 *k_idx,
-                                   const int32_t *ids, const float *gslot, __nv_bfloat16 *dq, float *dw, cudaStream_t st)
+                                   const int32_t *ids, const float *gslot, __nv_bfloat16 *dq, float *dw,
+                                   unsigned long long *sgn, cudaStream_t st)
 {
     using namespace bwg;
     CUtensorMap mq;
@@ -421,6 +432,7 @@ cudaError_t launch_dq_dw_gather_tc(const Geo &g, const __nv_bfloat16 *q_idx, con
     a.gslot = gslot;
     a.dq = dq;
     a.dw = dw;
+    a.sgn = sgn;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -103,6 +103,7 @@ struct Args {
     const float *gslot;
     const int32_t *ids;
     const int *toff;
+    const unsigned long long *sgn;   // signs of x by slot [rows][K], from the gathered row-owner
     int NT;
 };
 
@@ -1032,6 +1033,266 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ------------------------------------------------------------------ key-owner kernel from sign bits: dK, long key axes
+
+// On long key axes the gathered row-owner kernel has computed x for every selected (row, key) and stored its signs by
+// slot (sgn[row][slot], bit h: x_tjh > 0).  This kernel takes the same units as dk_tc_kernel (a key tile and a chunk
+// of up to 128 rows that see it) but forms, per row pair,
+//   G[key, (row, h)] = g_ts w_tj 1[x_tjs > 0]          (zero off the row's selection)
+// straight from g, w and the signs -- no X MMA and no k tile -- and MMA3 accumulates dK[key, d] += G q
+// (A = G from TMEM, B = the pair's q block read MN-major).  Two builder warps (alternate pairs) place each row's g
+// and signs for the tile's selected keys into shared memory from the slot range [lo, hi) of the per-row tile-offset
+// table; the epilogue expands them into G in TMEM.
+// Roles: warp 0 TMA (q blocks, w rows), warp 1 TMEM + MMA issue, warps 2..3 builders, warps 4..19 epilogue.
+constexpr int S_QSTG = 6;                                        // q blocks in flight
+constexpr int S_GSTG = 4;                                        // g / sign / w slots
+constexpr int S_XSTG = 3;                                        // G slots in TMEM, 64 columns each
+constexpr int S_OFF_B = 0;                                       // q blocks: 6 x 32 KB
+constexpr int S_OFF_GT = S_OFF_B + S_QSTG * QBLK;                // g: slots x 2 rows x 128 fp32
+constexpr int S_OFF_BT = S_OFF_GT + S_GSTG * RP * NKEY * 4;      // signs: slots x 2 rows x 128 u64
+constexpr int S_OFF_WT = S_OFF_BT + S_GSTG * RP * NKEY * 8;      // w rows: slots x 2 rows x 64 fp32
+constexpr int S_OFF_RNG = S_OFF_WT + S_GSTG * RP * HI * 4;       // per builder: a unit's slot ranges, CH x 2 int
+constexpr int S_OFF_MISC = S_OFF_RNG + 2 * CH * 2 * 4;
+constexpr int S_SMEM = S_OFF_MISC + 1024 + 1024;
+static_assert(S_SMEM <= 232448, "sign-bit key-owner shared memory exceeds the per-block limit");
+static_assert((2 * S_QSTG + 2 * S_GSTG + 2 * S_XSTG + 3) * 8 <= 256, "sign-bit key-owner barriers overlap the TMEM slot");
+
+__global__ void __launch_bounds__(THREADS, 1)
+dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w, Args a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *sB = smem + S_OFF_B;
+    float *sGT = reinterpret_cast<float *>(smem + S_OFF_GT);
+    unsigned long long *sBT = reinterpret_cast<unsigned long long *>(smem + S_OFF_BT);
+    float *sWT = reinterpret_cast<float *>(smem + S_OFF_WT);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S_OFF_MISC);
+    uint64_t *b_full = bars, *b_empty = bars + S_QSTG, *gt_full = bars + 2 * S_QSTG, *gt_empty = gt_full + S_GSTG;
+    uint64_t *gk_full = gt_empty + S_GSTG, *x_empty = gk_full + S_XSTG;
+    uint64_t *dk_full = x_empty + S_XSTG, *dk_empty = dk_full + 1, *mma_done = dk_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + S_OFF_MISC + 256);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S_OFF_MISC + 264);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Geo &g = a.g;
+    int *err = &g_bwd_error;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S_QSTG; i++) { mbar_init(b_full + i, 1); mbar_init(b_empty + i, 1); }
+        // a g/sign/w slot is full once its w copy has landed and a builder has placed g and the signs
+        for (int i = 0; i < S_GSTG; i++) { mbar_init(gt_full + i, 2); mbar_init(gt_empty + i, EPI / 32); }
+        for (int i = 0; i < S_XSTG; i++) { mbar_init(gk_full + i, EPI / 32); mbar_init(x_empty + i, 1); }
+        mbar_init(dk_full, 1);
+        mbar_init(dk_empty, EPI / 32);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        init_fence();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // TMEM: three G slots of 64 columns (bf16 pairs: K index (row, h) = 64 row + h at column (64 row + h) / 2), and
+    // dK (128 columns) at 256
+    const uint32_t tG = tmem, tDK = tmem + 256;
+    const int total = unit_total(a);
+
+    if (warp == 0) {
+        if (lane == 0) {  // ------------------------------------------------ TMA producer
+            int qs = 0, pc = 0;
+            for (int u = blockIdx.x; u < total; u += gridDim.x) {
+                const Unit U = decode_unit(a, u);
+                for (int pi = 0; pi < U.npairs; pi++) {
+                    // the pair's q rows and w rows, one copy each (a second row past the chunk's end is read, never used)
+                    const int s0 = U.s_lo + pi * RP;
+                    const PairAt at = pair_at(g, U.sg.b, s0, row_of(g, U.sg.b, s0));
+                    const int bs = qs % S_QSTG;
+                    wait_bar(b_empty + bs, ((qs / S_QSTG) & 1) ^ 1, abort_flag, err, 34);
+                    mbar_expect_tx(b_full + bs, QBLK);
+                    tma_load_5d(sB + bs * QBLK, &map_q, b_full + bs, 0, 0, at.y, at.z, 0);
+                    qs++;
+                    const int gs = pc % S_GSTG;
+                    wait_bar(gt_empty + gs, ((pc / S_GSTG) & 1) ^ 1, abort_flag, err, 35);
+                    mbar_expect_tx(gt_full + gs, (uint32_t)(RP * HI * 4));
+                    tma_load_3d(sWT + gs * RP * HI, &map_w, gt_full + gs, 0, at.y, at.z);
+                    pc++;
+                }
+            }
+            for (int q = qs - S_QSTG < 0 ? 0 : qs - S_QSTG; q < qs; q++) drain_bar(b_full + q % S_QSTG, (q / S_QSTG) & 1, err);
+            for (int q = pc - S_GSTG < 0 ? 0 : pc - S_GSTG; q < pc; q++) drain_bar(gt_full + q % S_GSTG, (q / S_GSTG) & 1, err);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------------------- MMA issue (whole warp)
+        //   dK[key, d] += G q   (A = G from TMEM, K index (row, h); B = the pair's q block read MN-major)
+        int qs = 0, xc = 0, uc = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit U = decode_unit(a, u);
+            if (U.npairs == 0) continue;
+            for (int pi = 0; pi < U.npairs; pi++) {
+                const int bs = qs % S_QSTG, xb = xc % S_XSTG;
+                if (pi == 0) wait_bar(dk_empty, (uc & 1) ^ 1, abort_flag, err, 36);
+                wait_bar(b_full + bs, (qs / S_QSTG) & 1, abort_flag, err, 37);
+                wait_bar(gk_full + xb, (xc / S_XSTG) & 1, abort_flag, err, 38);
+                fence_after();
+                const unsigned char *pq = sB + bs * QBLK;
+#pragma unroll
+                for (int s = 0; s < 8; s++)
+                    mma_bf16_ts_w(tDK, tG + (uint32_t)(xb * 64 + 8 * s), desc_sw128(pq + s * 2048, HALF, 1024), IDESC_DK,
+                                  (pi == 0 && s == 0) ? 0u : 1u);
+                mma_commit_w(x_empty + xb);
+                mma_commit_w(b_empty + bs);
+                qs++;
+                xc++;
+            }
+            mma_commit_w(dk_full);
+            uc++;
+        }
+        mma_commit_w(mma_done);
+        drain_bar(mma_done, 0, err);
+    } else if (warp == 2 || warp == 3) {
+        // ---------------------------------------------------------------- builders (pairs alternate between them)
+        // Per unit: the slot range [lo, hi) of its key tile in each of its rows.  Per row pair of this builder, into
+        // the pair's slot: half-warp r zeroes row r's 128 keys and places g and the signs of its slots lo .. hi - 1,
+        // all loaded at once (at most 128 per row and tile: eight per lane); keys outside the tile are never placed.
+        const int bw = warp - 2;
+        const int half = lane >> 4, hl = lane & 15;
+        const int K = g.K;
+        int *sRng = reinterpret_cast<int *>(smem + S_OFF_RNG) + bw * CH * 2;
+        int pc = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit U = decode_unit(a, u);
+            if (U.npairs == 0) continue;
+            const int nrow = U.s_hi - U.s_lo;
+            __syncwarp();
+            for (int r = lane; r < nrow; r += 32) {
+                const int *o = a.toff + row_of(g, U.sg.b, U.s_lo + r) * (long long)(a.NT + 1);
+                int lo = __ldg(o + U.kt), hi = __ldg(o + U.kt + 1);
+                lo = lo < 0 ? 0 : (lo > K ? K : lo);
+                hi = hi < lo ? lo : (hi > K ? K : hi);
+                sRng[2 * r] = lo;
+                sRng[2 * r + 1] = hi;
+            }
+            __syncwarp();
+            const long long k0 = U.sg.gid0 + (long long)U.kt * NKEY;
+            for (int pi = 0; pi < U.npairs; pi++, pc++) {
+                if ((pc & 1) != bw) continue;
+                const int gs = pc % S_GSTG;
+                const int r = pi * RP + half;
+                // the pair's entries, loaded before the slot is waited for
+                int32_t id[8];
+                float gv[8];
+                unsigned long long bv[8];
+                int lo = 0, hi = 0;
+                long long row = 0;
+                if (r < nrow) {
+                    row = row_of(g, U.sg.b, U.s_lo + r);
+                    lo = sRng[2 * r];
+                    hi = sRng[2 * r + 1];
+                }
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int sl = lo + hl + 16 * e;
+                    id[e] = -1;
+                    gv[e] = 0.f;
+                    bv[e] = 0ull;
+                    if (sl < hi) {
+                        id[e] = __ldg(a.ids + row * K + sl);
+                        gv[e] = __ldg(a.gslot + row * K + sl);
+                        bv[e] = __ldg(a.sgn + row * K + sl);
+                    }
+                }
+                wait_bar(gt_empty + gs, ((pc / S_GSTG) & 1) ^ 1, abort_flag, err, 39);
+                float *dg = sGT + (gs * RP + half) * NKEY;
+                unsigned long long *db = sBT + (gs * RP + half) * NKEY;
+                reinterpret_cast<float4 *>(dg)[2 * hl] = make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4 *>(dg)[2 * hl + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < 4; e++) reinterpret_cast<ulonglong2 *>(db)[4 * hl + e] = make_ulonglong2(0ull, 0ull);
+                __syncwarp();
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const long long j = (long long)id[e] - k0;
+                    if (id[e] >= 0 && j >= 0 && j < NKEY) {
+                        dg[j] = gv[e];
+                        db[j] = bv[e];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gt_full + gs);
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------------- epilogue (16 warps)
+        // Lane = key (quad * 32 + lane).  Warp sub = (warp - 4) / 4 of a quadrant forms G for heads [32 (sub % 2), +32)
+        // of row `half` = sub / 2 of the pair (16 pair columns at 32 half + 16 (sub % 2) of the G slot) and flushes d
+        // quarter sub of the unit's dK.
+        const int quad = warp & 3, sub = (warp - 4) >> 2, half = sub >> 1, hq = sub & 1;
+        const int k = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        int xc = 0, dkc = 0, pc = 0;
+        for (int u = blockIdx.x; u < total; u += gridDim.x) {
+            const Unit U = decode_unit(a, u);
+            for (int pi = 0; pi < U.npairs; pi++, pc++, xc++) {
+                const int gs = pc % S_GSTG, xb = xc % S_XSTG;
+                const bool row_ok = U.s_lo + pi * RP + half < U.s_hi;  // warp-uniform
+                wait_bar(gt_full + gs, (pc / S_GSTG) & 1, abort_flag, err, 40);
+                wait_bar(x_empty + xb, ((xc / S_XSTG) & 1) ^ 1, abort_flag, err, 41);
+                fence_after();
+                uint32_t pk[16];
+                if (row_ok) {
+                    const float gk = sGT[(gs * RP + half) * NKEY + k];
+                    const uint32_t bits = (uint32_t)(sBT[(gs * RP + half) * NKEY + k] >> (32 * hq));
+                    const float4 *wr4 = reinterpret_cast<const float4 *>(sWT + gs * RP * HI + half * HI + hq * 32);
+#pragma unroll
+                    for (int c = 0; c < 8; c++) {
+                        const float4 w4 = wr4[c];
+                        const float2 lo = mul2(make_float2(gk, gk), make_float2(w4.x, w4.y));
+                        const float2 hi = mul2(make_float2(gk, gk), make_float2(w4.z, w4.w));
+                        pk[2 * c] = pack_bf16((bits >> (4 * c)) & 1u ? lo.x : 0.f, (bits >> (4 * c + 1)) & 1u ? lo.y : 0.f);
+                        pk[2 * c + 1] = pack_bf16((bits >> (4 * c + 2)) & 1u ? hi.x : 0.f, (bits >> (4 * c + 3)) & 1u ? hi.y : 0.f);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; c++) pk[c] = 0u;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gt_empty + gs);
+                tmem_st16(tG + lane_off + (uint32_t)(xb * 64 + half * 32 + hq * 16), pk);
+                fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gk_full + xb);
+            }
+            if (U.npairs == 0) continue;
+            // ---- flush the unit's dK partial: lane = key, this warp's d quarter
+            wait_bar(dk_full, dkc & 1, abort_flag, err, 42);
+            fence_after();
+            uint32_t vv[32];
+            tmem_ld32_async(tDK + lane_off + (uint32_t)(sub * 32), vv);
+            tmem_wait_ld(vv);
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dk_empty);
+            dkc++;
+            const int j = U.kt * NKEY + k;
+            if (j < U.sg.nc) {
+                const long long gid = U.sg.gid0 + j;
+                const long long kr = g.layout == CSA_SBHD ? (gid % g.nc) * g.B + gid / g.nc : gid;
+                float *dst = a.dk_acc + kr * DI + sub * 32;
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    atomicAdd(reinterpret_cast<float4 *>(dst + 4 * c),
+                              make_float4(__uint_as_float(vv[4 * c]), __uint_as_float(vv[4 * c + 1]),
+                                          __uint_as_float(vv[4 * c + 2]), __uint_as_float(vv[4 * c + 3])));
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
 // Long key axis: toff[r][b] = the first slot of row r whose key (id minus the row's first key) lies at or above
 // 128 b, b = 0 .. NT (the slots hold ascending valid ids, then -1 pads; a pad or an invalid id counts as past the
 // last tile, and a virtual slot K closes the remaining boundaries).  One warp per row.
@@ -1108,9 +1369,16 @@ static size_t bwd_offsets_bytes(const Geo &g)
     return (offs + 255) & ~(size_t)255;
 }
 
+// long key axis: the tile-offset rows, then the signs of x by slot
+static size_t toff_bytes(const Geo &g)
+{
+    return ((sizeof(int) * (size_t)g.rows * (size_t)(tc_bwd_tiles(g) + 1)) + 255) & ~(size_t)255;
+}
+
 size_t tc_bwd_workspace_bytes(const Geo &g)
 {
-    if (tc_bwd_long(g)) return bwd_offsets_bytes(g) + sizeof(int) * (size_t)g.rows * (size_t)(tc_bwd_tiles(g) + 1);
+    if (tc_bwd_long(g))
+        return bwd_offsets_bytes(g) + toff_bytes(g) + sizeof(unsigned long long) * (size_t)g.rows * (size_t)g.K;
     return bwd_offsets_bytes(g) + sizeof(float) * (size_t)g.rows * (size_t)tc_bwd_ncp(g);
 }
 
@@ -1170,6 +1438,9 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
     a.ids = ids;
     a.NT = NT;
     a.toff = lng ? reinterpret_cast<const int *>(tc_bwd_gd(g, ws)) : nullptr;
+    unsigned long long *sgn =
+        lng ? reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(tc_bwd_gd(g, ws)) + toff_bytes(g)) : nullptr;
+    a.sgn = sgn;
     int upper_items, upper_units;
     if (g.layout == CSA_THD) {
         int *cu_g = static_cast<int *>(ws);
@@ -1206,7 +1477,7 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
     }
     if (lng) {
         // long key axis: the row-owner over each row's selected keys only
-        e = launch_dq_dw_gather_tc(g, q_idx, w, k_idx, ids, gslot, dq, dw, st);
+        e = launch_dq_dw_gather_tc(g, q_idx, w, k_idx, ids, gslot, dq, dw, sgn, st);
     } else {
         const int g1 = upper_items < sms ? (upper_items > 0 ? upper_items : 1) : sms;
         dq_dw_tc_kernel<<<g1, R_THREADS, R_SMEM, st>>>(mq, mk, mg, mw, a);
@@ -1214,6 +1485,15 @@ cudaError_t launch_bwd_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float 
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
+    if (lng && upper_units > 0) {
+        // long key axis: dK from the signs the row-owner has just written (stream order, no overlap)
+        e = cudaFuncSetAttribute(dk_sign_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S_SMEM);
+        if (e != cudaSuccess) return e;
+        const int g2 = upper_units < sms ? upper_units : sms;
+        dk_sign_tc_kernel<<<g2, THREADS, S_SMEM, st>>>(mq, mw, a);
+        note_launches(1);
+        return cudaGetLastError();
+    }
     if (upper_units > 0) {
         // launched as a programmatic dependent of the row-owner kernel (which it does not depend on), so its
         // CTAs start on the SMs the row-owner's last items leave idle
