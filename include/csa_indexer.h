@@ -241,6 +241,12 @@ csa_status csa_check_device_status(void *stream);
  * CUDA context stays usable.  The pages have no counterpart to this call. */
 csa_status csa_selftest_bounded_wait(void *stream);
 
+/* Where the last timeout that csa_check_device_status reported on this host thread happened, as
+ * 100 x kernel + wait site: kernel 1 the score / top-k kernel, 2 the backward, 3 the 64-head teacher, 4 the
+ * 128-head teacher, 5 the gathered row-owner backward, 9 the bounded-wait self-test; site 99 is a drain of the
+ * kernel's own copies that ran out after an abort.  0 before the first timeout; not cleared by later calls. */
+int32_t csa_last_timeout_site(void);
+
 /* Name of the last kernel path csa_indexer_fwd, csa_teacher, csa_teacher_from_lse or csa_indexer_bwd chose
  * on this host thread ("tcgen05", "generic", ...; for csa_indexer_bwd, its backward's).  Static string. */
 const char *csa_last_path(void);

@@ -80,6 +80,7 @@ for _name, _args, _res in [
      ctypes.c_int),
     ("csa_check_device_status", [_vp], ctypes.c_int),
     ("csa_selftest_bounded_wait", [_vp], ctypes.c_int),
+    ("csa_last_timeout_site", [], ctypes.c_int32),
     ("csa_last_path", [], ctypes.c_char_p),
     ("csa_last_cuda_error", [], ctypes.c_char_p),
     ("csa_kernel_launches", [], ctypes.c_uint64),
@@ -93,7 +94,8 @@ EXPORTED = ("csa_topk_width", "csa_key_width", "csa_teacher_width", "csa_rows", 
             "csa_workspace_size", "csa_indexer_fwd", "csa_teacher", "csa_teacher_from_lse", "csa_indexer_bwd",
             "csa_scores_debug",
             "csa_indexer_bwd_noalloc",
-            "csa_check_device_status", "csa_selftest_bounded_wait", "csa_last_path", "csa_last_cuda_error",
+            "csa_check_device_status", "csa_selftest_bounded_wait", "csa_last_timeout_site", "csa_last_path",
+            "csa_last_cuda_error",
             "csa_kernel_launches",
             "csa_status_string")
 
@@ -104,6 +106,8 @@ class CSAError(RuntimeError):
         msg = _lib.csa_status_string(status).decode()
         if status == 5:  # CSA_ERR_CUDA
             msg += " (" + _lib.csa_last_cuda_error().decode() + ")"
+        if status == 6:  # CSA_ERR_TIMEOUT
+            msg += f" (kernel {_lib.csa_last_timeout_site() // 100}, wait site {_lib.csa_last_timeout_site() % 100})"
         super().__init__(f"{call}: {msg}")
 
 
@@ -353,6 +357,11 @@ def csa_check_device_status(device=None):
 
 def csa_last_path() -> str:
     return _lib.csa_last_path().decode()
+
+
+def csa_last_timeout_site() -> int:
+    """100 x kernel + wait site of the last timeout csa_check_device_status reported (0 before any)."""
+    return int(_lib.csa_last_timeout_site())
 
 
 def csa_last_cuda_error() -> str:

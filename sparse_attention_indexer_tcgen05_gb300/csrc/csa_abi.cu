@@ -153,6 +153,7 @@ inline csa_status need(const void *ptr, long long elems)
     } while (0)
 
 thread_local const char *t_last_cuda_error = "no error";
+thread_local int32_t t_last_timeout_site = 0;
 
 // A failed CUDA call ends the entry point with CSA_ERR_CUDA and leaves its message for csa_last_cuda_error.
 #define CSA_CUDA(x)                                     \
@@ -478,8 +479,12 @@ csa_status csa_check_device_status(void *stream)
     int flag = 0, flag2 = 0;
     CSA_CUDA(tc_read_clear_error(&flag));
     CSA_CUDA(selftest_read_clear_error(&flag2));
-    return (flag != 0 || flag2 != 0) ? CSA_ERR_TIMEOUT : CSA_OK;
+    if (flag == 0 && flag2 == 0) return CSA_OK;
+    t_last_timeout_site = flag != 0 ? flag : 900 + flag2;
+    return CSA_ERR_TIMEOUT;
 }
+
+int32_t csa_last_timeout_site(void) { return t_last_timeout_site; }
 
 csa_status csa_selftest_bounded_wait(void *stream)
 {

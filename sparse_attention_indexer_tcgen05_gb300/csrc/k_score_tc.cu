@@ -28,7 +28,8 @@
 //               the exact k-th largest score by a bitwise search on order-preserving keys held in
 //               registers, then the selection written by a stable ballot compaction.
 //   (long key axis: warps 10..13, one per row, follow the epilogue tile by tile through a four-tile ring; each
-//    keeps the row's current best candidates and cuts them back to the top K with an 8-bit radix select.)
+//    keeps the row's current best candidates, cuts them back to about the top K with a radix walk when the
+//    buffer fills, and to exactly the top K at the row's end.)
 //
 // Every mbarrier wait is bounded: on expiry the kernel records an error code (read back by
 // csa_check_device_status), stops waiting (so every role still runs its loops to the end with uniform
@@ -62,7 +63,9 @@ cudaError_t tc_read_clear_error(int *flag)
     e = teacher_h128_read_clear_error(&f4);
     if (e != cudaSuccess) return e;
     e = bwd_gather_read_clear_error(&f5);
-    *flag = f1 != 0 ? f1 : (f2 != 0 ? f2 : (f3 != 0 ? f3 : (f4 != 0 ? f4 : f5)));
+    // the first kernel's code, as 100 x kernel + site (1 score, 2 backward, 3 64-head teacher, 4 128-head
+    // teacher, 5 gathered row-owner); site 99 is a drain that ran out
+    *flag = f1 != 0 ? 100 + f1 : (f2 != 0 ? 200 + f2 : (f3 != 0 ? 300 + f3 : (f4 != 0 ? 400 + f4 : (f5 != 0 ? 500 + f5 : 0))));
     return e;
 }
 
@@ -88,10 +91,12 @@ constexpr int TMEM_COLS = 512;
 //     and each row is selected by one warp once the item is done; two sets of four selection warps take
 //     alternate items; the q_idx rows of two items are resident (double buffer).
 //   long key axis: the score rows stream through a ring of key tiles; the selection warp of each row keeps a
-//     candidate buffer of at most CAP (key, index) entries in ascending key order, admits a new key only when
-//     it beats the row's current K-th best (strictly: a later key loses a tie), and cuts the buffer back to
-//     exactly K entries (the current top K, ties to the lower key) whenever the next tile might not fit, and
-//     once more at the row's end.  One set of four selection warps; one q_idx buffer.
+//     candidate buffer of at most CAP (key, index) entries in ascending key order and admits a new key only
+//     when it lies strictly above the row's current threshold, a value with at least K buffered keys at or above
+//     it (a later key loses a tie, so no key at or below it can reach the top K).  Whenever the next tile might
+//     not fit, the buffer is cut back to the keys at or above a radix bin edge with between K and K + 256 keys
+//     above it (that edge becomes the threshold); at the row's end it is cut to exactly the top K, ties to the
+//     lower key.  One set of four selection warps; one q_idx buffer.
 template <bool LONG> struct SC;
 template <> struct SC<false> {
     static constexpr int THREADS = 576;       // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..17 selection
@@ -121,7 +126,8 @@ template <> struct SC<true> {
 };
 static_assert(SC<false>::SMEM_ALLOC <= 232448, "score kernel exceeds the 227 KB of shared memory a CTA may use");
 static_assert(SC<true>::SMEM_ALLOC <= 232448, "long score kernel exceeds the 227 KB of shared memory a CTA may use");
-// largest K the long kernel takes: a cut leaves K entries and must leave room for one more tile
+// largest K the long kernel takes: an in-loop cut leaves at most K + slack entries, slack = min(256, CAP -
+// 2 NKEY - K) >= 0, so that two more tiles fit
 constexpr int LONG_KMAX = SC<true>::CAP - 2 * NKEY;
 constexpr int LONG_NCMAX = 65535;             // candidate indices are 16-bit
 
@@ -338,22 +344,43 @@ __device__ void select_row(const Args &a, const Item &it, int k, const float *sc
 
 // ------------------------------------------------------------------ long key axis: candidate buffers
 
-// The K-th largest of the n keys ck[0..n) (K <= n), one warp, by an 8-bit radix walk from the top byte with a
-// 256-bin histogram per pass.  Returns that key; `need_eq` receives how many entries equal to it belong to the
-// top K (the rest of the top K lies strictly above it).
-__device__ uint32_t kth_largest(const uint32_t *ck, int n, int K, uint32_t *hist, int &need_eq)
+// A cut point of the n keys ck[0..n), all in [lo, hi] (K <= n), one warp, by a radix walk in digits of up to
+// 8 bits with a 256-bin histogram per pass.  The walk starts at the highest bit in which lo and hi differ (the
+// bits above it are the same in every key, so no pass is spent on them).
+//   slack < 0: returns the K-th largest key T; `need_eq` receives how many entries equal to T belong to the top K
+//              (the rest of the top K lies strictly above T).
+//   slack >= 0: may stop early, at the first digit whose bin holding the K-th largest key has a lower edge L with
+//              at most K + slack keys at or above it; returns L (at least K keys lie at or above it), with
+//              `need_eq` = n (every key equal to L is kept).  Reaching the last digit gives the exact answer.
+__device__ uint32_t kth_search(const uint32_t *ck, int n, int K, uint32_t lo, uint32_t hi, int slack, uint32_t *hist,
+                               int &need_eq)
 {
     const int lane = threadIdx.x & 31;
-    uint32_t prefix = 0u, pmask = 0u;
+    if (lo == hi) {  // every key is the same: the first K of them
+        need_eq = K;
+        return lo;
+    }
+    int hb = 31 - __clz(lo ^ hi);                 // top bit of the current digit
+    uint32_t prefix = hi & ~((2u << hb) - 1u);    // the bits above it (2u << 31 wraps to 0: no common bits)
     int need = K;  // rank of the wanted entry among those matching the prefix, counted from the top
 #pragma unroll 1
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    while (true) {
+        const int lb = hb >= 7 ? hb - 7 : 0;      // digit bits lb .. hb
+        const uint32_t wmask = (2u << (hb - lb)) - 1u;
+        const uint32_t pmask = ~((2u << hb) - 1u);
 #pragma unroll
         for (int q = 0; q < 8; q++) hist[lane * 8 + q] = 0u;
         __syncwarp();
-        for (int e = lane; e < n; e += 32) {
-            const uint32_t k = ck[e];
-            if ((k & pmask) == prefix) atomicAdd(hist + ((k >> shift) & 255u), 1u);
+        for (int e0 = 0; e0 < n; e0 += 128) {
+            uint32_t kk[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int e = e0 + 32 * u + lane;
+                kk[u] = e < n ? ck[e] : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                if (e0 + 32 * u + lane < n && (kk[u] & pmask) == prefix) atomicAdd(hist + ((kk[u] >> lb) & wmask), 1u);
         }
         __syncwarp();
         // lane l owns bins 255 - 8 l .. 248 - 8 l (descending); an inclusive scan over lanes counts the entries
@@ -374,12 +401,15 @@ __device__ uint32_t kth_largest(const uint32_t *ck, int n, int K, uint32_t *hist
         const bool mine = before < (uint32_t)need && (uint32_t)need <= incl;
         const unsigned who = __ballot_sync(0xffffffffu, mine);
         int bin = 0;
-        uint32_t above = 0u;
+        uint32_t above = 0u, cnt = 0u;
         if (mine) {
             uint32_t acc = before;
 #pragma unroll
             for (int q = 0; q < 8; q++) {
-                if (bin == 0 && acc + c[q] >= (uint32_t)need) bin = 256 + 255 - 8 * lane - q;  // +256: found
+                if (bin == 0 && acc + c[q] >= (uint32_t)need) {
+                    bin = 256 + 255 - 8 * lane - q;  // +256: found
+                    cnt = c[q];
+                }
                 if (bin == 0) acc += c[q];
             }
             above = acc;
@@ -388,22 +418,33 @@ __device__ uint32_t kth_largest(const uint32_t *ck, int n, int K, uint32_t *hist
         const int src = __ffs(who) - 1;
         bin = __shfl_sync(0xffffffffu, bin, src);
         above = __shfl_sync(0xffffffffu, above, src);
-        prefix |= (uint32_t)bin << shift;
-        pmask |= 255u << shift;
+        cnt = __shfl_sync(0xffffffffu, cnt, src);
+        prefix |= (uint32_t)bin << lb;
         need -= (int)above;
         __syncwarp();
+        if (lb == 0) {
+            need_eq = need;
+            return prefix;
+        }
+        // keys at or above the bin's lower edge: K - need + cnt
+        if (slack >= 0 && (int)cnt - need <= slack) {
+            need_eq = n;
+            return prefix;
+        }
+        hb = lb - 1;
     }
-    need_eq = need;
-    return prefix;
 }
 
-// Cuts the candidate buffer (ascending key index) to its top K (K < n), ties to the lower index, keeping the
-// ascending order (stable in-place compaction).  Returns the new count (K) and the K-th largest key in `thr`.
-__device__ int cut_to_topk(uint32_t *ck, uint16_t *ci, int n, int K, uint32_t *hist, uint32_t &thr)
+// Cuts the candidate buffer (ascending key index, keys in [lo, hi]) back to the entries at or above the cut
+// point kth_search finds (exactly the top K, ties to the lower index, when slack < 0; otherwise every key at or
+// above a bin edge L, between K and K + slack of them), keeping the ascending order (stable in-place
+// compaction).  Returns the new count; `thr` receives T (or L): a later key can enter the top K only above it.
+__device__ int cut_candidates(uint32_t *ck, uint16_t *ci, int n, int K, uint32_t lo, uint32_t hi, int slack,
+                              uint32_t *hist, uint32_t &thr)
 {
     const int lane = threadIdx.x & 31;
     int need_eq = 0;
-    const uint32_t T = kth_largest(ck, n, K, hist, need_eq);
+    const uint32_t T = kth_search(ck, n, K, lo, hi, slack, hist, need_eq);
     const unsigned lt = (1u << lane) - 1u;
     int base = 0, eq_seen = 0;
     for (int c0 = 0; c0 < n; c0 += 32) {
@@ -725,6 +766,9 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
         uint32_t *hist = reinterpret_cast<uint32_t *>(smem + C::OFF_HIST) + k * 256;
         const float *ringb = reinterpret_cast<const float *>(smem + C::OFF_RING);
         const int K = g.K;
+        // an in-loop cut may keep up to cut_slack entries past the top K (the exact cut comes at the row's end);
+        // it must still leave room for two tiles, so the slack shrinks for K near the largest K taken
+        const int cut_slack = C::CAP - 2 * NKEY - K < 256 ? C::CAP - 2 * NKEY - K : 256;
         const unsigned lt = (1u << lane) - 1u;
         int tc = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x) {
@@ -739,6 +783,13 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
             const bool select = present && a.ids != nullptr;
             int n = 0;
             uint32_t thr = 0u;  // a key enters only above this (0: every score, before the first cut)
+            uint32_t klo = 0xffffffffu, khi = 0u;  // bounds of this lane's buffered keys (after a cut: [thr, max])
+            auto cut = [&](int slack) {
+                const uint32_t lo = __reduce_min_sync(0xffffffffu, klo), hi = __reduce_max_sync(0xffffffffu, khi);
+                n = cut_candidates(ck, ci, n, K, lo, hi, slack, hist, thr);
+                klo = thr;
+                khi = hi;
+            };
             for (int t = 0; t < nt; t++, tc++) {
                 const int slot = tc % C::NRING;
                 wait_bar(x_full + slot, (tc / C::NRING) & 1, abort_flag, &g_tc_error, 8);
@@ -755,7 +806,7 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
                     }
                 }
                 if (!select) continue;
-                if (n + NKEY > C::CAP) n = cut_to_topk(ck, ci, n, K, hist, thr);
+                if (n + NKEY > C::CAP) cut(cut_slack);
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
                     const int j = t * NKEY + 32 * c + lane;
@@ -766,6 +817,8 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
                         const int pos = n + __popc(m & lt);
                         ck[pos] = key;
                         ci[pos] = (uint16_t)j;
+                        klo = min(klo, key);
+                        khi = max(khi, key);
                     }
                     n += __popc(m);
                 }
@@ -774,7 +827,7 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
             if (dump_row != nullptr)
                 for (int j = nt * NKEY + lane; j < g.NC; j += 32) dump_row[j] = -INFINITY;
             if (!select) continue;
-            if (n > K) n = cut_to_topk(ck, ci, n, K, hist, thr);
+            if (n > K) cut(-1);
             __syncwarp();
             int32_t *orow = a.ids + r * K;
             float *srow = a.selscore + r * K;

@@ -12,11 +12,11 @@
 // memory holds only key tiles: D[h, key] = q[h] . key with N = 128 keys per tile (two 128-column fp32
 // accumulators next to q), K = D in 64-wide K-blocks, one 16 KB shared-memory stage per K-block.
 //   * one ring of twelve 16 KB stages carries, in order, each row's q, its window tiles and its compressed
-//     tiles (both passes), filled by one group of four producer warps: q, the window's original-KV rows and
-//     (dense loss) the contiguous compressed keys by TMA tile loads, the selected compressed keys (sparse loss)
-//     gathered with 16-byte cp.async copies, each written to its place in the 128-byte-swizzled K-major tile.
-//     (TMA's gather4 moves 512 bytes per instruction and measured about a tenth of the tile-load rate from L2,
-//     too slow for 2048 keys of 1 KB per row.)
+//     tiles (both passes), filled by one group of four producer warps: with the dense loss every stage is a TMA
+//     tile load; with the sparse loss every stage (the selected compressed keys, and with them the row's q and
+//     window rows) is copied by all four warps with 16-byte cp.async copies, each written to its place in the
+//     128-byte-swizzled K-major tile.  (TMA's gather4 moves 512 bytes per instruction and measured about a
+//     tenth of the tile-load rate from L2, too slow for 2048 keys of 1 KB per row.)
 //   pass 1: window tiles + compressed tiles -> per-head running sum against a reference maximum, then l_h with
 //           the sink (or a given sink-and-window log-sum-exp);
 //   pass 2: compressed tiles again -> exp(c - l_h) summed over the 128 heads into shared per-slot T;
@@ -71,7 +71,9 @@ struct Args {
     Geo g;
     const float *sink;
     const int32_t *ids;
-    const __nv_bfloat16 *kv_c;   // cp.async gather source
+    const __nv_bfloat16 *q;      // cp.async sources (sparse loss): the query rows, the original KV rows and the
+    const __nv_bfloat16 *kv;     // compressed keys
+    const __nv_bfloat16 *kv_c;
     float *teacher;
     int nkb;                     // D / 64
 };
@@ -130,17 +132,18 @@ __device__ Item decode(const Args &a, int i)
 __device__ __forceinline__ int ntiles(const Item &it) { return it.v > 0 ? it.nw + 2 * it.nct : 0; }
 // ring stages of a row: q, window tiles, both passes of the compressed tiles (one stage per K-block)
 __device__ __forceinline__ int row_stages(const Args &a, const Item &it) { return a.nkb * (1 + it.nw + 2 * it.nct); }
-// slot s of the row holds a usable key: a valid id of the row's segment within its visible range
-__device__ __forceinline__ long long slot_key_row(const Args &a, const Item &it, int s, bool &ok)
+// the id of slot s of the row (-1 past the K slots)
+__device__ __forceinline__ int32_t slot_id(const Args &a, const Item &it, int s)
 {
-    const Geo &g = a.g;
-    ok = false;
-    if (s >= g.K) return 0;
-    const int32_t id = __ldg(a.ids + it.row * g.K + s);
+    return s < a.g.K ? __ldg(a.ids + it.row * a.g.K + s) : -1;
+}
+// a slot holding id is usable when id is a key of the row's segment within its visible range; its kv_c row then
+// (row 0, never read for the loss, otherwise)
+__device__ __forceinline__ long long id_key_row(const Args &a, const Item &it, int32_t id, bool &ok)
+{
     const long long j = (long long)id - it.gid0;
-    if (id < 0 || j < 0 || j >= it.v) return 0;
-    ok = true;
-    return key_row(g, (long long)id);
+    ok = !(id < 0 || j < 0 || j >= it.v);
+    return ok ? key_row(a.g, (long long)id) : 0;
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -452,11 +455,17 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
             for (int x = lane; x < nz; x += 32) tz[x] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (g.sparse && ntiles(it) > 0) {
                 uint32_t *mk = sMask + ib * (TWMAX / 32);
-                for (int w0 = 0; w0 < it.ncs; w0 += 32) {
-                    bool ok;
-                    slot_key_row(a, it, w0 + lane, ok);
-                    const unsigned bits = __ballot_sync(0xffffffffu, ok && w0 + lane < it.ncs);
-                    if (lane == 0) mk[w0 >> 5] = bits;
+                for (int w0 = 0; w0 < it.ncs; w0 += 256) {  // eight independent loads in flight per lane
+                    int32_t idv[8];
+#pragma unroll
+                    for (int k = 0; k < 8; k++) idv[k] = w0 + 32 * k + lane < it.ncs ? slot_id(a, it, w0 + 32 * k + lane) : -1;
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        bool ok;
+                        id_key_row(a, it, idv[k], ok);
+                        const unsigned bits = __ballot_sync(0xffffffffu, ok);
+                        if (lane == 0 && w0 + 32 * k < it.ncs) mk[(w0 >> 5) + k] = bits;
+                    }
                 }
             }
             __syncwarp();
@@ -467,101 +476,123 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         if (ic > 0) writeout(prev, ic - 1);
     } else if (warp >= PROD_WARP0) {
         // ---------------------------------------------------------------- producers (one group, the whole stream)
-        // The four producer warps walk every stage of the stream in order and are its only producer, so each empty
-        // barrier has one waiter that sees every one of its phases (a barrier tested by parity must never be two
-        // phases away from its waiter, which two producers sharing the ring and skipping each other's stages
-        // cannot guarantee).  q, the window tiles and the dense loss's compressed tiles are TMA tile loads issued
-        // by thread 0 (their full barrier completes with the copy's bytes); a gathered tile of the sparse loss is
-        // copied by all 128 threads with 16-byte cp.async copies, each to its chunk of the 128-byte-swizzled row of
-        // its key slot: thread n takes chunk n % 8 of the slots n / 8 + 16 i (i = 0..7), so the eight consecutive
-        // threads of a slot read its whole 128-byte row and one warp instruction reads four rows.  A gathered stage is handed to
-        // the MMA once every thread's copies for it have completed and been made visible to the async proxy
-        // (cp.async.wait, proxy fence, a named barrier of the four warps, one arrival per stage).  The stages of a
-        // row's run of gathered stages go in groups of GRP, one commit group each; group j is handed over after
-        // group j + 1 has been issued (at most 2 GRP stages unsignalled, well inside the ring), and the run's last
-        // groups at its end.  With the dense loss only thread 0 works.
+        // The four producer warps walk every stage of the stream in order and are its only producer.  A barrier
+        // tested by parity must never be two phases away from a thread that waits on it; the two loss modes meet
+        // that differently.
+        //   Dense loss: thread 0 alone issues every stage as a TMA tile load (its full barrier completes with the
+        //     copy's bytes) and is the only thread that waits on the empty barriers, each in order.
+        //   Sparse loss: every stage (the row's q, its window tiles and its selected compressed keys) is copied by
+        //     all 128 threads with 16-byte cp.async copies, each to its chunk of the 128-byte-swizzled row of its
+        //     matrix row: thread n takes chunk n % 8 of the rows n / 8 + 16 i (i = 0..7), so the eight consecutive
+        //     threads of a row read its whole 128-byte segment and one warp instruction reads four rows.  Each
+        //     thread waits on a stage's empty barrier before issuing its copies for it.  A stage is handed over
+        //     (one arrival by thread 0) only after a named barrier of the four warps that every thread reaches
+        //     once its copies for the stage have completed and been made visible to the async proxy, so no stage
+        //     can be filled, let alone consumed, before every thread has passed its empty wait: no thread can
+        //     fall a phase behind.  (With TMA stages filled by thread 0 alone, a lagging warp could find a stage
+        //     already filled and consumed when it first tests the slot, and would then wait for good.)  The
+        //     stages of a row go in groups of GRP, one commit group each; group j is handed over after group
+        //     j + 1 has been issued (at most 2 GRP stages unsignalled, well inside the ring), and the row's last
+        //     groups at its end.  The ids of each thread's eight key slots are loaded one tile ahead (the first
+        //     gathered tile's at the row start), so that no tile waits for them.
         const int n = threadIdx.x - PROD_WARP0 * 32;
         if (g.sparse || n == 0) {
             const int D = g.D;
             int x = 0;
             bool tma_slot[NSTG];  // whether a slot's last stage was a TMA load of thread 0 (drained at the end)
             for (int st = 0; st < NSTG; st++) tma_slot[st] = false;
-            auto wait_slot = [&]() { wait_bar(empty + x % NSTG, ((x / NSTG) & 1) ^ 1, abort_flag, err, 61); };
-            // a TMA stage: thread 0 arms the stage's full barrier with its bytes and returns the destination
+            auto wait_slot = [&](int y) { wait_bar(empty + y % NSTG, ((y / NSTG) & 1) ^ 1, abort_flag, err, 61); };
+            // a TMA stage (dense loss, thread 0): wait for its slot, arm its full barrier, return the destination
             auto tma_dst = [&]() -> unsigned char * {
                 const int st = x % NSTG;
+                wait_slot(x);
                 tma_slot[st] = true;
-                if (n != 0) return nullptr;
                 mbar_expect_tx(full + st, STG);
                 return ring + st * STG;
             };
-            auto signal = [&](int y0, int y1) {  // gathered stages [y0, y1): this thread's copies are complete
+            auto signal = [&](int y0, int y1) {  // stages [y0, y1): this thread's copies are complete
                 fence_proxy_async();
                 named_bar(3, NPROD);
                 if (n == 0)
                     for (int y = y0; y < y1; y++) mbar_arrive(full + y % NSTG);
             };
+            const int cc = n & 7, kq = n >> 3;
             for (int i = blockIdx.x; i < total; i += gridDim.x) {
                 const Item it = decode(a, i);
                 if (ntiles(it) == 0) continue;
-                for (int kb = 0; kb < nkb; kb++, x++) {
-                    wait_slot();
-                    if (unsigned char *dst = tma_dst()) tma_load_3d(dst, &map_q, full + x % NSTG, kb * 64, 0, (int)it.row);
-                }
-                for (int t = 0; t < it.nw; t++) {
-                    const int p = it.p_lo + t * NK;
-                    for (int kb = 0; kb < nkb; kb++, x++) {
-                        wait_slot();
-                        if (unsigned char *dst = tma_dst()) {
+                if (!g.sparse) {  // thread 0 alone
+                    for (int kb = 0; kb < nkb; kb++, x++) tma_load_3d(tma_dst(), &map_q, full + x % NSTG, kb * 64, 0, (int)it.row);
+                    for (int t = 0; t < it.nw; t++) {
+                        const int p = it.p_lo + t * NK;
+                        for (int kb = 0; kb < nkb; kb++, x++) {
+                            unsigned char *dst = tma_dst();
                             if (sbhd) tma_load_3d(dst, &map_kv, full + x % NSTG, kb * 64, it.b, p);
                             else tma_load_2d(dst, &map_kv, full + x % NSTG, kb * 64, (int)(it.row - it.s + p));
                         }
                     }
-                }
-                if (!g.sparse) {
                     for (int pass = 0; pass < 2; pass++)
                         for (int t = 0; t < it.nct; t++)
                             for (int kb = 0; kb < nkb; kb++, x++) {
-                                wait_slot();
-                                if (unsigned char *dst = tma_dst()) {
-                                    if (sbhd) tma_load_3d(dst, &map_kvc, full + x % NSTG, kb * 64, it.b, t * NK);
-                                    else tma_load_2d(dst, &map_kvc, full + x % NSTG, kb * 64, (int)(it.key_y + t * NK));
-                                }
+                                unsigned char *dst = tma_dst();
+                                if (sbhd) tma_load_3d(dst, &map_kvc, full + x % NSTG, kb * 64, it.b, t * NK);
+                                else tma_load_2d(dst, &map_kvc, full + x % NSTG, kb * 64, (int)(it.key_y + t * NK));
                             }
                     continue;
                 }
-                const int cc = n & 7, kq = n >> 3;
-                int grp0 = x;              // first stage of the group being issued
-                int pend0 = -1, pend1 = -1;  // the issued group not yet handed over, [pend0, pend1)
-                for (int pass = 0; pass < 2; pass++)
-                    for (int t = 0; t < it.nct; t++) {
-                        const __nv_bfloat16 *src[8];
+                int32_t idn[8];
+                auto load_ids = [&](int t) {
+#pragma unroll
+                    for (int k = 0; k < 8; k++) idn[k] = slot_id(a, it, t * NK + kq + 16 * k);
+                };
+                load_ids(0);
+                const int nu = 2 * it.nct;      // gathered tiles: both passes
+                const int ntl = 1 + it.nw + nu;  // q, window tiles, gathered tiles
+                int grp0 = x;                    // first stage of the group being issued
+                int pend0 = -1, pend1 = -1;      // the issued group not yet handed over, [pend0, pend1)
+                for (int tl = 0; tl < ntl; tl++) {
+                    // this thread's eight source rows of the tile (matrix rows kq + 16 i), at chunk cc of K-block 0
+                    const __nv_bfloat16 *src[8];
+                    if (tl == 0) {  // q: head rows of the query row
+#pragma unroll
+                        for (int i = 0; i < 8; i++) src[i] = a.q + (it.row * H + kq + 16 * i) * D + cc * 8;
+                    } else if (tl <= it.nw) {  // window positions p (past the window: the row's own, never read)
+#pragma unroll
+                        for (int i = 0; i < 8; i++) {
+                            const int w = (tl - 1) * NK + kq + 16 * i;
+                            const int p = w < it.wcount ? it.p_lo + w : it.s;
+                            const long long mr = sbhd ? (long long)p * g.B + it.b : it.row - it.s + p;
+                            src[i] = a.kv + mr * D + cc * 8;
+                        }
+                    } else {  // selected compressed keys
+                        const int u = tl - 1 - it.nw;
 #pragma unroll
                         for (int i = 0; i < 8; i++) {
                             bool ok;
-                            src[i] = a.kv_c + slot_key_row(a, it, t * NK + kq + 16 * i, ok) * D + cc * 8;
+                            src[i] = a.kv_c + id_key_row(a, it, idn[i], ok) * D + cc * 8;
                         }
-                        for (int kb = 0; kb < nkb; kb++) {
-                            wait_slot();
-                            const int st = x % NSTG;
-                            tma_slot[st] = false;
-                            // row kq + 16 i, chunk cc; (kq + 16 i) & 7 == kq & 7
-                            unsigned char *dst = ring + st * STG + kq * 128 + ((cc ^ (kq & 7)) << 4);
+                        if (u + 1 < nu) load_ids(u + 1 < it.nct ? u + 1 : u + 1 - it.nct);
+                    }
+                    for (int kb = 0; kb < nkb; kb++) {
+                        wait_slot(x);
+                        const int st = x % NSTG;
+                        tma_slot[st] = false;
+                        // row kq + 16 i, chunk cc; (kq + 16 i) & 7 == kq & 7
+                        unsigned char *dst = ring + st * STG + kq * 128 + ((cc ^ (kq & 7)) << 4);
 #pragma unroll
-                            for (int i = 0; i < 8; i++) cp_async16(dst + i * 16 * 128, src[i] + kb * 64);
-                            x++;
-                            if (x - grp0 == GRP) {  // the group is complete: commit it, hand over the previous one
-                                cp_async_commit();
-                                if (pend0 >= 0) {
-                                    cp_async_wait<1>();
-                                    signal(pend0, pend1);
-                                }
-                                pend0 = grp0;
-                                pend1 = x;
-                                grp0 = x;
+                        for (int i = 0; i < 8; i++) cp_async16(dst + i * 16 * 128, src[i] + kb * 64);
+                        x++;
+                        if (x - grp0 == GRP) {  // the group is complete: commit it, hand over the previous one
+                            cp_async_commit();
+                            if (pend0 >= 0) {
+                                cp_async_wait<1>();
+                                signal(pend0, pend1);
                             }
+                            pend0 = grp0;
+                            pend1 = x;
+                            grp0 = x;
                         }
                     }
+                }
                 if (grp0 < x) cp_async_commit();  // a last, partial group
                 cp_async_wait<0>();
                 if (pend0 >= 0) signal(pend0, pend1);
@@ -634,6 +665,8 @@ cudaError_t launch_teacher_h128_tc(const Geo &g, const __nv_bfloat16 *q, const _
     a.g = g;
     a.sink = sink;
     a.ids = ids;
+    a.q = q;
+    a.kv = kv;
     a.kv_c = kv_c;
     a.teacher = teacher;
     a.nkb = g.D / 64;

@@ -436,6 +436,7 @@ def test_bounded_wait_times_out_and_the_context_stays_usable():
     stream = torch.cuda.current_stream().cuda_stream
     assert B._lib.csa_selftest_bounded_wait(stream) == 0
     assert B._lib.csa_check_device_status(stream) == 6      # CSA_ERR_TIMEOUT
+    assert B.csa_last_timeout_site() == 990                 # the self-test (9), its wait site 90
     assert B._lib.csa_check_device_status(stream) == 0      # read and cleared
     out = U.check_step(synth.generate(small(idx_heads=64, idx_dim=128, heads=64, seed=17)))
     assert out["fwd_path"] == "tcgen05"
