@@ -1,0 +1,241 @@
+// k_topk_rows.cu -- exact per-row top-K of the fp32 score rows that the long-key-axis score kernel writes to the
+// workspace (the second half of step 2 on key axes past 1024 keys).
+//
+// What it computes ("[Bug] DSV4 unfused CSA indexer loss uses a compressed-only teacher ..." (Megatron-LM issue
+// #5776), sec. 1 excerpt: min(index_topk, n_compressed) selected keys per row; sec. 3 excerpt: invalid slots
+// -1; "Megatron-LM PR #8539" item 1: global ids): for row t with v_t visible keys, the min(K, v_t) largest
+// scores, ties to the lower key, written as ascending global ids with their scores; slots past them hold -1 and
+// -inf.  The same selection as the fused score kernel's for short key axes.
+//
+// Mapping.  One CTA of 512 threads per row (persistent, rows with the most keys first, two CTAs per SM).  The
+// row's scores are staged in shared memory when they fit (16384 keys); longer rows are re-read from global
+// memory (L2) on every pass.  Scores become order-preserving 32-bit keys (-0.0 like +0.0).  The K-th largest key
+// T comes from a radix walk in digits of up to 8 bits that starts at the highest bit in which the row's smallest
+// and largest keys differ (the bits above it are common to every key): per pass each warp counts the keys that
+// match the prefix found so far into its own 256-bin histogram, 256 threads add the sixteen histograms and scan
+// them from the top bin, and the bin holding the K-th largest key extends the prefix.  The selection is then
+// written in key order: each warp owns a contiguous range of keys, counts the keys above T and equal to T in it,
+// and after one block-wide exclusive scan writes its keys above T and its share of the keys equal to T (the
+// lowest-index ones first) by ballot compaction.
+#include "csa_tc.cuh"
+#include "csa_internal.cuh"
+
+namespace csa {
+
+namespace tk {
+
+constexpr int THREADS = 512;
+constexpr int NWARP = THREADS / 32;
+constexpr int VSM = 16384;  // score row elements staged in shared memory
+
+struct Smem {
+    float sv[VSM];               // the row's scores (rows of at most VSM keys)
+    uint32_t hist[NWARP][256];   // per-warp radix histograms
+    uint32_t wred[2][NWARP];     // per-warp partials of block reductions
+    int cnt[2][NWARP];           // per-warp counts of keys above / equal to T
+    uint32_t res[4];             // a pass's result: bin, entries above it, entries in it
+};
+
+// inverse of score_key (-0.0 comes back as +0.0: the same value)
+__device__ __forceinline__ float key_to_score(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__global__ void __launch_bounds__(THREADS, 2)
+topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ ids, float *__restrict__ selscore)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    const int K = g.K;
+    for (int i = blockIdx.x; i < g.rows; i += gridDim.x) {
+        const long long row = (long long)g.rows - 1 - i;
+        const Row R = decode_row(g, row);
+        const int v = R.v;
+        const int kk = v < K ? v : K;
+        const long long gid0 = key_gid(g, R, 0);
+        int32_t *orow = ids + row * K;
+        float *srow = selscore + row * K;
+        const float *src = scores + row * (long long)g.NC;
+        const bool staged = v <= VSM;
+        const float *sp = staged ? S.sv : src;
+        __syncthreads();  // the previous row's readers of sv and of the reduction slots are done
+        // stage the row and find the range [lo, hi] of its keys
+        uint32_t lo = 0xffffffffu, hi = 0u;
+        for (int j = tid; j < v; j += THREADS) {
+            const float f = src[j];
+            if (staged) S.sv[j] = f;
+            const uint32_t k = score_key(f);
+            lo = min(lo, k);
+            hi = max(hi, k);
+        }
+        lo = __reduce_min_sync(0xffffffffu, lo);
+        hi = __reduce_max_sync(0xffffffffu, hi);
+        if (lane == 0) {
+            S.wred[0][warp] = lo;
+            S.wred[1][warp] = hi;
+        }
+        __syncthreads();
+        lo = 0xffffffffu;
+        hi = 0u;
+#pragma unroll
+        for (int w = 0; w < NWARP; w++) {
+            lo = min(lo, S.wred[0][w]);
+            hi = max(hi, S.wred[1][w]);
+        }
+        if (kk == v) {
+            // every visible key is selected: key order as is
+            for (int j = tid; j < v; j += THREADS) {
+                orow[j] = (int32_t)(gid0 + j);
+                srow[j] = key_to_score(score_key(sp[j]));
+            }
+        } else {
+            // ---------------------------------------------------------------- the K-th largest key T
+            uint32_t T;
+            int need_eq;  // entries equal to T that belong to the top K (the lowest-index ones)
+            if (lo == hi) {
+                T = lo;
+                need_eq = kk;
+            } else {
+                int hb = 31 - __clz(lo ^ hi);              // top bit of the current digit
+                uint32_t prefix = hi & ~((2u << hb) - 1u);  // bits above it (2u << 31 wraps to 0)
+                int need = kk;  // rank of the wanted key among those matching the prefix, from the top
+#pragma unroll 1
+                while (true) {
+                    const int lb = hb >= 7 ? hb - 7 : 0;
+                    const uint32_t wmask = (2u << (hb - lb)) - 1u;
+                    const uint32_t pmask = ~((2u << hb) - 1u);
+#pragma unroll
+                    for (int q = 0; q < 8; q++) S.hist[warp][lane * 8 + q] = 0u;
+                    __syncwarp();
+                    for (int j = tid; j < v; j += THREADS) {
+                        const uint32_t k = score_key(sp[j]);
+                        if ((k & pmask) == prefix) atomicAdd(&S.hist[warp][(k >> lb) & wmask], 1u);
+                    }
+                    __syncthreads();
+                    if (tid < 256) {
+                        // thread t takes bin 255 - t: an inclusive scan in thread order counts from the top bin
+                        const int bin = 255 - tid;
+                        uint32_t c = 0u;
+#pragma unroll
+                        for (int w = 0; w < NWARP; w++) c += S.hist[w][bin];
+                        uint32_t incl = c;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += y;
+                        }
+                        if (lane == 31) S.wred[0][warp] = incl;
+                        asm volatile("bar.sync 1, 256;" ::: "memory");
+                        uint32_t off = 0u;
+                        for (int w = 0; w < warp; w++) off += S.wred[0][w];
+                        incl += off;
+                        const uint32_t before = incl - c;
+                        if (before < (uint32_t)need && (uint32_t)need <= incl) {
+                            S.res[0] = (uint32_t)bin;
+                            S.res[1] = before;
+                            S.res[2] = c;
+                        }
+                    }
+                    __syncthreads();
+                    const uint32_t bin = S.res[0], above = S.res[1];
+                    prefix |= bin << lb;
+                    need -= (int)above;
+                    if (lb == 0) break;
+                    hb = lb - 1;
+                    __syncthreads();  // every thread has read res before the next pass may overwrite it
+                }
+                T = prefix;
+                need_eq = need;
+            }
+            // ---------------------------------------------------------------- the selection, in key order
+            // warp w owns keys [w seg, (w + 1) seg), seg a multiple of 32
+            const int seg = ((v + NWARP * 32 - 1) / (NWARP * 32)) * 32;
+            const int j0 = warp * seg, j1 = min(v, j0 + seg);
+            int ngt = 0, neq = 0;
+            for (int c0 = j0; c0 < j1; c0 += 32) {
+                const int j = c0 + lane;
+                const uint32_t k = j < j1 ? score_key(sp[j]) : 0u;
+                ngt += __popc(__ballot_sync(0xffffffffu, j < j1 && k > T));
+                neq += __popc(__ballot_sync(0xffffffffu, j < j1 && k == T));
+            }
+            if (lane == 0) {
+                S.cnt[0][warp] = ngt;
+                S.cnt[1][warp] = neq;
+            }
+            __syncthreads();
+            int eq_before = 0, sel_before = 0;
+            for (int w = 0; w < warp; w++) {
+                const int e = S.cnt[1][w];
+                const int take = min(max(need_eq - eq_before, 0), e);
+                sel_before += S.cnt[0][w] + take;
+                eq_before += e;
+            }
+            int base = sel_before, eq_seen = eq_before;
+            for (int c0 = j0; c0 < j1; c0 += 32) {
+                const int j = c0 + lane;
+                const uint32_t k = j < j1 ? score_key(sp[j]) : 0u;
+                const bool eq = j < j1 && k == T;
+                const unsigned meq = __ballot_sync(0xffffffffu, eq);
+                const bool sel = (j < j1 && k > T) || (eq && eq_seen + __popc(meq & lt) < need_eq);
+                eq_seen += __popc(meq);
+                const unsigned ms = __ballot_sync(0xffffffffu, sel);
+                if (sel) {
+                    const int pos = base + __popc(ms & lt);
+                    orow[pos] = (int32_t)(gid0 + j);
+                    srow[pos] = key_to_score(k);
+                }
+                base += __popc(ms);
+            }
+        }
+        for (int s2 = kk + tid; s2 < K; s2 += THREADS) {
+            orow[s2] = -1;
+            srow[s2] = -INFINITY;
+        }
+    }
+}
+
+// Debug copy: rows [row0, row0 + nrows) of the score rows into dump [nrows][NC], -inf where not visible.
+__global__ void dump_rows_kernel(const float *__restrict__ scores, Geo g, long long row0, long long nrows,
+                                 float *__restrict__ dump)
+{
+    for (long long r = blockIdx.x; r < nrows; r += gridDim.x) {
+        const long long row = row0 + r;
+        const int v = row < g.rows ? decode_row(g, row).v : 0;
+        for (int j = threadIdx.x; j < g.NC; j += blockDim.x)
+            dump[r * g.NC + j] = j < v ? scores[row * (long long)g.NC + j] : -INFINITY;
+    }
+}
+
+}  // namespace tk
+
+size_t topk_rows_smem_bytes() { return sizeof(tk::Smem); }
+
+cudaError_t launch_topk_rows(const Geo &g, const float *scores, int32_t *ids, float *selscore, cudaStream_t st)
+{
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tk::topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(tk::Smem));
+    if (e != cudaSuccess) return e;
+    const int grid = g.rows < 2 * sms ? g.rows : 2 * sms;
+    tk::topk_rows_kernel<<<grid, tk::THREADS, sizeof(tk::Smem), st>>>(scores, g, ids, selscore);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dump_rows(const Geo &g, const float *scores, long long row0, long long nrows, float *dump,
+                             cudaStream_t st)
+{
+    if (nrows <= 0) return cudaSuccess;
+    const int grid = nrows < 1024 ? (int)nrows : 1024;
+    tk::dump_rows_kernel<<<grid, 256, 0, st>>>(scores, g, row0, nrows, dump);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace csa
