@@ -198,8 +198,15 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         // -------------------------------------------------------------------- MMA issue (whole warp)
         // Rows are decoded lane-parallel (lane l: the CTA's row k + l) and the loop reads the tile count of row k
         // by a shuffle.  Per row: skip its q stages (the epilogue copies them into TMEM), wait for q in
-        // TMEM, then per tile and K-block four MMAs of K = 16 with A = q's columns of that K-block.
-        int x = 0, tc = 0, rc = 0, k = 0, nt_lane = 0;
+        // TMEM, then per tile and K-block four MMAs of K = 16 with A = q's columns of that K-block.  A barrier
+        // test costs the issuing thread a shared-memory round trip even when the phase is complete, so the next
+        // stage's full barrier (and, at a tile's last K-block, the next accumulator's empty barrier) is probed
+        // before this K-block's MMAs are issued; a probe that comes back false falls back to the bounded wait.
+        // (A probe passes only once the awaited phase has completed: the barrier cannot be two phases behind,
+        // since the stage one ring turn earlier has been consumed already.)
+        int st = 0, tc = 0, rc = 0, k = 0, nt_lane = 0;  // ring position of the next stage and its parity
+        uint32_t ph = 0;
+        bool f_ready = false, t_ready = false;
         for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
             if ((k & 31) == 0) {
                 const int il = i + lane * (int)gridDim.x;
@@ -207,24 +214,35 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
             }
             const int nt = __shfl_sync(0xffffffffu, nt_lane, k & 31);
             if (nt == 0) continue;
-            x += nkb;
+            st += nkb;  // the row's q stages
+            if (st >= NSTG) {
+                st -= NSTG;
+                ph ^= 1u;
+            }
             wait_bar(q_ready, rc & 1, abort_flag, err, 62);
             fence_after();
             for (int tt = 0; tt < nt; tt++) {
                 const int tb = tc & 1;
-                wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, err, 63);
+                if (!t_ready) wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, err, 63);
+                t_ready = false;
                 fence_after();
                 const uint32_t d = tmem + ACC0 + (uint32_t)(tb * NK);
-                for (int kb = 0; kb < nkb; kb++, x++) {
-                    const int st = x % NSTG;
-                    wait_bar(full + st, (x / NSTG) & 1, abort_flag, err, 64);
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!f_ready) wait_bar(full + st, ph, abort_flag, err, 64);
                     fence_after();
+                    const int st1 = st + 1 == NSTG ? 0 : st + 1;
+                    const uint32_t ph1 = st1 == 0 ? ph ^ 1u : ph;
+                    // the next stage is the row's (the next row's q stages are not the MMA's to wait for)
+                    f_ready = (kb + 1 < nkb || tt + 1 < nt) && mbar_test(full + st1, ph1);
+                    if (kb + 1 == nkb && tt + 1 < nt) t_ready = mbar_test(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1);
                     const unsigned char *pb = ring + st * STG;
 #pragma unroll
                     for (int k4 = 0; k4 < 4; k4++)
                         mma_bf16_ts_w(d, tmem + (uint32_t)(kb * 32 + k4 * 8), desc_kmajor(pb + k4 * 32), IDESC,
                                       (kb | k4) ? 1u : 0u);
                     mma_commit_w(empty + st);
+                    st = st1;
+                    ph = ph1;
                 }
                 mma_commit_w(t_full + tb);
                 tc++;

@@ -63,13 +63,25 @@ topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ 
         const float *sp = staged ? S.sv : src;
         __syncthreads();  // the previous row's readers of sv and of the reduction slots are done
         // stage the row and find the range [lo, hi] of its keys
+        // (eight loads in flight per thread: the row comes from DRAM)
         uint32_t lo = 0xffffffffu, hi = 0u;
-        for (int j = tid; j < v; j += THREADS) {
-            const float f = src[j];
-            if (staged) S.sv[j] = f;
-            const uint32_t k = score_key(f);
-            lo = min(lo, k);
-            hi = max(hi, k);
+        for (int j0 = 0; j0 < v; j0 += 8 * THREADS) {
+            float f[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int j = j0 + u * THREADS + tid;
+                f[u] = j < v ? src[j] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int j = j0 + u * THREADS + tid;
+                if (j < v) {
+                    if (staged) S.sv[j] = f[u];
+                    const uint32_t k = score_key(f[u]);
+                    lo = min(lo, k);
+                    hi = max(hi, k);
+                }
+            }
         }
         lo = __reduce_min_sync(0xffffffffu, lo);
         hi = __reduce_max_sync(0xffffffffu, hi);
@@ -110,9 +122,19 @@ topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ 
 #pragma unroll
                     for (int q = 0; q < 8; q++) S.hist[warp][lane * 8 + q] = 0u;
                     __syncwarp();
-                    for (int j = tid; j < v; j += THREADS) {
-                        const uint32_t k = score_key(sp[j]);
-                        if ((k & pmask) == prefix) atomicAdd(&S.hist[warp][(k >> lb) & wmask], 1u);
+                    for (int j0 = 0; j0 < v; j0 += 4 * THREADS) {
+                        float f[4];
+#pragma unroll
+                        for (int u = 0; u < 4; u++) {
+                            const int j = j0 + u * THREADS + tid;
+                            f[u] = j < v ? sp[j] : 0.f;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; u++) {
+                            const uint32_t k = score_key(f[u]);
+                            if (j0 + u * THREADS + tid < v && (k & pmask) == prefix)
+                                atomicAdd(&S.hist[warp][(k >> lb) & wmask], 1u);
+                        }
                     }
                     __syncthreads();
                     if (tid < 256) {
