@@ -366,13 +366,11 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
             if (t_in_row == 0) wait_bar(dq_empty, (rq & 1) ^ 1, abort_flag, err, 56);
             wait_bar(g_full + gb, (y / NX) & 1, abort_flag, err, 57);
             fence_after();
-            const unsigned char *pk = sK + (y % NKT) * KT;
-            const unsigned char *pg = sG + gb * GT;
-#pragma unroll
-            for (int s = 0; s < 8; s++)
-                mma_bf16_w(tDQ, desc_sw128(pk + s * 2048, KHALF, 1024), desc_sw128(pg + s * 2048, GT, 1024), IDESC_DQ,
-                           (t_in_row == 0 && s == 0) ? 0u : 1u);
-            mma_commit_w(k_empty + y % NKT);
+            // eight MMAs of K = 16 (both operands MN-major, 2 KB further per MMA) in two groups of four
+            const uint64_t dk = desc_sw128(sK + (y % NKT) * KT, KHALF, 1024), dg = desc_sw128(sG + gb * GT, GT, 1024);
+            mma4_ss_w(tDQ, dk, 2048 >> 4, dg, 2048 >> 4, IDESC_DQ, t_in_row == 0 ? 0u : 1u, 0u);
+            mma4_ss_w(tDQ, dk + (4 * 2048 >> 4), 2048 >> 4, dg + (4 * 2048 >> 4), 2048 >> 4, IDESC_DQ, 1u,
+                      su32(k_empty + y % NKT));
             mma_commit_w(g_empty + gb);
         };
         for (int i = blockIdx.x; i < total; i += gridDim.x) {
@@ -389,13 +387,10 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
                 wait_bar(x_empty + xb, ((x / NX) & 1) ^ 1, abort_flag, err, 60);
                 fence_after();
                 const unsigned char *pk = sK + st * KT;
-#pragma unroll
-                for (int kh = 0; kh < 2; kh++)
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; k4++)
-                        mma_bf16_w(tX + (uint32_t)(xb * 64), desc_kmajor(pk + kh * KHALF + k4 * 32),
-                                   desc_kmajor(pq + kh * QHALF + k4 * 32), IDESC_X, (kh | k4) ? 1u : 0u);
-                mma_commit_w(x_full + xb);
+                // per 64-wide K-half four MMAs of K = 16 (both operands K-major, 32 bytes further per MMA)
+                mma4_ss_w(tX + (uint32_t)(xb * 64), desc_kmajor(pk), 2, desc_kmajor(pq), 2, IDESC_X, 0u, 0u);
+                mma4_ss_w(tX + (uint32_t)(xb * 64), desc_kmajor(pk + KHALF), 2, desc_kmajor(pq + QHALF), 2, IDESC_X, 1u,
+                          su32(x_full + xb));
                 if (t == it.nt - 1) mma_commit_w(q_empty + qb);  // the row's q is read by its X groups only
                 if (t >= 2) mma2(x - 2, t - 2);
                 x++;

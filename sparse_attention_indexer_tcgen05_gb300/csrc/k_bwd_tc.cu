@@ -1135,12 +1135,12 @@ dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 wait_bar(b_full + bs, (qs / S_QSTG) & 1, abort_flag, err, 37);
                 wait_bar(gk_full + xb, (xc / S_XSTG) & 1, abort_flag, err, 38);
                 fence_after();
-                const unsigned char *pq = sB + bs * QBLK;
-#pragma unroll
-                for (int s = 0; s < 8; s++)
-                    mma_bf16_ts_w(tDK, tG + (uint32_t)(xb * 64 + 8 * s), desc_sw128(pq + s * 2048, HALF, 1024), IDESC_DK,
-                                  (pi == 0 && s == 0) ? 0u : 1u);
-                mma_commit_w(x_empty + xb);
+                // eight MMAs of K = 16 (A: G columns 8 s of the slot; B: the q block, 2 KB further per MMA) in two
+                // groups of four under one elect each, then the commits
+                const uint64_t bq = desc_sw128(sB + bs * QBLK, HALF, 1024);
+                mma4_ts_w(tDK, tG + (uint32_t)(xb * 64), 8, 16, bq, 2048 >> 4, IDESC_DK, pi == 0 ? 0u : 1u, 0u);
+                mma4_ts_w(tDK, tG + (uint32_t)(xb * 64 + 32), 8, 16, bq + (4 * 2048 >> 4), 2048 >> 4, IDESC_DK, 1u,
+                          su32(x_empty + xb));
                 mma_commit_w(b_empty + bs);
                 qs++;
                 xc++;

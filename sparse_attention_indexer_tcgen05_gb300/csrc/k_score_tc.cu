@@ -489,10 +489,8 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
                     fence_after();
                     const unsigned char *pa = sA + st * A_HALF;
                     const unsigned char *pb = pb0 + kh * B_HALF;
-#pragma unroll
-                    for (int kk = 0; kk < 4; kk++)
-                        mma_bf16_w(d, desc_kmajor(pa + kk * 32), desc_kmajor(pb + kk * 32), IDESC, (kh | kk) != 0);
-                    mma_commit_w(a_empty + st);
+                    // four MMAs of K = 16 under one elect, then the stage's commit
+                    mma4_ss_w(d, desc_kmajor(pa), 2, desc_kmajor(pb), 2, IDESC, kh != 0 ? 1u : 0u, su32(a_empty + st));
                     st = st1;
                     aph = ph1;
                 }

@@ -204,6 +204,7 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         // before this K-block's MMAs are issued; a probe that comes back false falls back to the bounded wait.
         // (A probe passes only once the awaited phase has completed: the barrier cannot be two phases behind,
         // since the stage one ring turn earlier has been consumed already.)
+        const uint64_t ring_desc = desc_kmajor(ring);  // stage st: + st * STG / 16 in the address field
         int st = 0, tc = 0, rc = 0, k = 0, nt_lane = 0;  // ring position of the next stage and its parity
         uint32_t ph = 0;
         bool f_ready = false, t_ready = false;
@@ -235,12 +236,9 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                     // the next stage is the row's (the next row's q stages are not the MMA's to wait for)
                     f_ready = (kb + 1 < nkb || tt + 1 < nt) && mbar_test(full + st1, ph1);
                     if (kb + 1 == nkb && tt + 1 < nt) t_ready = mbar_test(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1);
-                    const unsigned char *pb = ring + st * STG;
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; k4++)
-                        mma_bf16_ts_w(d, tmem + (uint32_t)(kb * 32 + k4 * 8), desc_kmajor(pb + k4 * 32), IDESC,
-                                      (kb | k4) ? 1u : 0u);
-                    mma_commit_w(empty + st);
+                    // four MMAs of K = 16 (A: q's columns of K-block kb; B: 32 bytes further per MMA), one commit
+                    mma4_ts_w(d, tmem + (uint32_t)(kb * 32), 8, 16, ring_desc + (uint64_t)(st * (STG >> 4)), 2, IDESC,
+                              kb != 0 ? 1u : 0u, su32(empty + st));
                     st = st1;
                     ph = ph1;
                 }

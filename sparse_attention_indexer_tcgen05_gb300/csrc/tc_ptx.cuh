@@ -152,6 +152,51 @@ __device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, 
                  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
+// Four MMAs of K = 16 under one elect.sync, for issuing warps that share their scheduler with busy warps (every
+// instruction of the issue loop then waits for an issue slot): A from TMEM columns a, a + s1, a + s2, a + s1 + s2
+// (s1 = 8, s2 = 16: four consecutive K-steps of 16 bf16), B the shared-memory descriptor b advanced by db per MMA (db in the descriptor's 16-byte address units; the address field must not
+// carry, i.e. the operands lie below 256 KB of shared memory), k = 0..3.  D is accumulated except by the first
+// MMA when acc0 == 0.  If bar != 0 (a shared-memory address), the four MMAs (and every earlier one of this
+// thread) are then committed to that mbarrier.
+__device__ __forceinline__ void mma4_ts_w(uint32_t d, uint32_t a, uint32_t s1, uint32_t s2, uint64_t b, uint64_t db,
+                                          uint32_t idesc, uint32_t acc0, uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e, p, t, c, ec;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.b32 p, %5, 0;\n\t"
+                 "setp.ne.b32 t, %4, 0;\n\t"  // the instruction descriptor is never 0: always true
+                 "setp.ne.b32 c, %6, 0;\n\t"
+                 "and.pred ec, e, c;\n\t"
+                 "add.s64 b1, %2, %3;\n\tadd.s64 b2, b1, %3;\n\tadd.s64 b3, b2, %3;\n\t"
+                 "add.u32 a1, %1, %7;\n\tadd.u32 a2, %1, %8;\n\tadd.u32 a3, a1, %8;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, t;\n\t"
+                 "@ec tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+                 ::"r"(d), "r"(a), "l"(b), "l"(db), "r"(idesc), "r"(acc0), "r"(bar), "r"(s1), "r"(s2)
+                 : "memory");
+}
+// The same with A also in shared memory: A descriptor a advanced by da per MMA.
+__device__ __forceinline__ void mma4_ss_w(uint32_t d, uint64_t a, uint64_t da, uint64_t b, uint64_t db, uint32_t idesc,
+                                          uint32_t acc0, uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e, p, t, c, ec;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.b32 p, %6, 0;\n\t"
+                 "setp.ne.b32 t, %5, 0;\n\t"
+                 "setp.ne.b32 c, %7, 0;\n\t"
+                 "and.pred ec, e, c;\n\t"
+                 "add.s64 a1, %1, %2;\n\tadd.s64 a2, a1, %2;\n\tadd.s64 a3, a2, %2;\n\t"
+                 "add.s64 b1, %3, %4;\n\tadd.s64 b2, b1, %4;\n\tadd.s64 b3, b2, %4;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %5, p;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %5, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %5, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %5, t;\n\t"
+                 "@ec tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
+                 ::"r"(d), "l"(a), "l"(da), "l"(b), "l"(db), "r"(idesc), "r"(acc0), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void mma_commit_w(uint64_t *bar)
 {
     asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
