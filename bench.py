@@ -54,10 +54,18 @@ def stage_kernels(cfg, key_width: int) -> dict:
     """The main kernel of each stage the roofline may be reported for, and the source file it is built from: the
     score stage is one fused kernel on key axes up to 1024, and on longer ones the score-row kernel (all of the
     stage's MMAs) followed by the top-k kernel."""
+    if cfg.dtype != "bf16":  # fp32 values take the CUDA-core kernels
+        return {"score_topk": ("score_topk_generic_kernel", "k_generic.cu"),
+                "teacher": ("teacher_generic_kernel", "k_generic.cu")}
     score = ("score_rows_long_tc_kernel" if key_width > 1024 else "score_topk_tc_kernel", "k_score_tc.cu")
     teacher = (("teacher_h128_tc_kernel", "k_teacher_h128_tc.cu") if cfg.heads == 128
                else ("teacher_tc_kernel", "k_teacher_tc.cu"))
     return {"score_topk": score, "teacher": teacher}
+
+
+# fp32 FMA peak of the GB300 (CUDA cores): 152 SMs x 128 fp32 lanes x 2 flops per FMA x 2.07 GHz (the maximum SM
+# clock), the ceiling of the CUDA-core kernels that fp32 values take
+FP32_FMA_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def _kernel_sha1(source: str) -> str:
@@ -381,6 +389,9 @@ def run_ours(args, cfg):
     tensor_peak = peaks["bf16_tflops"] if peaks else 1900.0
     hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
     peak_src = "measured" if peaks else "fallback"
+    bound = "tensor"
+    if cfg.dtype != "bf16":  # CUDA-core fp32 FMA: a peak derived from unit counts and the clock
+        tensor_peak, bound, peak_src = FP32_FMA_PEAK_TFLOPS, "alu", "derived (152 SMs x 128 FP32 lanes x 2 x 2.07 GHz)"
     achieved_tf = fl[dom] / (stage_ms[dom] / 1e3) / 1e12
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -389,7 +400,7 @@ def run_ours(args, cfg):
     kname, ksrc = kernels[dom]
     if kname in rec.get("per_launch_bytes", {}) and rec.get("kernel_source_sha1", {}).get(kname) == _kernel_sha1(ksrc):
         traffic = rec["per_launch_bytes"][kname]
-    roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": tensor_peak, "unit": "TFLOP/s",
+    roofline = {"bound": bound, "achieved": achieved_tf, "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": achieved_tf / tensor_peak, "traffic": traffic, "kernel": single_kernel[dom], "stage": dom,
                 "peak_source": peak_src,
                 "stage_ms": stage_ms,
