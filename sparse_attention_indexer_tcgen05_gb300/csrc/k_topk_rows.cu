@@ -8,15 +8,17 @@
 // -inf.  The same selection as the fused score kernel's for short key axes.
 //
 // Mapping.  One CTA of 512 threads per row (persistent, rows with the most keys first, two CTAs per SM).  The
-// row's scores are staged in shared memory when they fit (16384 keys); longer rows are re-read from global
-// memory (L2) on every pass.  Scores become order-preserving 32-bit keys (-0.0 like +0.0).  The K-th largest key
-// T comes from a radix walk in digits of up to 8 bits that starts at the highest bit in which the row's smallest
-// and largest keys differ (the bits above it are common to every key): per pass each warp counts the keys that
-// match the prefix found so far into its own 256-bin histogram, 256 threads add the sixteen histograms and scan
-// them from the top bin, and the bin holding the K-th largest key extends the prefix.  The selection is then
-// written in key order: each warp owns a contiguous range of keys, counts the keys above T and equal to T in it,
-// and after one block-wide exclusive scan writes its keys above T and its share of the keys equal to T (the
-// lowest-index ones first) by ballot compaction.
+// row's scores become order-preserving 32-bit keys (-0.0 like +0.0), staged in shared memory when the row has at
+// most 16384 keys (longer rows are re-read from global memory, L2, on every pass), together with the smallest and
+// largest key.  The K-th largest key T: the bits above the highest bit in which the smallest and largest keys
+// differ are common to every key; one pass counts the keys into 2048 bins of the next 11 bits (two
+// sub-histograms, alternate warps), a block-wide scan from the top bin finds the bin that holds the K-th largest
+// key, and a second pass collects that bin's keys (usually a few dozen) into a short list in which one warp
+// finds T exactly by a bitwise search.  A bin of more than 1024 keys (heavy ties or a very narrow range) is
+// refined by the next 11 bits instead.  The selection is then written in key order: each warp owns a
+// contiguous range of keys, counts its keys above T and equal to T, and after one block-wide scan of those
+// counts writes its keys above T and its share of the keys equal to T (the lowest-index ones first) by ballot
+// compaction.
 #include "csa_tc.cuh"
 #include "csa_internal.cuh"
 
@@ -26,14 +28,18 @@ namespace tk {
 
 constexpr int THREADS = 512;
 constexpr int NWARP = THREADS / 32;
-constexpr int VSM = 16384;  // score row elements staged in shared memory
+constexpr int VSM = 16384;   // keys of a row staged in shared memory
+constexpr int DB = 11;       // digit bits per histogram pass
+constexpr int NBIN = 1 << DB;
+constexpr int CMAX = 1024;   // candidate list (the keys of the bin holding the K-th largest key)
 
 struct Smem {
-    float sv[VSM];               // the row's scores (rows of at most VSM keys)
-    uint32_t hist[NWARP][256];   // per-warp radix histograms
+    uint32_t sk[VSM];            // the row's keys (rows of at most VSM keys)
+    uint32_t hist[2][NBIN];      // sub-histograms of even and odd warps
+    uint32_t cand[CMAX];         // keys of the boundary bin
     uint32_t wred[2][NWARP];     // per-warp partials of block reductions
     int cnt[2][NWARP];           // per-warp counts of keys above / equal to T
-    uint32_t res[4];             // a pass's result: bin, entries above it, entries in it
+    uint32_t res[4];             // results passed between phases
 };
 
 // inverse of score_key (-0.0 comes back as +0.0: the same value)
@@ -60,10 +66,10 @@ topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ 
         float *srow = selscore + row * K;
         const float *src = scores + row * (long long)g.NC;
         const bool staged = v <= VSM;
-        const float *sp = staged ? S.sv : src;
-        __syncthreads();  // the previous row's readers of sv and of the reduction slots are done
-        // stage the row and find the range [lo, hi] of its keys
-        // (eight loads in flight per thread: the row comes from DRAM)
+        // key j of the row: from shared memory when staged, else converted from the score row in global memory
+        auto key_at = [&](int j) -> uint32_t { return staged ? S.sk[j] : score_key(src[j]); };
+        __syncthreads();  // the previous row's readers of shared memory are done
+        // ---- stage the keys (eight loads in flight per thread: the row comes from DRAM) and their range
         uint32_t lo = 0xffffffffu, hi = 0u;
         for (int j0 = 0; j0 < v; j0 += 8 * THREADS) {
             float f[8];
@@ -76,8 +82,8 @@ topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ 
             for (int u = 0; u < 8; u++) {
                 const int j = j0 + u * THREADS + tid;
                 if (j < v) {
-                    if (staged) S.sv[j] = f[u];
                     const uint32_t k = score_key(f[u]);
+                    if (staged) S.sk[j] = k;
                     lo = min(lo, k);
                     hi = max(hi, k);
                 }
@@ -101,7 +107,7 @@ topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ 
             // every visible key is selected: key order as is
             for (int j = tid; j < v; j += THREADS) {
                 orow[j] = (int32_t)(gid0 + j);
-                srow[j] = key_to_score(score_key(sp[j]));
+                srow[j] = key_to_score(key_at(j));
             }
         } else {
             // ---------------------------------------------------------------- the K-th largest key T
@@ -114,63 +120,118 @@ topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ 
                 int hb = 31 - __clz(lo ^ hi);              // top bit of the current digit
                 uint32_t prefix = hi & ~((2u << hb) - 1u);  // bits above it (2u << 31 wraps to 0)
                 int need = kk;  // rank of the wanted key among those matching the prefix, from the top
+                bool done = false;
 #pragma unroll 1
-                while (true) {
-                    const int lb = hb >= 7 ? hb - 7 : 0;
+                while (!done) {
+                    const int lb = hb >= DB - 1 ? hb - (DB - 1) : 0;  // digit bits lb .. hb
                     const uint32_t wmask = (2u << (hb - lb)) - 1u;
                     const uint32_t pmask = ~((2u << hb) - 1u);
-#pragma unroll
-                    for (int q = 0; q < 8; q++) S.hist[warp][lane * 8 + q] = 0u;
-                    __syncwarp();
+                    for (int b = tid; b < 2 * NBIN; b += THREADS) (&S.hist[0][0])[b] = 0u;
+                    __syncthreads();
+                    uint32_t *h = S.hist[warp & 1];
                     for (int j0 = 0; j0 < v; j0 += 4 * THREADS) {
-                        float f[4];
+                        uint32_t kq[4];
 #pragma unroll
                         for (int u = 0; u < 4; u++) {
                             const int j = j0 + u * THREADS + tid;
-                            f[u] = j < v ? sp[j] : 0.f;
+                            kq[u] = j < v ? key_at(j) : 0u;
                         }
 #pragma unroll
-                        for (int u = 0; u < 4; u++) {
-                            const uint32_t k = score_key(f[u]);
-                            if (j0 + u * THREADS + tid < v && (k & pmask) == prefix)
-                                atomicAdd(&S.hist[warp][(k >> lb) & wmask], 1u);
+                        for (int u = 0; u < 4; u++)
+                            if (j0 + u * THREADS + tid < v && (kq[u] & pmask) == prefix)
+                                atomicAdd(h + ((kq[u] >> lb) & wmask), 1u);
+                    }
+                    __syncthreads();
+                    // thread t takes bins NBIN - 1 - (4 t + q): an inclusive scan in thread order counts from the top
+                    uint32_t c[4], tot = 0u;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const int bin = NBIN - 1 - (4 * tid + q);
+                        c[q] = S.hist[0][bin] + S.hist[1][bin];
+                        tot += c[q];
+                    }
+                    uint32_t incl = tot;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    if (lane == 31) S.wred[0][warp] = incl;
+                    __syncthreads();
+                    uint32_t off = 0u;
+                    for (int w = 0; w < warp; w++) off += S.wred[0][w];
+                    incl += off;
+                    const uint32_t before = incl - tot;
+                    if (before < (uint32_t)need && (uint32_t)need <= incl) {
+                        uint32_t acc = before;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            if (acc + c[q] >= (uint32_t)need) {
+                                S.res[0] = (uint32_t)(NBIN - 1 - (4 * tid + q));
+                                S.res[1] = acc;
+                                S.res[2] = c[q];
+                                break;
+                            }
+                            acc += c[q];
                         }
                     }
                     __syncthreads();
-                    if (tid < 256) {
-                        // thread t takes bin 255 - t: an inclusive scan in thread order counts from the top bin
-                        const int bin = 255 - tid;
-                        uint32_t c = 0u;
-#pragma unroll
-                        for (int w = 0; w < NWARP; w++) c += S.hist[w][bin];
-                        uint32_t incl = c;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                            if (lane >= o) incl += y;
-                        }
-                        if (lane == 31) S.wred[0][warp] = incl;
-                        asm volatile("bar.sync 1, 256;" ::: "memory");
-                        uint32_t off = 0u;
-                        for (int w = 0; w < warp; w++) off += S.wred[0][w];
-                        incl += off;
-                        const uint32_t before = incl - c;
-                        if (before < (uint32_t)need && (uint32_t)need <= incl) {
-                            S.res[0] = (uint32_t)bin;
-                            S.res[1] = before;
-                            S.res[2] = c;
-                        }
-                    }
-                    __syncthreads();
-                    const uint32_t bin = S.res[0], above = S.res[1];
+                    const uint32_t bin = S.res[0], above = S.res[1], cnt = S.res[2];
                     prefix |= bin << lb;
                     need -= (int)above;
-                    if (lb == 0) break;
-                    hb = lb - 1;
-                    __syncthreads();  // every thread has read res before the next pass may overwrite it
+                    if (lb == 0) {  // the bin is a single key value
+                        T = prefix;
+                        need_eq = need;
+                        done = true;
+                    } else if (cnt <= (uint32_t)CMAX) {
+                        // collect the bin's keys, then one warp finds the need-th largest of them bit by bit
+                        const uint32_t cmask = ~((1u << lb) - 1u);
+                        if (tid == 0) S.res[3] = 0u;
+                        __syncthreads();
+                        for (int j0 = 0; j0 < v; j0 += 4 * THREADS) {
+                            uint32_t kq[4];
+#pragma unroll
+                            for (int u = 0; u < 4; u++) {
+                                const int j = j0 + u * THREADS + tid;
+                                kq[u] = j < v ? key_at(j) : 0u;
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; u++)
+                                if (j0 + u * THREADS + tid < v && (kq[u] & cmask) == prefix)
+                                    S.cand[atomicAdd(&S.res[3], 1u)] = kq[u];
+                        }
+                        __syncthreads();
+                        if (warp == 0) {
+                            uint32_t key[CMAX / 32];
+#pragma unroll
+                            for (int e = 0; e < CMAX / 32; e++) key[e] = 32 * e + lane < (int)cnt ? S.cand[32 * e + lane] : 0u;
+                            uint32_t t = prefix;  // every candidate is at or above it
+#pragma unroll 1
+                            for (int bit = lb - 1; bit >= 0; bit--) {
+                                const uint32_t cc = t | (1u << bit);
+                                unsigned c2 = 0u;
+#pragma unroll
+                                for (int e = 0; e < CMAX / 32; e++) c2 += key[e] >= cc ? 1u : 0u;
+                                if ((int)__reduce_add_sync(0xffffffffu, c2) >= need) t = cc;
+                            }
+                            unsigned gt = 0u;
+#pragma unroll
+                            for (int e = 0; e < CMAX / 32; e++) gt += key[e] > t ? 1u : 0u;
+                            gt = __reduce_add_sync(0xffffffffu, gt);
+                            if (lane == 0) {
+                                S.res[0] = t;
+                                S.res[1] = (uint32_t)(need - (int)gt);
+                            }
+                        }
+                        __syncthreads();
+                        T = S.res[0];
+                        need_eq = (int)S.res[1];
+                        done = true;
+                    } else {
+                        hb = lb - 1;  // a crowded bin: refine by the next digit
+                    }
+                    __syncthreads();  // every thread has read res before it is written again
                 }
-                T = prefix;
-                need_eq = need;
             }
             // ---------------------------------------------------------------- the selection, in key order
             // warp w owns keys [w seg, (w + 1) seg), seg a multiple of 32
@@ -179,7 +240,7 @@ topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ 
             int ngt = 0, neq = 0;
             for (int c0 = j0; c0 < j1; c0 += 32) {
                 const int j = c0 + lane;
-                const uint32_t k = j < j1 ? score_key(sp[j]) : 0u;
+                const uint32_t k = j < j1 ? key_at(j) : 0u;
                 ngt += __popc(__ballot_sync(0xffffffffu, j < j1 && k > T));
                 neq += __popc(__ballot_sync(0xffffffffu, j < j1 && k == T));
             }
@@ -198,7 +259,7 @@ topk_rows_kernel(const float *__restrict__ scores, Geo g, int32_t *__restrict__ 
             int base = sel_before, eq_seen = eq_before;
             for (int c0 = j0; c0 < j1; c0 += 32) {
                 const int j = c0 + lane;
-                const uint32_t k = j < j1 ? score_key(sp[j]) : 0u;
+                const uint32_t k = j < j1 ? key_at(j) : 0u;
                 const bool eq = j < j1 && k == T;
                 const unsigned meq = __ballot_sync(0xffffffffu, eq);
                 const bool sel = (j < j1 && k > T) || (eq && eq_seen + __popc(meq & lt) < need_eq);
