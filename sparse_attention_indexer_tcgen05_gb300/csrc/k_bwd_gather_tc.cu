@@ -360,11 +360,17 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
         // ---------------------------------------------------------------- MMA issue (whole warp)
         // Per row: MMA1 of tile t, then MMA2 of tile t - 2 (whose G' the epilogue has had two tiles' time to
         // write); the row's last two MMA2 close it.
+        // Barrier tests cost the issuing thread a shared-memory round trip, so after each MMA group the barriers
+        // the next groups need are probed (two per round trip) while the MMAs just issued run; the warp waits only
+        // on a barrier no probe has seen complete.  (None of them can be two phases behind: their previous uses
+        // have been consumed.)
         int x = 0, rq = 0;
+        bool g_rdy = false, k_rdy = false, x_rdy = false;  // G' of the next MMA2; k tile and X slot of the next tile
         auto mma2 = [&](int y, int t_in_row) {  // dQ'^T += k^T G' for the tile at ring position y
             const int gb = y % NX;
             if (t_in_row == 0) wait_bar(dq_empty, (rq & 1) ^ 1, abort_flag, err, 56);
-            wait_bar(g_full + gb, (y / NX) & 1, abort_flag, err, 57);
+            if (!g_rdy) wait_bar(g_full + gb, (y / NX) & 1, abort_flag, err, 57);
+            g_rdy = false;
             fence_after();
             // eight MMAs of K = 16 (both operands MN-major, 2 KB further per MMA) in two groups of four
             const uint64_t dk = desc_sw128(sK + (y % NKT) * KT, KHALF, 1024), dg = desc_sw128(sG + gb * GT, GT, 1024);
@@ -372,6 +378,10 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
             mma4_ss_w(tDQ, dk + (4 * 2048 >> 4), 2048 >> 4, dg + (4 * 2048 >> 4), 2048 >> 4, IDESC_DQ, 1u,
                       su32(k_empty + y % NKT));
             mma_commit_w(g_empty + gb);
+            // the next tile's X slot (and its k tile, if not yet seen), while these MMAs run
+            const uint32_t m = mbar_test2(x_empty + x % NX, ((x / NX) & 1) ^ 1, k_full + x % NKT, (x / NKT) & 1);
+            x_rdy = (m & 1u) != 0u;
+            k_rdy = k_rdy || (m & 2u) != 0u;
         };
         for (int i = blockIdx.x; i < total; i += gridDim.x) {
             const Item it = decode(a, i);
@@ -383,8 +393,9 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
             const int x0 = x;
             for (int t = 0; t < it.nt; t++) {
                 const int st = x % NKT, xb = x % NX;
-                wait_bar(k_full + st, (x / NKT) & 1, abort_flag, err, 59);
-                wait_bar(x_empty + xb, ((x / NX) & 1) ^ 1, abort_flag, err, 60);
+                if (!k_rdy) wait_bar(k_full + st, (x / NKT) & 1, abort_flag, err, 59);
+                if (!x_rdy) wait_bar(x_empty + xb, ((x / NX) & 1) ^ 1, abort_flag, err, 60);
+                k_rdy = x_rdy = false;
                 fence_after();
                 const unsigned char *pk = sK + st * KT;
                 // per 64-wide K-half four MMAs of K = 16 (both operands K-major, 32 bytes further per MMA)
@@ -392,8 +403,15 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
                 mma4_ss_w(tX + (uint32_t)(xb * 64), desc_kmajor(pk + KHALF), 2, desc_kmajor(pq + QHALF), 2, IDESC_X, 1u,
                           su32(x_full + xb));
                 if (t == it.nt - 1) mma_commit_w(q_empty + qb);  // the row's q is read by its X groups only
-                if (t >= 2) mma2(x - 2, t - 2);
                 x++;
+                if (t >= 2) {
+                    // G' of tile t - 2 and the next tile's k, while MMA1 runs
+                    const int y = x - 3;
+                    const uint32_t m = mbar_test2(g_full + y % NX, (y / NX) & 1, k_full + x % NKT, (x / NKT) & 1);
+                    g_rdy = (m & 1u) != 0u;
+                    k_rdy = (m & 2u) != 0u;
+                    mma2(y, t - 2);
+                }
             }
             for (int t = it.nt >= 2 ? it.nt - 2 : 0; t < it.nt; t++) mma2(x0 + t, t);
             mma_commit_w(dq_full);

@@ -1125,15 +1125,21 @@ dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     } else if (warp == 1) {
         // -------------------------------------------------------------------- MMA issue (whole warp)
         //   dK[key, d] += G q   (A = G from TMEM, K index (row, h); B = the pair's q block read MN-major)
+        // After each pair's MMAs the next pair's q block and G slot are probed in one shared-memory round trip,
+        // which overlaps the MMAs just queued; the warp waits only when either was not yet complete.  (The next
+        // pair's barriers cannot be two phases behind: their previous uses have been consumed.)
         int qs = 0, xc = 0, uc = 0;
+        bool rdy = false;  // the next pair's q block and G slot are known complete
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
             const Unit U = decode_unit(a, u);
             if (U.npairs == 0) continue;
             for (int pi = 0; pi < U.npairs; pi++) {
                 const int bs = qs % S_QSTG, xb = xc % S_XSTG;
                 if (pi == 0) wait_bar(dk_empty, (uc & 1) ^ 1, abort_flag, err, 36);
-                wait_bar(b_full + bs, (qs / S_QSTG) & 1, abort_flag, err, 37);
-                wait_bar(gk_full + xb, (xc / S_XSTG) & 1, abort_flag, err, 38);
+                if (!rdy) {
+                    wait_bar(b_full + bs, (qs / S_QSTG) & 1, abort_flag, err, 37);
+                    wait_bar(gk_full + xb, (xc / S_XSTG) & 1, abort_flag, err, 38);
+                }
                 fence_after();
                 // eight MMAs of K = 16 (A: G columns 8 s of the slot; B: the q block, 2 KB further per MMA) in two
                 // groups of four under one elect each, then the commits
@@ -1144,6 +1150,7 @@ dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                 mma_commit_w(b_empty + bs);
                 qs++;
                 xc++;
+                rdy = mbar_test2(b_full + qs % S_QSTG, (qs / S_QSTG) & 1, gk_full + xc % S_XSTG, (xc / S_XSTG) & 1) == 3u;
             }
             mma_commit_w(dk_full);
             uc++;

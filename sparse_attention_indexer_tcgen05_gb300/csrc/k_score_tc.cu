@@ -456,10 +456,10 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
         // ---------------------------------------------------------- MMA issue (whole warp)
         // The warp runs the loop together (warp-uniform stage indices and descriptors); one elected lane issues
         // each MMA and commit.  Items are decoded lane-parallel (lane l: the CTA's item k + l), the loop reads
-        // the tile count of item k by a shuffle.  A-stage ring position (st, parity aph).  The next stage's full
-        // barrier and the next accumulator's empty barrier are probed early (mbar_test) so that their
-        // shared-memory round trips overlap the MMAs issued in between; a probe that comes back false falls back
-        // to the bounded wait.
+        // the tile count of item k by a shuffle.  A-stage ring position (st, parity aph).  After each K-half's
+        // MMAs the next stage's full barrier and the next accumulator's empty barrier are probed in one
+        // shared-memory round trip, which overlaps the MMAs just queued (a probe placed before them would leave
+        // the tensor pipe idle for its latency); a probe that comes back false falls back to the bounded wait.
         int st = 0, ai = 0, tc = 0, k = 0, nt_lane = 0;
         uint32_t aph = 0;
         bool a_ready = false, t_ready = false;
@@ -484,13 +484,16 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
                     if (!a_ready) wait_bar(a_full + st, aph, abort_flag, &g_tc_error, 5);
                     const int st1 = st + 1 == A_STAGES ? 0 : st + 1;
                     const uint32_t ph1 = st1 == 0 ? aph ^ 1u : aph;
-                    a_ready = mbar_test(a_full + st1, ph1);
-                    if (kh == 1) t_ready = mbar_test(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1);
                     fence_after();
                     const unsigned char *pa = sA + st * A_HALF;
                     const unsigned char *pb = pb0 + kh * B_HALF;
                     // four MMAs of K = 16 under one elect, then the stage's commit
                     mma4_ss_w(d, desc_kmajor(pa), 2, desc_kmajor(pb), 2, IDESC, kh != 0 ? 1u : 0u, su32(a_empty + st));
+                    // probe the next stage (and, after the tile's last K-half, the next accumulator) now that the
+                    // MMAs are queued: the round trip overlaps them
+                    const uint32_t m = mbar_test2(a_full + st1, ph1, t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1);
+                    a_ready = (m & 1u) != 0u;
+                    if (kh == 1) t_ready = (m & 2u) != 0u;
                     st = st1;
                     aph = ph1;
                 }

@@ -199,15 +199,18 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         // Rows are decoded lane-parallel (lane l: the CTA's row k + l) and the loop reads the tile count of row k
         // by a shuffle.  Per row: skip its q stages (the epilogue copies them into TMEM), wait for q in
         // TMEM, then per tile and K-block four MMAs of K = 16 with A = q's columns of that K-block.  A barrier
-        // test costs the issuing thread a shared-memory round trip even when the phase is complete, so the next
-        // stage's full barrier (and, at a tile's last K-block, the next accumulator's empty barrier) is probed
-        // before this K-block's MMAs are issued; a probe that comes back false falls back to the bounded wait.
-        // (A probe passes only once the awaited phase has completed: the barrier cannot be two phases behind,
-        // since the stage one ring turn earlier has been consumed already.)
+        // test costs the issuing thread a shared-memory round trip even when the phase is complete (several
+        // hundred cycles under this kernel's shared-memory load, against 256 cycles for a K-block's MMAs), so the
+        // warp never tests before issuing: after each K-block's MMAs it probes the next two stages of the row in one
+        // round trip (at a tile's last K-block: the next accumulator and the next stage), which overlaps the MMAs
+        // already queued, and waits only when no stage ahead is known full.  (A probe passes only once the awaited
+        // phase has completed: a stage at most two ahead cannot be two phases behind, since the stages one ring
+        // turn earlier have been consumed already.)
         const uint64_t ring_desc = desc_kmajor(ring);  // stage st: + st * STG / 16 in the address field
         int st = 0, tc = 0, rc = 0, k = 0, nt_lane = 0;  // ring position of the next stage and its parity
         uint32_t ph = 0;
-        bool f_ready = false, t_ready = false;
+        bool t_ready = false;
+        int ready = 0;  // consecutive stages from st on known to be full (never past the row's last stage)
         for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
             if ((k & 31) == 0) {
                 const int il = i + lane * (int)gridDim.x;
@@ -220,6 +223,7 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                 st -= NSTG;
                 ph ^= 1u;
             }
+            ready = 0;
             wait_bar(q_ready, rc & 1, abort_flag, err, 62);
             fence_after();
             for (int tt = 0; tt < nt; tt++) {
@@ -229,18 +233,32 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                 fence_after();
                 const uint32_t d = tmem + ACC0 + (uint32_t)(tb * NK);
                 for (int kb = 0; kb < nkb; kb++) {
-                    if (!f_ready) wait_bar(full + st, ph, abort_flag, err, 64);
+                    if (ready == 0) {
+                        wait_bar(full + st, ph, abort_flag, err, 64);
+                        ready = 1;
+                    }
                     fence_after();
-                    const int st1 = st + 1 == NSTG ? 0 : st + 1;
-                    const uint32_t ph1 = st1 == 0 ? ph ^ 1u : ph;
-                    // the next stage is the row's (the next row's q stages are not the MMA's to wait for)
-                    f_ready = (kb + 1 < nkb || tt + 1 < nt) && mbar_test(full + st1, ph1);
-                    if (kb + 1 == nkb && tt + 1 < nt) t_ready = mbar_test(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1);
                     // four MMAs of K = 16 (A: q's columns of K-block kb; B: 32 bytes further per MMA), one commit
                     mma4_ts_w(d, tmem + (uint32_t)(kb * 32), 8, 16, ring_desc + (uint64_t)(st * (STG >> 4)), 2, IDESC,
                               kb != 0 ? 1u : 0u, su32(empty + st));
-                    st = st1;
-                    ph = ph1;
+                    if (++st == NSTG) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                    ready--;
+                    // probe ahead, now that the MMAs are queued (the next row's q stages are not the MMA's to wait for)
+                    const int left = (nt - 1 - tt) * nkb + (nkb - 1 - kb);  // the row's stages after this one
+                    if (kb + 1 == nkb && tt + 1 < nt) {
+                        const uint32_t m = mbar_test2(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1, full + st, ph);
+                        t_ready = (m & 1u) != 0u;
+                        if (ready == 0) ready = (int)((m >> 1) & 1u);
+                    } else if (ready == 0 && left > 0) {
+                        const int st2 = st + 1 == NSTG ? 0 : st + 1;
+                        const uint32_t ph2 = st2 == 0 ? ph ^ 1u : ph;
+                        const bool two = left >= 2;
+                        const uint32_t m = mbar_test2(full + st, ph, full + (two ? st2 : st), two ? ph2 : ph);
+                        ready = (m & 1u) ? ((two && (m & 2u)) ? 2 : 1) : 0;
+                    }
                 }
                 mma_commit_w(t_full + tb);
                 tc++;

@@ -47,6 +47,22 @@ __device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity)
                  : "memory");
     return ok != 0;
 }
+// Two non-blocking probes in one shared-memory round trip: bit 0 = phase `p0` of b0 complete, bit 1 = phase
+// `p1` of b1 complete.  Meant to be issued right after a group of MMAs, so that the round trip overlaps the MMAs
+// already queued on the tensor pipe (a probe placed before them leaves the pipe idle for its latency).
+__device__ __forceinline__ uint32_t mbar_test2(uint64_t *b0, uint32_t p0, uint64_t *b1, uint32_t p1)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred q0, q1;\n\t.reg .b32 r0, r1;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+                 "selp.u32 r0, 1, 0, q0;\n\tselp.u32 r1, 2, 0, q1;\n\t"
+                 "or.b32 %0, r0, r1;\n\t}"
+                 : "=r"(r)
+                 : "r"(su32(b0)), "r"(p0), "r"(su32(b1)), "r"(p1)
+                 : "memory");
+    return r;
+}
 __device__ __forceinline__ void init_fence()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
