@@ -198,19 +198,19 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         // -------------------------------------------------------------------- MMA issue (whole warp)
         // Rows are decoded lane-parallel (lane l: the CTA's row k + l) and the loop reads the tile count of row k
         // by a shuffle.  Per row: skip its q stages (the epilogue copies them into TMEM), wait for q in
-        // TMEM, then per tile and K-block four MMAs of K = 16 with A = q's columns of that K-block.  A barrier
-        // test costs the issuing thread a shared-memory round trip even when the phase is complete (several
-        // hundred cycles under this kernel's shared-memory load, against 256 cycles for a K-block's MMAs), so the
-        // warp never tests before issuing: after each K-block's MMAs it probes the next two stages of the row in one
-        // round trip (at a tile's last K-block: the next accumulator and the next stage), which overlaps the MMAs
-        // already queued, and waits only when no stage ahead is known full.  (A probe passes only once the awaited
-        // phase has completed: a stage at most two ahead cannot be two phases behind, since the stages one ring
-        // turn earlier have been consumed already.)
+        // TMEM, then per tile and K-block four MMAs of K = 16 with A = q's columns of that K-block.
+        // A barrier wait costs the issuing thread a shared-memory round trip even when the phase is complete (under
+        // this kernel's shared-memory load, close to a K-block's 256 cycles of MMAs), so the warp waits as rarely as
+        // the hand-over allows.  With the sparse loss the producers hand a row's stages over in groups of GRP counted
+        // from the row's first stage, one thread arriving on a group's full barriers in order once every copy of the
+        // group is visible; the arrivals release and the wait acquires, so a group's last barrier seen complete
+        // shows the whole group complete, and the warp waits once per group (on its last stage; a group's stages
+        // are at most GRP - 1 ahead, so that barrier cannot be two phases behind).  With the dense loss every stage
+        // is a TMA load completing on its own, and each is waited for.  A wait placed at a group's (or a tile's)
+        // start overlaps the MMAs still queued from the one before.
         const uint64_t ring_desc = desc_kmajor(ring);  // stage st: + st * STG / 16 in the address field
-        int st = 0, tc = 0, rc = 0, k = 0, nt_lane = 0;  // ring position of the next stage and its parity
-        uint32_t ph = 0;
-        bool t_ready = false;
-        int ready = 0;  // consecutive stages from st on known to be full (never past the row's last stage)
+        int xs = 0, tc = 0, rc = 0, k = 0, nt_lane = 0;  // xs: absolute index of the next stage in the stream
+        int ready_to = -1;                               // every stage up to this one is known full
         for (int i = blockIdx.x; i < total; i += gridDim.x, k++) {
             if ((k & 31) == 0) {
                 const int il = i + lane * (int)gridDim.x;
@@ -218,47 +218,31 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
             }
             const int nt = __shfl_sync(0xffffffffu, nt_lane, k & 31);
             if (nt == 0) continue;
-            st += nkb;  // the row's q stages
-            if (st >= NSTG) {
-                st -= NSTG;
-                ph ^= 1u;
-            }
-            ready = 0;
+            const int x0 = xs;                               // the row's first stage (its q)
+            const int xend = x0 + nkb * (1 + nt);            // one past the row's last stage (nt = nw + 2 nct)
+            xs += nkb;                                       // the row's q stages
             wait_bar(q_ready, rc & 1, abort_flag, err, 62);
             fence_after();
             for (int tt = 0; tt < nt; tt++) {
                 const int tb = tc & 1;
-                if (!t_ready) wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, err, 63);
-                t_ready = false;
+                wait_bar(t_empty + tb, ((tc >> 1) & 1) ^ 1, abort_flag, err, 63);
                 fence_after();
                 const uint32_t d = tmem + ACC0 + (uint32_t)(tb * NK);
-                for (int kb = 0; kb < nkb; kb++) {
-                    if (ready == 0) {
-                        wait_bar(full + st, ph, abort_flag, err, 64);
-                        ready = 1;
+                for (int kb = 0; kb < nkb; kb++, xs++) {
+                    if (xs > ready_to) {
+                        int gl = xs;
+                        if (g.sparse) {
+                            gl = x0 + ((xs - x0) / GRP) * GRP + GRP - 1;
+                            if (gl > xend - 1) gl = xend - 1;
+                        }
+                        wait_bar(full + gl % NSTG, (gl / NSTG) & 1, abort_flag, err, 64);
+                        fence_after();
+                        ready_to = gl;
                     }
-                    fence_after();
+                    const int st = xs % NSTG;
                     // four MMAs of K = 16 (A: q's columns of K-block kb; B: 32 bytes further per MMA), one commit
                     mma4_ts_w(d, tmem + (uint32_t)(kb * 32), 8, 16, ring_desc + (uint64_t)(st * (STG >> 4)), 2, IDESC,
                               kb != 0 ? 1u : 0u, su32(empty + st));
-                    if (++st == NSTG) {
-                        st = 0;
-                        ph ^= 1u;
-                    }
-                    ready--;
-                    // probe ahead, now that the MMAs are queued (the next row's q stages are not the MMA's to wait for)
-                    const int left = (nt - 1 - tt) * nkb + (nkb - 1 - kb);  // the row's stages after this one
-                    if (kb + 1 == nkb && tt + 1 < nt) {
-                        const uint32_t m = mbar_test2(t_empty + (tb ^ 1), (((tc + 1) >> 1) & 1) ^ 1, full + st, ph);
-                        t_ready = (m & 1u) != 0u;
-                        if (ready == 0) ready = (int)((m >> 1) & 1u);
-                    } else if (ready == 0 && left > 0) {
-                        const int st2 = st + 1 == NSTG ? 0 : st + 1;
-                        const uint32_t ph2 = st2 == 0 ? ph ^ 1u : ph;
-                        const bool two = left >= 2;
-                        const uint32_t m = mbar_test2(full + st, ph, full + (two ? st2 : st), two ? ph2 : ph);
-                        ready = (m & 1u) ? ((two && (m & 2u)) ? 2 : 1) : 0;
-                    }
                 }
                 mma_commit_w(t_full + tb);
                 tc++;
@@ -360,103 +344,140 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                         else if (g.sparse) mw[c] = c0 < it.ncs ? sMaskb[c0 >> 5] & range_bits(0, it.ncs - 1 - c0) : 0u;
                         else mw[c] = range_bits(0, it.ncs - 1 - c0);
                     }
-                    if ((mw[0] | mw[1]) != 0u) {
-                        if (!pass2) {
-                            // running sum against a reference max, one 32-column chunk at a time; a chunk is re-based
-                            // on its own max only when its sum leaves the safe range
-#pragma unroll 1
-                            for (int c = 0; c < 2; c++) {
-                                if (mw[c] == 0u) continue;
-                                float x[32];
-                                tmem_ld32(tmem + lane_off + ACC0 + (uint32_t)(tb * NK + col_of(c)), x);
-                                if (s2_pos) {
-                                    if (mw[c] != 0xffffffffu) {
+                    // the accumulator goes back to the MMA as soon as this warp holds its columns in registers: the
+                    // math below then overlaps the next tiles' MMAs (two accumulators alone would leave the MMA waiting
+                    // for the epilogue's whole per-tile latency chain)
+                    auto release = [&]() {
+                        fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(t_empty + tb);
+                    };
+                    const uint32_t ca0 = tmem + lane_off + ACC0 + (uint32_t)(tb * NK + col_of(0));
+                    const uint32_t ca1 = tmem + lane_off + ACC0 + (uint32_t)(tb * NK + col_of(1));
+                    if ((mw[0] | mw[1]) == 0u) {
+                        release();
+                    } else if (!pass2) {
+                        // running sum against a reference max, one 32-column chunk at a time; a chunk is re-based
+                        // on its own max only when its sum leaves the safe range
+                        uint32_t r0[32], r1[32];
+                        if (mw[0] != 0u) tmem_ld32_async(ca0, r0);
+                        else
 #pragma unroll
-                                        for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? x[q] : -INFINITY;
-                                    }
+                            for (int q = 0; q < 32; q++) r0[q] = 0u;
+                        if (mw[1] != 0u) tmem_ld32_async(ca1, r1);
+                        else
+#pragma unroll
+                            for (int q = 0; q < 32; q++) r1[q] = 0u;
+                        tmem_wait_ld(r0);
+                        tmem_wait_ld(r1);
+                        release();
+                        const float sc = s2_pos ? s2 : 1.f;
+                        auto chunk1 = [&](const uint32_t (&r)[32], uint32_t mwc) {
+                            float x[32];
+                            if (s2_pos) {
+                                if (mwc != 0xffffffffu) {
+#pragma unroll
+                                    for (int q = 0; q < 32; q++) x[q] = (mwc >> q) & 1u ? __uint_as_float(r[q]) : -INFINITY;
                                 } else {
 #pragma unroll
-                                    for (int q = 0; q < 32; q++) x[q] = (mw[c] >> q) & 1u ? x[q] * s2 : -INFINITY;
+                                    for (int q = 0; q < 32; q++) x[q] = __uint_as_float(r[q]);
                                 }
-                                const float sc = s2_pos ? s2 : 1.f;
-                                auto chunk_max = [&]() -> float {
-                                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                            } else {
 #pragma unroll
-                                    for (int q = 0; q < 32; q++) mx[q & 3] = fmaxf(mx[q & 3], x[q]);
-                                    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
-                                };
-                                auto chunk_sum = [&]() -> float {
-                                    float2 sm[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-                                    for (int q2 = 0; q2 < 16; q2++) {
-                                        const float2 arg = fma2(make_float2(x[2 * q2], x[2 * q2 + 1]), make_float2(sc, sc),
-                                                                make_float2(-m, -m));
-                                        sm[q2 & 1] = add2(sm[q2 & 1], make_float2(ex2(arg.x), ex2(arg.y)));
-                                    }
-                                    return (sm[0].x + sm[0].y) + (sm[1].x + sm[1].y);
-                                };
-                                if (m == -INFINITY) m = chunk_max();
-                                float cs = chunk_sum();
-                                if (!(cs <= 0x1p64f)) {
-                                    const float cm = chunk_max();
-                                    if (cm > m) {
-                                        ssum *= ex2(m - cm);
-                                        m = cm;
-                                    }
-                                    cs = chunk_sum();
-                                }
-                                ssum += cs;
+                                for (int q = 0; q < 32; q++) x[q] = (mwc >> q) & 1u ? __uint_as_float(r[q]) * s2 : -INFINITY;
                             }
+                            auto chunk_max = [&]() -> float {
+                                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                                for (int q = 0; q < 32; q++) mx[q & 3] = fmaxf(mx[q & 3], x[q]);
+                                return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+                            };
+                            auto chunk_sum = [&]() -> float {
+                                float2 sm[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                                for (int q2 = 0; q2 < 16; q2++) {
+                                    const float2 arg = fma2(make_float2(x[2 * q2], x[2 * q2 + 1]), make_float2(sc, sc),
+                                                            make_float2(-m, -m));
+                                    sm[q2 & 1] = add2(sm[q2 & 1], make_float2(ex2(arg.x), ex2(arg.y)));
+                                }
+                                return (sm[0].x + sm[0].y) + (sm[1].x + sm[1].y);
+                            };
+                            if (m == -INFINITY) m = chunk_max();
+                            float cs = chunk_sum();
+                            if (!(cs <= 0x1p64f)) {
+                                const float cm = chunk_max();
+                                if (cm > m) {
+                                    ssum *= ex2(m - cm);
+                                    m = cm;
+                                }
+                                cs = chunk_sum();
+                            }
+                            ssum += cs;
+                        };
+                        if (mw[0] != 0u) chunk1(r0, mw[0]);
+                        if (mw[1] != 0u) chunk1(r1, mw[1]);
+                    } else {
+                        // pass 2 in the 16-lane shape: a thread holds heads g, g + 8, g + 16, g + 24 (g = lane / 4)
+                        // of columns 8 p + 2 u + e (u = lane % 4); four heads are added in registers and the eight
+                        // threads of a column set reduce-scatter over g
+                        const int u4 = lane & 3, g8 = lane >> 2;
+                        uint32_t a0[16], b0[16], a1[16], b1[16];
+                        if (mw[0] != 0u) {
+                            tmem_ld16x256_x4_async(ca0, a0);
+                            tmem_ld16x256_x4_async(ca0 + (16u << 16), b0);
                         } else {
-                            // pass 2 in the 16-lane shape: a thread holds heads g, g + 8, g + 16, g + 24 (g = lane / 4)
-                            // of columns 8 p + 2 u + e (u = lane % 4); four heads are added in registers and the eight
-                            // threads of a column set reduce-scatter over g
-                            const int u4 = lane & 3, g8 = lane >> 2;
-#pragma unroll 1
-                            for (int c = 0; c < 2; c++) {
-                                if (mw[c] == 0u) continue;
-                                const uint32_t ca = tmem + lane_off + ACC0 + (uint32_t)(tb * NK + col_of(c));
-                                uint32_t ra[16], rb[16];
-                                tmem_ld16x256_x4(ca, ra);
-                                tmem_ld16x256_x4(ca + (16u << 16), rb);
-                                const bool full = mw[c] == 0xffffffffu;
-                                float s8[8];
 #pragma unroll
-                                for (int p4 = 0; p4 < 4; p4++) {
-                                    const int col = 8 * p4 + 2 * u4;
-                                    const bool b0 = full || ((mw[c] >> col) & 1u), b1 = full || ((mw[c] >> (col + 1)) & 1u);
-                                    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                                    for (int k4 = 0; k4 < 4; k4++) {
-                                        const uint32_t *r = k4 < 2 ? ra : rb;
-                                        const int o = 4 * p4 + 2 * (k4 & 1);
-                                        const float2 arg = fma2(make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])),
-                                                                make_float2(s2, s2), make_float2(-ell4[k4], -ell4[k4]));
-                                        const float e0 = ex2(arg.x), e1 = ex2(arg.y);
-                                        acc = add2(acc, make_float2(b0 ? e0 : 0.f, b1 ? e1 : 0.f));
-                                    }
-                                    s8[2 * p4] = acc.x;
-                                    s8[2 * p4 + 1] = acc.y;
-                                }
-#pragma unroll
-                                for (int hv = 4; hv >= 1; hv >>= 1) {
-                                    const int off = hv * 4;
-                                    const bool up = (lane & off) != 0;
-#pragma unroll
-                                    for (int q = 0; q < hv; q++) {
-                                        const float send = up ? s8[q] : s8[q + hv];
-                                        const float keep = up ? s8[q + hv] : s8[q];
-                                        s8[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                                    }
-                                }
-                                const int j = t * NK + col_of(c) + 8 * (g8 >> 1) + 2 * u4 + (g8 & 1);
-                                if (j < TWMAX && s8[0] != 0.f) atomicAdd(sTb + j, s8[0]);
-                            }
+                            for (int q = 0; q < 16; q++) a0[q] = b0[q] = 0u;
                         }
+                        if (mw[1] != 0u) {
+                            tmem_ld16x256_x4_async(ca1, a1);
+                            tmem_ld16x256_x4_async(ca1 + (16u << 16), b1);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; q++) a1[q] = b1[q] = 0u;
+                        }
+                        tmem_wait_ld16(a0);
+                        tmem_wait_ld16(b0);
+                        tmem_wait_ld16(a1);
+                        tmem_wait_ld16(b1);
+                        release();
+                        auto chunk2 = [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], uint32_t mwc, int c) {
+                            const bool full = mwc == 0xffffffffu;
+                            float s8[8];
+#pragma unroll
+                            for (int p4 = 0; p4 < 4; p4++) {
+                                const int col = 8 * p4 + 2 * u4;
+                                const bool e0m = full || ((mwc >> col) & 1u), e1m = full || ((mwc >> (col + 1)) & 1u);
+                                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                                for (int k4 = 0; k4 < 4; k4++) {
+                                    const uint32_t *r = k4 < 2 ? ra : rb;
+                                    const int o = 4 * p4 + 2 * (k4 & 1);
+                                    const float2 arg = fma2(make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])),
+                                                            make_float2(s2, s2), make_float2(-ell4[k4], -ell4[k4]));
+                                    const float e0 = ex2(arg.x), e1 = ex2(arg.y);
+                                    acc = add2(acc, make_float2(e0m ? e0 : 0.f, e1m ? e1 : 0.f));
+                                }
+                                s8[2 * p4] = acc.x;
+                                s8[2 * p4 + 1] = acc.y;
+                            }
+#pragma unroll
+                            for (int hv = 4; hv >= 1; hv >>= 1) {
+                                const int off = hv * 4;
+                                const bool up = (lane & off) != 0;
+#pragma unroll
+                                for (int q = 0; q < hv; q++) {
+                                    const float send = up ? s8[q] : s8[q + hv];
+                                    const float keep = up ? s8[q + hv] : s8[q];
+                                    s8[q] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                                }
+                            }
+                            const int j = t * NK + col_of(c) + 8 * (g8 >> 1) + 2 * u4 + (g8 & 1);
+                            if (j < TWMAX && s8[0] != 0.f) atomicAdd(sTb + j, s8[0]);
+                        };
+                        if (mw[0] != 0u) chunk2(a0, b0, mw[0], 0);
+                        if (mw[1] != 0u) chunk2(a1, b1, mw[1], 1);
                     }
-                    fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(t_empty + tb);
                     tc++;
                 }
                 x = x_next;
