@@ -485,6 +485,97 @@ kl_warp_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__
     }
 }
 
+// The same step for the sparse support with 512 < K <= 4096 slots: one CTA of 256 threads per row, the row's
+// ids, scores and teacher values held in registers (slot s = tid + 256 i, coalesced), so the row is read once;
+// block reductions for the max, the normaliser and the pair (A, L); the arithmetic of kl_row_warp.
+constexpr int kKlBlkPer = 16;  // slots per thread: K <= 4096
+__global__ void __launch_bounds__(kThreads)
+kl_block_kernel(Geo g, const int32_t *__restrict__ ids, const float *__restrict__ selscore,
+                const float *__restrict__ teacher, float *__restrict__ gbuf, float *__restrict__ row_loss,
+                float *__restrict__ gd, int ncp)
+{
+    __shared__ float red[2][kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int K = g.K;
+    for (long long r = blockIdx.x; r < g.rows; r += gridDim.x) {
+        const Row R = decode_row(g, r);
+        const long long lo = key_gid(g, R, 0);
+        int jj[kKlBlkPer];
+        float x[kKlBlkPer], t[kKlBlkPer];
+#pragma unroll
+        for (int i = 0; i < kKlBlkPer; i++) {  // every load issued before any is used
+            const int s = tid + kThreads * i;
+            const bool in = s < K;
+            jj[i] = in ? __ldg(ids + r * K + s) : -1;
+            x[i] = in ? __ldg(selscore + r * K + s) : 0.f;
+            t[i] = in ? __ldg(teacher + r * K + s) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kKlBlkPer; i++) {
+            const long long j = jj[i] >= 0 ? (long long)jj[i] - lo : -1;
+            jj[i] = (j >= 0 && j < R.v) ? (int)j : -1;
+        }
+        float *grow = gbuf != nullptr ? gbuf + r * K : nullptr;
+        float *drow = gd != nullptr ? gd + gd_row_of(g, R.b, R.s, r) * ncp : nullptr;
+        if (drow != nullptr)  // zero the visible range
+            for (int j = tid; j < R.v; j += kThreads) drow[j] = 0.f;
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kKlBlkPer; i++)
+            if (jj[i] >= 0) m = fmaxf(m, x[i]);
+        m = block_reduce(m, red[0], true);  // its barriers also order the zeroing above before the writes below
+        if (m == -INFINITY) {  // empty support: no loss, no gradient
+            if (grow != nullptr)
+#pragma unroll
+                for (int i = 0; i < kKlBlkPer; i++)
+                    if (tid + kThreads * i < K) grow[tid + kThreads * i] = 0.f;
+            if (tid == 0) row_loss[r] = 0.f;
+            continue;
+        }
+        float z = 0.f;
+#pragma unroll
+        for (int i = 0; i < kKlBlkPer; i++) {
+            x[i] = jj[i] >= 0 ? __expf(x[i] - m) : 0.f;
+            z += x[i];
+        }
+        z = block_reduce(z, red[0], false);
+        const float inv_z = 1.f / z;
+        float A = 0.f, L = 0.f;
+#pragma unroll
+        for (int i = 0; i < kKlBlkPer; i++) {
+            if (jj[i] < 0) continue;
+            const float p = x[i] * inv_z;
+            A += t[i] * p / (p + kKlEps);
+            L += t[i] * (logf(t[i] + kKlEps) - logf(p + kKlEps));
+        }
+        // A and L in one block reduction
+        A = warp_sum(A);
+        L = warp_sum(L);
+        if (lane == 0) {
+            red[0][wid] = A;
+            red[1][wid] = L;
+        }
+        __syncthreads();
+        A = 0.f;
+        L = 0.f;
+        for (int w = 0; w < kWarps; w++) {
+            A += red[0][w];
+            L += red[1][w];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kKlBlkPer; i++) {
+            const int s = tid + kThreads * i;
+            if (s >= K) continue;
+            const float p = x[i] * inv_z;
+            const float gv = jj[i] >= 0 ? g.factor * p * (A - t[i] / (p + kKlEps)) : 0.f;
+            if (grow != nullptr) grow[s] = gv;
+            if (drow != nullptr && jj[i] >= 0) drow[jj[i]] = gv;
+        }
+        if (tid == 0) row_loss[r] = L;
+    }
+}
+
 cudaError_t launch_kl(const Geo &g, const int32_t *ids, const float *selscore, const float *dense_scores,
                       const float *teacher, float *gbuf, float *row_loss, float *gd, int ncp, cudaStream_t st)
 {
@@ -493,6 +584,21 @@ cudaError_t launch_kl(const Geo &g, const int32_t *ids, const float *selscore, c
         const long long blocks = (g.rows + kWarps - 1) / kWarps;
         const int grid = blocks < 152 * 16 ? (int)blocks : 152 * 16;
         kl_warp_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, teacher, gbuf, row_loss, gd, ncp);
+        note_launches(1);
+        return cudaGetLastError();
+    }
+    if (g.sparse && dense_scores == nullptr && g.TW == g.K && g.K <= kThreads * kKlBlkPer) {
+        // as many CTAs as can be resident (each loops over rows): no late wave of CTAs at the end
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kl_block_kernel, kThreads, 0);
+        if (e != cudaSuccess) return e;
+        const long long resident = (long long)sms * (per_sm > 0 ? per_sm : 1);
+        const int grid = g.rows < resident ? g.rows : (int)resident;
+        kl_block_kernel<<<grid, kThreads, 0, st>>>(g, ids, selscore, teacher, gbuf, row_loss, gd, ncp);
         note_launches(1);
         return cudaGetLastError();
     }
