@@ -51,13 +51,11 @@ def parse():
 
 
 def stage_kernels(cfg, key_width: int) -> dict:
-    """The main kernel of each stage the roofline may be reported for, and the source file it is built from: the
-    score stage is one fused kernel on key axes up to 1024, and on longer ones the score-row kernel (all of the
-    stage's MMAs) followed by the top-k kernel."""
+    """The one kernel each stage the roofline may be reported for launches, and the source file it is built from."""
     if cfg.dtype != "bf16":  # fp32 values take the CUDA-core kernels
         return {"score_topk": ("score_topk_generic_kernel", "k_generic.cu"),
                 "teacher": ("teacher_generic_kernel", "k_generic.cu")}
-    score = ("score_rows_long_tc_kernel" if key_width > 1024 else "score_topk_tc_kernel", "k_score_tc.cu")
+    score = ("score_topk_long_tc_kernel" if key_width > 1024 else "score_topk_tc_kernel", "k_score_tc.cu")
     teacher = (("teacher_h128_tc_kernel", "k_teacher_h128_tc.cu") if cfg.heads == 128
                else ("teacher_tc_kernel", "k_teacher_tc.cu"))
     return {"score_topk": score, "teacher": teacher}

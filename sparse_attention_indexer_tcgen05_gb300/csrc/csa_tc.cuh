@@ -7,19 +7,12 @@
 
 namespace csa {
 
-// True when the tcgen05 score kernels take this shape (bf16 values, H_I = 64, D_I = 128): key axes up to 1024
-// with the top-k fused, longer ones with the score rows written to the workspace and a separate top-k kernel.
+// True when the tcgen05 score + top-k kernels take this shape (bf16 values, H_I = 64, D_I = 128): key axes up to
+// 1024 with whole score rows in shared memory, longer ones with streamed score tiles and per-row candidate buffers.
 bool tc_score_supported(const Geo &g, bool bf16);
 
-// Workspace the tensor-core score path needs: THD work-item offsets, and on long key axes the fp32 score rows
-// [rows][key width].
+// Workspace the tensor-core kernels need (0 when none).
 size_t tc_workspace_bytes(const Geo &g);
-
-// Exact per-row top-K of fp32 score rows [rows][NC] (visible keys only are read): ascending global ids and their
-// scores, -1 / -inf past min(K, v).  And the debug copy of rows [row0, row0 + nrows) with -inf where not visible.
-cudaError_t launch_topk_rows(const Geo &g, const float *scores, int32_t *ids, float *selscore, cudaStream_t st);
-cudaError_t launch_dump_rows(const Geo &g, const float *scores, long long row0, long long nrows, float *dump,
-                             cudaStream_t st);
 
 cudaError_t launch_score_topk_tc(const Geo &g, const __nv_bfloat16 *q_idx, const float *w,
                                  const __nv_bfloat16 *k_idx, int32_t *ids, float *selscore, void *ws,

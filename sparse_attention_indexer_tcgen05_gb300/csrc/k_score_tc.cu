@@ -8,10 +8,9 @@
 //   (ties to the lower key), written as ascending global ids with their fp32 scores.
 //
 // Shape taken: bf16 values, H_I = 64 indexer heads, D_I = 128.  Key axes up to 1024 keep an item's score rows
-// whole in shared memory and select in the same kernel (score_topk_tc_kernel); longer ones write each row's
-// fp32 scores once to the workspace (score_rows_long_tc_kernel) and a CTA per row selects from there
-// (topk_rows_kernel, k_topk_rows.cu), so that the selection never holds up the MMAs.  Other shapes and fp32
-// values take the CUDA-core kernels.
+// whole in shared memory (score_topk_tc_kernel); longer ones (up to 65535 keys, K <= 3840) stream the score
+// tiles into per-row candidate buffers (score_topk_long_tc_kernel, below).  Other shapes and fp32 values take
+// the CUDA-core kernels.
 //
 // Mapping.  A work item is 4 consecutive query positions of one sequence (or THD segment).  The MMA computes
 // D[key, (row, head)] = k_idx[key] . q_idx[row, head] with M = 128 keys (A = a k_idx tile, K-major, streamed
@@ -28,7 +27,9 @@
 //               epilogue runs the following items:
 //               the exact k-th largest score by a bitwise search on order-preserving keys held in
 //               registers, then the selection written by a stable ballot compaction.
-//   (long key axis: no selection warps; the epilogue writes each tile's visible scores to the score rows.)
+//   (long key axis: warps 10..13, one per row, follow the epilogue tile by tile through a four-tile ring; each
+//    keeps the row's current best candidates, cuts them back to about the top K with a radix walk when the
+//    buffer fills, and to exactly the top K at the row's end.)
 //
 // Every mbarrier wait is bounded: on expiry the kernel records an error code (read back by
 // csa_check_device_status), stops waiting (so every role still runs its loops to the end with uniform
@@ -89,8 +90,13 @@ constexpr int TMEM_COLS = 512;
 //   short key axis (<= NCMAX keys): an item's score rows are kept whole in shared memory (three item buffers)
 //     and each row is selected by one warp once the item is done; two sets of four selection warps take
 //     alternate items; the q_idx rows of two items are resident (double buffer).
-//   long key axis: the epilogue writes the visible scores of each key tile straight to the rows' fp32 score
-//     rows in the workspace; no selection warps; the q_idx rows of two items are resident (double buffer).
+//   long key axis: the score rows stream through a ring of key tiles; the selection warp of each row keeps a
+//     candidate buffer of at most CAP (key, index) entries in ascending key order and admits a new key only
+//     when it lies strictly above the row's current threshold, a value with at least K buffered keys at or above
+//     it (a later key loses a tie, so no key at or below it can reach the top K).  Whenever the next tile might
+//     not fit, the buffer is cut back to the keys at or above a radix bin edge with between K and K + 256 keys
+//     above it (that edge becomes the threshold); at the row's end it is cut to exactly the top K, ties to the
+//     lower key.  One set of four selection warps; one q_idx buffer.
 template <bool LONG> struct SC;
 template <> struct SC<false> {
     static constexpr int THREADS = 576;       // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..17 selection
@@ -104,17 +110,26 @@ template <> struct SC<false> {
     static constexpr int SMEM_ALLOC = OFF_MISC + 1024 + 1024;      // slack to align the base to 1024 B
 };
 template <> struct SC<true> {
-    static constexpr int THREADS = 320;       // warps 0 TMA, 1 MMA, 2..9 epilogue
-    static constexpr int NB = 2;
+    static constexpr int THREADS = 448;       // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..13 selection
+    static constexpr int NB = 1;
+    static constexpr int NRING = 4;           // score tiles in flight between epilogue and selection
+    static constexpr int CAP = 4096;          // candidate entries per row
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + A_STAGES * A_HALF;        // 48 KB
-    static constexpr int OFF_W = OFF_B + NB * B_BUF;               // 176 KB
-    static constexpr int OFF_MISC = OFF_W + ROWS * HI * 4;
+    static constexpr int OFF_RING = OFF_B + NB * B_BUF;            // 112 KB
+    static constexpr int OFF_W = OFF_RING + NRING * ROWS * NKEY * 4;
+    static constexpr int OFF_CK = OFF_W + ROWS * HI * 4;           // candidate keys [ROWS][CAP] u32
+    static constexpr int OFF_CI = OFF_CK + ROWS * CAP * 4;         // candidate indices [ROWS][CAP] u16
+    static constexpr int OFF_HIST = OFF_CI + ROWS * CAP * 2;       // radix histograms [ROWS][256] u32
+    static constexpr int OFF_MISC = OFF_HIST + ROWS * 256 * 4;
     static constexpr int SMEM_ALLOC = OFF_MISC + 1024 + 1024;
 };
 static_assert(SC<false>::SMEM_ALLOC <= 232448, "score kernel exceeds the 227 KB of shared memory a CTA may use");
 static_assert(SC<true>::SMEM_ALLOC <= 232448, "long score kernel exceeds the 227 KB of shared memory a CTA may use");
-constexpr int LONG_NCMAX = 1 << 22;           // longest key axis taken (score rows are written to the workspace)
+// largest K the long kernel takes: an in-loop cut leaves at most K + slack entries, slack = min(256, CAP -
+// 2 NKEY - K) >= 0, so that two more tiles fit
+constexpr int LONG_KMAX = SC<true>::CAP - 2 * NKEY;
+constexpr int LONG_NCMAX = 65535;             // candidate indices are 16-bit
 
 constexpr uint32_t IDESC = idesc_bf16(NKEY, NCOL, false, false);  // A, B both K-major
 
@@ -125,7 +140,6 @@ struct Args {
     float *selscore;
     float *dump;
     long long dump_row0, dump_rows;
-    float *scores;       // long key axis: fp32 score rows [rows][NC] (visible keys only)
     const int *cu_g;     // THD: work-item offsets per segment [nseg+1]
     int total;           // SBHD/BSHD: number of work items (THD: read from cu_g[nseg])
 };
@@ -328,6 +342,172 @@ __device__ void select_row(const Args &a, const Item &it, int k, const float *sc
     }
 }
 
+// ------------------------------------------------------------------ long key axis: candidate buffers
+
+// A cut point of the n keys ck[0..n), all in [lo, hi] (K <= n), one warp, by a radix walk in digits of up to
+// 8 bits with a 256-bin histogram per pass.  The walk starts at the highest bit in which lo and hi differ (the
+// bits above it are the same in every key, so no pass is spent on them).
+//   slack < 0: returns the K-th largest key T; `need_eq` receives how many entries equal to T belong to the top K
+//              (the rest of the top K lies strictly above T).
+//   slack >= 0: may stop early, at the first digit whose bin holding the K-th largest key has a lower edge L with
+//              at most K + slack keys at or above it; returns L (at least K keys lie at or above it), with
+//              `need_eq` = n (every key equal to L is kept).  Reaching the last digit gives the exact answer.
+// Once the bin holding the K-th largest key has at most 256 keys, they are collected into the histogram's space and
+// the rest of the exact answer is found bit by bit in registers.
+__device__ uint32_t kth_search(const uint32_t *ck, int n, int K, uint32_t lo, uint32_t hi, int slack, uint32_t *hist,
+                               int &need_eq)
+{
+    const int lane = threadIdx.x & 31;
+    if (lo == hi) {  // every key is the same: the first K of them
+        need_eq = K;
+        return lo;
+    }
+    int hb = 31 - __clz(lo ^ hi);                 // top bit of the current digit
+    uint32_t prefix = hi & ~((2u << hb) - 1u);    // the bits above it (2u << 31 wraps to 0: no common bits)
+    int need = K;  // rank of the wanted entry among those matching the prefix, counted from the top
+#pragma unroll 1
+    while (true) {
+        const int lb = hb >= 7 ? hb - 7 : 0;      // digit bits lb .. hb
+        const uint32_t wmask = (2u << (hb - lb)) - 1u;
+        const uint32_t pmask = ~((2u << hb) - 1u);
+#pragma unroll
+        for (int q = 0; q < 8; q++) hist[lane * 8 + q] = 0u;
+        __syncwarp();
+        for (int e0 = 0; e0 < n; e0 += 128) {
+            uint32_t kk[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int e = e0 + 32 * u + lane;
+                kk[u] = e < n ? ck[e] : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                if (e0 + 32 * u + lane < n && (kk[u] & pmask) == prefix) atomicAdd(hist + ((kk[u] >> lb) & wmask), 1u);
+        }
+        __syncwarp();
+        // lane l owns bins 255 - 8 l .. 248 - 8 l (descending); an inclusive scan over lanes counts the entries
+        // in bins at or above each lane's lowest bin
+        uint32_t c[8], tot = 0u;
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            c[q] = hist[255 - 8 * lane - q];
+            tot += c[q];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t before = incl - tot;
+        const bool mine = before < (uint32_t)need && (uint32_t)need <= incl;
+        const unsigned who = __ballot_sync(0xffffffffu, mine);
+        int bin = 0;
+        uint32_t above = 0u, cnt = 0u;
+        if (mine) {
+            uint32_t acc = before;
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                if (bin == 0 && acc + c[q] >= (uint32_t)need) {
+                    bin = 256 + 255 - 8 * lane - q;  // +256: found
+                    cnt = c[q];
+                }
+                if (bin == 0) acc += c[q];
+            }
+            above = acc;
+            bin -= 256;
+        }
+        const int src = __ffs(who) - 1;
+        bin = __shfl_sync(0xffffffffu, bin, src);
+        above = __shfl_sync(0xffffffffu, above, src);
+        cnt = __shfl_sync(0xffffffffu, cnt, src);
+        prefix |= (uint32_t)bin << lb;
+        need -= (int)above;
+        __syncwarp();
+        if (lb == 0) {
+            need_eq = need;
+            return prefix;
+        }
+        // keys at or above the bin's lower edge: K - need + cnt
+        if (slack >= 0 && (int)cnt - need <= slack) {
+            need_eq = n;
+            return prefix;
+        }
+        if (cnt <= 256u) {
+            // few keys in the bin: collect them (into the histogram's space) and find the need-th largest bit by bit,
+            // eight per lane in registers, instead of a histogram pass per remaining digit
+            const uint32_t cmask = ~((1u << lb) - 1u);
+            int base = 0;
+            for (int e0 = 0; e0 < n; e0 += 32) {
+                const int e = e0 + lane;
+                const uint32_t k = e < n ? ck[e] : 0u;
+                const bool in = e < n && (k & cmask) == prefix;
+                const unsigned mk = __ballot_sync(0xffffffffu, in);
+                if (in) hist[base + __popc(mk & ((1u << lane) - 1u))] = k;
+                base += __popc(mk);
+            }
+            __syncwarp();
+            uint32_t key[8];
+#pragma unroll
+            for (int q = 0; q < 8; q++) key[q] = 32 * q + lane < (int)cnt ? hist[32 * q + lane] : 0u;
+            uint32_t t = prefix;  // every collected key is at or above it
+#pragma unroll 1
+            for (int bit = lb - 1; bit >= 0; bit--) {
+                const uint32_t cc = t | (1u << bit);
+                unsigned c2 = 0u;
+#pragma unroll
+                for (int q = 0; q < 8; q++) c2 += key[q] >= cc ? 1u : 0u;
+                if ((int)__reduce_add_sync(0xffffffffu, c2) >= need) t = cc;
+            }
+            unsigned gt = 0u;
+#pragma unroll
+            for (int q = 0; q < 8; q++) gt += key[q] > t ? 1u : 0u;
+            need_eq = need - (int)__reduce_add_sync(0xffffffffu, gt);
+            __syncwarp();  // the list is read before the next cut zeroes the histogram
+            return t;
+        }
+        hb = lb - 1;
+    }
+}
+
+// Cuts the candidate buffer (ascending key index, keys in [lo, hi]) back to the entries at or above the cut
+// point kth_search finds (exactly the top K, ties to the lower index, when slack < 0; otherwise every key at or
+// above a bin edge L, between K and K + slack of them), keeping the ascending order (stable in-place
+// compaction).  Returns the new count; `thr` receives T (or L): a later key can enter the top K only above it.
+__device__ int cut_candidates(uint32_t *ck, uint16_t *ci, int n, int K, uint32_t lo, uint32_t hi, int slack,
+                              uint32_t *hist, uint32_t &thr)
+{
+    const int lane = threadIdx.x & 31;
+    int need_eq = 0;
+    const uint32_t T = kth_search(ck, n, K, lo, hi, slack, hist, need_eq);
+    const unsigned lt = (1u << lane) - 1u;
+    int base = 0, eq_seen = 0;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int e = c0 + lane;
+        uint32_t k = 0u;
+        uint16_t ix = 0;
+        if (e < n) {
+            k = ck[e];
+            ix = ci[e];
+        }
+        const bool eq = e < n && k == T;
+        const unsigned meq = __ballot_sync(0xffffffffu, eq);
+        const bool keep = e < n && (k > T || (eq && eq_seen + __popc(meq & lt) < need_eq));
+        eq_seen += __popc(meq);
+        const unsigned mk = __ballot_sync(0xffffffffu, keep);
+        __syncwarp();  // every lane has read its entry before any is overwritten (writes land at or below c0 + 31)
+        if (keep) {
+            const int pos = base + __popc(mk & lt);
+            ck[pos] = k;
+            ci[pos] = ix;
+        }
+        base += __popc(mk);
+        __syncwarp();
+    }
+    thr = T;
+    return base;
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <bool LONG>
@@ -361,7 +541,12 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
             mbar_init(t_full + i, 1);
             mbar_init(t_empty + i, 8);
         }
-        if constexpr (!LONG) {
+        if constexpr (LONG) {
+            for (int i = 0; i < C::NRING; i++) {
+                mbar_init(x_full + i, EPI / 32);
+                mbar_init(x_empty + i, ROWS);
+            }
+        } else {
             for (int i = 0; i < C::NSC; i++) {
                 mbar_init(x_full + i, EPI / 32);
                 mbar_init(x_empty + i, ROWS);
@@ -564,13 +749,15 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
                 __syncwarp();
                 if (lane == 0) mbar_arrive(t_empty + tb);
                 if constexpr (LONG) {
-                    // the tile's visible scores of rows 2 half, 2 half + 1 into their score rows (one key per lane:
-                    // 128-byte stores per warp and row)
-#pragma unroll
-                    for (int rr = 0; rr < 2; rr++) {
-                        const int k = half * 2 + rr;
-                        if (k < it.n && j < it.v[k]) a.scores[it.row[k] * (long long)g.NC + j] = accs[rr];
-                    }
+                    // the tile's scores of rows 2 half, 2 half + 1 into ring slot tc % NRING (keys past a row's
+                    // visible count are written too; the selection masks them)
+                    const int slot = tc % C::NRING;
+                    wait_bar(x_empty + slot, ((tc / C::NRING) & 1) ^ 1, abort_flag, &g_tc_error, 7);
+                    float *ring = reinterpret_cast<float *>(smem + C::OFF_RING) + slot * ROWS * NKEY;
+                    ring[(half * 2) * NKEY + quad * 32 + lane] = accs[0];
+                    ring[(half * 2 + 1) * NKEY + quad * 32 + lane] = accs[1];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(x_full + slot);
                 }
                 tc++;
             }
@@ -606,6 +793,90 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
                 if (lane == 0) mbar_arrive(x_empty + sb);
             }
         }
+    } else {
+        // ---------------------------------------------------------- selection, long key axis (warps 10..13, one
+        // row each): consume the score tiles of every item in order; keep the row's candidates in shared memory
+        const int k = warp - SEL_WARP0;
+        uint32_t *ck = reinterpret_cast<uint32_t *>(smem + C::OFF_CK) + k * C::CAP;
+        uint16_t *ci = reinterpret_cast<uint16_t *>(smem + C::OFF_CI) + k * C::CAP;
+        uint32_t *hist = reinterpret_cast<uint32_t *>(smem + C::OFF_HIST) + k * 256;
+        const float *ringb = reinterpret_cast<const float *>(smem + C::OFF_RING);
+        const int K = g.K;
+        // an in-loop cut may keep up to cut_slack entries past the top K (the exact cut comes at the row's end);
+        // it must still leave room for two tiles, so the slack shrinks for K near the largest K taken
+        const int cut_slack = C::CAP - 2 * NKEY - K < 256 ? C::CAP - 2 * NKEY - K : 256;
+        const unsigned lt = (1u << lane) - 1u;
+        int tc = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+            const Item it = decode_item(a, i, total);
+            const int nt = (it.vmax + NKEY - 1) / NKEY;
+            const bool present = k < it.n;
+            const int v = present ? it.v[k] : 0;
+            const long long r = present ? it.row[k] : -1;
+            float *dump_row = (present && a.dump != nullptr && r >= a.dump_row0 && r < a.dump_row0 + a.dump_rows)
+                                  ? a.dump + (r - a.dump_row0) * (long long)g.NC
+                                  : nullptr;
+            const bool select = present && a.ids != nullptr;
+            int n = 0;
+            uint32_t thr = 0u;  // a key enters only above this (0: every score, before the first cut)
+            uint32_t klo = 0xffffffffu, khi = 0u;  // bounds of this lane's buffered keys (after a cut: [thr, max])
+            auto cut = [&](int slack) {
+                const uint32_t lo = __reduce_min_sync(0xffffffffu, klo), hi = __reduce_max_sync(0xffffffffu, khi);
+                n = cut_candidates(ck, ci, n, K, lo, hi, slack, hist, thr);
+                klo = thr;
+                khi = hi;
+            };
+            for (int t = 0; t < nt; t++, tc++) {
+                const int slot = tc % C::NRING;
+                wait_bar(x_full + slot, (tc / C::NRING) & 1, abort_flag, &g_tc_error, 8);
+                float s[4];
+#pragma unroll
+                for (int c = 0; c < 4; c++) s[c] = ringb[(slot * ROWS + k) * NKEY + 32 * c + lane];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(x_empty + slot);
+                if (dump_row != nullptr) {
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        const int j = t * NKEY + 32 * c + lane;
+                        if (j < g.NC) dump_row[j] = j < v ? s[c] : -INFINITY;
+                    }
+                }
+                if (!select) continue;
+                if (n + NKEY > C::CAP) cut(cut_slack);
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    const int j = t * NKEY + 32 * c + lane;
+                    const uint32_t key = score_key(s[c]);
+                    const bool in = j < v && key > thr;
+                    const unsigned m = __ballot_sync(0xffffffffu, in);
+                    if (in) {
+                        const int pos = n + __popc(m & lt);
+                        ck[pos] = key;
+                        ci[pos] = (uint16_t)j;
+                        klo = min(klo, key);
+                        khi = max(khi, key);
+                    }
+                    n += __popc(m);
+                }
+                __syncwarp();
+            }
+            if (dump_row != nullptr)
+                for (int j = nt * NKEY + lane; j < g.NC; j += 32) dump_row[j] = -INFINITY;
+            if (!select) continue;
+            if (n > K) cut(-1);
+            __syncwarp();
+            int32_t *orow = a.ids + r * K;
+            float *srow = a.selscore + r * K;
+            for (int s2 = lane; s2 < n; s2 += 32) {
+                orow[s2] = (int32_t)(it.gid0 + ci[s2]);
+                srow[s2] = key_score(ck[s2]);
+            }
+            for (int s2 = n + lane; s2 < K; s2 += 32) {
+                orow[s2] = -1;
+                srow[s2] = -INFINITY;
+            }
+            __syncwarp();
+        }
     }
     fence_before();
     __syncthreads();
@@ -620,7 +891,7 @@ score_topk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_con
 }
 
 __global__ void __launch_bounds__(SC<true>::THREADS, 1)
-score_rows_long_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
+score_topk_long_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k, Args a)
 {
     score_body<true>(&map_q, &map_k, a);
 }
@@ -683,20 +954,11 @@ bool tc_score_supported(const Geo &g, bool bf16)
     if (f != nullptr && f[0] == '1') return false;
     if (!(bf16 && g.HI == tcs::HI && g.DI == tcs::DI && g.NC >= 1 && g.K >= 1 && g.rows > 0 && g.key_rows > 0))
         return false;
-    // short key axis: whole score rows in shared memory; long: score rows through the workspace
-    return g.NC <= tcs::NCMAX || g.NC <= tcs::LONG_NCMAX;
+    // short key axis: whole score rows in shared memory; long: streamed tiles and candidate buffers
+    return g.NC <= tcs::NCMAX || (g.NC <= tcs::LONG_NCMAX && g.K <= tcs::LONG_KMAX);
 }
 
-// workspace: THD work-item offsets, then (long key axis) the score rows
-static size_t score_rows_offset(const Geo &g)
-{
-    return (sizeof(int) * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1) + 255) & ~(size_t)255;
-}
-
-size_t tc_workspace_bytes(const Geo &g)
-{
-    return score_rows_offset(g) + (g.NC > tcs::NCMAX ? sizeof(float) * (size_t)g.rows * (size_t)g.NC : 0);
-}
+size_t tc_workspace_bytes(const Geo &g) { return sizeof(int) * (size_t)(g.layout == CSA_THD ? g.B + 1 : 1); }
 
 bool tc_encode_q_map(CUtensorMap *m, const void *q_idx, const Geo &g)
 {
@@ -737,7 +999,6 @@ static cudaError_t launch_tc(const Geo &g, const __nv_bfloat16 *q_idx, const flo
     a.dump_rows = nrows;
     a.cu_g = nullptr;
     a.total = 0;
-    a.scores = g.NC > NCMAX ? reinterpret_cast<float *>(static_cast<char *>(ws) + score_rows_offset(g)) : nullptr;
     int upper;
     if (g.layout == CSA_THD) {
         int *cu_g = static_cast<int *>(ws);
@@ -760,16 +1021,10 @@ static cudaError_t launch_tc(const Geo &g, const __nv_bfloat16 *q_idx, const flo
         if (e != cudaSuccess) return e;
         score_topk_tc_kernel<<<grid, SC<false>::THREADS, SC<false>::SMEM_ALLOC, st>>>(mq, mk, a);
     } else {
-        // long key axis: the score rows to the workspace, then the top-k (or the debug copy) from there
-        e = cudaFuncSetAttribute(score_rows_long_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(score_topk_long_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SC<true>::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        score_rows_long_tc_kernel<<<grid, SC<true>::THREADS, SC<true>::SMEM_ALLOC, st>>>(mq, mk, a);
-        note_launches(1);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        if (dump != nullptr) return launch_dump_rows(g, a.scores, row0, nrows, dump, st);
-        return launch_topk_rows(g, a.scores, ids, selscore, st);
+        score_topk_long_tc_kernel<<<grid, SC<true>::THREADS, SC<true>::SMEM_ALLOC, st>>>(mq, mk, a);
     }
     note_launches(1);
     return cudaGetLastError();
