@@ -438,13 +438,18 @@ __device__ uint32_t kth_search(const uint32_t *ck, int n, int K, uint32_t lo, ui
             // eight per lane in registers, instead of a histogram pass per remaining digit
             const uint32_t cmask = ~((1u << lb) - 1u);
             int base = 0;
-            for (int e0 = 0; e0 < n; e0 += 32) {
-                const int e = e0 + lane;
-                const uint32_t k = e < n ? ck[e] : 0u;
-                const bool in = e < n && (k & cmask) == prefix;
-                const unsigned mk = __ballot_sync(0xffffffffu, in);
-                if (in) hist[base + __popc(mk & ((1u << lane) - 1u))] = k;
-                base += __popc(mk);
+            for (int e0 = 0; e0 < n; e0 += 128) {  // four chunks per step: the loads and ballots overlap
+                uint32_t k[4];
+                unsigned mk[4];
+#pragma unroll
+                for (int u = 0; u < 4; u++) k[u] = e0 + 32 * u + lane < n ? ck[e0 + 32 * u + lane] : 0u;
+#pragma unroll
+                for (int u = 0; u < 4; u++) mk[u] = __ballot_sync(0xffffffffu, e0 + 32 * u + lane < n && (k[u] & cmask) == prefix);
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    if ((mk[u] >> lane) & 1u) hist[base + __popc(mk[u] & ((1u << lane) - 1u))] = k[u];
+                    base += __popc(mk[u]);
+                }
             }
             __syncwarp();
             uint32_t key[8];
@@ -482,26 +487,40 @@ __device__ int cut_candidates(uint32_t *ck, uint16_t *ci, int n, int K, uint32_t
     const uint32_t T = kth_search(ck, n, K, lo, hi, slack, hist, need_eq);
     const unsigned lt = (1u << lane) - 1u;
     int base = 0, eq_seen = 0;
-    for (int c0 = 0; c0 < n; c0 += 32) {
-        const int e = c0 + lane;
-        uint32_t k = 0u;
-        uint16_t ix = 0;
-        if (e < n) {
-            k = ck[e];
-            ix = ci[e];
+    // four 32-entry chunks per step, loaded and decided before any is written (one warp has little else to
+    // overlap its shared-memory latency with); writes land at or below the step's own entries
+    for (int c0 = 0; c0 < n; c0 += 128) {
+        uint32_t k[4];
+        uint16_t ix[4];
+        unsigned meq[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int e = c0 + 32 * u + lane;
+            k[u] = e < n ? ck[e] : 0u;
+            ix[u] = e < n ? ci[e] : (uint16_t)0;
         }
-        const bool eq = e < n && k == T;
-        const unsigned meq = __ballot_sync(0xffffffffu, eq);
-        const bool keep = e < n && (k > T || (eq && eq_seen + __popc(meq & lt) < need_eq));
-        eq_seen += __popc(meq);
-        const unsigned mk = __ballot_sync(0xffffffffu, keep);
-        __syncwarp();  // every lane has read its entry before any is overwritten (writes land at or below c0 + 31)
-        if (keep) {
-            const int pos = base + __popc(mk & lt);
-            ck[pos] = k;
-            ci[pos] = ix;
+#pragma unroll
+        for (int u = 0; u < 4; u++) meq[u] = __ballot_sync(0xffffffffu, c0 + 32 * u + lane < n && k[u] == T);
+        bool keep[4];
+        unsigned mk[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const bool in = c0 + 32 * u + lane < n;
+            const bool eq = ((meq[u] >> lane) & 1u) != 0u;
+            keep[u] = in && (k[u] > T || (eq && eq_seen + __popc(meq[u] & lt) < need_eq));
+            eq_seen += __popc(meq[u]);
+            mk[u] = __ballot_sync(0xffffffffu, keep[u]);
         }
-        base += __popc(mk);
+        __syncwarp();  // every lane has read its entries before any is overwritten
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            if (keep[u]) {
+                const int pos = base + __popc(mk[u] & lt);
+                ck[pos] = k[u];
+                ci[pos] = ix[u];
+            }
+            base += __popc(mk[u]);
+        }
         __syncwarp();
     }
     thr = T;
