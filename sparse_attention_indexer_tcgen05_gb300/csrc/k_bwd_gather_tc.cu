@@ -49,25 +49,26 @@ using namespace ptx;
 constexpr int HI = 64, DI = 128, NKEY = 128;
 constexpr int KHALF = NKEY * 64 * 2;            // 16 KB: 128 keys x 64 d
 constexpr int KT = 2 * KHALF;                   // 32 KB: a gathered k tile, two 64-wide K-halves
-constexpr int NKT = 4;                          // k tiles in the ring
+constexpr int NKT = 5;                          // k tiles in the ring
 constexpr int QHALF = HI * 64 * 2;              // 8 KB: 64 heads x 64 d
 constexpr int QT = 2 * QHALF;                   // 16 KB: a row's q_idx
 constexpr int GT = NKEY * HI * 2;               // 16 KB: G' [128 keys][64 heads] bf16
 constexpr int THREADS = 288;                    // 9 warps
 constexpr int NPROD = 128, EPI = 128;
 constexpr int EPI_WARP0 = 4, MMA_WARP = 8;
-constexpr int NX = 3;                           // X accumulators and G' tiles in flight (MMA2 runs two tiles behind)
-constexpr uint32_t TMEM_COLS = 256;             // X buffers at 0, 64, 128; dQ'^T at 192
+constexpr int NX = 2;                           // X accumulators and G' tiles in flight (MMA2 runs one tile behind)
+constexpr uint32_t TMEM_COLS = 256;             // X buffers at 0, 64; dQ'^T at 192
 constexpr uint32_t IDESC_X = idesc_bf16(128, HI, false, false);   // A = k tile, B = q, both K-major
 constexpr uint32_t IDESC_DQ = idesc_bf16(128, HI, true, true);    // A = k tile read MN-major, B = G' MN-major
 
 constexpr int OFF_K = 0;                                         // NKT x 32 KB
-constexpr int OFF_Q = OFF_K + NKT * KT;                          // 128 KB: 2 x 16 KB
-constexpr int OFF_G = OFF_Q + 2 * QT;                            // 160 KB: NX x 16 KB
-constexpr int OFF_W = OFF_G + NX * GT;                           // 208 KB: w rows, 2 x 64 fp32
+constexpr int OFF_Q = OFF_K + NKT * KT;                          // 160 KB: 2 x 16 KB
+constexpr int OFF_G = OFF_Q + 2 * QT;                            // 192 KB: NX x 16 KB
+constexpr int OFF_W = OFF_G + NX * GT;                           // 224 KB: w rows, 2 x 64 fp32
 constexpr int OFF_DW = OFF_W + 2 * HI * 4;                       // dW partials, 4 warps x 64 fp32
-constexpr int OFF_MISC = OFF_DW + 4 * HI * 4;
-constexpr int SMEM = OFF_MISC + 1024 + 1024;
+constexpr int OFF_MISC = OFF_DW + 4 * HI * 4;                    // barriers (< 256 B), TMEM slot, abort flag
+constexpr int SMEM = OFF_MISC + 512 + 1024;                      // + slack to align the base to 1024 B
+static_assert((2 * NKT + 4 + 4 * NX + 3) * 8 <= 256, "gathered row-owner barriers overlap the TMEM slot");
 static_assert(SMEM <= 232448, "gathered row-owner shared memory exceeds the per-block limit");
 
 struct Args {
@@ -135,8 +136,8 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
     uint64_t *q_full = bars + 2 * NKT, *q_empty = q_full + 2;
     uint64_t *x_full = q_full + 4, *x_empty = x_full + NX, *g_full = x_empty + NX, *g_empty = g_full + NX;
     uint64_t *dq_full = g_empty + NX, *dq_empty = dq_full + 1, *mma_done = dq_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 512);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 520);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC + 256);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 264);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Geo &g = a.g;
@@ -167,7 +168,7 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tX = tmem, tDQ = tmem + NX * 64;
+    const uint32_t tX = tmem, tDQ = tmem + 192;
 
     if (warp < EPI_WARP0) {
         // ---------------------------------------------------------------- producers
@@ -358,8 +359,9 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
         }
     } else {
         // ---------------------------------------------------------------- MMA issue (whole warp)
-        // Per row: MMA1 of tile t, then MMA2 of tile t - 2 (whose G' the epilogue has had two tiles' time to
-        // write); the row's last two MMA2 close it.
+        // Per row: MMA1 of tile t, then MMA2 of tile t - 1 (whose G' the epilogue has had MMA1's time to write);
+        // the row's last MMA2 closes it.  (Two tiles of lag would hold each k tile one tile longer, and the k ring's
+        // prefetch, not the epilogue, sets this kernel's pace.)
         // Barrier tests cost the issuing thread a shared-memory round trip, so after each MMA group the barriers
         // the next groups need are probed (two per round trip) while the MMAs just issued run; the warp waits only
         // on a barrier no probe has seen complete.  (None of them can be two phases behind: their previous uses
@@ -404,16 +406,16 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
                           su32(x_full + xb));
                 if (t == it.nt - 1) mma_commit_w(q_empty + qb);  // the row's q is read by its X groups only
                 x++;
-                if (t >= 2) {
-                    // G' of tile t - 2 and the next tile's k, while MMA1 runs
-                    const int y = x - 3;
+                if (t >= 1) {
+                    // G' of tile t - 1 and the next tile's k, while MMA1 runs
+                    const int y = x - 2;
                     const uint32_t m = mbar_test2(g_full + y % NX, (y / NX) & 1, k_full + x % NKT, (x / NKT) & 1);
                     g_rdy = (m & 1u) != 0u;
                     k_rdy = (m & 2u) != 0u;
-                    mma2(y, t - 2);
+                    mma2(y, t - 1);
                 }
             }
-            for (int t = it.nt >= 2 ? it.nt - 2 : 0; t < it.nt; t++) mma2(x0 + t, t);
+            mma2(x0 + it.nt - 1, it.nt - 1);
             mma_commit_w(dq_full);
             rq++;
         }
