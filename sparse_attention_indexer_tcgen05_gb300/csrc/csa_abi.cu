@@ -229,8 +229,10 @@ csa_status run_fwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
 
 template <typename T>
 csa_status run_teacher(Plan &P, const void *q, const void *kv, const void *kv_c, const float *sink,
-                       const int32_t *ids, float *teacher, void *ws, cudaStream_t st)
+                       const int32_t *ids, float *teacher, void *ws, cudaStream_t st, const TeacherKl *kl = nullptr,
+                       bool *kl_done = nullptr)
 {
+    if (kl_done != nullptr) *kl_done = false;
     if (tc_teacher_supported(P.g, sizeof(T) == 2)) {
         t_last_path = "tcgen05";
         CSA_CUDA(launch_teacher_tc(P.g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kv,
@@ -240,7 +242,8 @@ csa_status run_teacher(Plan &P, const void *q, const void *kv, const void *kv_c,
     if (tc_teacher_h128_supported(P.g, sizeof(T) == 2)) {
         t_last_path = "tcgen05";
         CSA_CUDA(launch_teacher_h128_tc(P.g, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)kv,
-                                        (const __nv_bfloat16 *)kv_c, sink, ids, teacher, st));
+                                        (const __nv_bfloat16 *)kv_c, sink, ids, teacher, kl, st));
+        if (kl_done != nullptr) *kl_done = kl != nullptr;
         return CSA_OK;
     }
     CSA_TRY(check_smem(teacher_generic_smem(P.g, sizeof(T) == 2)));
@@ -257,20 +260,6 @@ csa_status run_bwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
 {
     CSA_TRY(prologue(P, ws, st));
     const Geo &g = P.g;
-    const float *teacher = teacher_in;
-    if (teacher == nullptr) {
-        float *tbuf = reinterpret_cast<float *>(ws_at(ws, P.off_teacher));
-        CSA_TRY(run_teacher<T>(P, q, kv, kv_c, sink, ids, tbuf, ws, st));
-        teacher = tbuf;
-    }
-    const float *dense_scores = nullptr;
-    if (P.dense_rescore) {
-        float *ds = reinterpret_cast<float *>(ws_at(ws, P.off_dense));
-        CSA_TRY(check_smem(score_topk_generic_smem(g)));
-        CSA_CUDA(launch_score_topk_generic<T>(g, (const T *)q_idx, w, (const T *)k_idx, nullptr, nullptr, ds, 0,
-                                              g.rows, st));
-        dense_scores = ds;
-    }
     float *gbuf = reinterpret_cast<float *>(ws_at(ws, P.off_g));
     float *row_loss = row_loss_out ? row_loss_out : reinterpret_cast<float *>(ws_at(ws, P.off_rowloss));
     const bool tc = tc_bwd_supported(g, sizeof(T) == 2);
@@ -279,8 +268,29 @@ csa_status run_bwd(Plan &P, const void *q_idx, const float *w, const void *k_idx
     float *gd = by_key ? tc_bwd_gd(g, btc) : nullptr;
     // the tensor-core backward on short key axes reads g by key only; the slot-layout rows serve the CUDA-core
     // backward and the tensor-core one on long key axes
-    CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, by_key ? nullptr : gbuf, row_loss, gd,
-                       by_key ? tc_bwd_ncp(g) : 0, st));
+    float *g_slot = by_key ? nullptr : gbuf;
+    const int ncp = by_key ? tc_bwd_ncp(g) : 0;
+    const float *teacher = teacher_in;
+    bool kl_done = false;
+    if (teacher == nullptr) {
+        // with the sparse loss the 128-head teacher takes the KL step itself (its rows then never go to memory)
+        const TeacherKl kl = {selscore, g_slot, gd, ncp, row_loss};
+        const bool fuse = g.sparse && !P.dense_rescore && g.TW == g.K;
+        float *tbuf = reinterpret_cast<float *>(ws_at(ws, P.off_teacher));
+        CSA_TRY(run_teacher<T>(P, q, kv, kv_c, sink, ids, tbuf, ws, st, fuse ? &kl : nullptr, &kl_done));
+        teacher = tbuf;
+    }
+    if (!kl_done) {
+        const float *dense_scores = nullptr;
+        if (P.dense_rescore) {
+            float *ds = reinterpret_cast<float *>(ws_at(ws, P.off_dense));
+            CSA_TRY(check_smem(score_topk_generic_smem(g)));
+            CSA_CUDA(launch_score_topk_generic<T>(g, (const T *)q_idx, w, (const T *)k_idx, nullptr, nullptr, ds, 0,
+                                                  g.rows, st));
+            dense_scores = ds;
+        }
+        CSA_CUDA(launch_kl(g, ids, selscore, dense_scores, teacher, g_slot, row_loss, gd, ncp, st));
+    }
     if (g.key_rows * g.DI > 0)
         CSA_CUDA(cudaMemsetAsync(dk_acc, 0, sizeof(float) * (size_t)g.key_rows * g.DI, st));
     if (tc) {

@@ -68,9 +68,20 @@ cudaError_t teacher_tc_read_clear_error(int *flag);
 // Tensor-core teacher for bf16, H = 128, D a multiple of 64 up to 512, teacher rows up to 2048 wide: one query
 // row per work item, q in TMEM, the selected compressed keys gathered (sparse loss) or tiled (dense loss).
 bool tc_teacher_h128_supported(const Geo &g, bool bf16);
+// The KL step taken inside the teacher (sparse loss, teacher width K): from the row's selected scores and its
+// normalised teacher, the row's KL goes to row_loss and g to gslot (by slot, [rows][K]) and/or gkey (by key,
+// row gd_row_of(...) of stride ncp, its visible range zeroed first); either may be null.  The teacher rows are
+// then not written.
+struct TeacherKl {
+    const float *selscore;
+    float *gslot;
+    float *gkey;
+    int ncp;
+    float *row_loss;
+};
 cudaError_t launch_teacher_h128_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *kv,
                                    const __nv_bfloat16 *kv_c, const float *sink, const int32_t *ids, float *teacher,
-                                   cudaStream_t st);
+                                   const TeacherKl *kl, cudaStream_t st);
 cudaError_t teacher_h128_read_clear_error(int *flag);
 
 // One tiny kernel whose bounded wait (about 1 ms) on a barrier nothing arrives on runs out (k_selftest.cu), and

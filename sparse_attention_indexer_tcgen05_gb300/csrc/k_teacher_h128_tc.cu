@@ -20,7 +20,9 @@
 //   pass 1: window tiles + compressed tiles -> per-head running sum against a reference maximum, then l_h with
 //           the sink (or a given sink-and-window log-sum-exp);
 //   pass 2: compressed tiles again -> exp(c - l_h) summed over the 128 heads into shared per-slot T;
-//   the helper warp then L1-normalises the row and writes it out.
+//   the helper warp then L1-normalises the row and writes it out; inside the backward (sparse loss) it takes the
+//   row's KL step from the normalised row instead (loss and g from the selected scores), so the teacher rows
+//   never go to memory and no separate KL launch runs.
 // Between rows the epilogue warps copy the next row's q from its ring stages into TMEM once the current row's
 // last MMAs have completed (the accumulators are double-buffered, the q columns are not).
 // Roles: warp 1 TMEM + MMA issue, warps 2..9 epilogue (two per TMEM lane quadrant), warp 10 per-row helper,
@@ -64,7 +66,8 @@ constexpr int OFF_T = OFF_RING + NSTG * STG;                    // 192 KB: per-s
 constexpr int OFF_MASK = OFF_T + 2 * TWMAX * 4;                 // slot-validity words, 2 x TWMAX / 32
 constexpr int OFF_PART = OFF_MASK + 2 * (TWMAX / 32) * 4;       // (m, s) partials: 2 parities x 2 halves x 128
 constexpr int OFF_MISC = OFF_PART + 2 * 2 * H * 8;
-constexpr int SMEM = OFF_MISC + 1024 + 1024;
+constexpr int OFF_KLE = OFF_MISC + 1024;                         // the KL step's exp(x - m) per slot, TWMAX
+constexpr int SMEM = OFF_KLE + TWMAX * 4 + 1024;                 // + the 1024-byte alignment slack
 static_assert(SMEM <= 232448, "teacher shared memory exceeds the per-block limit");
 
 struct Args {
@@ -76,6 +79,12 @@ struct Args {
     const __nv_bfloat16 *kv_c;
     float *teacher;
     int nkb;                     // D / 64
+    int kl;                      // the KL step runs in the helper warp (sparse loss, TW == K): the fields below
+    const float *selscore;       // [rows][K] selected scores
+    float *gslot;                // g by slot [rows][K], or null
+    float *gkey;                 // g by key (row gd_row_of, stride ncp), or null
+    int ncp;
+    float *row_loss;             // [rows]
 };
 
 struct Item {
@@ -489,16 +498,94 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
         // ---------------------------------------------------------------- per-row helper
         // For row ic (buffer ic & 1): zero its T row, build its slot-validity words (sparse loss), signal
         // mask_full; then, once the epilogue has summed row ic - 1 into the other buffer (t_done), L1-normalise
-        // that row and write it out.  Buffer reuse is ordered by this warp's program order.
+        // that row and write it out, or (a.kl) take the row's KL step from it.  Buffer reuse is ordered by this
+        // warp's program order.
+        //
+        // KL step of a row ([BUG] sec. 2 excerpt; the arithmetic of the KL kernels): p = softmax of the selected
+        // scores over the support C (the slots whose id is a visible key of the row, the validity words), t the
+        // normalised teacher (0 past the first min(v, K) slots), L = sum_C t (log(t + eps) - log(p + eps)) and
+        // g_s = f p_s (A - t_s / (p_s + eps)) with A = sum_C t p / (p + eps).  The scores' maximum and the
+        // exponentials exp(x - m) (in sE) need no teacher, so they are taken before waiting for the epilogue.
+        float *sE = reinterpret_cast<float *>(smem + OFF_KLE);
+        constexpr int KLB = 16;  // score loads in flight per lane
+        auto in_support = [&](const uint32_t *mk, int j) { return ((mk[j >> 5] >> (j & 31)) & 1u) != 0u; };
         auto writeout = [&](const Item &it, int icw) {
             const int ib = icw & 1;
+            const int K = g.K;
+            const uint32_t *mk = sMask + ib * (TWMAX / 32);
+            const bool any = it.v > 0;  // otherwise no validity words were built: the support is empty
+            float m = -INFINITY, z = 0.f;
+            if (a.kl && any) {
+                const float *xrow = a.selscore + it.row * K;
+                for (int j0 = 0; j0 < K; j0 += 32 * KLB) {
+                    float xv[KLB];
+#pragma unroll
+                    for (int k = 0; k < KLB; k++) {
+                        const int j = j0 + 32 * k + lane;
+                        xv[k] = j < K && in_support(mk, j) ? __ldg(xrow + j) : -INFINITY;
+                    }
+#pragma unroll
+                    for (int k = 0; k < KLB; k++) {
+                        const int j = j0 + 32 * k + lane;
+                        if (j < K) sE[j] = xv[k];
+                        m = fmaxf(m, xv[k]);
+                    }
+                }
+                m = warp_max(m);
+                if (m != -INFINITY) {
+                    for (int j = lane; j < K; j += 32) {  // each lane rereads only its own slots
+                        const float e = __expf(sE[j] - m);  // 0 off the support (x = -inf)
+                        sE[j] = e;
+                        z += e;
+                    }
+                    z = warp_sum(z);
+                }
+            }
             wait_bar(t_done + ib, (icw >> 1) & 1, abort_flag, err, 69);
             const float *tr = sT + ib * TWMAX;
             float part = 0.f;
             for (int j = lane; j < it.ncs; j += 32) part += tr[j];
             const float inv = 1.f / fmaxf(warp_sum(part), 1e-10f);
-            float *trow = a.teacher + it.row * g.TW;
-            for (int j = lane; j < g.TW; j += 32) trow[j] = j < it.ncs ? tr[j] * inv : 0.f;
+            if (!a.kl) {
+                float *trow = a.teacher + it.row * g.TW;
+                for (int j = lane; j < g.TW; j += 32) trow[j] = j < it.ncs ? tr[j] * inv : 0.f;
+                return;
+            }
+            float *grow = a.gslot != nullptr ? a.gslot + it.row * K : nullptr;
+            float *drow = a.gkey != nullptr ? a.gkey + gd_row_of(g, it.b, it.s, it.row) * a.ncp : nullptr;
+            if (drow != nullptr) {  // zero the visible range (16-byte stores: the row stride is a multiple of 4)
+                for (int j4 = lane; 4 * j4 < it.v; j4 += 32)
+                    reinterpret_cast<float4 *>(drow)[j4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                __syncwarp();
+            }
+            if (m == -INFINITY) {  // empty support: no loss, no gradient
+                if (grow != nullptr)
+                    for (int j = lane; j < K; j += 32) grow[j] = 0.f;
+                if (lane == 0) a.row_loss[it.row] = 0.f;
+                return;
+            }
+            const float inv_z = 1.f / z;
+            float A = 0.f, L = 0.f;
+            for (int j = lane; j < K; j += 32) {
+                if (!in_support(mk, j)) continue;
+                const float p = sE[j] * inv_z;
+                const float t = j < it.ncs ? tr[j] * inv : 0.f;
+                A += t * p / (p + kKlEps);
+                L += t * (logf(t + kKlEps) - logf(p + kKlEps));
+            }
+            A = warp_sum(A);
+            L = warp_sum(L);
+            const int32_t *irow = a.ids + it.row * K;
+#pragma unroll 4
+            for (int j = lane; j < K; j += 32) {
+                const bool in = in_support(mk, j);
+                const float p = sE[j] * inv_z;
+                const float t = j < it.ncs ? tr[j] * inv : 0.f;
+                const float gv = in ? g.factor * p * (A - t / (p + kKlEps)) : 0.f;
+                if (grow != nullptr) grow[j] = gv;
+                if (drow != nullptr && in) drow[__ldg(irow + j) - it.gid0] = gv;
+            }
+            if (lane == 0) a.row_loss[it.row] = L;
         };
         Item prev;
         int ic = 0;
@@ -509,17 +596,19 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
             const int nz = (it.ncs + 3) / 4;
             for (int x = lane; x < nz; x += 32) tz[x] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (g.sparse && ntiles(it) > 0) {
+                // the teacher reads the words of the first ncs slots; the KL step those of all K slots
+                const int nmk = a.kl ? g.K : it.ncs;
                 uint32_t *mk = sMask + ib * (TWMAX / 32);
-                for (int w0 = 0; w0 < it.ncs; w0 += 256) {  // eight independent loads in flight per lane
+                for (int w0 = 0; w0 < nmk; w0 += 256) {  // eight independent loads in flight per lane
                     int32_t idv[8];
 #pragma unroll
-                    for (int k = 0; k < 8; k++) idv[k] = w0 + 32 * k + lane < it.ncs ? slot_id(a, it, w0 + 32 * k + lane) : -1;
+                    for (int k = 0; k < 8; k++) idv[k] = w0 + 32 * k + lane < nmk ? slot_id(a, it, w0 + 32 * k + lane) : -1;
 #pragma unroll
                     for (int k = 0; k < 8; k++) {
                         bool ok;
                         id_key_row(a, it, idv[k], ok);
                         const unsigned bits = __ballot_sync(0xffffffffu, ok);
-                        if (lane == 0 && w0 + 32 * k < it.ncs) mk[(w0 >> 5) + k] = bits;
+                        if (lane == 0 && w0 + 32 * k < nmk) mk[(w0 >> 5) + k] = bits;
                     }
                 }
             }
@@ -680,7 +769,7 @@ bool tc_teacher_h128_supported(const Geo &g, bool bf16)
 
 cudaError_t launch_teacher_h128_tc(const Geo &g, const __nv_bfloat16 *q, const __nv_bfloat16 *kv,
                                    const __nv_bfloat16 *kv_c, const float *sink, const int32_t *ids, float *teacher,
-                                   cudaStream_t st)
+                                   const TeacherKl *kl, cudaStream_t st)
 {
     using namespace tw;
     CUtensorMap mq, mkv, mkc;
@@ -725,6 +814,15 @@ cudaError_t launch_teacher_h128_tc(const Geo &g, const __nv_bfloat16 *q, const _
     a.kv_c = kv_c;
     a.teacher = teacher;
     a.nkb = g.D / 64;
+    if (kl != nullptr) {  // the KL step needs the sparse support and one teacher slot per selected slot
+        if (!g.sparse || g.TW != g.K || kl->selscore == nullptr || kl->row_loss == nullptr) return cudaErrorInvalidValue;
+        a.kl = 1;
+        a.selscore = kl->selscore;
+        a.gslot = kl->gslot;
+        a.gkey = kl->gkey;
+        a.ncp = kl->ncp;
+        a.row_loss = kl->row_loss;
+    }
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
