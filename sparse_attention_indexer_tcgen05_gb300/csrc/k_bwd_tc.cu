@@ -225,7 +225,15 @@ struct Unit {
     int npairs;
 };
 
-__device__ Unit decode_unit(const Args &a, int u)
+// A role visits its units in ascending order, so the walk over a segment's row chunks resumes where the previous
+// unit's walk stopped (a cursor per thread); it restarts from chunk 0 when the segment changes or the index goes
+// back.  (Walking from chunk 0 for every unit cost each warp ~340 iterations of two integer divisions per unit on
+// a 512-chunk sequence.)
+struct UnitCursor {
+    int b = -1, c = 0, base = 0;  // segment, current chunk, units of the chunks before it
+};
+
+__device__ Unit decode_unit(const Args &a, int u, UnitCursor &cur)
 {
     const Geo &g = a.g;
     Unit U;
@@ -240,19 +248,53 @@ __device__ Unit decode_unit(const Args &a, int u)
     U.sg = seg_of(g, b);
     U.kt = 0;
     U.s_lo = U.s_hi = 0;
+    if (b != cur.b || lu < cur.base) {
+        cur.b = b;
+        cur.c = 0;
+        cur.base = 0;
+    }
     const int nch = (U.sg.len_real + CH - 1) / CH;
-    for (int c = 0; c < nch; c++) {
-        const int nt = chunk_tiles(c, U.sg.len_real, U.sg.nc, g.ratio);
-        if (lu < nt) {
-            U.kt = lu;
-            U.s_lo = c * CH;
+    while (cur.c < nch) {
+        const int nt = chunk_tiles(cur.c, U.sg.len_real, U.sg.nc, g.ratio);
+        if (lu - cur.base < nt) {
+            U.kt = lu - cur.base;
+            U.s_lo = cur.c * CH;
             U.s_hi = min(U.sg.len_real, U.s_lo + CH);
             break;
         }
-        lu -= nt;
+        cur.base += nt;
+        cur.c++;
     }
     U.npairs = (U.s_hi - U.s_lo + 1) / RP;
     return U;
+}
+
+// The slot ranges [lo, hi) of key tile U.kt in the unit's rows, from the tile-offset rows, into sRng[r][2] (clamped to
+// [0, K]); every load of the warp is issued before any is used (at most CH = 128 rows: four per lane).
+__device__ __forceinline__ void load_ranges(const Args &a, const Unit &U, int nrow, int *sRng, int lane)
+{
+    static_assert(CH == 128, "four rows per lane");
+    const int K = a.g.K;
+    int lo[4], hi[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int r = lane + 32 * i;
+        lo[i] = hi[i] = 0;
+        if (r < nrow) {
+            const int *o = a.toff + row_of(a.g, U.sg.b, U.s_lo + r) * (long long)(a.NT + 1);
+            lo[i] = __ldg(o + U.kt);
+            hi[i] = __ldg(o + U.kt + 1);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int r = lane + 32 * i;
+        if (r < nrow) {
+            const int l = lo[i] < 0 ? 0 : (lo[i] > K ? K : lo[i]);
+            sRng[2 * r] = l;
+            sRng[2 * r + 1] = hi[i] < l ? l : (hi[i] > K ? K : hi[i]);
+        }
+    }
 }
 
 __device__ __forceinline__ int unit_total(const Args &a)
@@ -791,8 +833,9 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
             int last_qs[K_BSTG];
             for (int x = 0; x < K_BSTG; x++) last_qs[x] = -1;
             int last_uc = -1;
+            UnitCursor cur;
             for (int u = blockIdx.x; u < total; u += gridDim.x) {
-                const Unit U = decode_unit(a, u);
+                const Unit U = decode_unit(a, u, cur);
                 if (U.npairs == 0) continue;
                 wait_bar(a_empty, (uc & 1) ^ 1, abort_flag, err, 21);
                 mbar_expect_tx(a_full, KTILE);
@@ -836,10 +879,11 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         const bool xw = warp == 1;
         int uc = 0, bs = 0, k = 0, np_lane = 0, xb = 0;
         uint32_t bph = 0, xph = 0;
+        UnitCursor lcur;  // lane l decodes units u + l * gridDim.x, ascending across refills
         for (int u = blockIdx.x; u < total; u += gridDim.x, k++) {
             if ((k & 31) == 0) {
                 const int ul = u + lane * (int)gridDim.x;
-                np_lane = ul < total ? decode_unit(a, ul).npairs : 0;
+                np_lane = ul < total ? decode_unit(a, ul, lcur).npairs : 0;
             }
             const int npairs = __shfl_sync(0xffffffffu, np_lane, k & 31);
             if (npairs == 0) continue;
@@ -900,19 +944,13 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         const int K = g.K;
         int *sRng = reinterpret_cast<int *>(smem + K_OFF_RNG);  // [CH][2]
         int pc = 0;
+        UnitCursor cur;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit U = decode_unit(a, u);
+            const Unit U = decode_unit(a, u, cur);
             if (U.npairs == 0) continue;
             const int nrow = U.s_hi - U.s_lo;
             __syncwarp();
-            for (int r = lane; r < nrow; r += 32) {
-                const int *o = a.toff + row_of(g, U.sg.b, U.s_lo + r) * (long long)(a.NT + 1);
-                int lo = __ldg(o + U.kt), hi = __ldg(o + U.kt + 1);
-                lo = lo < 0 ? 0 : (lo > K ? K : lo);
-                hi = hi < lo ? lo : (hi > K ? K : hi);
-                sRng[2 * r] = lo;
-                sRng[2 * r + 1] = hi;
-            }
+            load_ranges(a, U, nrow, sRng, lane);
             __syncwarp();
             const long long k0 = U.sg.gid0 + (long long)U.kt * NKEY;
             for (int pi = 0; pi < U.npairs; pi++, pc++) {
@@ -946,8 +984,9 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         int xb = 0, dkc = 0, pc = 0;
         uint32_t xph = 0;
+        UnitCursor cur;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit U = decode_unit(a, u);
+            const Unit U = decode_unit(a, u, cur);
             for (int pi = 0; pi < U.npairs; pi++, pc++) {
                 const int gs = pc % K_GSTG;
                 const uint32_t gph = (pc / K_GSTG) & 1;
@@ -1101,8 +1140,9 @@ dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------------ TMA producer
             int qs = 0, pc = 0;
+            UnitCursor cur;
             for (int u = blockIdx.x; u < total; u += gridDim.x) {
-                const Unit U = decode_unit(a, u);
+                const Unit U = decode_unit(a, u, cur);
                 for (int pi = 0; pi < U.npairs; pi++) {
                     // the pair's q rows and w rows, one copy each (a second row past the chunk's end is read, never used)
                     const int s0 = U.s_lo + pi * RP;
@@ -1130,8 +1170,9 @@ dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         // pair's barriers cannot be two phases behind: their previous uses have been consumed.)
         int qs = 0, xc = 0, uc = 0;
         bool rdy = false;  // the next pair's q block and G slot are known complete
+        UnitCursor cur;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit U = decode_unit(a, u);
+            const Unit U = decode_unit(a, u, cur);
             if (U.npairs == 0) continue;
             for (int pi = 0; pi < U.npairs; pi++) {
                 const int bs = qs % S_QSTG, xb = xc % S_XSTG;
@@ -1167,19 +1208,13 @@ dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int K = g.K;
         int *sRng = reinterpret_cast<int *>(smem + S_OFF_RNG) + bw * CH * 2;
         int pc = 0;
+        UnitCursor cur;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit U = decode_unit(a, u);
+            const Unit U = decode_unit(a, u, cur);
             if (U.npairs == 0) continue;
             const int nrow = U.s_hi - U.s_lo;
             __syncwarp();
-            for (int r = lane; r < nrow; r += 32) {
-                const int *o = a.toff + row_of(g, U.sg.b, U.s_lo + r) * (long long)(a.NT + 1);
-                int lo = __ldg(o + U.kt), hi = __ldg(o + U.kt + 1);
-                lo = lo < 0 ? 0 : (lo > K ? K : lo);
-                hi = hi < lo ? lo : (hi > K ? K : hi);
-                sRng[2 * r] = lo;
-                sRng[2 * r + 1] = hi;
-            }
+            load_ranges(a, U, nrow, sRng, lane);
             __syncwarp();
             const long long k0 = U.sg.gid0 + (long long)U.kt * NKEY;
             for (int pi = 0; pi < U.npairs; pi++, pc++) {
@@ -1238,8 +1273,9 @@ dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
         const int k = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         int xc = 0, dkc = 0, pc = 0;
+        UnitCursor cur;
         for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit U = decode_unit(a, u);
+            const Unit U = decode_unit(a, u, cur);
             for (int pi = 0; pi < U.npairs; pi++, pc++, xc++) {
                 const int gs = pc % S_GSTG, xb = xc % S_XSTG;
                 const bool row_ok = U.s_lo + pi * RP + half < U.s_hi;  // warp-uniform
