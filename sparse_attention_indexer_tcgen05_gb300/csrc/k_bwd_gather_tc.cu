@@ -125,7 +125,7 @@ dq_dw_gather_tc_kernel(const __grid_constant__ CUtensorMap map_q, Args a)
     // the key-owner kernel reads nothing this one writes: let it take each SM this kernel leaves
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = smem_align1024(smem_raw);
     unsigned char *sK = smem + OFF_K;
     unsigned char *sQ = smem + OFF_Q;
     unsigned char *sG = smem + OFF_G;

@@ -337,7 +337,7 @@ dq_dw_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant
     // the key-owner kernel reads nothing this one writes: let it take each SM this kernel leaves
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = smem_align1024(smem_raw);
     unsigned char *sA = smem + R_OFF_A;
     unsigned char *sB = smem + R_OFF_B;
     float *sGD = reinterpret_cast<float *>(smem + R_OFF_GD);
@@ -780,7 +780,7 @@ dk_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ 
              const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_w, Args a)
 {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = smem_align1024(smem_raw);
     unsigned char *sA = smem + K_OFF_A;
     unsigned char *sB = smem + K_OFF_B;
     float *sGT = reinterpret_cast<float *>(smem + K_OFF_GT);
@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 dk_sign_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w, Args a)
 {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = smem_align1024(smem_raw);
     unsigned char *sB = smem + S_OFF_B;
     float *sGT = reinterpret_cast<float *>(smem + S_OFF_GT);
     unsigned long long *sBT = reinterpret_cast<unsigned long long *>(smem + S_OFF_BT);

@@ -535,7 +535,7 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
     using C = SC<LONG>;
     constexpr int NB = C::NB;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = smem_align1024(smem_raw);
     unsigned char *sA = smem + C::OFF_A;
     unsigned char *sB = smem + C::OFF_B;
     float *sW = reinterpret_cast<float *>(smem + C::OFF_W);

@@ -160,6 +160,8 @@ teacher_h128_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_c
                        const __grid_constant__ CUtensorMap map_kvc, Args a)
 {
     extern __shared__ unsigned char smem_raw[];
+    // aligned through an integer, unlike the other tensor-core kernels (smem_align1024): with the shared-window
+    // form the compiler's register allocation for this kernel spills, and the kernel measured about 1 % slower
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *ring = smem + OFF_RING;
     float *sT = reinterpret_cast<float *>(smem + OFF_T);             // [2][TWMAX]

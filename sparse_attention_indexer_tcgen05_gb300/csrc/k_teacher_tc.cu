@@ -174,7 +174,7 @@ teacher_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_consta
                   const __grid_constant__ CUtensorMap map_kvc, Args a)
 {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char *smem = smem_align1024(smem_raw);
     unsigned char *sQ = smem + OFF_Q;
     unsigned char *sB = smem + OFF_B;
     float *sT = reinterpret_cast<float *>(smem + OFF_T);                // [2][RP][NCMAX]

@@ -13,6 +13,16 @@ constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// The dynamic shared memory aligned up to 1024 bytes (what 128-byte-swizzled TMA and MMA tiles need), by pointer
+// arithmetic on the __shared__ array itself: the compiler then knows that every access through the result is a
+// shared-memory one.  (Rounding the address through an integer hides that, and every load, store and atomic made
+// through such a pointer becomes a generic-address one, which measured slower in the latency-bound loops.)  The
+// alignment is taken on the shared-window address, the one TMA and the MMA descriptors use.
+__device__ __forceinline__ unsigned char *smem_align1024(unsigned char *raw)
+{
+    return raw + ((1024u - (su32(raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
