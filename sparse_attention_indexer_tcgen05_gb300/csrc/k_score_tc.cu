@@ -348,7 +348,7 @@ __device__ void select_row(const Args &a, const Item &it, int k, const float *sc
 // 8 bits with a 256-bin histogram per pass.  The walk starts at the highest bit in which lo and hi differ (the
 // bits above it are the same in every key, so no pass is spent on them).
 //   slack < 0: returns the K-th largest key T; `need_eq` receives how many entries equal to T belong to the top K
-//              (the rest of the top K lies strictly above T).
+//              (the rest of the top K lies strictly above T), or n when every entry equal to T does.
 //   slack >= 0: may stop early, at the first digit whose bin holding the K-th largest key has a lower edge L with
 //              at most K + slack keys at or above it; returns L (at least K keys lie at or above it), with
 //              `need_eq` = n (every key equal to L is kept).  Reaching the last digit gives the exact answer.
@@ -359,7 +359,7 @@ __device__ uint32_t kth_search(const uint32_t *ck, int n, int K, uint32_t lo, ui
 {
     const int lane = threadIdx.x & 31;
     if (lo == hi) {  // every key is the same: the first K of them
-        need_eq = K;
+        need_eq = K < n ? K : n;
         return lo;
     }
     int hb = 31 - __clz(lo ^ hi);                 // top bit of the current digit
@@ -371,17 +371,17 @@ __device__ uint32_t kth_search(const uint32_t *ck, int n, int K, uint32_t lo, ui
         const uint32_t wmask = (2u << (hb - lb)) - 1u;
         const uint32_t pmask = ~((2u << hb) - 1u);
 #pragma unroll
-        for (int q = 0; q < 8; q++) hist[lane * 8 + q] = 0u;
+        for (int q = 0; q < 8; q++) hist[32 * q + lane] = 0u;
         __syncwarp();
-        for (int e0 = 0; e0 < n; e0 += 128) {
-            uint32_t kk[4];
+        for (int e0 = 0; e0 < n; e0 += 256) {  // eight loads in flight per lane
+            uint32_t kk[8];
 #pragma unroll
-            for (int u = 0; u < 4; u++) {
+            for (int u = 0; u < 8; u++) {
                 const int e = e0 + 32 * u + lane;
                 kk[u] = e < n ? ck[e] : 0u;
             }
 #pragma unroll
-            for (int u = 0; u < 4; u++)
+            for (int u = 0; u < 8; u++)
                 if (e0 + 32 * u + lane < n && (kk[u] & pmask) == prefix) atomicAdd(hist + ((kk[u] >> lb) & wmask), 1u);
         }
         __syncwarp();
@@ -425,7 +425,7 @@ __device__ uint32_t kth_search(const uint32_t *ck, int n, int K, uint32_t lo, ui
         need -= (int)above;
         __syncwarp();
         if (lb == 0) {
-            need_eq = need;
+            need_eq = need == (int)cnt ? n : need;  // cnt entries equal the whole key
             return prefix;
         }
         // keys at or above the bin's lower edge: K - need + cnt
@@ -464,10 +464,14 @@ __device__ uint32_t kth_search(const uint32_t *ck, int n, int K, uint32_t lo, ui
                 for (int q = 0; q < 8; q++) c2 += key[q] >= cc ? 1u : 0u;
                 if ((int)__reduce_add_sync(0xffffffffu, c2) >= need) t = cc;
             }
-            unsigned gt = 0u;
+            unsigned gt = 0u, eq = 0u;
 #pragma unroll
-            for (int q = 0; q < 8; q++) gt += key[q] > t ? 1u : 0u;
+            for (int q = 0; q < 8; q++) {
+                gt += key[q] > t ? 1u : 0u;
+                eq += 32 * q + lane < (int)cnt && key[q] == t ? 1u : 0u;
+            }
             need_eq = need - (int)__reduce_add_sync(0xffffffffu, gt);
+            if (need_eq == (int)__reduce_add_sync(0xffffffffu, eq)) need_eq = n;  // every entry equal to t is kept
             __syncwarp();  // the list is read before the next cut zeroes the histogram
             return t;
         }
@@ -487,6 +491,37 @@ __device__ int cut_candidates(uint32_t *ck, uint16_t *ci, int n, int K, uint32_t
     const uint32_t T = kth_search(ck, n, K, lo, hi, slack, hist, need_eq);
     const unsigned lt = (1u << lane) - 1u;
     int base = 0, eq_seen = 0;
+    if (need_eq >= n) {
+        // every key at or above T is kept (a slack cut's bin edge, or a cut that splits no tie): no tie count, and
+        // eight chunks per step (the loop is bound by its shared-memory latency, not by its instructions).  A step
+        // writes only at or below its own entries, all read before the step's barrier.
+        for (int c0 = 0; c0 < n; c0 += 256) {
+            uint32_t k[8];
+            uint16_t ix[8];
+            unsigned mk[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int e = c0 + 32 * u + lane;
+                k[u] = e < n ? ck[e] : 0u;
+                ix[u] = e < n ? ci[e] : (uint16_t)0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; u++) mk[u] = __ballot_sync(0xffffffffu, c0 + 32 * u + lane < n && k[u] >= T);
+            __syncwarp();  // every lane has read its entries before any is overwritten
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                if ((mk[u] >> lane) & 1u) {
+                    const int pos = base + __popc(mk[u] & lt);
+                    ck[pos] = k[u];
+                    ci[pos] = ix[u];
+                }
+                base += __popc(mk[u]);
+            }
+        }
+        __syncwarp();
+        thr = T;
+        return base;
+    }
     // four 32-entry chunks per step, loaded and decided before any is written (one warp has little else to
     // overlap its shared-memory latency with); writes land at or below the step's own entries
     for (int c0 = 0; c0 < n; c0 += 128) {
