@@ -479,6 +479,58 @@ __device__ uint32_t kth_search(const uint32_t *ck, int n, int K, uint32_t lo, ui
     }
 }
 
+// A slack cut point by sampling (slack >= 0): a key L of the buffer with between K and K + slack keys at or above
+// it, or false.  The pivot is the sampled key whose rank among 128 keys spread over the buffer matches the window's
+// middle (found bit by bit in registers, from the highest bit in which lo and hi differ); one counting pass over
+// the buffer checks it (compares and a warp sum, no atomics), and a miss moves the sample rank by the miss scaled
+// to the sample, three tries at most.  The caller falls back to the radix walk.
+__device__ __forceinline__ bool sample_cut(const uint32_t *ck, int n, int K, int slack, uint32_t lo, uint32_t hi,
+                                           uint32_t &L)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t sk[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) sk[q] = ck[(int)(((long long)(32 * q + lane) * n) >> 7)];
+    const int target = K + slack / 2;
+    int r = (int)(((long long)target * 128 + n / 2) / n);  // the target's rank among the samples, from the top
+    const int hb = lo == hi ? -1 : 31 - __clz(lo ^ hi);
+    const uint32_t prefix = hb < 0 ? lo : (hi & ~((2u << hb) - 1u));
+#pragma unroll 1
+    for (int attempt = 0; attempt < 3; attempt++) {
+        r = r < 1 ? 1 : (r > 128 ? 128 : r);
+        // P: the r-th largest sample (the largest value with at least r samples at or above it)
+        uint32_t P = prefix;
+#pragma unroll 1
+        for (int bit = hb; bit >= 0; bit--) {
+            const uint32_t cand = P | (1u << bit);
+            unsigned c = 0u;
+#pragma unroll
+            for (int q = 0; q < 4; q++) c += sk[q] >= cand ? 1u : 0u;
+            if ((int)__reduce_add_sync(0xffffffffu, c) >= r) P = cand;
+        }
+        unsigned cnt = 0u;
+        for (int e0 = 0; e0 < n; e0 += 256) {  // eight loads in flight per lane
+            uint32_t kk[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int e = e0 + 32 * u + lane;
+                kk[u] = e < n ? ck[e] : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; u++) cnt += (e0 + 32 * u + lane < n && kk[u] >= P) ? 1u : 0u;
+        }
+        const int C = (int)__reduce_add_sync(0xffffffffu, cnt);
+        if (C >= K && C <= K + slack) {
+            L = P;
+            return true;
+        }
+        int step = (int)(((long long)(target - C) * 128) / n);
+        if (step == 0) step = C < K ? 1 : -1;
+        r += step;
+    }
+    return false;
+}
+
 // Cuts the candidate buffer (ascending key index, keys in [lo, hi]) back to the entries at or above the cut
 // point kth_search finds (exactly the top K, ties to the lower index, when slack < 0; otherwise every key at or
 // above a bin edge L, between K and K + slack of them), keeping the ascending order (stable in-place
@@ -487,8 +539,9 @@ __device__ int cut_candidates(uint32_t *ck, uint16_t *ci, int n, int K, uint32_t
                               uint32_t *hist, uint32_t &thr)
 {
     const int lane = threadIdx.x & 31;
-    int need_eq = 0;
-    const uint32_t T = kth_search(ck, n, K, lo, hi, slack, hist, need_eq);
+    int need_eq = n;
+    uint32_t T = 0u;
+    if (!(slack >= 0 && sample_cut(ck, n, K, slack, lo, hi, T))) T = kth_search(ck, n, K, lo, hi, slack, hist, need_eq);
     const unsigned lt = (1u << lane) - 1u;
     int base = 0, eq_seen = 0;
     if (need_eq >= n) {
