@@ -126,8 +126,8 @@ template <> struct SC<true> {
 };
 static_assert(SC<false>::SMEM_ALLOC <= 232448, "score kernel exceeds the 227 KB of shared memory a CTA may use");
 static_assert(SC<true>::SMEM_ALLOC <= 232448, "long score kernel exceeds the 227 KB of shared memory a CTA may use");
-// largest K the long kernel takes: an in-loop cut leaves at most K + slack entries, slack = min(256, CAP -
-// 2 NKEY - K) >= 0, so that two more tiles fit
+// largest K the long kernel takes: an in-loop cut leaves room for two more tiles (at most K + slack entries, slack =
+// min(256, CAP - 2 NKEY - K) >= 0, or a sampled pivot's at most n - 2 NKEY)
 constexpr int LONG_KMAX = SC<true>::CAP - 2 * NKEY;
 constexpr int LONG_NCMAX = 65535;             // candidate indices are 16-bit
 
@@ -531,17 +531,22 @@ __device__ __forceinline__ bool sample_cut(const uint32_t *ck, int n, int K, int
     return false;
 }
 
-// Cuts the candidate buffer (ascending key index, keys in [lo, hi]) back to the entries at or above the cut
-// point kth_search finds (exactly the top K, ties to the lower index, when slack < 0; otherwise every key at or
-// above a bin edge L, between K and K + slack of them), keeping the ascending order (stable in-place
-// compaction).  Returns the new count; `thr` receives T (or L): a later key can enter the top K only above it.
+// Cuts the candidate buffer (ascending key index, keys in [lo, hi]) back to the entries at or above a cut point
+// (exactly the top K, ties to the lower index, when slack < 0, found by kth_search; otherwise every key at or above
+// a point L with at least K of them: a sampled pivot with at most K + 512 of them, and never more than n - 2 NKEY,
+// else kth_search's bin edge with at most K + slack), keeping the ascending order (stable in-place compaction).
+// Returns the new count; `thr` receives T (or L): a later key can enter the top K only above it.
 __device__ int cut_candidates(uint32_t *ck, uint16_t *ci, int n, int K, uint32_t lo, uint32_t hi, int slack,
                               uint32_t *hist, uint32_t &thr)
 {
     const int lane = threadIdx.x & 31;
     int need_eq = n;
     uint32_t T = 0u;
-    if (!(slack >= 0 && sample_cut(ck, n, K, slack, lo, hi, T))) T = kth_search(ck, n, K, lo, hi, slack, hist, need_eq);
+    // the sampled pivot may keep up to 512 keys past K (fewer when two more tiles would not fit after the cut):
+    // a wider window than the radix walk's costs a few more cuts but misses less often
+    const int wide = n - 2 * NKEY - K < 512 ? n - 2 * NKEY - K : 512;
+    if (!(slack >= 0 && sample_cut(ck, n, K, wide > slack ? wide : slack, lo, hi, T)))
+        T = kth_search(ck, n, K, lo, hi, slack, hist, need_eq);
     const unsigned lt = (1u << lane) - 1u;
     int base = 0, eq_seen = 0;
     if (need_eq >= n) {
