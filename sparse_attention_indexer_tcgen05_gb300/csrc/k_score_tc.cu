@@ -27,7 +27,7 @@
 //               epilogue runs the following items:
 //               the exact k-th largest score by a bitwise search on order-preserving keys held in
 //               registers, then the selection written by a stable ballot compaction.
-//   (long key axis: warps 10..13, one per row, follow the epilogue tile by tile through a four-tile ring; each
+//   (long key axis: warps 10..13, one per row, follow the epilogue tile by tile through a six-tile ring; each
 //    keeps the row's current best candidates, cuts them back to about the top K with a radix walk when the
 //    buffer fills, and to exactly the top K at the row's end.)
 //
@@ -112,7 +112,7 @@ template <> struct SC<false> {
 template <> struct SC<true> {
     static constexpr int THREADS = 448;       // warps 0 TMA, 1 MMA, 2..9 epilogue, 10..13 selection
     static constexpr int NB = 1;
-    static constexpr int NRING = 4;           // score tiles in flight between epilogue and selection
+    static constexpr int NRING = 6;           // score tiles in flight between epilogue and selection (2 KB each)
     static constexpr int CAP = 4096;          // candidate entries per row
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + A_STAGES * A_HALF;        // 48 KB
@@ -126,6 +126,11 @@ template <> struct SC<true> {
 };
 static_assert(SC<false>::SMEM_ALLOC <= 232448, "score kernel exceeds the 227 KB of shared memory a CTA may use");
 static_assert(SC<true>::SMEM_ALLOC <= 232448, "long score kernel exceeds the 227 KB of shared memory a CTA may use");
+// the epilogue -> selection barriers: X_BARS full and X_BARS empty ones after the 17 pipeline barriers, all below
+// the TMEM slot at byte 256 of the barrier area
+constexpr int X_BARS = 6;
+static_assert(SC<true>::NRING <= X_BARS && SC<false>::NSC <= X_BARS && (17 + 2 * X_BARS) * 8 <= 256,
+              "score kernel barriers overlap the TMEM slot");
 // largest K the long kernel takes: an in-loop cut leaves room for two more tiles (at most K + slack entries, slack =
 // min(256, CAP - 2 NKEY - K) >= 0, or a sampled pivot's at most n - 2 NKEY)
 constexpr int LONG_KMAX = SC<true>::CAP - 2 * NKEY;
@@ -637,7 +642,7 @@ __device__ __forceinline__ void score_body(const CUtensorMap *map_q, const CUten
     uint64_t *t_full = bars + 12, *t_empty = bars + 14, *mma_done = bars + 16;
     // short axis: score rows of an item, epilogue -> selection (sc_full / sc_empty, NSC each);
     // long axis: score tiles (ring_full / ring_empty, NRING each)
-    uint64_t *x_full = bars + 17, *x_empty = bars + 17 + 4;
+    uint64_t *x_full = bars + 17, *x_empty = bars + 17 + X_BARS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC + 256);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 264);
 
