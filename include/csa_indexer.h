@@ -187,7 +187,10 @@ csa_status csa_teacher_from_lse(const csa_params *p, const void *q, const void *
  *   dk_idx [compressed rows, D_I] = sum_t sum_j g_ts w_tj 1[x_tjs > 0] q_idx[t,j]   (rows never selected: 0)
  * with x_tjs = q_idx[t,j].k_idx[s].  No gradient flows to q, kv, kv_c or the sink (the follow-up
  * proposal: teacher-side inputs stay detached).  loss_out is one device fp32; row_loss_out (optional, NULL to
- * skip) receives the unscaled per-row KL L_t [rows] fp32 (0 for padding rows and rows without keys). */
+ * skip) receives the unscaled per-row KL L_t [rows] fp32 (0 for padding rows and rows without keys).
+ * With teacher_or_null NULL, 128 main heads and the sparse loss, the KL step runs inside the teacher kernel, which
+ * reduces a row's maximum and normaliser in another order than the separate KL kernel that a given teacher takes:
+ * the two calls then agree to fp32 rounding (and the bf16 outputs to a unit in the last place), not bit for bit. */
 csa_status csa_indexer_bwd(const csa_params *p, const void *q_idx, const float *w, const void *k_idx,
                            const void *q, const void *kv, const void *kv_c, const float *sink,
                            const int32_t *ids, const float *selscore, const float *teacher_or_null,
